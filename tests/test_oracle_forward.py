@@ -1,0 +1,199 @@
+"""Pins of the oracle's attention recurrence.
+
+* The exact (FP64, quantisers bypassed) mode runs the same tiled skeleton as
+  the quantised contract; it must equal brute-force softmax(Q K^T * scale) V
+  computed with numpy (causal bottom-right mask, GQA, ragged lengths, any
+  tile size), and K smoothing must not change it (shift invariance).
+* The quantised mode: constant V reproduces V exactly, a dominant key selects
+  its dequantised V row, the result does not depend on the tile size when the
+  running max never changes, and it stays close to exact attention.
+"""
+import numpy as np
+import pytest
+
+import synth
+
+
+def _bf(x):
+    return synth.to_bf16_bits(np.asarray(x, dtype=np.float64))
+
+
+def _f64(bits):
+    return synth.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def brute_attention(q, k, v, causal, scale=None):
+    """softmax(q k^T * scale) v per head; causal keeps j <= i + (Nkv - Nq)."""
+    B, Hq, Nq, D = q.shape
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    scale = 1.0 / np.sqrt(D) if scale is None else scale
+    out = np.empty_like(q)
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // (Hq // Hkv)
+            s = q[b, h] @ k[b, hk].T * scale
+            if causal:
+                i = np.arange(Nq)[:, None]
+                j = np.arange(Nkv)[None, :]
+                s = np.where(j <= i + (Nkv - Nq), s, -np.inf)
+            s = s - s.max(axis=1, keepdims=True)
+            p = np.exp(s)
+            out[b, h] = (p / p.sum(axis=1, keepdims=True)) @ v[b, hk]
+    return out
+
+
+CASES = [  # B, Hq, Hkv, Nq, Nkv, causal, tile
+    (1, 1, 1, 128, 192, False, 128),
+    (1, 2, 2, 37, 300, False, 64),
+    (2, 4, 2, 70, 70, True, 32),
+    (1, 4, 1, 50, 131, True, 128),      # causal with Nq < Nkv: bottom-right diagonal
+    (1, 2, 1, 1, 1, False, 16),
+    (1, 2, 2, 129, 129, True, 128),
+    (1, 1, 1, 5, 5, True, 2),
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_exact_mode_equals_brute_force_softmax(oracle_mod, case):
+    B, Hq, Hkv, Nq, Nkv, causal, tile = case
+    rng = np.random.default_rng(Nq * 7 + Nkv)
+    q = rng.standard_normal((B, Hq, Nq, 128)) * 1.5
+    k = rng.standard_normal((B, Hkv, Nkv, 128)) + 2.0 * rng.standard_normal((B, Hkv, 1, 128))
+    v = rng.standard_normal((B, Hkv, Nkv, 128))
+    got = oracle_mod.forward_exact(q, k, v, causal, smooth=False, tile=tile)
+    ref = brute_attention(q, k, v, causal)
+    assert np.abs(got - ref).max() <= 1e-12
+
+
+@pytest.mark.parametrize("case", CASES[:4])
+def test_exact_mode_shift_invariance_of_k_smoothing(oracle_mod, case):
+    B, Hq, Hkv, Nq, Nkv, causal, tile = case
+    rng = np.random.default_rng(3 + Nq)
+    q = rng.standard_normal((B, Hq, Nq, 128))
+    k = rng.standard_normal((B, Hkv, Nkv, 128)) + 3.0 * rng.standard_normal((B, Hkv, 1, 128))
+    v = rng.standard_normal((B, Hkv, Nkv, 128))
+    a = oracle_mod.forward_exact(q, k, v, causal, smooth=False, tile=tile)
+    b = oracle_mod.forward_exact(q, k, v, causal, smooth=True, tile=tile)
+    assert np.abs(a - b).max() <= 1e-12
+
+
+def _quant(oracle_mod, q, k, v, causal, tile=128, smooth=True):
+    p = oracle_mod.prepare(q, k, v, smooth=smooth)
+    return p, oracle_mod.forward(p, q.shape[2], k.shape[2], causal, tile=tile)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_v_gives_that_constant_exactly(oracle_mod, causal):
+    rng = np.random.default_rng(11)
+    Nq, Nkv = 100, 300
+    q = rng.standard_normal((1, 2, Nq, 128))
+    k = rng.standard_normal((1, 1, Nkv, 128))
+    # scores grow with the key index, so the running max rises in every tile
+    # and every rescale factor alpha is below one
+    q[..., 0] = 2.0
+    k[..., 0] = np.linspace(-6, 6, Nkv)[None, None, :]
+    v0 = _bf(rng.standard_normal(128))
+    v = np.broadcast_to(synth.bf16_bits_to_f32(v0), (1, 1, Nkv, 128))
+    for tile in (32, 64, 128):
+        _, (ob, _) = _quant(oracle_mod, _bf(q), _bf(k), _bf(v), causal, tile)
+        assert np.array_equal(ob, np.broadcast_to(v0, ob.shape)), tile
+
+
+def test_dominant_key_selects_its_value_row(oracle_mod):
+    rng = np.random.default_rng(12)
+    Nq, Nkv, star = 40, 400, 263              # the dominant key sits in tile 2 of 4
+    q = np.full((1, 1, Nq, 128), 4.0)
+    k = rng.standard_normal((1, 1, Nkv, 128)) * 0.1
+    k[0, 0, star] = 4.0
+    v = rng.standard_normal((1, 1, Nkv, 128))
+    p, (ob, of) = _quant(oracle_mod, _bf(q), _bf(k), _bf(v), False)
+    row = oracle_mod.e4m3_to_f32(p["v_codes"][0, 0, star]).astype(np.float64) * p["v_scales"][0, 0]
+    got = synth.bf16_bits_to_f32(ob[0, 0]).astype(np.float64)
+    ulp = np.abs(row) * 2.0 ** -7
+    assert np.all(np.abs(got - row[None, :]) <= ulp[None, :] + 1e-30)
+
+
+def test_tile_size_invariance_when_running_max_is_fixed(oracle_mod):
+    rng = np.random.default_rng(13)
+    Nq, Nkv = 64, 512
+    q = rng.standard_normal((1, 1, Nq, 128))
+    k = rng.standard_normal((1, 1, Nkv, 128))
+    v = rng.standard_normal((1, 1, Nkv, 128))
+    q[..., 0] = 4.0
+    k[0, 0, 0, 0] = 24.0          # key 0 (tile 0) holds every row's maximum score
+    outs = []
+    for tile in (16, 64, 128, 256):
+        _, (_, of) = _quant(oracle_mod, _bf(q), _bf(k), _bf(v), False, tile)
+        outs.append(of.astype(np.float64))
+    for o in outs[1:]:
+        # only the FP32 grouping of the PV sums differs between tilings
+        assert np.abs(o - outs[0]).max() <= 1e-5 * np.abs(outs[0]).max()
+    # the property is not vacuous: without a fixed maximum the tilings differ
+    k2 = rng.standard_normal((1, 1, Nkv, 128))
+    _, (_, a) = _quant(oracle_mod, _bf(q), _bf(k2), _bf(v), False, 16)
+    _, (_, b) = _quant(oracle_mod, _bf(q), _bf(k2), _bf(v), False, 256)
+    assert np.abs(a - b).max() > 1e-4
+
+
+def _cos(a, b):
+    a, b = a.ravel(), b.ravel()
+    return float(a @ b / np.linalg.norm(a) / np.linalg.norm(b))
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_quantised_mode_is_close_to_exact_attention(oracle_mod, case):
+    B, Hq, Hkv, Nq, Nkv, causal, tile = case
+    rng = np.random.default_rng(21 + Nq)
+    q = _bf(rng.standard_normal((B, Hq, Nq, 128)))
+    k = _bf(rng.standard_normal((B, Hkv, Nkv, 128)) + 2.0 * rng.standard_normal((B, Hkv, 1, 128)))
+    v = _bf(rng.standard_normal((B, Hkv, Nkv, 128)))
+    _, (_, of) = _quant(oracle_mod, q, k, v, causal, tile)
+    ref = brute_attention(_f64(q), _f64(k), _f64(v), causal)
+    for b in range(B):
+        for h in range(Hq):
+            for i in range(Nq):
+                assert _cos(of[b, h, i], ref[b, h, i]) > 0.99, (b, h, i)
+    assert _cos(of, ref) > 0.999
+
+
+def test_smoothing_reduces_error_on_biased_k(oracle_mod):
+    w = synth.workload("c1")
+    q, k, v = synth.make_inputs(w)
+    ref = brute_attention(_f64(q), _f64(k), _f64(v), False)
+    _, (_, with_s) = _quant(oracle_mod, q, k, v, False, smooth=True)
+    _, (_, without) = _quant(oracle_mod, q, k, v, False, smooth=False)
+    assert np.abs(with_s - ref).max() < np.abs(without - ref).max()
+    assert _cos(with_s, ref) > _cos(without, ref)
+
+
+def test_single_key_returns_dequantised_value(oracle_mod):
+    rng = np.random.default_rng(14)
+    q = _bf(rng.standard_normal((1, 3, 7, 128)))
+    k = _bf(rng.standard_normal((1, 1, 1, 128)))
+    v = _bf(rng.standard_normal((1, 1, 1, 128)))
+    p, (ob, _) = _quant(oracle_mod, q, k, v, False)
+    row = oracle_mod.e4m3_to_f32(p["v_codes"][0, 0, 0]).astype(np.float64) * p["v_scales"][0, 0]
+    got = synth.bf16_bits_to_f32(ob).astype(np.float64)
+    assert np.all(np.abs(got - row) <= np.abs(row) * 2.0 ** -7 + 1e-30)
+
+
+def test_row_subset_matches_full_forward(oracle_mod):
+    w = synth.workload("c2", Hq=2, Hkv=2, Nq=300, Nkv=300, causal=True)
+    q, k, v = synth.make_inputs(w)
+    p = oracle_mod.prepare(q, k, v)
+    full_b, full_f = oracle_mod.forward(p, w.Nq, w.Nkv, True)
+    rows = np.array([0, 1, 299, 300, 457, 599])
+    sb, sf = oracle_mod.forward(p, w.Nq, w.Nkv, True, rows=rows)
+    assert np.array_equal(sb, full_b.reshape(-1, 128)[rows])
+    assert np.array_equal(sf, full_f.reshape(-1, 128)[rows])
+
+
+def test_forward_rejects_bad_shapes(oracle_mod):
+    rng = np.random.default_rng(0)
+    q = _bf(rng.standard_normal((1, 1, 9, 128)))
+    k = _bf(rng.standard_normal((1, 1, 8, 128)))
+    p = oracle_mod.prepare(q, k, k)
+    with pytest.raises(ValueError):
+        oracle_mod.forward(p, 9, 8, causal=True)       # causal needs Nq <= Nkv
+    with pytest.raises(ValueError):
+        oracle_mod.forward(p, 9, 8, causal=False, tile=0)
