@@ -1,0 +1,179 @@
+/*
+ * sattn.h -- C ABI of libsattn.so: quantized exact attention with K smoothing
+ * on GB300 (compute capability 10.3, sm_103a).
+ *
+ * What is computed (the "Experiment Log" page, vortex_exact_attention, entry
+ * "Phase 0 Import And Verification": Q/K preparation, K smoothing, INT8
+ * quantization, QK traversal, online softmax, FP8 V/P, two-level PV
+ * accumulation, final conversion, ragged-tail contract; entry "Phase 1
+ * State-Ownership Decision": strict tile order, exact FP8 score bytes,
+ * per-tile RO rescaling, two-level PV accumulation, final conversion):
+ *
+ *   sattn_prepare   K smoothing (K minus its per-channel mean over the
+ *                   sequence), INT8 codes of Q and smoothed K with one FP32
+ *                   scale per 32-token block, FP8 E4M3 codes of V with one
+ *                   FP32 scale per channel.
+ *   sattn_forward   attention over the codes: exact integer QK^T, online
+ *                   softmax over KV tiles in strictly increasing order, P
+ *                   quantised to FP8 E4M3 (p * 448), inner per-tile FP32 PV
+ *                   partial plus outer FP32 RO rescaled every tile, final
+ *                   reciprocal of the denominator and BF16 output.
+ *
+ * Arithmetic, stated fully:
+ *   mean[c]   FP32 sum over 64-token chunks in ascending token order, chunk
+ *             sums added in ascending order, divided by Nkv (IEEE RN).
+ *   ks        fl32(k - mean[c]).
+ *   INT8      per block of 32 tokens x 128 channels: s = amax / 127,
+ *             code = clamp(rint(x / s), -127, 127) (IEEE division, ties to
+ *             even); amax = 0 gives s = 0 and codes 0.
+ *   FP8 V     s_v[c] = amax_c / 448 over all Nkv tokens;
+ *             code = E4M3(v / s_v[c]) round-to-nearest-even, saturating.
+ *   score     s2 = float(acc) * ((s_q * s_k) * c0), acc = exact int32 dot
+ *             product of the codes, c0 = sm_scale * log2(e) (FP32).
+ *   softmax   per KV tile of 128 keys, ascending: m' = max(m, max s2),
+ *             alpha = exp2(m - m') (0 while m = -inf),
+ *             p8 = E4M3(exp2(s2 - m') * 448);
+ *             RO = RO * alpha + sum_j p8_j * v8_j,  d = d * alpha + sum_j p8_j.
+ *   output    out[c] = bf16_rne((RO[c] * (1 / d)) * s_v[c]).
+ *   mask      key j of query row i is kept when j < Nkv and, if causal,
+ *             j <= i + (Nkv - Nq).
+ *   GQA       query head h reads KV head h / (Hq / Hkv).
+ *
+ * Ownership and synchronisation: the caller allocates every buffer (device
+ * memory unless stated otherwise) and owns the stream.  Calls only enqueue
+ * work on `stream` (a cudaStream_t; NULL is the legacy default stream) and
+ * return; they never allocate, free or synchronise, except
+ * sattn_check_status which synchronises the stream by design.  All device
+ * pointers must be 16-byte aligned.  Buffers of one call must not overlap.
+ *
+ * Errors: every entry point returns an sattn_status; no exception crosses
+ * the ABI.  Argument checks happen before anything is enqueued; a failing
+ * call enqueues nothing (except SATTN_ERR_LAUNCH, see below).
+ */
+#ifndef SATTN_H
+#define SATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SATTN_HEAD_DIM 128   /* the only supported head dimension */
+#define SATTN_QBLOCK 32      /* tokens per INT8 quantisation block */
+#define SATTN_KV_TILE 128    /* keys per KV tile of the forward pass */
+
+typedef enum {
+    SATTN_OK = 0,
+    SATTN_ERR_INVALID = 1,     /* null pointer, D != 128, Hq % Hkv != 0, N < 1,
+                                  causal with Nq > Nkv, sizes beyond limits */
+    SATTN_ERR_MISALIGNED = 2,  /* a pointer is not 16-byte aligned */
+    SATTN_ERR_DEVICE = 3,      /* current device is not compute capability 10.3,
+                                  or a CUDA runtime query failed */
+    SATTN_ERR_LAUNCH = 4,      /* a kernel launch failed (cudaGetLastError);
+                                  earlier kernels of the call may have run */
+    SATTN_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out; the
+                                  outputs of that call are undefined */
+} sattn_status;
+
+/* Problem shape.  Q is [B][Hq][Nq][D], K and V are [B][Hkv][Nkv][D]. */
+typedef struct {
+    int32_t B, Hq, Hkv, Nq, Nkv, D;
+    int32_t causal;      /* 0 or 1 */
+    float sm_scale;      /* softmax scale; <= 0 selects 1 / sqrt(D) */
+} sattn_shape;
+
+/* Byte sizes of every buffer for a shape (all multiples of 16). */
+typedef struct {
+    size_t q, k, v;             /* BF16 inputs */
+    size_t q_codes, q_scales;   /* int8 [B][Hq][Nq32][128], FP32 [B][Hq][Nq32/32] */
+    size_t k_codes, k_scales;   /* int8 [B][Hkv][Nkv32][128], FP32 [B][Hkv][Nkv32/32] */
+    size_t k_mean;              /* FP32 [B][Hkv][128] */
+    size_t v_codes, v_scales;   /* E4M3 [B][Hkv][128][Nkv128] (channel-major), FP32 [B][Hkv][128] */
+    size_t out;                 /* BF16 [B][Hq][Nq][128] */
+    size_t prepare_workspace;   /* scratch of sattn_prepare */
+    size_t forward_workspace;   /* scratch of sattn_forward */
+    size_t arena;               /* one device block holding all of the above,
+                                   for sattn_attention_host */
+} sattn_sizes;
+/* NX = N rounded up to a multiple of X. */
+
+/*
+ * sattn_query_sizes -- fill `sizes` for `shape`.  Pure host function.
+ * Returns SATTN_OK or SATTN_ERR_INVALID.
+ */
+int sattn_query_sizes(const sattn_shape *shape, sattn_sizes *sizes);
+
+/*
+ * sattn_prepare -- Q/K preparation, K smoothing, INT8 quantisation of Q and
+ * K, FP8 preparation of V (page entry "Phase 0 Import And Verification",
+ * first three contract stages and "FP8 V").
+ *   q, k, v     in:  BF16, [B][Hq][Nq][128] and [B][Hkv][Nkv][128], contiguous
+ *   q_codes     out: int8, rows Nq .. Nq32-1 of each head are 0
+ *   q_scales    out: FP32, one per 32-token block
+ *   k_codes     out: int8 codes of the smoothed K, pad rows 0
+ *   k_scales    out: FP32, one per 32-token block
+ *   k_mean      out: FP32 per-channel mean of K that was subtracted
+ *   v_codes     out: E4M3 bytes, channel-major [B][Hkv][128][Nkv128];
+ *               keys Nkv .. Nkv128-1 are 0
+ *   v_scales    out: FP32 per channel
+ *   workspace   scratch, sizes.prepare_workspace bytes; contents on entry
+ *               are ignored
+ * Codes and scales are bit-exact functions of the inputs (the arithmetic is
+ * fixed above, including the summation order of the mean).
+ */
+int sattn_prepare(const sattn_shape *shape, const void *q, const void *k, const void *v,
+                  int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
+                  float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace,
+                  void *stream);
+
+/*
+ * sattn_forward -- QK traversal, online softmax, FP8 P, two-level PV
+ * accumulation, final conversion and ragged tails (page entries "Phase 0
+ * Import And Verification" and "Phase 1 State-Ownership Decision").
+ *   q_codes .. v_scales  in: as written by sattn_prepare for the same shape
+ *   out         out: BF16 [B][Hq][Nq][128]
+ *   workspace   scratch, sizes.forward_workspace bytes: holds the K codes
+ *               widened to the FP16 carrier of the tensor-core product and a
+ *               status word; contents on entry are ignored
+ * Exactness: QK^T is computed from the codes with products and sums that are
+ * exact integers; P, PV and the output follow the arithmetic above, with the
+ * inner PV sum in the tensor core's FP32 order and exp2 by the hardware
+ * approximation.
+ */
+int sattn_forward(const sattn_shape *shape, const int8_t *q_codes, const float *q_scales,
+                  const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
+                  const float *v_scales, void *out, void *workspace, void *stream);
+
+/*
+ * sattn_check_status -- synchronise `stream` and read the status word that
+ * sattn_forward left in `forward_workspace`.  Returns SATTN_OK, or
+ * SATTN_ERR_TIMEOUT if a bounded device wait ran out, or SATTN_ERR_DEVICE if
+ * the synchronisation itself failed.  Blocks the calling host thread.
+ */
+int sattn_check_status(const void *forward_workspace, void *stream);
+
+/*
+ * sattn_attention_host -- the whole path from host buffers: copies q, k, v
+ * from host memory to the device, runs sattn_prepare and sattn_forward, and
+ * copies the BF16 output back to host memory, all enqueued on `stream`.
+ *   q_host, k_host, v_host   in:  BF16 host arrays (pinned memory lets the
+ *                                 copies run asynchronously)
+ *   out_host                 out: BF16 host array, valid after the stream
+ *                                 has been synchronised
+ *   arena                    device scratch of sizes.arena bytes (holds the
+ *                            inputs, codes, scales, workspaces and output)
+ */
+int sattn_attention_host(const sattn_shape *shape, const void *q_host, const void *k_host,
+                         const void *v_host, void *out_host, void *arena, size_t arena_bytes,
+                         void *stream);
+
+/* A static, human-readable name for a status code. */
+const char *sattn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SATTN_H */

@@ -1,0 +1,12 @@
+"""GB300-native quantized exact attention with K smoothing.
+
+The computation lives in libsattn.so (hand-written sm_103a CUDA kernels behind
+the C ABI of include/sattn.h); this package is its Python binding.
+"""
+from ._binding import (HEAD_DIM, QBLOCK, KV_TILE, STATUS, SattnError, attention, attention_host,
+                       check_status, declared_functions, forward, library_path, load_library,
+                       make_shape, prepare, prepare_buffers, query_sizes, sattn_shape, sattn_sizes)
+
+__all__ = ["HEAD_DIM", "QBLOCK", "KV_TILE", "STATUS", "SattnError", "attention", "attention_host",
+           "check_status", "declared_functions", "forward", "library_path", "load_library",
+           "make_shape", "prepare", "prepare_buffers", "query_sizes", "sattn_shape", "sattn_sizes"]

@@ -1,0 +1,223 @@
+"""ctypes binding of libsattn.so: the same entry points as include/sattn.h.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI.  PyTorch supplies device memory and streams.  There
+is no CPU fallback; if the library cannot be built or loaded, or a tensor is
+not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+from . import build as _build
+
+HEAD_DIM = 128
+QBLOCK = 32
+KV_TILE = 128
+
+_SIZE_FIELDS = ["q", "k", "v", "q_codes", "q_scales", "k_codes", "k_scales", "k_mean", "v_codes",
+                "v_scales", "out", "prepare_workspace", "forward_workspace", "arena"]
+
+
+class sattn_shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("Nq", ctypes.c_int32), ("Nkv", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("causal", ctypes.c_int32), ("sm_scale", ctypes.c_float)]
+
+
+class sattn_sizes(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in _SIZE_FIELDS]
+
+
+STATUS = {0: "SATTN_OK", 1: "SATTN_ERR_INVALID", 2: "SATTN_ERR_MISALIGNED", 3: "SATTN_ERR_DEVICE",
+          4: "SATTN_ERR_LAUNCH", 5: "SATTN_ERR_TIMEOUT"}
+
+
+class SattnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({_lib_status_string(code)})")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(build: bool = True):
+    """Load libsattn.so, building it first (nvcc) when missing or stale."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.build() if build else _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"libsattn.so not found at {path}; build it with "
+                           "quantized_exact_attention_smoothing_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    SP = ctypes.POINTER(sattn_shape)
+    lib.sattn_query_sizes.argtypes = [SP, ctypes.POINTER(sattn_sizes)]
+    lib.sattn_prepare.argtypes = [SP] + [P] * 12
+    lib.sattn_forward.argtypes = [SP] + [P] * 9
+    lib.sattn_check_status.argtypes = [P, P]
+    lib.sattn_attention_host.argtypes = [SP, P, P, P, P, P, ctypes.c_size_t, P]
+    lib.sattn_status_string.argtypes = [ctypes.c_int]
+    lib.sattn_status_string.restype = ctypes.c_char_p
+    for name in ("sattn_query_sizes", "sattn_prepare", "sattn_forward", "sattn_check_status",
+                 "sattn_attention_host"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _lib_status_string(code: int) -> str:
+    try:
+        return load_library(build=False).sattn_status_string(code).decode()
+    except Exception:  # the message is best effort; the code is in the exception
+        return "?"
+
+
+def declared_functions(header: str | None = None) -> list[str]:
+    """Names of the functions include/sattn.h declares."""
+    header = header or os.path.join(_build.ROOT, "include", "sattn.h")
+    with open(header) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(sattn_\w+)\s*\(", text, re.M)))
+
+
+def make_shape(B, Hq, Hkv, Nq, Nkv, causal=False, sm_scale=0.0) -> sattn_shape:
+    return sattn_shape(B, Hq, Hkv, Nq, Nkv, HEAD_DIM, int(bool(causal)), float(sm_scale))
+
+
+def query_sizes(shape: sattn_shape) -> dict:
+    z = sattn_sizes()
+    rc = load_library().sattn_query_sizes(ctypes.byref(shape), ctypes.byref(z))
+    if rc != 0:
+        raise SattnError(rc, "sattn_query_sizes")
+    return {n: getattr(z, n) for n in _SIZE_FIELDS}
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need_cuda(*ts: torch.Tensor):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("libsattn runs on CUDA tensors only (no CPU path)")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def _empty(nbytes: int, device, dtype=torch.uint8) -> torch.Tensor:
+    n = max(1, nbytes // torch.empty(0, dtype=dtype).element_size())
+    return torch.empty(n, dtype=dtype, device=device)
+
+
+def prepare_buffers(shape: sattn_shape, device) -> dict:
+    """Device buffers for sattn_prepare's outputs, shaped as documented."""
+    B, Hq, Hkv, Nq, Nkv = shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.Nkv
+    nq32 = -(-Nq // QBLOCK) * QBLOCK
+    nk32 = -(-Nkv // QBLOCK) * QBLOCK
+    nk128 = -(-Nkv // KV_TILE) * KV_TILE
+    z = query_sizes(shape)
+    return dict(
+        q_codes=torch.empty((B, Hq, nq32, HEAD_DIM), dtype=torch.int8, device=device),
+        q_scales=torch.empty((B, Hq, nq32 // QBLOCK), dtype=torch.float32, device=device),
+        k_codes=torch.empty((B, Hkv, nk32, HEAD_DIM), dtype=torch.int8, device=device),
+        k_scales=torch.empty((B, Hkv, nk32 // QBLOCK), dtype=torch.float32, device=device),
+        k_mean=torch.empty((B, Hkv, HEAD_DIM), dtype=torch.float32, device=device),
+        v_codes=torch.empty((B, Hkv, HEAD_DIM, nk128), dtype=torch.uint8, device=device),
+        v_scales=torch.empty((B, Hkv, HEAD_DIM), dtype=torch.float32, device=device),
+        workspace=_empty(z["prepare_workspace"], device),
+    )
+
+
+def prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+            sm_scale: float = 0.0, buffers: dict | None = None, stream=None) -> dict:
+    """sattn_prepare on BF16 device tensors q [B,Hq,Nq,128], k/v [B,Hkv,Nkv,128]."""
+    _need_cuda(q, k, v)
+    B, Hq, Nq, _ = q.shape
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    shape = make_shape(B, Hq, Hkv, Nq, Nkv, causal, sm_scale)
+    buf = buffers if buffers is not None else prepare_buffers(shape, q.device)
+    rc = load_library().sattn_prepare(
+        ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(buf["q_codes"]), _ptr(buf["q_scales"]),
+        _ptr(buf["k_codes"]), _ptr(buf["k_scales"]), _ptr(buf["k_mean"]), _ptr(buf["v_codes"]),
+        _ptr(buf["v_scales"]), _ptr(buf["workspace"]), _stream(stream))
+    if rc != 0:
+        raise SattnError(rc, "sattn_prepare")
+    buf["shape"] = shape
+    return buf
+
+
+def forward(prep: dict, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+            stream=None) -> torch.Tensor:
+    """sattn_forward on the buffers returned by prepare(); returns BF16 [B,Hq,Nq,128]."""
+    shape = prep["shape"]
+    dev = prep["q_codes"].device
+    if out is None:
+        out = torch.empty((shape.B, shape.Hq, shape.Nq, HEAD_DIM), dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        workspace = prep.get("forward_workspace")
+        if workspace is None:
+            workspace = _empty(query_sizes(shape)["forward_workspace"], dev)
+            prep["forward_workspace"] = workspace
+    _need_cuda(out, workspace)
+    rc = load_library().sattn_forward(
+        ctypes.byref(shape), _ptr(prep["q_codes"]), _ptr(prep["q_scales"]), _ptr(prep["k_codes"]),
+        _ptr(prep["k_scales"]), _ptr(prep["v_codes"]), _ptr(prep["v_scales"]), _ptr(out),
+        _ptr(workspace), _stream(stream))
+    if rc != 0:
+        raise SattnError(rc, "sattn_forward")
+    return out
+
+
+def check_status(workspace: torch.Tensor, stream=None) -> int:
+    """sattn_check_status: synchronises the stream, returns the status code."""
+    return int(load_library().sattn_check_status(_ptr(workspace), _stream(stream)))
+
+
+def attention(q, k, v, causal=False, sm_scale=0.0, stream=None) -> torch.Tensor:
+    """prepare + forward on device tensors."""
+    return forward(prepare(q, k, v, causal, sm_scale, stream=stream), stream=stream)
+
+
+def attention_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal=False, sm_scale=0.0,
+                   out: torch.Tensor | None = None, arena: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """sattn_attention_host: host BF16 tensors in, host BF16 tensor out.
+
+    The copies, both passes and the copy back are enqueued on the stream; the
+    result is valid after the stream is synchronised.  Pinned host tensors
+    let the copies run asynchronously.
+    """
+    for t in (q, k, v):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("attention_host takes contiguous host tensors")
+    B, Hq, Nq, _ = q.shape
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    shape = make_shape(B, Hq, Hkv, Nq, Nkv, causal, sm_scale)
+    z = query_sizes(shape)
+    if arena is None:
+        arena = _empty(z["arena"], torch.device("cuda", torch.cuda.current_device()))
+    if out is None:
+        out = torch.empty((B, Hq, Nq, HEAD_DIM), dtype=torch.bfloat16, pin_memory=True)
+    rc = load_library().sattn_attention_host(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                             _ptr(arena), ctypes.c_size_t(arena.numel() * arena.element_size()),
+                                             _stream(stream))
+    if rc != 0:
+        raise SattnError(rc, "sattn_attention_host")
+    return out

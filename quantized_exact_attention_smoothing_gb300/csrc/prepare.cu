@@ -1,0 +1,259 @@
+// prepare.cu -- Q/K preparation, K smoothing, INT8 quantisation of Q and K,
+// FP8 E4M3 preparation of V ("Experiment Log" page, entry "Phase 0 Import And
+// Verification": the first contract stages and "FP8 V").
+//
+// Four streaming passes, all bound by HBM bandwidth:
+//   kv_chunk_stats  per (KV head, 64-token chunk): FP32 column sums of K in
+//                   ascending token order, and column max |V|
+//   kv_finalize     per KV head: chunk sums added in ascending chunk order,
+//                   mean = sum / Nkv; s_v = amax / 448
+//   quant_int8      per 32-token block: (K - mean) or Q, amax, s = amax / 127,
+//                   codes = clamp(rint(x / s), -127, 127)
+//   quant_v         per 128-token tile: E4M3(v / s_v) written channel-major
+// Every FP32 operation that decides a code is an IEEE operation in a fixed
+// order, so codes and scales are bit-exact functions of the inputs.
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+#include "sattn_internal.cuh"
+
+namespace sattn {
+namespace {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4 &a, float (&f)[8])
+{
+    f[0] = bf16_lo(a.x); f[1] = bf16_hi(a.x);
+    f[2] = bf16_lo(a.y); f[3] = bf16_hi(a.y);
+    f[4] = bf16_lo(a.z); f[5] = bf16_hi(a.z);
+    f[6] = bf16_lo(a.w); f[7] = bf16_hi(a.w);
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// Block: 16 chunks x 16 channel groups of 8 channels.  Each thread walks its
+// chunk's tokens in ascending order, one FP32 add per token and channel.
+__global__ void __launch_bounds__(256) kv_chunk_stats_kernel(const uint4 *__restrict__ k,
+                                                             const uint4 *__restrict__ v, int Nkv,
+                                                             int nchunks, float *__restrict__ ksum,
+                                                             float *__restrict__ vmax)
+{
+    const int bh = blockIdx.y;
+    const int g = threadIdx.x & 15;
+    const int chunk = blockIdx.x * 16 + (threadIdx.x >> 4);
+    if (chunk >= nchunks)
+        return;
+    const int t0 = chunk * kMeanChunk;
+    const int t1 = min(Nkv, t0 + kMeanChunk);
+    const size_t row0 = static_cast<size_t>(bh) * Nkv + t0;
+    const uint4 *kp = k + row0 * 16 + g;
+    const uint4 *vp = v + row0 * 16 + g;
+    float s[8], mx[8], f[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        s[i] = 0.0f;
+        mx[i] = 0.0f;
+    }
+#pragma unroll 8
+    for (int t = t0; t < t1; ++t) {
+        const uint4 a = ld_stream(kp);
+        const uint4 c = ld_stream(vp);
+        kp += 16;
+        vp += 16;
+        unpack8(a, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            s[i] = __fadd_rn(s[i], f[i]);
+        unpack8(c, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            mx[i] = fmaxf(mx[i], fabsf(f[i]));
+    }
+    const size_t o = (static_cast<size_t>(bh) * nchunks + chunk) * kHeadDim + g * 8;
+    reinterpret_cast<float4 *>(ksum + o)[0] = make_float4(s[0], s[1], s[2], s[3]);
+    reinterpret_cast<float4 *>(ksum + o)[1] = make_float4(s[4], s[5], s[6], s[7]);
+    reinterpret_cast<float4 *>(vmax + o)[0] = make_float4(mx[0], mx[1], mx[2], mx[3]);
+    reinterpret_cast<float4 *>(vmax + o)[1] = make_float4(mx[4], mx[5], mx[6], mx[7]);
+}
+
+// One thread per (KV head, channel): chunk sums in ascending chunk order.
+__global__ void __launch_bounds__(128) kv_finalize_kernel(const float *__restrict__ ksum,
+                                                          const float *__restrict__ vmax, int Nkv,
+                                                          int nchunks, float *__restrict__ k_mean,
+                                                          float *__restrict__ v_scales)
+{
+    const int bh = blockIdx.x, c = threadIdx.x;
+    const float *ks = ksum + static_cast<size_t>(bh) * nchunks * kHeadDim + c;
+    const float *vm = vmax + static_cast<size_t>(bh) * nchunks * kHeadDim + c;
+    float total = 0.0f, amax = 0.0f;
+#pragma unroll 8
+    for (int ch = 0; ch < nchunks; ++ch) {
+        total = __fadd_rn(total, ks[static_cast<size_t>(ch) * kHeadDim]);
+        amax = fmaxf(amax, vm[static_cast<size_t>(ch) * kHeadDim]);
+    }
+    k_mean[bh * kHeadDim + c] = __fdiv_rn(total, static_cast<float>(Nkv));
+    v_scales[bh * kHeadDim + c] = __fdiv_rn(amax, 448.0f);
+}
+
+// One CTA per 32-token block of one head; thread = (token, quarter of the channels).
+template <bool kSmooth>
+__global__ void __launch_bounds__(128) quant_int8_kernel(const uint4 *__restrict__ x, int N,
+                                                         int64_t npad, int nblk,
+                                                         const float *__restrict__ mean,
+                                                         int8_t *__restrict__ codes,
+                                                         float *__restrict__ scales)
+{
+    __shared__ float warp_max[4];
+    const int bh = blockIdx.y, blk = blockIdx.x;
+    const int r = threadIdx.x >> 2, quarter = threadIdx.x & 3;
+    const int t = blk * kQBlock + r;
+    const bool valid = t < N;
+    float val[32];
+    if (valid) {
+        const uint4 *src = x + (static_cast<size_t>(bh) * N + t) * 16 + quarter * 4;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            float f[8];
+            unpack8(ld_stream(src + w), f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                val[w * 8 + i] = f[i];
+        }
+        if (kSmooth) {
+            const float *mu = mean + bh * kHeadDim + quarter * 32;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                val[i] = __fsub_rn(val[i], mu[i]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            val[i] = 0.0f;
+    }
+    float am = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        am = fmaxf(am, fabsf(val[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    if ((threadIdx.x & 31) == 0)
+        warp_max[threadIdx.x >> 5] = am;
+    __syncthreads();
+    const float amax = fmaxf(fmaxf(warp_max[0], warp_max[1]), fmaxf(warp_max[2], warp_max[3]));
+    const float s = __fdiv_rn(amax, 127.0f);
+    uint32_t packed[8];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            int code = 0;
+            if (valid && s > 0.0f) {
+                const float q = rintf(__fdiv_rn(val[w * 4 + b], s));
+                code = static_cast<int>(fminf(fmaxf(q, -127.0f), 127.0f));
+            }
+            word |= (static_cast<uint32_t>(code) & 0xffu) << (8 * b);
+        }
+        packed[w] = word;
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(codes + (static_cast<size_t>(bh) * npad + t) * kHeadDim +
+                                           quarter * 32);
+    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    if (threadIdx.x == 0)
+        scales[static_cast<size_t>(bh) * nblk + blk] = s;
+}
+
+// One CTA per 128-token tile of one KV head: E4M3 codes staged in shared
+// memory as [channel][token] and written out channel-major.
+constexpr int kVRow = 144;   // shared row stride in bytes (16-byte multiple)
+
+__global__ void __launch_bounds__(256) quant_v_kernel(const uint4 *__restrict__ v, int Nkv,
+                                                      int64_t nk128,
+                                                      const float *__restrict__ v_scales,
+                                                      uint8_t *__restrict__ vcodes)
+{
+    __shared__ __align__(16) uint8_t tile[kHeadDim * kVRow];
+    __shared__ float sv[kHeadDim];
+    const int bh = blockIdx.y;
+    const int t0 = blockIdx.x * kKvTile;
+    if (threadIdx.x < kHeadDim)
+        sv[threadIdx.x] = v_scales[bh * kHeadDim + threadIdx.x];
+    __syncthreads();
+#pragma unroll 2
+    for (int it = 0; it < 8; ++it) {
+        const int item = threadIdx.x + it * 256;
+        const int row = item >> 4, g = item & 15;
+        const int t = t0 + row;
+        float f[8];
+        if (t < Nkv)
+            unpack8(ld_stream(v + (static_cast<size_t>(bh) * Nkv + t) * 16 + g), f);
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            const int c = g * 8 + i;
+            float y0 = 0.0f, y1 = 0.0f;
+            if (t < Nkv) {
+                if (sv[c] > 0.0f)
+                    y0 = __fdiv_rn(f[i], sv[c]);
+                if (sv[c + 1] > 0.0f)
+                    y1 = __fdiv_rn(f[i + 1], sv[c + 1]);
+            }
+            const uint32_t two = ptx::cvt_e4m3x2(y1, y0);
+            tile[c * kVRow + row] = static_cast<uint8_t>(two & 0xffu);
+            tile[(c + 1) * kVRow + row] = static_cast<uint8_t>(two >> 8);
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int idx = threadIdx.x + it * 256;
+        const int c = idx >> 3, w = idx & 7;
+        const uint4 val = *reinterpret_cast<const uint4 *>(tile + c * kVRow + w * 16);
+        *reinterpret_cast<uint4 *>(vcodes + (static_cast<size_t>(bh) * kHeadDim + c) * nk128 + t0 +
+                                   w * 16) = val;
+    }
+}
+
+}  // namespace
+
+size_t prepare_workspace_bytes(const Geometry &g)
+{
+    return 2 * static_cast<size_t>(g.B) * g.Hkv * g.nchunks * kHeadDim * sizeof(float);
+}
+
+cudaError_t launch_prepare(const Geometry &g, const void *q, const void *k, const void *v,
+                           int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
+                           float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace,
+                           cudaStream_t stream)
+{
+    const int bhk = g.B * g.Hkv, bhq = g.B * g.Hq;
+    float *ksum = static_cast<float *>(workspace);
+    float *vmax = ksum + static_cast<size_t>(bhk) * g.nchunks * kHeadDim;
+    const uint4 *q4 = static_cast<const uint4 *>(q);
+    const uint4 *k4 = static_cast<const uint4 *>(k);
+    const uint4 *v4 = static_cast<const uint4 *>(v);
+
+    kv_chunk_stats_kernel<<<dim3(static_cast<unsigned>((g.nchunks + 15) / 16), bhk), 256, 0,
+                            stream>>>(k4, v4, g.Nkv, static_cast<int>(g.nchunks), ksum, vmax);
+    kv_finalize_kernel<<<bhk, kHeadDim, 0, stream>>>(ksum, vmax, g.Nkv, static_cast<int>(g.nchunks),
+                                                     k_mean, v_scales);
+    quant_int8_kernel<true><<<dim3(static_cast<unsigned>(g.nbk), bhk), 128, 0, stream>>>(
+        k4, g.Nkv, g.nk32, static_cast<int>(g.nbk), k_mean, k_codes, k_scales);
+    quant_v_kernel<<<dim3(static_cast<unsigned>(g.nk128 / kKvTile), bhk), 256, 0, stream>>>(
+        v4, g.Nkv, g.nk128, v_scales, v_codes);
+    quant_int8_kernel<false><<<dim3(static_cast<unsigned>(g.nbq), bhq), 128, 0, stream>>>(
+        q4, g.Nq, g.nq32, static_cast<int>(g.nbq), nullptr, q_codes, q_scales);
+    return cudaGetLastError();
+}
+
+}  // namespace sattn

@@ -1,0 +1,262 @@
+// sattn_api.cu -- the extern "C" boundary of libsattn.so (declared in include/sattn.h):
+// argument validation, buffer sizes, and the stream-ordered launches.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sattn.h"
+#include "sattn_internal.cuh"
+
+namespace {
+
+using sattn::Geometry;
+
+constexpr int64_t kMaxElems = int64_t(1) << 40;   // per tensor, keeps every index in int64
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int make_geometry(const sattn_shape *s, Geometry *g)
+{
+    if (!s || !g)
+        return SATTN_ERR_INVALID;
+    if (s->D != sattn::kHeadDim || s->B < 1 || s->Hq < 1 || s->Hkv < 1 || s->Hq % s->Hkv != 0 ||
+        s->Nq < 1 || s->Nkv < 1 || (s->causal != 0 && s->causal != 1) ||
+        (s->causal && s->Nq > s->Nkv))
+        return SATTN_ERR_INVALID;
+    if (static_cast<int64_t>(s->B) * s->Hq > 65535 || static_cast<int64_t>(s->B) * s->Hkv > 65535)
+        return SATTN_ERR_INVALID;   // grid y limit of the launches
+    const int64_t nq32 = sattn::pad_up(s->Nq, sattn::kQBlock);
+    const int64_t nk128 = sattn::pad_up(s->Nkv, sattn::kKvTile);
+    if (static_cast<int64_t>(s->B) * s->Hq * nq32 * sattn::kHeadDim > kMaxElems ||
+        static_cast<int64_t>(s->B) * s->Hkv * nk128 * sattn::kHeadDim > kMaxElems)
+        return SATTN_ERR_INVALID;
+    if (s->Nq > (1 << 30) || s->Nkv > (1 << 30))
+        return SATTN_ERR_INVALID;
+    g->B = s->B;
+    g->Hq = s->Hq;
+    g->Hkv = s->Hkv;
+    g->Nq = s->Nq;
+    g->Nkv = s->Nkv;
+    g->causal = s->causal;
+    g->sm_scale = s->sm_scale;
+    g->nq32 = nq32;
+    g->nk32 = sattn::pad_up(s->Nkv, sattn::kQBlock);
+    g->nk128 = nk128;
+    g->nbq = nq32 / sattn::kQBlock;
+    g->nbk = g->nk32 / sattn::kQBlock;
+    g->nchunks = (s->Nkv + sattn::kMeanChunk - 1) / sattn::kMeanChunk;
+    return SATTN_OK;
+}
+
+size_t r16(size_t n) { return (n + 15) / 16 * 16; }
+size_t r256(size_t n) { return (n + 255) / 256 * 256; }
+
+void fill_sizes(const Geometry &g, sattn_sizes *z)
+{
+    const size_t bhq = static_cast<size_t>(g.B) * g.Hq, bhk = static_cast<size_t>(g.B) * g.Hkv;
+    const size_t D = sattn::kHeadDim;
+    z->q = r16(bhq * g.Nq * D * 2);
+    z->k = r16(bhk * g.Nkv * D * 2);
+    z->v = z->k;
+    z->q_codes = r16(bhq * g.nq32 * D);
+    z->q_scales = r16(bhq * g.nbq * 4);
+    z->k_codes = r16(bhk * g.nk32 * D);
+    z->k_scales = r16(bhk * g.nbk * 4);
+    z->k_mean = r16(bhk * D * 4);
+    z->v_codes = r16(bhk * D * g.nk128);
+    z->v_scales = r16(bhk * D * 4);
+    z->out = r16(bhq * g.Nq * D * 2);
+    z->prepare_workspace = r16(sattn::prepare_workspace_bytes(g));
+    z->forward_workspace = r16(sattn::forward_workspace_bytes(g));
+    z->arena = r256(z->q) + r256(z->k) + r256(z->v) + r256(z->q_codes) + r256(z->q_scales) +
+               r256(z->k_codes) + r256(z->k_scales) + r256(z->k_mean) + r256(z->v_codes) +
+               r256(z->v_scales) + r256(z->out) + r256(z->prepare_workspace) +
+               r256(z->forward_workspace);
+}
+
+// The current device must be compute capability 10.3; the answer is cached per device.
+int check_device()
+{
+    static int verdict[64];   // 0 unknown, 1 good, 2 bad
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return SATTN_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(mu);
+    if (verdict[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return SATTN_ERR_DEVICE;
+        verdict[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    }
+    return verdict[dev] == 1 ? SATTN_OK : SATTN_ERR_DEVICE;
+}
+
+int prepare_impl(const Geometry &g, const void *q, const void *k, const void *v, int8_t *q_codes,
+                 float *q_scales, int8_t *k_codes, float *k_scales, float *k_mean, uint8_t *v_codes,
+                 float *v_scales, void *workspace, cudaStream_t stream)
+{
+    const void *ptrs[] = {q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes, v_scales, workspace};
+    for (const void *p : ptrs) {
+        if (!p)
+            return SATTN_ERR_INVALID;
+        if (!aligned16(p))
+            return SATTN_ERR_MISALIGNED;
+    }
+    const int dev = check_device();
+    if (dev != SATTN_OK)
+        return dev;
+    return sattn::launch_prepare(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes,
+                                 v_scales, workspace, stream) == cudaSuccess
+               ? SATTN_OK
+               : SATTN_ERR_LAUNCH;
+}
+
+int forward_impl(const Geometry &g, const int8_t *q_codes, const float *q_scales,
+                 const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
+                 const float *v_scales, void *out, void *workspace, cudaStream_t stream)
+{
+    const void *ptrs[] = {q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, out, workspace};
+    for (const void *p : ptrs) {
+        if (!p)
+            return SATTN_ERR_INVALID;
+        if (!aligned16(p))
+            return SATTN_ERR_MISALIGNED;
+    }
+    const int dev = check_device();
+    if (dev != SATTN_OK)
+        return dev;
+    const int rc = sattn::launch_forward(g, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales,
+                                         out, workspace, stream);
+    if (rc == 1)
+        return SATTN_ERR_DEVICE;   // no tensor-map encoder in this driver
+    return rc == 0 ? SATTN_OK : SATTN_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sattn_query_sizes(const sattn_shape *shape, sattn_sizes *sizes)
+{
+    Geometry g;
+    const int rc = make_geometry(shape, &g);
+    if (rc != SATTN_OK)
+        return rc;
+    if (!sizes)
+        return SATTN_ERR_INVALID;
+    fill_sizes(g, sizes);
+    return SATTN_OK;
+}
+
+int sattn_prepare(const sattn_shape *shape, const void *q, const void *k, const void *v,
+                  int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
+                  float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace, void *stream)
+{
+    Geometry g;
+    const int rc = make_geometry(shape, &g);
+    if (rc != SATTN_OK)
+        return rc;
+    return prepare_impl(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes, v_scales,
+                        workspace, static_cast<cudaStream_t>(stream));
+}
+
+int sattn_forward(const sattn_shape *shape, const int8_t *q_codes, const float *q_scales,
+                  const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
+                  const float *v_scales, void *out, void *workspace, void *stream)
+{
+    Geometry g;
+    const int rc = make_geometry(shape, &g);
+    if (rc != SATTN_OK)
+        return rc;
+    return forward_impl(g, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, out, workspace,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int sattn_check_status(const void *forward_workspace, void *stream)
+{
+    if (!forward_workspace)
+        return SATTN_ERR_INVALID;
+    if (!aligned16(forward_workspace))
+        return SATTN_ERR_MISALIGNED;
+    uint32_t words[2] = {0, 0};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return SATTN_ERR_DEVICE;
+    if (cudaMemcpy(words, forward_workspace, sizeof words, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SATTN_ERR_DEVICE;
+    return words[0] != 0 ? SATTN_ERR_TIMEOUT : SATTN_OK;
+}
+
+int sattn_attention_host(const sattn_shape *shape, const void *q_host, const void *k_host,
+                         const void *v_host, void *out_host, void *arena, size_t arena_bytes,
+                         void *stream)
+{
+    Geometry g;
+    int rc = make_geometry(shape, &g);
+    if (rc != SATTN_OK)
+        return rc;
+    if (!q_host || !k_host || !v_host || !out_host || !arena)
+        return SATTN_ERR_INVALID;
+    if (!aligned16(arena))
+        return SATTN_ERR_MISALIGNED;
+    sattn_sizes z;
+    fill_sizes(g, &z);
+    if (arena_bytes < z.arena)
+        return SATTN_ERR_INVALID;
+    rc = check_device();
+    if (rc != SATTN_OK)
+        return rc;
+    char *p = static_cast<char *>(arena);
+    auto take = [&p](size_t n) {
+        char *r = p;
+        p += r256(n);
+        return r;
+    };
+    void *q = take(z.q), *k = take(z.k), *v = take(z.v);
+    int8_t *q_codes = reinterpret_cast<int8_t *>(take(z.q_codes));
+    float *q_scales = reinterpret_cast<float *>(take(z.q_scales));
+    int8_t *k_codes = reinterpret_cast<int8_t *>(take(z.k_codes));
+    float *k_scales = reinterpret_cast<float *>(take(z.k_scales));
+    float *k_mean = reinterpret_cast<float *>(take(z.k_mean));
+    uint8_t *v_codes = reinterpret_cast<uint8_t *>(take(z.v_codes));
+    float *v_scales = reinterpret_cast<float *>(take(z.v_scales));
+    void *out = take(z.out);
+    void *pws = take(z.prepare_workspace);
+    void *fws = take(z.forward_workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t qb = static_cast<size_t>(g.B) * g.Hq * g.Nq * sattn::kHeadDim * 2;
+    const size_t kb = static_cast<size_t>(g.B) * g.Hkv * g.Nkv * sattn::kHeadDim * 2;
+    if (cudaMemcpyAsync(q, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(k, k_host, kb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(v, v_host, kb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return SATTN_ERR_LAUNCH;
+    rc = prepare_impl(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes, v_scales,
+                      pws, s);
+    if (rc != SATTN_OK)
+        return rc;
+    rc = forward_impl(g, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, out, fws, s);
+    if (rc != SATTN_OK)
+        return rc;
+    if (cudaMemcpyAsync(out_host, out, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SATTN_ERR_LAUNCH;
+    return SATTN_OK;
+}
+
+const char *sattn_status_string(int status)
+{
+    switch (status) {
+    case SATTN_OK: return "ok";
+    case SATTN_ERR_INVALID: return "invalid argument";
+    case SATTN_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case SATTN_ERR_DEVICE: return "unsupported device or CUDA runtime failure";
+    case SATTN_ERR_LAUNCH: return "kernel launch failed";
+    case SATTN_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

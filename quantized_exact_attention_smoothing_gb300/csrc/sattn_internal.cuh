@@ -1,0 +1,44 @@
+// sattn_internal.cuh -- shared declarations of the libsattn kernels and launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sattn {
+
+constexpr int kHeadDim = 128;
+constexpr int kQBlock = 32;      // tokens per INT8 quantisation block
+constexpr int kMeanChunk = 64;   // tokens per K-mean partial sum
+constexpr int kKvTile = 128;     // keys per KV tile of the forward pass
+constexpr int kQTile = 128;      // query rows per CTA of the forward pass
+
+inline int64_t pad_up(int64_t n, int64_t m) { return (n + m - 1) / m * m; }
+
+// Geometry shared by the host code of prepare and forward.
+struct Geometry {
+    int B, Hq, Hkv, Nq, Nkv, causal;
+    float sm_scale;
+    int64_t nq32, nk32, nk128;     // padded token counts
+    int64_t nbq, nbk;              // INT8 blocks per head
+    int64_t nchunks;               // K-mean chunks per KV head
+};
+
+// ---- prepare (prepare.cu) ----
+// Workspace: [B*Hkv][nchunks][128] FP32 K column sums, then the same for V max |v|.
+size_t prepare_workspace_bytes(const Geometry &g);
+cudaError_t launch_prepare(const Geometry &g, const void *q, const void *k, const void *v,
+                           int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
+                           float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace,
+                           cudaStream_t stream);
+
+// ---- forward (attn_fwd.cu) ----
+// Workspace: 256-byte status block, then the FP16 carrier of the K codes [B*Hkv][Nkv][128].
+constexpr size_t kStatusBytes = 256;
+size_t forward_workspace_bytes(const Geometry &g);
+// Returns 0 on success, 1 if a tensor map could not be encoded, or a CUDA error.
+int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scales,
+                   const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
+                   const float *v_scales, void *out, void *workspace, cudaStream_t stream);
+
+}  // namespace sattn

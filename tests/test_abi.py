@@ -1,0 +1,78 @@
+"""The C-ABI library builds, loads and exports every symbol include/sattn.h
+declares; host-side argument checks answer without touching a GPU."""
+import ctypes
+
+import pytest
+
+import quantized_exact_attention_smoothing_gb300 as sattn
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return sattn.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = sattn.declared_functions()
+    assert set(names) >= {"sattn_query_sizes", "sattn_prepare", "sattn_forward",
+                          "sattn_check_status", "sattn_attention_host", "sattn_status_string"}
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_query_sizes_headline_shape():
+    z = sattn.query_sizes(sattn.make_shape(4, 32, 8, 8192, 8192, True))
+    assert z["q"] == 4 * 32 * 8192 * 128 * 2
+    assert z["q_codes"] == 4 * 32 * 8192 * 128
+    assert z["v_codes"] == 4 * 8 * 128 * 8192
+    assert z["q_scales"] == 4 * 32 * 256 * 4
+    assert z["forward_workspace"] == 256 + 4 * 8 * 8192 * 128 * 2
+    assert all(v % 16 == 0 for v in z.values())
+
+
+def test_query_sizes_ragged_padding():
+    z = sattn.query_sizes(sattn.make_shape(1, 2, 1, 33, 129, False))
+    assert z["q_codes"] == 2 * 64 * 128                    # 33 -> 64 (32-token blocks)
+    assert z["k_codes"] == 160 * 128                       # 129 -> 160
+    assert z["v_codes"] == 128 * 256                       # 129 -> 256 keys (128-key tiles)
+
+
+@pytest.mark.parametrize("args", [
+    (1, 3, 2, 8, 8, False),          # Hq % Hkv != 0
+    (1, 1, 1, 0, 8, False),          # Nq < 1
+    (1, 1, 1, 8, 0, False),          # Nkv < 1
+    (1, 1, 1, 9, 8, True),           # causal with Nq > Nkv
+    (0, 1, 1, 8, 8, False),          # B < 1
+])
+def test_invalid_shapes_rejected(args):
+    with pytest.raises(sattn.SattnError) as e:
+        sattn.query_sizes(sattn.make_shape(*args))
+    assert e.value.code == 1
+
+
+def test_head_dim_other_than_128_rejected(lib):
+    s = sattn.make_shape(1, 1, 1, 8, 8)
+    s.D = 64
+    z = sattn.sattn_sizes()
+    assert lib.sattn_query_sizes(ctypes.byref(s), ctypes.byref(z)) == 1
+
+
+def test_null_and_misaligned_pointers_rejected_before_any_device_work(lib):
+    s = sattn.make_shape(1, 1, 1, 8, 8)
+    good = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(11)]
+    args = list(good)
+    args[3] = None
+    assert lib.sattn_prepare(ctypes.byref(s), *args, None) == 1
+    args = list(good)
+    args[5] = ctypes.c_void_p(0x1008)
+    assert lib.sattn_prepare(ctypes.byref(s), *args, None) == 2
+    fwd = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(8)]
+    fwd[6] = ctypes.c_void_p(0x2004)
+    assert lib.sattn_forward(ctypes.byref(s), *fwd, None) == 2
+    assert lib.sattn_check_status(None, None) == 1
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.sattn_status_string(code)
+    assert lib.sattn_status_string(99) == b"unknown status"
