@@ -73,8 +73,10 @@ typedef enum {
                                   or a CUDA runtime query failed */
     SATTN_ERR_LAUNCH = 4,      /* a kernel launch failed (cudaGetLastError);
                                   earlier kernels of the call may have run */
-    SATTN_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out; the
+    SATTN_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out; the
                                   outputs of that call are undefined */
+    SATTN_ERR_SCRATCH_LIMIT = 6 /* the shape needs more scratch than the fixed
+                                  array of sattn_prepare_noalloc holds */
 } sattn_status;
 
 /* Problem shape.  Q is [B][Hq][Nq][D], K and V are [B][Hkv][Nkv][D]. */
@@ -168,6 +170,39 @@ int sattn_check_status(const void *forward_workspace, void *stream);
 int sattn_attention_host(const sattn_shape *shape, const void *q_host, const void *k_host,
                          const void *v_host, void *out_host, void *arena, size_t arena_bytes,
                          void *stream);
+
+/*
+ * sattn_prepare_noalloc -- sattn_prepare without a workspace argument.  The
+ * page has no counterpart to this entry point; it exists for callers that
+ * cannot hand the library scratch memory: programs whose device memory is
+ * owned by an allocator they do not expose, callers that may not call
+ * cudaMalloc because it synchronises the whole device, and plain C callers
+ * with no device allocator of their own.  The caller still provides every
+ * input and output buffer, exactly as for sattn_prepare, and receives the
+ * same codes and scales bit for bit.
+ *
+ * Scratch: a fixed array of SATTN_NOALLOC_SCRATCH_BYTES (8 MiB) in the
+ * library's device memory, which every GPU that loads the library holds until
+ * the process exits.  The shape must need at most that much:
+ * B * Hkv * ceil(Nkv / 64) <= 8192 (for example B4 Hkv8 Nkv8192 needs 4096,
+ * B1 Hkv16 Nkv32760 needs 8192); larger shapes return
+ * SATTN_ERR_SCRATCH_LIMIT before anything is enqueued.  Nothing in the
+ * array needs to start at zero: each call writes every scratch element it
+ * reads.  The array keeps the last call's contents.
+ *
+ * Set-up: the first call on each device (with that device current) looks up
+ * the array's device address once (cudaGetSymbolAddress) and caches it; make
+ * that first call before any stream capture begins on that device.
+ *
+ * Concurrency: all calls on one device share the one array, so calls whose
+ * kernels may overlap on the GPU (different streams without ordering between
+ * them) race on it; order them on one stream or with events.
+ * The function never calls cudaMalloc, cudaFree or any allocating routine.
+ */
+#define SATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
+int sattn_prepare_noalloc(const sattn_shape *shape, const void *q, const void *k, const void *v,
+                          int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
+                          float *k_mean, uint8_t *v_codes, float *v_scales, void *stream);
 
 /* A static, human-readable name for a status code. */
 const char *sattn_status_string(int status);

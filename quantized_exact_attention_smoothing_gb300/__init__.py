@@ -5,8 +5,10 @@ the C ABI of include/sattn.h); this package is its Python binding.
 """
 from ._binding import (HEAD_DIM, QBLOCK, KV_TILE, STATUS, SattnError, attention, attention_host,
                        check_status, declared_functions, forward, library_path, load_library,
-                       make_shape, prepare, prepare_buffers, query_sizes, sattn_shape, sattn_sizes)
+                       make_shape, prepare, prepare_buffers, prepare_noalloc, query_sizes, sattn_shape,
+                       sattn_sizes, NOALLOC_SCRATCH_BYTES)
 
 __all__ = ["HEAD_DIM", "QBLOCK", "KV_TILE", "STATUS", "SattnError", "attention", "attention_host",
            "check_status", "declared_functions", "forward", "library_path", "load_library",
-           "make_shape", "prepare", "prepare_buffers", "query_sizes", "sattn_shape", "sattn_sizes"]
+           "make_shape", "prepare", "prepare_buffers", "prepare_noalloc", "query_sizes", "sattn_shape",
+           "sattn_sizes", "NOALLOC_SCRATCH_BYTES"]

@@ -34,7 +34,10 @@ class sattn_sizes(ctypes.Structure):
 
 
 STATUS = {0: "SATTN_OK", 1: "SATTN_ERR_INVALID", 2: "SATTN_ERR_MISALIGNED", 3: "SATTN_ERR_DEVICE",
-          4: "SATTN_ERR_LAUNCH", 5: "SATTN_ERR_TIMEOUT"}
+          4: "SATTN_ERR_LAUNCH", 5: "SATTN_ERR_TIMEOUT", 6: "SATTN_ERR_SCRATCH_LIMIT"}
+
+# Scratch held by sattn_prepare_noalloc (a fixed array in the library's device memory).
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class SattnError(RuntimeError):
@@ -65,12 +68,13 @@ def load_library(build: bool = True):
     lib.sattn_query_sizes.argtypes = [SP, ctypes.POINTER(sattn_sizes)]
     lib.sattn_prepare.argtypes = [SP] + [P] * 12
     lib.sattn_forward.argtypes = [SP] + [P] * 9
+    lib.sattn_prepare_noalloc.argtypes = [SP] + [P] * 11
     lib.sattn_check_status.argtypes = [P, P]
     lib.sattn_attention_host.argtypes = [SP, P, P, P, P, P, ctypes.c_size_t, P]
     lib.sattn_status_string.argtypes = [ctypes.c_int]
     lib.sattn_status_string.restype = ctypes.c_char_p
     for name in ("sattn_query_sizes", "sattn_prepare", "sattn_forward", "sattn_check_status",
-                 "sattn_attention_host"):
+                 "sattn_attention_host", "sattn_prepare_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -159,6 +163,34 @@ def prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fa
         _ptr(buf["v_scales"]), _ptr(buf["workspace"]), _stream(stream))
     if rc != 0:
         raise SattnError(rc, "sattn_prepare")
+    buf["shape"] = shape
+    return buf
+
+
+def prepare_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                    sm_scale: float = 0.0, buffers: dict | None = None, stream=None) -> dict:
+    """sattn_prepare_noalloc: as prepare(), without a workspace.
+
+    For callers that cannot give the library scratch memory (their device
+    memory belongs to an allocator they do not expose, or they may not call
+    cudaMalloc because it synchronises the device).  The library keeps the
+    scratch in a fixed 8 MiB array of its own device memory, shared by every
+    call on a device: calls that may overlap on the GPU race on it.  Shapes
+    with B * Hkv * ceil(Nkv / 64) > 8192 raise SattnError
+    (SATTN_ERR_SCRATCH_LIMIT).  The output buffers (``buffers``) are still
+    the caller's; without them this wrapper allocates them with PyTorch.
+    """
+    _need_cuda(q, k, v)
+    B, Hq, Nq, _ = q.shape
+    Hkv, Nkv = k.shape[1], k.shape[2]
+    shape = make_shape(B, Hq, Hkv, Nq, Nkv, causal, sm_scale)
+    buf = buffers if buffers is not None else prepare_buffers(shape, q.device)
+    rc = load_library().sattn_prepare_noalloc(
+        ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(buf["q_codes"]), _ptr(buf["q_scales"]),
+        _ptr(buf["k_codes"]), _ptr(buf["k_scales"]), _ptr(buf["k_mean"]), _ptr(buf["v_codes"]),
+        _ptr(buf["v_scales"]), _stream(stream))
+    if rc != 0:
+        raise SattnError(rc, "sattn_prepare_noalloc")
     buf["shape"] = shape
     return buf
 

@@ -255,8 +255,72 @@ const char *sattn_status_string(int status)
     case SATTN_ERR_DEVICE: return "unsupported device or CUDA runtime failure";
     case SATTN_ERR_LAUNCH: return "kernel launch failed";
     case SATTN_ERR_TIMEOUT: return "device wait timed out";
+    case SATTN_ERR_SCRATCH_LIMIT: return "shape needs more than the fixed no-alloc scratch array";
     default: return "unknown status";
     }
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// sattn_prepare_noalloc: the preparation pass with its scratch (per-chunk K
+// column sums and V column maxima) in a fixed array of this library's device
+// memory instead of a caller-provided workspace.  Declared in sattn.h.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_prepare_scratch[SATTN_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_prepare_scratch on the current device, looked up once per
+// device.  In host code the array's name is only a host-side handle; the
+// kernels must be given this address.
+int prepare_scratch_address(void **out)
+{
+    static void *addr[64];
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return SATTN_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_prepare_scratch) != cudaSuccess || !p)
+            return SATTN_ERR_DEVICE;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return SATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int sattn_prepare_noalloc(const sattn_shape *shape, const void *q, const void *k,
+                                     const void *v, int8_t *q_codes, float *q_scales,
+                                     int8_t *k_codes, float *k_scales, float *k_mean,
+                                     uint8_t *v_codes, float *v_scales, void *stream)
+{
+    Geometry g;
+    int rc = make_geometry(shape, &g);
+    if (rc != SATTN_OK)
+        return rc;
+    const void *ptrs[] = {q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes, v_scales};
+    for (const void *p : ptrs) {
+        if (!p)
+            return SATTN_ERR_INVALID;
+        if (!aligned16(p))
+            return SATTN_ERR_MISALIGNED;
+    }
+    if (sattn::prepare_workspace_bytes(g) > SATTN_NOALLOC_SCRATCH_BYTES)
+        return SATTN_ERR_SCRATCH_LIMIT;
+    rc = check_device();
+    if (rc != SATTN_OK)
+        return rc;
+    void *scratch = nullptr;
+    rc = prepare_scratch_address(&scratch);
+    if (rc != SATTN_OK)
+        return rc;
+    return sattn::launch_prepare(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes,
+                                 v_scales, scratch, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SATTN_OK
+               : SATTN_ERR_LAUNCH;
+}
