@@ -30,7 +30,7 @@
  *             code = E4M3(v / s_v[c]) round-to-nearest-even, saturating.
  *   score     s2 = float(acc) * ((s_q * s_k) * c0), acc = exact int32 dot
  *             product of the codes, c0 = sm_scale * log2(e) (FP32).
- *   softmax   per KV tile of 128 keys, ascending: m' = max(m, max s2),
+ *   softmax   per KV tile of 256 keys, ascending: m' = max(m, max s2),
  *             alpha = exp2(m - m') (0 while m = -inf),
  *             p8 = E4M3(exp2(s2 - m') * 448);
  *             RO = RO * alpha + sum_j p8_j * v8_j,  d = d * alpha + sum_j p8_j.
@@ -62,7 +62,9 @@ extern "C" {
 
 #define SATTN_HEAD_DIM 128   /* the only supported head dimension */
 #define SATTN_QBLOCK 32      /* tokens per INT8 quantisation block */
-#define SATTN_KV_TILE 128    /* keys per KV tile of the forward pass */
+#define SATTN_KV_TILE 256    /* keys per KV tile of the forward pass; the tiling is
+                                part of the result (P8 is relative to the running
+                                max at each tile) */
 
 typedef enum {
     SATTN_OK = 0,

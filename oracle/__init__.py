@@ -157,7 +157,7 @@ def prepare(q: np.ndarray, k: np.ndarray, v: np.ndarray, smooth: bool = True) ->
 
 # --- forward ----------------------------------------------------------------
 
-def forward(prep: dict, Nq: int, Nkv: int, causal: bool, sm_scale: float = 0.0, tile: int = 128,
+def forward(prep: dict, Nq: int, Nkv: int, causal: bool, sm_scale: float = 0.0, tile: int = 256,
             rows: np.ndarray | None = None, nthreads: int = 0):
     """Quantised attention.  Returns (out_bf16_bits, out_f32).
 
@@ -186,7 +186,7 @@ def forward(prep: dict, Nq: int, Nkv: int, causal: bool, sm_scale: float = 0.0, 
 
 
 def forward_exact(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool, smooth: bool,
-                  sm_scale: float = 0.0, tile: int = 128) -> np.ndarray:
+                  sm_scale: float = 0.0, tile: int = 256) -> np.ndarray:
     """The same tiled recurrence in FP64 with every quantiser bypassed."""
     lib = _load()
     q = np.ascontiguousarray(q, dtype=np.float64)

@@ -17,7 +17,8 @@ from . import build as _build
 
 HEAD_DIM = 128
 QBLOCK = 32
-KV_TILE = 128
+KV_TILE = 256      # keys per KV tile of the forward pass (part of the numerical contract)
+V_PAD = 128        # V codes are padded to a multiple of 128 keys
 
 _SIZE_FIELDS = ["q", "k", "v", "q_codes", "q_scales", "k_codes", "k_scales", "k_mean", "v_codes",
                 "v_scales", "out", "prepare_workspace", "forward_workspace", "arena"]
@@ -135,7 +136,7 @@ def prepare_buffers(shape: sattn_shape, device) -> dict:
     B, Hq, Hkv, Nq, Nkv = shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.Nkv
     nq32 = -(-Nq // QBLOCK) * QBLOCK
     nk32 = -(-Nkv // QBLOCK) * QBLOCK
-    nk128 = -(-Nkv // KV_TILE) * KV_TILE
+    nk128 = -(-Nkv // V_PAD) * V_PAD
     z = query_sizes(shape)
     return dict(
         q_codes=torch.empty((B, Hq, nq32, HEAD_DIM), dtype=torch.int8, device=device),

@@ -5,23 +5,27 @@
 // per-tile RO rescaling, two-level PV accumulation, final conversion).
 //
 // One CTA computes 128 query rows of one (batch, query head) and visits the
-// KV tiles of 128 keys in increasing order.  Ten warps, each with one job
-// (the state-ownership split of the page's "paired owners" design, mapped
-// onto tensor memory):
-//   warp 0      TMA producer: K tiles (FP16 carrier of the INT8 codes) and V
-//               tiles (E4M3, channel-major) into two mbarrier rings
-//   warp 1      TMEM allocation and the single MMA-issuing thread:
-//                 S_j  = Q * K_j^T   tcgen05 kind::f16, A = Q from TMEM
-//                 PV_j = P_j * V_j   tcgen05 kind::f8f6f4, A = P from TMEM,
-//                                    N = 144: V rows plus a row of ones whose
-//                                    column gives sum_j p8_j
-//   warps 2-5   softmax owners (thread = query row = TMEM lane): score
-//               scaling, masks, running max m, alpha, FP8 P written back into
-//               TMEM over the S buffer
-//   warps 6-9   PV / RO owners (thread = query row): RO = RO * alpha + PV_j,
-//               d = d * alpha + sum p8, then the final conversion
-// Tensor memory (512 columns): S/P double buffer [0,256), PV partial
-// [256,400), Q carrier [416,480).
+// KV tiles of 256 keys in increasing order.  Twelve warps:
+//   warps 0-7   two compute warpgroups, thread = query row = TMEM lane; half h
+//               owns keys [128h, 128h + 128) of every tile and output channels
+//               [64h, 64h + 64): score scaling, masks, running max m (exchanged
+//               between the halves), alpha, the FP8 P bytes (written to shared
+//               memory), then RO = RO * alpha + PV and d = d * alpha + sum p8
+//               for the previous tile, and the final conversion
+//   warp 8      TMA producer: K tiles (FP16 carrier of the INT8 codes) and V
+//               half-tiles (E4M3, channel-major) into mbarrier rings
+//   warp 9      TMEM allocation and the single MMA-issuing thread:
+//                 S_j  = Q * K_j^T   tcgen05 kind::f16, A = Q from TMEM, N = 256
+//                 PV_j = P_j * V_j   tcgen05 kind::f8f6f4, A = P from shared
+//                                    memory, N = 144: V rows plus a row of ones
+//                                    whose column gives sum_j p8_j
+//   warps 10-11 idle
+// Twelve warps launch at 168 registers each; setmaxnreg then gives the compute
+// warpgroups 232 (128 scores and 64 RO values per thread) and the
+// producer/MMA warpgroup 40.
+// Tensor memory (512 columns): S [0,256), PV partial [256,400), Q carrier
+// [448,512).  A tcgen05.mma instruction costs about the same time for any N up
+// to 256 on this part, hence the 256-key tiles: QK runs at N = 256.
 //
 // Exactness of QK: INT8 codes are carried as FP16 values (integers of
 // magnitude <= 127 are exact in FP16); every product is an integer <= 16129 and
@@ -30,7 +34,8 @@
 //
 // Every mbarrier wait is bounded: after about a second, or as soon as another
 // CTA has reported a failure, the thread records the failure in the status
-// word, stops, waits for its own copies in flight, and the CTA frees its TMEM.
+// word, stops, waits for its own copies and MMAs in flight, and the CTA frees
+// its TMEM.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -45,51 +50,63 @@
 namespace sattn {
 namespace {
 
-constexpr int BM = kQTile, BN = kKvTile, HD = kHeadDim;
-constexpr int KSTAGES = 3, VSTAGES = 3;
-constexpr uint32_t K_HALF_BYTES = BN * 64 * 2;          // 128 keys x 64 channels, FP16
-constexpr uint32_t K_STAGE_BYTES = 2 * K_HALF_BYTES;    // 32 KB
+constexpr int BM = kQTile, BN = kKvTile, HD = kHeadDim;   // 128 rows x 256 keys
+constexpr int KSTAGES = 2, VSLOTS = 3;
+constexpr uint32_t K_HALF_BYTES = BN * 64 * 2;          // 256 keys x 64 channels, FP16
+constexpr uint32_t K_STAGE_BYTES = 2 * K_HALF_BYTES;    // 64 KB
 constexpr uint32_t PV_N = 144;                          // V rows + ones row + zero rows
-constexpr uint32_t V_STAGE_BYTES = PV_N * BN;           // 18 KB
-constexpr uint32_t V_TMA_BYTES = HD * BN;               // 16 KB loaded per tile
+constexpr uint32_t V_SLOT_BYTES = PV_N * 128;           // one 128-key half tile, 18 KB
+constexpr uint32_t V_TMA_BYTES = HD * 128;              // 16 KB loaded per half tile
+constexpr uint32_t P_HALF_BYTES = BM * 128;             // 128 rows x 128 keys, E4M3
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_S = 0;
 constexpr uint32_t TM_PV = 256;
-constexpr uint32_t TM_Q = 416;
-constexpr int NTHREADS = 320;
-constexpr uint32_t IDESC_QK = ptx::make_idesc(0, 0, BM, BN);     // F16 x F16 -> F32
+constexpr uint32_t TM_Q = 448;
+// warp roles: 0-7 compute (two warpgroups), 8 TMA producer, 9 MMA issuer and
+// TMEM owner, 10-11 idle
+constexpr int WARP_PRODUCER = 8, WARP_MMA = 9;
+constexpr int NTHREADS = 12 * 32;
+// Registers: launched at 168 per thread (384 x 168 = 64512), then rebalanced
+// per warpgroup; the shares add up to exactly the launch total.
+constexpr int kLaunchRegs = 168, kRegsCompute = 232, kRegsOther = 40;
+static_assert(2 * 128 * kRegsCompute + 128 * kRegsOther == NTHREADS * kLaunchRegs,
+              "register split must add up to the launch total");
+constexpr uint32_t IDESC_QK = ptx::make_idesc(0, 0, BM, BN);     // F16 x F16 -> F32, N = 256
 constexpr uint32_t IDESC_PV = ptx::make_idesc(0, 0, BM, PV_N);   // E4M3 x E4M3 -> F32
 constexpr uint64_t TIMEOUT_NS = 1000000000ull;
 
 // shared memory map, offsets from a 1024-byte aligned base
 constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_V = OFF_K + KSTAGES * K_STAGE_BYTES;
-constexpr uint32_t OFF_ALPHA = OFF_V + VSTAGES * V_STAGE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_ALPHA + 2 * BM * 4;
+constexpr uint32_t OFF_P = OFF_V + VSLOTS * V_SLOT_BYTES;
+constexpr uint32_t OFF_MAXX = OFF_P + 2 * P_HALF_BYTES;     // [tile parity][half][row] row maxima
+constexpr uint32_t OFF_BAR = OFF_MAXX + 4 * BM * 4;
 enum Bar : int {
     KFULL = 0,
     KEMPTY = KFULL + KSTAGES,
     VFULL = KEMPTY + KSTAGES,
-    VEMPTY = VFULL + VSTAGES,
-    QFULL = VEMPTY + VSTAGES,
-    SFULL = QFULL + 1,       // 2
-    PFULL = SFULL + 2,       // 2
-    PVFULL = PFULL + 2,
+    VEMPTY = VFULL + VSLOTS,
+    QFULL = VEMPTY + VSLOTS,
+    SFULL = QFULL + 1,
+    SFREE = SFULL + 1,
+    PFULL = SFREE + 1,
+    PDONE = PFULL + 1,
+    PVFULL = PDONE + 1,
     PVEMPTY = PVFULL + 1,
-    AFULL = PVEMPTY + 1,     // 2
-    AEMPTY = AFULL + 2,      // 2
-    MMADONE = AEMPTY + 2,
+    MMADONE = PVEMPTY + 1,
     NBARS = MMADONE + 1
 };
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBARS * 8;
 constexpr uint32_t OFF_FLAG = OFF_TMEM_SLOT + 4;
 constexpr uint32_t SMEM_BYTES = OFF_FLAG + 4 + 1024;   // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-static_assert(OFF_V % 1024 == 0 && V_STAGE_BYTES % 1024 == 0, "swizzle atoms must be 1024-aligned");
+static_assert(OFF_V % 1024 == 0 && V_SLOT_BYTES % 1024 == 0 && OFF_P % 1024 == 0,
+              "swizzle atoms must be 1024-aligned");
 
 // where a wait gave up (second status word)
 enum Site : uint32_t {
-    SITE_KE = 1, SITE_VE, SITE_Q, SITE_K, SITE_P, SITE_V, SITE_PVE, SITE_DONE, SITE_S, SITE_AE,
-    SITE_PV, SITE_A, SITE_DRAIN
+    SITE_KE = 1, SITE_VE, SITE_Q, SITE_K, SITE_P, SITE_V, SITE_PVE, SITE_DONE, SITE_S,
+    SITE_PV, SITE_DRAIN, SITE_SFREE, SITE_PDONE
 };
 
 struct FwdParams {
@@ -102,11 +119,26 @@ struct FwdParams {
     float c0;
 #ifdef SATTN_DEBUG_DUMP
     // intermediates of query tile 0 of (batch 0, head 0), KV tile 0:
-    // [0, 16384) raw S accumulators, [16384, 20480) packed P8 words,
-    // [20480, 20480 + 128 * 144) first PV partial (all 144 columns)
+    // [0, 32768) raw S accumulators (128 x 256), [32768, 40960) P8 words
+    // (128 x 64), [40960, 40960 + 128 * 144) first PV partial; clock stamps
+    // of one CTA from float offset 61440 (16 events x 256 tiles, 64-bit)
     float *dbg;
 #endif
 };
+
+#ifdef SATTN_DEBUG_DUMP
+// Debug builds only: SM clock stamps of one CTA (the first in launch order:
+// the last query tile, batch 0, head 0), event `id` of KV tile `j`.
+#define SATTN_TRACE(p, t, id, j)                                                                 \
+    do {                                                                                         \
+        if ((p).dbg && blockIdx.x == 0 && (t).hq == 0 && (t).b == 0 && (j) < 256)               \
+            reinterpret_cast<unsigned long long *>((p).dbg + 61440)[(id) * 256 + (j)] = clock64(); \
+    } while (0)
+#else
+#define SATTN_TRACE(p, t, id, j) \
+    do {                         \
+    } while (0)
+#endif
 
 struct Waiter {
     uint32_t *status;
@@ -133,7 +165,7 @@ struct Waiter {
         }
     }
 
-    // Wait for copies this thread issued; ignores the abort flag, still bounded.
+    // Wait for copies or MMAs this thread issued; ignores the abort flag, still bounded.
     __device__ void drain(uint32_t bar, uint32_t parity) const
     {
         const uint64_t t0 = ptx::globaltimer();
@@ -161,15 +193,16 @@ struct Tile {
     int b, hq, hk, q0, ntiles, mask_from;
 };
 
-__device__ __forceinline__ void producer_role(const CUtensorMap *tm_k, const CUtensorMap *tm_v,
-                                              uint32_t sb, const Tile &t, int bhk, const Waiter &wt)
+__device__ __forceinline__ void producer_role(const FwdParams &p, const CUtensorMap *tm_k,
+                                              const CUtensorMap *tm_v, uint32_t sb, const Tile &t, int bhk,
+                                              const Waiter &wt)
 {
     auto bar = [sb](int i) { return sb + OFF_BAR + 8u * i; };
     ptx::prefetch_tensormap(tm_k);
     ptx::prefetch_tensormap(tm_v);
     int issued_k = -1, issued_v = -1;
     bool ok = true;
-    for (int j = 0; j < t.ntiles; ++j) {
+    for (int j = 0; j < t.ntiles && ok; ++j) {
         const int ks = j % KSTAGES;
         if (!wt.wait(bar(KEMPTY + ks), ((j / KSTAGES) & 1) ^ 1, SITE_KE)) {
             ok = false;
@@ -179,61 +212,83 @@ __device__ __forceinline__ void producer_role(const CUtensorMap *tm_k, const CUt
         ptx::mbar_arrive_expect_tx(bar(KFULL + ks), K_STAGE_BYTES);
         ptx::tma_load_3d(kdst, tm_k, bar(KFULL + ks), 0, j * BN, bhk);
         ptx::tma_load_3d(kdst + K_HALF_BYTES, tm_k, bar(KFULL + ks), 64, j * BN, bhk);
+        SATTN_TRACE(p, t, 11, j);
         issued_k = j;
-        const int vs = j % VSTAGES;
-        if (!wt.wait(bar(VEMPTY + vs), ((j / VSTAGES) & 1) ^ 1, SITE_VE)) {
-            ok = false;
-            break;
+        for (int h = 0; h < 2; ++h) {
+            const int u = 2 * j + h, vs = u % VSLOTS;
+            if (!wt.wait(bar(VEMPTY + vs), ((u / VSLOTS) & 1) ^ 1, SITE_VE)) {
+                ok = false;
+                break;
+            }
+            ptx::mbar_arrive_expect_tx(bar(VFULL + vs), V_TMA_BYTES);
+            ptx::tma_load_3d(sb + OFF_V + vs * V_SLOT_BYTES, tm_v, bar(VFULL + vs), j * BN + 128 * h, 0, bhk);
+            issued_v = u;
         }
-        ptx::mbar_arrive_expect_tx(bar(VFULL + vs), V_TMA_BYTES);
-        ptx::tma_load_3d(sb + OFF_V + vs * V_STAGE_BYTES, tm_v, bar(VFULL + vs), j * BN, 0, bhk);
-        issued_v = j;
+        SATTN_TRACE(p, t, 12, j);
     }
     if (!ok) {
         for (int j = max(0, issued_k - KSTAGES + 1); j <= issued_k; ++j)
             wt.drain(bar(KFULL + j % KSTAGES), (j / KSTAGES) & 1);
-        for (int j = max(0, issued_v - VSTAGES + 1); j <= issued_v; ++j)
-            wt.drain(bar(VFULL + j % VSTAGES), (j / VSTAGES) & 1);
+        for (int u = max(0, issued_v - VSLOTS + 1); u <= issued_v; ++u)
+            wt.drain(bar(VFULL + u % VSLOTS), (u / VSLOTS) & 1);
     }
 }
 
-__device__ __forceinline__ void mma_role(uint32_t sb, uint32_t tmem, const Tile &t, const Waiter &wt)
+__device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32_t tmem, const Tile &t,
+                                         const Waiter &wt)
 {
     auto bar = [sb](int i) { return sb + OFF_BAR + 8u * i; };
     if (wt.wait(bar(QFULL), 0, SITE_Q)) {
         ptx::tc_fence_after();
         for (int j = 0; j <= t.ntiles; ++j) {
-            if (j < t.ntiles) {                     // S_j = Q K_j^T
+            if (j < t.ntiles) {                     // S_j = Q K_j^T (256 keys)
                 const int ks = j % KSTAGES;
                 if (!wt.wait(bar(KFULL + ks), (j / KSTAGES) & 1, SITE_K))
                     break;
+                if (j >= 1 && !wt.wait(bar(SFREE), (j - 1) & 1, SITE_SFREE))
+                    break;
                 ptx::tc_fence_after();
-                const uint32_t d_s = tmem + static_cast<uint32_t>((j & 1) * BN);
+                SATTN_TRACE(p, t, 8, j);
                 const uint32_t kb = sb + OFF_K + ks * K_STAGE_BYTES;
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
-                    ptx::mma_f16_ts(d_s, tmem + TM_Q + 8 * s,
+                    ptx::mma_f16_ts(tmem + TM_S, tmem + TM_Q + 8 * s,
                                     ptx::sw128_desc(kb + (s >> 2) * K_HALF_BYTES + (s & 3) * 32),
                                     IDESC_QK, s > 0);
+                SATTN_TRACE(p, t, 9, j);
                 ptx::mma_commit(bar(KEMPTY + ks));
-                ptx::mma_commit(bar(SFULL + (j & 1)));
+                ptx::mma_commit(bar(SFULL));
+                SATTN_TRACE(p, t, 4, j);
             }
             if (j >= 1) {                           // PV_{j-1} = P_{j-1} V_{j-1}
-                const int jj = j - 1, bs = jj & 1, vs = jj % VSTAGES;
-                if (!wt.wait(bar(PFULL + bs), (jj >> 1) & 1, SITE_P))
-                    break;
-                if (!wt.wait(bar(VFULL + vs), (jj / VSTAGES) & 1, SITE_V))
+                const int jj = j - 1;
+                if (!wt.wait(bar(PFULL), jj & 1, SITE_P))
                     break;
                 if (!wt.wait(bar(PVEMPTY), (jj & 1) ^ 1, SITE_PVE))
                     break;
-                ptx::tc_fence_after();
-                const uint32_t vb = sb + OFF_V + vs * V_STAGE_BYTES;
+                bool ok = true;
+                for (int h = 0; h < 2 && ok; ++h) {
+                    const int u = 2 * jj + h, vs = u % VSLOTS;
+                    if (!wt.wait(bar(VFULL + vs), (u / VSLOTS) & 1, SITE_V)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    if (h == 0)
+                        SATTN_TRACE(p, t, 5, jj);
+                    const uint32_t vb = sb + OFF_V + vs * V_SLOT_BYTES;
+                    const uint32_t pb = sb + OFF_P + h * P_HALF_BYTES;
 #pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    ptx::mma_f8_ts(tmem + TM_PV, tmem + static_cast<uint32_t>(bs * BN + 8 * s),
-                                   ptx::sw128_desc(vb + s * 32), IDESC_PV, s > 0);
-                ptx::mma_commit(bar(VEMPTY + vs));
+                    for (int s = 0; s < 4; ++s)
+                        ptx::mma_f8_ss(tmem + TM_PV, ptx::sw128_desc(pb + s * 32), ptx::sw128_desc(vb + s * 32),
+                                       IDESC_PV, (h | s) != 0);
+                    ptx::mma_commit(bar(VEMPTY + vs));
+                }
+                if (!ok)
+                    break;
+                SATTN_TRACE(p, t, 10, jj);
                 ptx::mma_commit(bar(PVFULL));
+                ptx::mma_commit(bar(PDONE));
             }
         }
     }
@@ -242,48 +297,45 @@ __device__ __forceinline__ void mma_role(uint32_t sb, uint32_t tmem, const Tile 
     wt.drain(bar(MMADONE), 0);
 }
 
-__device__ __forceinline__ void softmax_role(const FwdParams &p, uint32_t sb, uint8_t *smem,
+// Compute warpgroups.  Half h owns S columns [128h, 128h + 128) of every tile
+// and writes the P8 bytes of those keys into shared-memory half h (K-major,
+// 128-byte swizzle); the row max is exchanged through shared memory under a
+// named barrier, so both halves hold the same running max m and alpha.  Half
+// h also owns RO columns [64h, 64h + 64): after writing P_j it folds the
+// partial PV_{j-1} into RO with alpha_{j-1} (both halves keep d).
+__device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, uint8_t *smem,
                                              uint32_t tmem, int warp, int lane, const Tile &t,
                                              const Waiter &wt)
 {
     auto bar = [sb](int i) { return sb + OFF_BAR + 8u * i; };
+    const int half = warp >> 2;                               // 0 or 1
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;                       // query row in the tile = TMEM lane
+    const int r = quarter * 32 + lane;                        // query row in the tile = TMEM lane
     const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const int i = t.q0 + r;
 
-    // Q codes of row i -> FP16 carrier -> TMEM columns [TM_Q, TM_Q + 64)
+    // Q codes 64h .. 64h+63 of row i -> FP16 carrier -> TMEM columns [TM_Q + 32h, TM_Q + 32h + 32)
     {
-        uint32_t h0[32], h1[32];
+        uint32_t h[32];
         if (i < p.nq32) {
             const uint4 *src = reinterpret_cast<const uint4 *>(
-                p.q_codes + (static_cast<size_t>(t.b * p.Hq + t.hq) * p.nq32 + i) * HD);
+                p.q_codes + (static_cast<size_t>(t.b * p.Hq + t.hq) * p.nq32 + i) * HD + 64 * half);
 #pragma unroll
-            for (int w = 0; w < 8; ++w) {
+            for (int w = 0; w < 4; ++w) {
                 const uint4 a = src[w];
                 const uint32_t words[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int pair = w * 8 + e * 2;          // element pair index (0..63)
-                    const uint32_t lo = f16x2_of_i8(words[e], 0), hi = f16x2_of_i8(words[e], 2);
-                    if (pair < 32) {
-                        h0[pair] = lo;
-                        h0[pair + 1] = hi;
-                    } else {
-                        h1[pair - 32] = lo;
-                        h1[pair - 31] = hi;
-                    }
+                    h[w * 8 + e * 2] = f16x2_of_i8(words[e], 0);
+                    h[w * 8 + e * 2 + 1] = f16x2_of_i8(words[e], 2);
                 }
             }
         } else {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                h0[c] = 0u;
-                h1[c] = 0u;
-            }
+            for (int c = 0; c < 32; ++c)
+                h[c] = 0u;
         }
-        ptx::tmem_st32(taddr + TM_Q, h0);
-        ptx::tmem_st32(taddr + TM_Q + 32, h1);
+        ptx::tmem_st32(taddr + TM_Q + 32 * half, h);
         ptx::tmem_wait_st();
     }
     ptx::tc_fence_before();
@@ -293,148 +345,181 @@ __device__ __forceinline__ void softmax_role(const FwdParams &p, uint32_t sb, ui
                                   : 0.0f;
     const int lim = p.causal ? i + (p.Nkv - p.Nq) : 0x7fffffff;   // last kept key of row i
     const float *ksc = p.k_scales + static_cast<size_t>(t.b * p.Hkv + t.hk) * p.nbk;
-    float *alpha_s = reinterpret_cast<float *>(smem + OFF_ALPHA);
+    float *maxx = reinterpret_cast<float *>(smem + OFF_MAXX);
+    uint8_t *prow = smem + OFF_P + half * P_HALF_BYTES + r * 128;  // this row's 128 P8 bytes
+    constexpr float kLog2_448 = 8.8073549220576041f;          // log2(448): P is stored as p * 448
     float m = -INFINITY;
-
-    for (int j = 0; j < t.ntiles; ++j) {
-        const int bs = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!wt.wait(bar(SFULL + bs), ph, SITE_S))
-            return;
-        ptx::tc_fence_after();
-        float sig[4];
+    float ro[64];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int kb = j * (BN / kQBlock) + c;
-            const float sk = kb < p.nbk ? ksc[kb] : 0.0f;
-            sig[c] = __fmul_rn(__fmul_rn(sq, sk), p.c0);
-        }
-        uint32_t s[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            ptx::tmem_ld32(taddr + static_cast<uint32_t>(bs * BN + 32 * c), s[c]);
-        ptx::tmem_wait_ld();
-#ifdef SATTN_DEBUG_DUMP
-        if (p.dbg && j == 0 && t.q0 == 0 && t.hq == 0 && t.b == 0)
-            for (int k = 0; k < BN; ++k)
-                p.dbg[r * BN + k] = __uint_as_float(s[k >> 5][k & 31]);
-#endif
-
-        // scores in the log2 domain, masks, tile max
-        float tmax = -INFINITY;
-        if (j < t.mask_from) {
-#pragma unroll
-            for (int k = 0; k < BN; ++k) {
-                const float x = __fmul_rn(__uint_as_float(s[k >> 5][k & 31]), sig[k >> 5]);
-                s[k >> 5][k & 31] = __float_as_uint(x);
-                tmax = fmaxf(tmax, x);
-            }
-        } else {
-            const int kbase = j * BN;
-#pragma unroll
-            for (int k = 0; k < BN; ++k) {
-                const int key = kbase + k;
-                const float x = (key < p.Nkv && key <= lim)
-                                    ? __fmul_rn(__uint_as_float(s[k >> 5][k & 31]), sig[k >> 5])
-                                    : -INFINITY;
-                s[k >> 5][k & 31] = __float_as_uint(x);
-                tmax = fmaxf(tmax, x);
-            }
-        }
-        const float mn = fmaxf(m, tmax);
-        const float alpha = (m == -INFINITY) ? 0.0f : ptx::ex2_approx(__fsub_rn(m, mn));
-
-        // P as E4M3 bytes of exp2(s - m') * 448, four keys per 32-bit TMEM column
-        uint32_t pk[32];
-#pragma unroll
-        for (int w = 0; w < 32; ++w) {
-            float e[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int k = 4 * w + u;
-                const float x = __uint_as_float(s[k >> 5][k & 31]);
-                e[u] = __fmul_rn(ptx::ex2_approx(__fsub_rn(x, mn)), 448.0f);
-            }
-            pk[w] = ptx::cvt_e4m3x2(e[1], e[0]) | (ptx::cvt_e4m3x2(e[3], e[2]) << 16);
-        }
-        ptx::tmem_st32(taddr + static_cast<uint32_t>(bs * BN), pk);
-        ptx::tmem_wait_st();
-#ifdef SATTN_DEBUG_DUMP
-        if (p.dbg && j == 0 && t.q0 == 0 && t.hq == 0 && t.b == 0)
-            for (int w = 0; w < 32; ++w)
-                p.dbg[16384 + r * 32 + w] = __uint_as_float(pk[w]);
-#endif
-
-        if (!wt.wait(bar(AEMPTY + bs), ph ^ 1, SITE_AE))
-            return;
-        alpha_s[bs * BM + r] = alpha;
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(PFULL + bs));
-        ptx::mbar_arrive(bar(AFULL + bs));
-        m = mn;
-    }
-}
-
-__device__ __forceinline__ void correction_role(const FwdParams &p, uint32_t sb, uint8_t *smem,
-                                                uint32_t tmem, int warp, int lane, const Tile &t,
-                                                const Waiter &wt)
-{
-    auto bar = [sb](int i) { return sb + OFF_BAR + 8u * i; };
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int i = t.q0 + r;
-    const float *alpha_s = reinterpret_cast<const float *>(smem + OFF_ALPHA);
-
-    float ro[HD];
-#pragma unroll
-    for (int c = 0; c < HD; ++c)
+    for (int c = 0; c < 64; ++c)
         ro[c] = 0.0f;
-    float d = 0.0f;
+    float d = 0.0f, alpha_prev = 0.0f;
 
-    for (int j = 0; j < t.ntiles; ++j) {
-        const int bs = j & 1;
-        if (!wt.wait(bar(PVFULL), j & 1, SITE_PV))
-            return;
+    // RO = RO * alpha + PV partial of tile jj (this half's 64 channels), d likewise
+    auto fold_partial = [&](int jj, float alpha) -> bool {
+        if (!wt.wait(bar(PVFULL), jj & 1, SITE_PV))
+            return false;
         ptx::tc_fence_after();
-        if (!wt.wait(bar(AFULL + bs), (j >> 1) & 1, SITE_A))
-            return;
-        const float alpha = alpha_s[bs * BM + r];
-        ptx::mbar_arrive(bar(AEMPTY + bs));
+        if (r == 0 && half == 0)
+            SATTN_TRACE(p, t, 6, jj);
 #ifdef SATTN_DEBUG_DUMP
-        if (p.dbg && j == 0 && t.q0 == 0 && t.hq == 0 && t.b == 0) {
+        if (p.dbg && jj == 0 && t.q0 == 0 && t.hq == 0 && t.b == 0 && half == 0) {
             for (int c = 0; c < static_cast<int>(PV_N); ++c) {
                 uint32_t x;
                 ptx::tmem_ld1(taddr + TM_PV + c, x);
                 ptx::tmem_wait_ld();
-                p.dbg[20480 + r * PV_N + c] = __uint_as_float(x);
+                p.dbg[40960 + r * PV_N + c] = __uint_as_float(x);
             }
         }
 #endif
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-            uint32_t part[32];
-            ptx::tmem_ld32(taddr + TM_PV + 32 * c4, part);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-                ro[32 * c4 + k] = fmaf(ro[32 * c4 + k], alpha, __uint_as_float(part[k]));
-        }
-        uint32_t ds;
+        uint32_t part[2][32], ds;
+        ptx::tmem_ld32(taddr + TM_PV + 64 * half, part[0]);
+        ptx::tmem_ld32(taddr + TM_PV + 64 * half + 32, part[1]);
         ptx::tmem_ld1(taddr + TM_PV + 128, ds);
         ptx::tmem_wait_ld();
-        d = fmaf(d, alpha, __uint_as_float(ds));
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(PVEMPTY));
+        ptx::mbar_arrive(bar(PVEMPTY));                        // the partial buffer may be reused
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+            ro[c] = fmaf(ro[c], alpha, __uint_as_float(part[c >> 5][c & 31]));
+        d = fmaf(d, alpha, __uint_as_float(ds));
+        if (r == 0 && half == 0)
+            SATTN_TRACE(p, t, 7, jj);
+        return true;
+    };
+
+    // block scales of this half's four 32-key blocks, one tile ahead
+    auto kscale = [&](int j, int c) {
+        const int kb = j * (BN / kQBlock) + 4 * half + c;
+        return kb < p.nbk ? ksc[kb] : 0.0f;
+    };
+    float sk[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        sk[c] = kscale(0, c);
+
+    for (int j = 0; j < t.ntiles; ++j) {
+        float sig[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            sig[c] = __fmul_rn(__fmul_rn(sq, sk[c]), p.c0);
+            sk[c] = kscale(j + 1, c);
+        }
+        if (!wt.wait(bar(SFULL), j & 1, SITE_S))
+            return;
+        ptx::tc_fence_after();
+        if (r == 0 && half == 0)
+            SATTN_TRACE(p, t, 0, j);
+        uint32_t s[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            ptx::tmem_ld32(taddr + TM_S + static_cast<uint32_t>(128 * half + 32 * c), s[c]);
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(SFREE));                          // S may be overwritten now
+        if (r == 0 && half == 0)
+            SATTN_TRACE(p, t, 1, j);
+#ifdef SATTN_DEBUG_DUMP
+        if (p.dbg && j == 0 && t.q0 == 0 && t.hq == 0 && t.b == 0)
+            for (int k = 0; k < 128; ++k)
+                p.dbg[r * BN + 128 * half + k] = __uint_as_float(s[k >> 5][k & 31]);
+#endif
+        // keys of this half that row i keeps: the first `nvalid` (the mask is a
+        // suffix of the half-tile: keys >= Nkv and, if causal, keys > lim)
+        const bool masked = j >= t.mask_from;
+        int nvalid = 128;
+        if (masked) {
+            const int lo = j * BN + 128 * half;
+            nvalid = max(0, min(128, min(p.Nkv - 1, lim) - lo + 1));
+        }
+        // max of the raw accumulators per 32-key block: the block scale is
+        // positive (or zero), so fl(max(acc) * sig) = max(fl(acc * sig)) exactly
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float b;
+            if (!masked) {
+                // eight independent three-input max chains, then a short tree
+                float q[8];
+#pragma unroll
+                for (int a = 0; a < 8; ++a)
+                    q[a] = ptx::fmax3(__uint_as_float(s[c][a]), __uint_as_float(s[c][a + 8]),
+                                      __uint_as_float(s[c][a + 16]));
+#pragma unroll
+                for (int a = 0; a < 8; ++a)
+                    q[a] = fmaxf(q[a], __uint_as_float(s[c][a + 24]));
+                b = fmaxf(ptx::fmax3(q[0], q[1], q[2]), ptx::fmax3(q[3], q[4], q[5]));
+                b = ptx::fmax3(b, q[6], q[7]);
+            } else {
+                float q[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    q[k & 3] = fmaxf(q[k & 3], 32 * c + k < nvalid ? __uint_as_float(s[c][k]) : -INFINITY);
+                b = fmaxf(fmaxf(q[0], q[1]), fmaxf(q[2], q[3]));
+            }
+            tmax = fmaxf(tmax, (b == -INFINITY) ? -INFINITY : __fmul_rn(b, sig[c]));
+        }
+        // exchange the half-row maxima (double-buffered by tile parity)
+        maxx[((j & 1) * 2 + half) * BM + r] = tmax;
+        ptx::named_bar_sync(1, 2 * BM);
+        tmax = fmaxf(tmax, maxx[((j & 1) * 2 + (half ^ 1)) * BM + r]);
+        if (r == 0 && half == 0)
+            SATTN_TRACE(p, t, 2, j);
+
+        const float mn = fmaxf(m, tmax);
+        const float alpha = (m == -INFINITY) ? 0.0f : ptx::ex2_approx(__fsub_rn(m, mn));
+        const float nb = kLog2_448 - mn;                     // exponent offset of p * 448
+
+        // the P buffer is free once PV_{j-1} has read it
+        if (j >= 1 && !wt.wait(bar(PDONE), (j - 1) & 1, SITE_PDONE))
+            return;
+        // P8 = E4M3(exp2(acc * sig - m') * 448), four keys per 32-bit word,
+        // stored 32 keys at a time (16-byte chunk c of the row lands at chunk
+        // c ^ (row % 8): the 128-byte swizzle of the K-major operand)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                float e[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int k = 4 * w + u;
+                    float x = fmaf(__uint_as_float(s[c][k]), sig[c], nb);
+                    if (masked)
+                        x = (32 * c + k < nvalid) ? x : -INFINITY;
+                    e[u] = ptx::ex2_approx(x);
+                }
+                pk[w] = ptx::cvt_e4m3x2(e[1], e[0]) | (ptx::cvt_e4m3x2(e[3], e[2]) << 16);
+            }
+#ifdef SATTN_DEBUG_DUMP
+            if (p.dbg && j == 0 && t.q0 == 0 && t.hq == 0 && t.b == 0)
+                for (int w = 0; w < 8; ++w)
+                    p.dbg[32768 + r * 64 + 32 * half + 8 * c + w] = __uint_as_float(pk[w]);
+#endif
+            *reinterpret_cast<uint4 *>(prow + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4 *>(prow + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(bar(PFULL));
+        if (r == 0 && half == 0)
+            SATTN_TRACE(p, t, 3, j);
+        if (j >= 1 && !fold_partial(j - 1, alpha_prev))
+            return;
+        alpha_prev = alpha;
+        m = mn;
     }
+    if (t.ntiles > 0 && !fold_partial(t.ntiles - 1, alpha_prev))
+        return;
 
     // final conversion: reciprocal of d, per-channel V scale, BF16
     if (i < p.Nq) {
         const float rcp = d > 0.0f ? __frcp_rn(d) : 0.0f;
-        const float *sv = p.v_scales + static_cast<size_t>(t.b * p.Hkv + t.hk) * HD;
-        uint4 *dst = reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(t.b * p.Hq + t.hq) * p.Nq + i) * HD);
+        const float *sv = p.v_scales + static_cast<size_t>(t.b * p.Hkv + t.hk) * HD + 64 * half;
+        uint4 *dst = reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(t.b * p.Hq + t.hq) * p.Nq + i) * HD +
+                                               64 * half);
 #pragma unroll
-        for (int w = 0; w < 16; ++w) {
+        for (int w = 0; w < 8; ++w) {
             uint32_t u[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -483,31 +568,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ptx::mbar_init(b0 + 8u * (KFULL + s), 1);
             ptx::mbar_init(b0 + 8u * (KEMPTY + s), 1);
         }
-        for (int s = 0; s < VSTAGES; ++s) {
+        for (int s = 0; s < VSLOTS; ++s) {
             ptx::mbar_init(b0 + 8u * (VFULL + s), 1);
             ptx::mbar_init(b0 + 8u * (VEMPTY + s), 1);
         }
-        ptx::mbar_init(b0 + 8u * QFULL, BM);
-        for (int s = 0; s < 2; ++s) {
-            ptx::mbar_init(b0 + 8u * (SFULL + s), 1);
-            ptx::mbar_init(b0 + 8u * (PFULL + s), BM);
-            ptx::mbar_init(b0 + 8u * (AFULL + s), BM);
-            ptx::mbar_init(b0 + 8u * (AEMPTY + s), BM);
-        }
+        ptx::mbar_init(b0 + 8u * QFULL, 2 * BM);
+        ptx::mbar_init(b0 + 8u * SFULL, 1);
+        ptx::mbar_init(b0 + 8u * SFREE, 2 * BM);
+        ptx::mbar_init(b0 + 8u * PFULL, 2 * BM);
+        ptx::mbar_init(b0 + 8u * PDONE, 1);
         ptx::mbar_init(b0 + 8u * PVFULL, 1);
-        ptx::mbar_init(b0 + 8u * PVEMPTY, BM);
+        ptx::mbar_init(b0 + 8u * PVEMPTY, 2 * BM);
         ptx::mbar_init(b0 + 8u * MMADONE, 1);
         ptx::fence_mbar_init();
     }
-    // constant rows of every V stage: row 128 holds E4M3 1.0 (0x38), rows 129..143 hold 0
-    for (int idx = threadIdx.x; idx < VSTAGES * 16 * 8; idx += NTHREADS) {
+    // constant rows of every V slot: row 128 holds E4M3 1.0 (0x38), rows 129..143 hold 0
+    for (int idx = threadIdx.x; idx < VSLOTS * 16 * 8; idx += NTHREADS) {
         const int st = idx / 128, w = idx % 128, row = 128 + w / 8, ch = w % 8;
         const uint32_t val = (row == 128) ? 0x38383838u : 0u;
-        *reinterpret_cast<uint4 *>(smem + OFF_V + st * V_STAGE_BYTES + row * 128 + ch * 16) =
+        *reinterpret_cast<uint4 *>(smem + OFF_V + st * V_SLOT_BYTES + row * 128 + ch * 16) =
             make_uint4(val, val, val, val);
     }
     ptx::fence_proxy_async_smem();
-    if (warp == 1) {
+    if (warp == WARP_MMA) {
         ptx::tmem_alloc(sb + OFF_TMEM_SLOT, TMEM_COLS);
         ptx::tmem_relinquish();
     }
@@ -517,22 +600,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + OFF_TMEM_SLOT);
 
     if (*flag == 0) {
-        if (warp == 0) {
-            if (lane == 0)
-                producer_role(&tm_k, &tm_v, sb, t, t.b * p.Hkv + t.hk, wt);
-        } else if (warp == 1) {
-            if (lane == 0)
-                mma_role(sb, tmem, t, wt);
-            __syncwarp();
-        } else if (warp < 6) {
-            softmax_role(p, sb, smem, tmem, warp, lane, t, wt);
+        if (warp < WARP_PRODUCER) {
+            ptx::setmaxnreg_inc<kRegsCompute>();
+            compute_role(p, sb, smem, tmem, warp, lane, t, wt);
         } else {
-            correction_role(p, sb, smem, tmem, warp, lane, t, wt);
+            ptx::setmaxnreg_dec<kRegsOther>();
+            if (warp == WARP_PRODUCER) {
+                if (lane == 0)
+                    producer_role(p, &tm_k, &tm_v, sb, t, t.b * p.Hkv + t.hk, wt);
+            } else if (warp == WARP_MMA) {
+                if (lane == 0)
+                    mma_role(p, sb, tmem, t, wt);
+            }
+            __syncwarp();
         }
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == WARP_MMA) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
     }
@@ -607,7 +692,7 @@ int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scal
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(g.Nkv),
                                     static_cast<cuuint64_t>(bhk)};
         const cuuint64_t strides[2] = {HD * sizeof(__half), static_cast<cuuint64_t>(g.Nkv) * HD * sizeof(__half)};
-        const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BN), 1};
+        const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BN), 1};   // 256 keys x 64 channels
         const cuuint32_t estr[3] = {1, 1, 1};
         if (encode(&tmk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, carrier, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -619,7 +704,7 @@ int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scal
                                     static_cast<cuuint64_t>(bhk)};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(g.nk128),
                                        static_cast<cuuint64_t>(g.nk128) * HD};
-        const cuuint32_t box[3] = {static_cast<cuuint32_t>(BN), static_cast<cuuint32_t>(HD), 1};
+        const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(HD), 1};   // 128 keys x 128 channels
         const cuuint32_t estr[3] = {1, 1, 1};
         if (encode(&tmv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(v_codes), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -627,11 +712,18 @@ int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scal
             return 1;
     }
 
+    // The per-warpgroup register split only adds up when the kernel is launched
+    // with exactly kLaunchRegs registers per thread; refuse to launch otherwise.
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(SMEM_BYTES));
+        cudaFuncAttributes fa;
+        attr_err = cudaFuncGetAttributes(&fa, attn_fwd_kernel);
+        if (attr_err == cudaSuccess && fa.numRegs != kLaunchRegs)
+            attr_err = cudaErrorInvalidConfiguration;
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(SMEM_BYTES));
     });
     if (attr_err != cudaSuccess)
         return static_cast<int>(attr_err);

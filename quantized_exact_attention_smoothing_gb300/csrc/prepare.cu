@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint4 *__restrict__ 
     __shared__ __align__(16) uint8_t tile[kHeadDim * kVRow];
     __shared__ float sv[kHeadDim];
     const int bh = blockIdx.y;
-    const int t0 = blockIdx.x * kKvTile;
+    const int t0 = blockIdx.x * kVPad;
     if (threadIdx.x < kHeadDim)
         sv[threadIdx.x] = v_scales[bh * kHeadDim + threadIdx.x];
     __syncthreads();
@@ -249,7 +249,7 @@ cudaError_t launch_prepare(const Geometry &g, const void *q, const void *k, cons
                                                      k_mean, v_scales);
     quant_int8_kernel<true><<<dim3(static_cast<unsigned>(g.nbk), bhk), 128, 0, stream>>>(
         k4, g.Nkv, g.nk32, static_cast<int>(g.nbk), k_mean, k_codes, k_scales);
-    quant_v_kernel<<<dim3(static_cast<unsigned>(g.nk128 / kKvTile), bhk), 256, 0, stream>>>(
+    quant_v_kernel<<<dim3(static_cast<unsigned>(g.nk128 / kVPad), bhk), 256, 0, stream>>>(
         v4, g.Nkv, g.nk128, v_scales, v_codes);
     quant_int8_kernel<false><<<dim3(static_cast<unsigned>(g.nbq), bhq), 128, 0, stream>>>(
         q4, g.Nq, g.nq32, static_cast<int>(g.nbq), nullptr, q_codes, q_scales);

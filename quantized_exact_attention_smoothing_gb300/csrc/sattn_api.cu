@@ -28,7 +28,7 @@ int make_geometry(const sattn_shape *s, Geometry *g)
     if (static_cast<int64_t>(s->B) * s->Hq > 65535 || static_cast<int64_t>(s->B) * s->Hkv > 65535)
         return SATTN_ERR_INVALID;   // grid y limit of the launches
     const int64_t nq32 = sattn::pad_up(s->Nq, sattn::kQBlock);
-    const int64_t nk128 = sattn::pad_up(s->Nkv, sattn::kKvTile);
+    const int64_t nk128 = sattn::pad_up(s->Nkv, sattn::kVPad);
     if (static_cast<int64_t>(s->B) * s->Hq * nq32 * sattn::kHeadDim > kMaxElems ||
         static_cast<int64_t>(s->B) * s->Hkv * nk128 * sattn::kHeadDim > kMaxElems)
         return SATTN_ERR_INVALID;

@@ -10,7 +10,8 @@ namespace sattn {
 constexpr int kHeadDim = 128;
 constexpr int kQBlock = 32;      // tokens per INT8 quantisation block
 constexpr int kMeanChunk = 64;   // tokens per K-mean partial sum
-constexpr int kKvTile = 128;     // keys per KV tile of the forward pass
+constexpr int kVPad = 128;       // V codes are padded to a multiple of 128 keys
+constexpr int kKvTile = 256;     // keys per KV tile of the forward pass (part of the contract)
 constexpr int kQTile = 128;      // query rows per CTA of the forward pass
 
 inline int64_t pad_up(int64_t n, int64_t m) { return (n + m - 1) / m * m; }
