@@ -13,7 +13,9 @@
 //               memory), then RO = RO * alpha + PV and d = d * alpha + sum p8
 //               for the previous tile, and the final conversion
 //   warp 8      TMA producer: K tiles (FP16 carrier of the INT8 codes) and V
-//               half-tiles (E4M3, channel-major) into mbarrier rings
+//               half-tiles (E4M3, channel-major): one K stage (the next tile
+//               loads while PV of the previous one runs) and a ring of four
+//               V half-tile slots
 //   warp 9      TMEM allocation and the single MMA-issuing thread:
 //                 S_j  = Q * K_j^T   tcgen05 kind::f16, A = Q from TMEM, N = 256
 //                 PV_j = P_j * V_j   tcgen05 kind::f8f6f4, A = P from shared
@@ -24,8 +26,10 @@
 // warpgroups 232 (128 scores and 64 RO values per thread) and the
 // producer/MMA warpgroup 40.
 // Tensor memory (512 columns): S [0,256), PV partial [256,400), Q carrier
-// [448,512).  A tcgen05.mma instruction costs about the same time for any N up
-// to 256 on this part, hence the 256-key tiles: QK runs at N = 256.
+// [448,512).  P is double-buffered in shared memory, so the softmax of tile
+// j + 1 never waits for PV of tile j.  A tcgen05.mma instruction costs about
+// the same time for any N up to 256 on this part, hence the 256-key tiles: QK
+// runs at N = 256.
 //
 // Exactness of QK: INT8 codes are carried as FP16 values (integers of
 // magnitude <= 127 are exact in FP16); every product is an integer <= 16129 and
@@ -51,13 +55,14 @@ namespace sattn {
 namespace {
 
 constexpr int BM = kQTile, BN = kKvTile, HD = kHeadDim;   // 128 rows x 256 keys
-constexpr int KSTAGES = 2, VSLOTS = 3;
+constexpr int KSTAGES = 1, VSLOTS = 4;
 constexpr uint32_t K_HALF_BYTES = BN * 64 * 2;          // 256 keys x 64 channels, FP16
 constexpr uint32_t K_STAGE_BYTES = 2 * K_HALF_BYTES;    // 64 KB
 constexpr uint32_t PV_N = 144;                          // V rows + ones row + zero rows
 constexpr uint32_t V_SLOT_BYTES = PV_N * 128;           // one 128-key half tile, 18 KB
 constexpr uint32_t V_TMA_BYTES = HD * 128;              // 16 KB loaded per half tile
 constexpr uint32_t P_HALF_BYTES = BM * 128;             // 128 rows x 128 keys, E4M3
+constexpr uint32_t P_BUF_BYTES = 2 * P_HALF_BYTES;      // one tile's P (double-buffered)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;
 constexpr uint32_t TM_PV = 256;
@@ -79,7 +84,7 @@ constexpr uint64_t TIMEOUT_NS = 1000000000ull;
 constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_V = OFF_K + KSTAGES * K_STAGE_BYTES;
 constexpr uint32_t OFF_P = OFF_V + VSLOTS * V_SLOT_BYTES;
-constexpr uint32_t OFF_MAXX = OFF_P + 2 * P_HALF_BYTES;     // [tile parity][half][row] row maxima
+constexpr uint32_t OFF_MAXX = OFF_P + 2 * P_BUF_BYTES;      // [tile parity][half][row] row maxima
 constexpr uint32_t OFF_BAR = OFF_MAXX + 4 * BM * 4;
 enum Bar : int {
     KFULL = 0,
@@ -89,9 +94,9 @@ enum Bar : int {
     QFULL = VEMPTY + VSLOTS,
     SFULL = QFULL + 1,
     SFREE = SFULL + 1,
-    PFULL = SFREE + 1,
-    PDONE = PFULL + 1,
-    PVFULL = PDONE + 1,
+    PFULL = SFREE + 1,       // 2 (per P buffer)
+    PDONE = PFULL + 2,       // 2 (per P buffer)
+    PVFULL = PDONE + 2,
     PVEMPTY = PVFULL + 1,
     MMADONE = PVEMPTY + 1,
     NBARS = MMADONE + 1
@@ -261,8 +266,8 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
                 SATTN_TRACE(p, t, 4, j);
             }
             if (j >= 1) {                           // PV_{j-1} = P_{j-1} V_{j-1}
-                const int jj = j - 1;
-                if (!wt.wait(bar(PFULL), jj & 1, SITE_P))
+                const int jj = j - 1, pbuf = jj & 1;
+                if (!wt.wait(bar(PFULL + pbuf), (jj >> 1) & 1, SITE_P))
                     break;
                 if (!wt.wait(bar(PVEMPTY), (jj & 1) ^ 1, SITE_PVE))
                     break;
@@ -277,7 +282,7 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
                     if (h == 0)
                         SATTN_TRACE(p, t, 5, jj);
                     const uint32_t vb = sb + OFF_V + vs * V_SLOT_BYTES;
-                    const uint32_t pb = sb + OFF_P + h * P_HALF_BYTES;
+                    const uint32_t pb = sb + OFF_P + pbuf * P_BUF_BYTES + h * P_HALF_BYTES;
 #pragma unroll
                     for (int s = 0; s < 4; ++s)
                         ptx::mma_f8_ss(tmem + TM_PV, ptx::sw128_desc(pb + s * 32), ptx::sw128_desc(vb + s * 32),
@@ -288,7 +293,7 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
                     break;
                 SATTN_TRACE(p, t, 10, jj);
                 ptx::mma_commit(bar(PVFULL));
-                ptx::mma_commit(bar(PDONE));
+                ptx::mma_commit(bar(PDONE + pbuf));
             }
         }
     }
@@ -346,7 +351,7 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
     const int lim = p.causal ? i + (p.Nkv - p.Nq) : 0x7fffffff;   // last kept key of row i
     const float *ksc = p.k_scales + static_cast<size_t>(t.b * p.Hkv + t.hk) * p.nbk;
     float *maxx = reinterpret_cast<float *>(smem + OFF_MAXX);
-    uint8_t *prow = smem + OFF_P + half * P_HALF_BYTES + r * 128;  // this row's 128 P8 bytes
+    uint8_t *prow0 = smem + OFF_P + half * P_HALF_BYTES + r * 128;  // this row's 128 P8 bytes (buffer 0)
     constexpr float kLog2_448 = 8.8073549220576041f;          // log2(448): P is stored as p * 448
     float m = -INFINITY;
     float ro[64];
@@ -470,8 +475,10 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
         const float alpha = (m == -INFINITY) ? 0.0f : ptx::ex2_approx(__fsub_rn(m, mn));
         const float nb = kLog2_448 - mn;                     // exponent offset of p * 448
 
-        // the P buffer is free once PV_{j-1} has read it
-        if (j >= 1 && !wt.wait(bar(PDONE), (j - 1) & 1, SITE_PDONE))
+        // P buffer j % 2 is free once PV_{j-2} has read it
+        const int pbuf = j & 1;
+        uint8_t *prow = prow0 + pbuf * P_BUF_BYTES;
+        if (j >= 2 && !wt.wait(bar(PDONE + pbuf), ((j >> 1) - 1) & 1, SITE_PDONE))
             return;
         // P8 = E4M3(exp2(acc * sig - m') * 448), four keys per 32-bit word,
         // stored 32 keys at a time (16-byte chunk c of the row lands at chunk
@@ -501,7 +508,7 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
             *reinterpret_cast<uint4 *>(prow + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
         ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(bar(PFULL));
+        ptx::mbar_arrive(bar(PFULL + pbuf));
         if (r == 0 && half == 0)
             SATTN_TRACE(p, t, 3, j);
         if (j >= 1 && !fold_partial(j - 1, alpha_prev))
@@ -575,8 +582,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ptx::mbar_init(b0 + 8u * QFULL, 2 * BM);
         ptx::mbar_init(b0 + 8u * SFULL, 1);
         ptx::mbar_init(b0 + 8u * SFREE, 2 * BM);
-        ptx::mbar_init(b0 + 8u * PFULL, 2 * BM);
-        ptx::mbar_init(b0 + 8u * PDONE, 1);
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(b0 + 8u * (PFULL + s), 2 * BM);
+            ptx::mbar_init(b0 + 8u * (PDONE + s), 1);
+        }
         ptx::mbar_init(b0 + 8u * PVFULL, 1);
         ptx::mbar_init(b0 + 8u * PVEMPTY, 2 * BM);
         ptx::mbar_init(b0 + 8u * MMADONE, 1);
