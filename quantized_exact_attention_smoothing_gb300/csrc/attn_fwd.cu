@@ -45,6 +45,7 @@
 
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include <cudaTypedefs.h>
 
@@ -482,31 +483,42 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
             return;
         // P8 = E4M3(exp2(acc * sig - m') * 448), four keys per 32-bit word,
         // stored 32 keys at a time (16-byte chunk c of the row lands at chunk
-        // c ^ (row % 8): the 128-byte swizzle of the K-major operand)
+        // c ^ (row % 8): the 128-byte swizzle of the K-major operand).  The
+        // masked and unmasked forms are separate copies so that the common,
+        // unmasked tiles carry no per-key select.
+        auto write_p = [&](auto masked_tag) {
+            constexpr bool kMasked = decltype(masked_tag)::value;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t pk[8];
+            for (int c = 0; c < 4; ++c) {
+                uint32_t pk[8];
 #pragma unroll
-            for (int w = 0; w < 8; ++w) {
-                float e[4];
+                for (int w = 0; w < 8; ++w) {
+                    float e[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int k = 4 * w + u;
-                    float x = fmaf(__uint_as_float(s[c][k]), sig[c], nb);
-                    if (masked)
-                        x = (32 * c + k < nvalid) ? x : -INFINITY;
-                    e[u] = ptx::ex2_approx(x);
+                    for (int u = 0; u < 4; ++u) {
+                        const int k = 4 * w + u;
+                        float x = fmaf(__uint_as_float(s[c][k]), sig[c], nb);
+                        if (kMasked)
+                            x = (32 * c + k < nvalid) ? x : -INFINITY;
+                        e[u] = ptx::ex2_approx(x);
+                    }
+                    pk[w] = ptx::cvt_e4m3x4(e[0], e[1], e[2], e[3]);
                 }
-                pk[w] = ptx::cvt_e4m3x2(e[1], e[0]) | (ptx::cvt_e4m3x2(e[3], e[2]) << 16);
-            }
 #ifdef SATTN_DEBUG_DUMP
-            if (p.dbg && j == 0 && t.q0 == 0 && t.hq == 0 && t.b == 0)
-                for (int w = 0; w < 8; ++w)
-                    p.dbg[32768 + r * 64 + 32 * half + 8 * c + w] = __uint_as_float(pk[w]);
+                if (p.dbg && j == 0 && t.q0 == 0 && t.hq == 0 && t.b == 0)
+                    for (int w = 0; w < 8; ++w)
+                        p.dbg[32768 + r * 64 + 32 * half + 8 * c + w] = __uint_as_float(pk[w]);
 #endif
-            *reinterpret_cast<uint4 *>(prow + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            *reinterpret_cast<uint4 *>(prow + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        }
+                *reinterpret_cast<uint4 *>(prow + (((2 * c) ^ (r & 7)) << 4)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4 *>(prow + (((2 * c + 1) ^ (r & 7)) << 4)) =
+                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+        };
+        if (masked)
+            write_p(std::true_type{});
+        else
+            write_p(std::false_type{});
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(bar(PFULL + pbuf));
         if (r == 0 && half == 0)

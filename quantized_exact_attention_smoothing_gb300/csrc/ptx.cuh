@@ -221,6 +221,18 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo)
 }
 
 // max of three FP32 values (sm_100+ three-input form)
+// four floats -> four E4M3 bytes (RNE, saturating), x0 in the low byte
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float x0, float x1, float x2, float x3)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r) : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+    return r;
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c)
 {
     float d;
