@@ -43,9 +43,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cfloat>
 #include <cstring>
 #include <mutex>
-#include <type_traits>
 
 #include <cudaTypedefs.h>
 
@@ -85,14 +85,19 @@ constexpr uint64_t TIMEOUT_NS = 1000000000ull;
 constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_V = OFF_K + KSTAGES * K_STAGE_BYTES;
 constexpr uint32_t OFF_P = OFF_V + VSLOTS * V_SLOT_BYTES;
-constexpr uint32_t OFF_MAXX = OFF_P + 2 * P_BUF_BYTES;      // [tile parity][half][row] row maxima
-constexpr uint32_t OFF_BAR = OFF_MAXX + 4 * BM * 4;
+constexpr uint32_t OFF_QS = OFF_P + 2 * P_BUF_BYTES;        // INT8 Q tile of the next item (TMA, 128B swizzle)
+constexpr uint32_t QS_BYTES = BM * HD;
+constexpr uint32_t OFF_MAXX = OFF_QS + QS_BYTES;             // [tile parity][half][row] row maxima
+constexpr uint32_t OFF_SV = OFF_MAXX + 4 * BM * 4;          // [item % 3][128] V channel scales
+constexpr uint32_t SV_BYTES = HD * 4;
+constexpr uint32_t OFF_BAR = OFF_SV + 3 * SV_BYTES;
 enum Bar : int {
     KFULL = 0,
     KEMPTY = KFULL + KSTAGES,
     VFULL = KEMPTY + KSTAGES,
     VEMPTY = VFULL + VSLOTS,
-    QFULL = VEMPTY + VSLOTS,
+    QSTAGE = VEMPTY + VSLOTS,   // INT8 Q codes of an item landed in shared memory
+    QFULL = QSTAGE + 1,         // its FP16 carrier is in TMEM
     SFULL = QFULL + 1,
     SFREE = SFULL + 1,
     PFULL = SFREE + 1,       // 2 (per P buffer)
@@ -106,13 +111,13 @@ constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBARS * 8;
 constexpr uint32_t OFF_FLAG = OFF_TMEM_SLOT + 4;
 constexpr uint32_t SMEM_BYTES = OFF_FLAG + 4 + 1024;   // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-static_assert(OFF_V % 1024 == 0 && V_SLOT_BYTES % 1024 == 0 && OFF_P % 1024 == 0,
+static_assert(OFF_V % 1024 == 0 && V_SLOT_BYTES % 1024 == 0 && OFF_P % 1024 == 0 && OFF_QS % 1024 == 0,
               "swizzle atoms must be 1024-aligned");
 
 // where a wait gave up (second status word)
 enum Site : uint32_t {
     SITE_KE = 1, SITE_VE, SITE_Q, SITE_K, SITE_P, SITE_V, SITE_PVE, SITE_DONE, SITE_S,
-    SITE_PV, SITE_DRAIN, SITE_SFREE, SITE_PDONE
+    SITE_PV, SITE_DRAIN, SITE_SFREE, SITE_PDONE, SITE_QS, SITE_QE
 };
 
 struct FwdParams {
@@ -120,7 +125,9 @@ struct FwdParams {
     const float *q_scales, *k_scales, *v_scales;
     __nv_bfloat16 *out;
     uint32_t *status;
-    int Hq, Hkv, Nq, Nkv, group, n_qtiles, causal;
+    int B, Hq, Hkv, Nq, Nkv, group, n_qtiles, n_items, causal;
+    // reciprocals for exact division by Hq * B, Hq and group (see udiv)
+    unsigned long long m_hb, m_hq, m_group;
     int nq32, nbq, nbk;
     float c0;
 #ifdef SATTN_DEBUG_DUMP
@@ -137,8 +144,9 @@ struct FwdParams {
 // the last query tile, batch 0, head 0), event `id` of KV tile `j`.
 #define SATTN_TRACE(p, t, id, j)                                                                 \
     do {                                                                                         \
-        if ((p).dbg && blockIdx.x == 0 && (t).hq == 0 && (t).b == 0 && (j) < 256)               \
-            reinterpret_cast<unsigned long long *>((p).dbg + 61440)[(id) * 256 + (j)] = clock64(); \
+        if ((p).dbg && (t).trace && (t).g0 + (j) < 256)                                         \
+            reinterpret_cast<unsigned long long *>((p).dbg + 61440)[(id) * 256 + (t).g0 + (j)] =  \
+                clock64();                                                                       \
     } while (0)
 #else
 #define SATTN_TRACE(p, t, id, j) \
@@ -185,74 +193,166 @@ struct Waiter {
     }
 };
 
+// Bytes `byte`, `byte + 1` of `word` (INT8 codes) -> FP16 pair, exactly: with
+// u = x + 128 (the code with its top bit flipped), the FP16 pattern 0x6400 | u
+// is 1024 + u, and subtracting 1152 leaves x.  One byte permute and one packed
+// FP16 subtract per pair, both on the fast pipes (integer-to-FP16 conversion
+// instructions run on the quarter-rate unit).
 __device__ __forceinline__ uint32_t f16x2_of_i8(uint32_t word, int byte)
 {
-    const int lo = static_cast<int8_t>((word >> (8 * byte)) & 0xffu);
-    const int hi = static_cast<int8_t>((word >> (8 * byte + 8)) & 0xffu);
-    const __half2 h = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
-    uint32_t u;
-    memcpy(&u, &h, sizeof u);
-    return u;
+    const uint32_t u = __byte_perm(word ^ 0x80808080u, 0x64646464u, byte == 0 ? 0x5140u : 0x7362u);
+    uint32_t h;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h) : "r"(u), "r"(0x64806480u));
+    return h;
 }
 
 struct Tile {
     int b, hq, hk, q0, ntiles, mask_from;
+    bool trace;   // debug builds: clock stamps of this CTA's items are recorded
+    int g0;       // debug builds: index of the item's first KV tile among the CTA's tiles
 };
 
+// floor(x / d) for 0 <= x < 2^31 and 1 <= d < 2^31, with m = floor((2^64 - 1) / d) + 1
+// (m = 0 for d = 1): x * m / 2^64 exceeds x / d by less than 2^-33, and the
+// fractional part of x / d is at most 1 - 1/d < 1 - 2^-31, so the floor is
+// exact.  A multiply-high replaces the reciprocal-based integer division,
+// whose reciprocal would queue behind the softmax exponentials.
+__device__ __forceinline__ int udiv(int x, int d, unsigned long long m)
+{
+    return d == 1 ? x : static_cast<int>(__umul64hi(static_cast<unsigned long long>(x), m));
+}
+
+// Work item `it` of [0, n_items): query tiles in decreasing order (with a
+// causal mask the last rows visit the most KV tiles, so the longest items are
+// scheduled first), then heads, then batches.  Every item has at least one KV
+// tile: a causal mask requires Nq <= Nkv, so each row keeps key 0.
+__device__ __forceinline__ Tile item_tile(const FwdParams &p, int it)
+{
+    Tile t;
+    const int hb = p.Hq * p.B;
+    const int qi = udiv(it, hb, p.m_hb);
+    const int qt = p.n_qtiles - 1 - qi;
+    const int rem = it - qi * hb;
+    t.b = udiv(rem, p.Hq, p.m_hq);
+    t.hq = rem - t.b * p.Hq;
+    t.hk = udiv(t.hq, p.group, p.m_group);
+    t.q0 = qt * BM;
+    const int off = p.Nkv - p.Nq;
+    int kv_end = p.Nkv;
+    if (p.causal)
+        kv_end = min(p.Nkv, min(t.q0 + BM, p.Nq) + off);
+    t.ntiles = (kv_end + BN - 1) / BN;
+    t.mask_from = p.Nkv / BN;                                  // tiles holding keys >= Nkv
+    if (p.causal)
+        t.mask_from = min(t.mask_from, (t.q0 + off + 1) / BN); // tiles crossing row q0's diagonal
+    t.trace = (blockIdx.x == 0);
+    t.g0 = 0;
+    return t;
+}
+
+// TMA producer.  The K stage and V slot rings run on one tile counter over all
+// items of the CTA, so loads of the next item start as soon as slots free up.
 __device__ __forceinline__ void producer_role(const FwdParams &p, const CUtensorMap *tm_k,
-                                              const CUtensorMap *tm_v, uint32_t sb, const Tile &t, int bhk,
+                                              const CUtensorMap *tm_v, const CUtensorMap *tm_q, uint32_t sb,
                                               const Waiter &wt)
 {
     auto bar = [sb](int i) { return sb + OFF_BAR + 8u * i; };
     ptx::prefetch_tensormap(tm_k);
     ptx::prefetch_tensormap(tm_v);
-    int issued_k = -1, issued_v = -1;
+    ptx::prefetch_tensormap(tm_q);
+    // INT8 Q tile of item `tq` into the staging buffer, and its V channel
+    // scales into slot nq % 3 (the final conversion of item nq - 3, the last
+    // reader of that slot, ends before QFULL of item nq - 1 is arrived)
+    auto load_q = [&](const Tile &tq, int nq) {
+        ptx::mbar_arrive_expect_tx(bar(QSTAGE), QS_BYTES + SV_BYTES);
+        ptx::tma_load_3d(sb + OFF_QS, tm_q, bar(QSTAGE), 0, tq.q0, tq.b * p.Hq + tq.hq);
+        ptx::bulk_load(sb + OFF_SV + (nq % 3) * SV_BYTES, p.v_scales + static_cast<size_t>(tq.b * p.Hkv + tq.hk) * HD,
+                       SV_BYTES, bar(QSTAGE));
+    };
+    int issued_k = -1, issued_v = -1, issued_q = -1;
     bool ok = true;
-    for (int j = 0; j < t.ntiles && ok; ++j) {
-        const int ks = j % KSTAGES;
-        if (!wt.wait(bar(KEMPTY + ks), ((j / KSTAGES) & 1) ^ 1, SITE_KE)) {
-            ok = false;
-            break;
+    int g = 0, n = 0;   // KV tiles and items of this CTA before the current item
+    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++n) {
+        Tile t = item_tile(p, it);
+        t.g0 = g;
+        const int bhk = t.b * p.Hkv + t.hk;
+        if (n == 0) {
+            load_q(t, 0);
+            issued_q = 0;
         }
-        const uint32_t kdst = sb + OFF_K + ks * K_STAGE_BYTES;
-        ptx::mbar_arrive_expect_tx(bar(KFULL + ks), K_STAGE_BYTES);
-        ptx::tma_load_3d(kdst, tm_k, bar(KFULL + ks), 0, j * BN, bhk);
-        ptx::tma_load_3d(kdst + K_HALF_BYTES, tm_k, bar(KFULL + ks), 64, j * BN, bhk);
-        SATTN_TRACE(p, t, 11, j);
-        issued_k = j;
-        for (int h = 0; h < 2; ++h) {
-            const int u = 2 * j + h, vs = u % VSLOTS;
-            if (!wt.wait(bar(VEMPTY + vs), ((u / VSLOTS) & 1) ^ 1, SITE_VE)) {
+        for (int j = 0; j < t.ntiles; ++j) {
+            const int gj = g + j, ks = gj % KSTAGES;
+            if (!wt.wait(bar(KEMPTY + ks), ((gj / KSTAGES) & 1) ^ 1, SITE_KE)) {
                 ok = false;
                 break;
             }
-            ptx::mbar_arrive_expect_tx(bar(VFULL + vs), V_TMA_BYTES);
-            ptx::tma_load_3d(sb + OFF_V + vs * V_SLOT_BYTES, tm_v, bar(VFULL + vs), j * BN + 128 * h, 0, bhk);
-            issued_v = u;
+            const uint32_t kdst = sb + OFF_K + ks * K_STAGE_BYTES;
+            ptx::mbar_arrive_expect_tx(bar(KFULL + ks), K_STAGE_BYTES);
+            ptx::tma_load_3d(kdst, tm_k, bar(KFULL + ks), 0, j * BN, bhk);
+            ptx::tma_load_3d(kdst + K_HALF_BYTES, tm_k, bar(KFULL + ks), 64, j * BN, bhk);
+            SATTN_TRACE(p, t, 11, j);
+            issued_k = gj;
+            for (int h = 0; h < 2; ++h) {
+                const int u = 2 * gj + h, vs = u % VSLOTS;
+                if (!wt.wait(bar(VEMPTY + vs), ((u / VSLOTS) & 1) ^ 1, SITE_VE)) {
+                    ok = false;
+                    break;
+                }
+                ptx::mbar_arrive_expect_tx(bar(VFULL + vs), V_TMA_BYTES);
+                ptx::tma_load_3d(sb + OFF_V + vs * V_SLOT_BYTES, tm_v, bar(VFULL + vs), j * BN + 128 * h, 0, bhk);
+                issued_v = u;
+            }
+            if (!ok)
+                break;
+            SATTN_TRACE(p, t, 12, j);
+            // after the first tile's loads: once this item's Q has left the
+            // staging buffer (QFULL), stage the next item's Q
+            const int nx = it + static_cast<int>(gridDim.x);
+            if (j == 0 && nx < p.n_items) {
+                if (!wt.wait(bar(QFULL), n & 1, SITE_QE)) {
+                    ok = false;
+                    break;
+                }
+                load_q(item_tile(p, nx), n + 1);
+                issued_q = n + 1;
+            }
         }
-        SATTN_TRACE(p, t, 12, j);
+        g += t.ntiles;
     }
     if (!ok) {
         for (int j = max(0, issued_k - KSTAGES + 1); j <= issued_k; ++j)
             wt.drain(bar(KFULL + j % KSTAGES), (j / KSTAGES) & 1);
         for (int u = max(0, issued_v - VSLOTS + 1); u <= issued_v; ++u)
             wt.drain(bar(VFULL + u % VSLOTS), (u / VSLOTS) & 1);
+        if (issued_q >= 0)
+            wt.drain(bar(QSTAGE), issued_q & 1);
     }
 }
 
-__device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32_t tmem, const Tile &t,
-                                         const Waiter &wt)
+// Single MMA-issuing thread.  Per item: wait for Q in TMEM, then S_j = Q K_j^T
+// followed by PV_{j-1}; the last PV of an item is issued before the first QK
+// of the next one.
+__device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32_t tmem, const Waiter &wt)
 {
     auto bar = [sb](int i) { return sb + OFF_BAR + 8u * i; };
-    if (wt.wait(bar(QFULL), 0, SITE_Q)) {
+    bool ok = true;
+    int g = 0, n = 0;
+    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++n) {
+        Tile t = item_tile(p, it);
+        t.g0 = g;
+        SATTN_TRACE(p, t, 39, 0);
+        if (!wt.wait(bar(QFULL), n & 1, SITE_Q))
+            break;
+        SATTN_TRACE(p, t, 40, 0);
         ptx::tc_fence_after();
-        for (int j = 0; j <= t.ntiles; ++j) {
+        for (int j = 0; j <= t.ntiles && ok; ++j) {
             if (j < t.ntiles) {                     // S_j = Q K_j^T (256 keys)
-                const int ks = j % KSTAGES;
-                if (!wt.wait(bar(KFULL + ks), (j / KSTAGES) & 1, SITE_K))
+                const int gj = g + j, ks = gj % KSTAGES;
+                if (!wt.wait(bar(KFULL + ks), (gj / KSTAGES) & 1, SITE_K) ||
+                    (gj >= 1 && !wt.wait(bar(SFREE), (gj - 1) & 1, SITE_SFREE))) {
+                    ok = false;
                     break;
-                if (j >= 1 && !wt.wait(bar(SFREE), (j - 1) & 1, SITE_SFREE))
-                    break;
+                }
                 ptx::tc_fence_after();
                 SATTN_TRACE(p, t, 8, j);
                 const uint32_t kb = sb + OFF_K + ks * K_STAGE_BYTES;
@@ -267,21 +367,21 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
                 SATTN_TRACE(p, t, 4, j);
             }
             if (j >= 1) {                           // PV_{j-1} = P_{j-1} V_{j-1}
-                const int jj = j - 1, pbuf = jj & 1;
-                if (!wt.wait(bar(PFULL + pbuf), (jj >> 1) & 1, SITE_P))
+                const int gg = g + j - 1, pbuf = gg & 1;
+                if (!wt.wait(bar(PFULL + pbuf), (gg >> 1) & 1, SITE_P) ||
+                    !wt.wait(bar(PVEMPTY), (gg & 1) ^ 1, SITE_PVE)) {
+                    ok = false;
                     break;
-                if (!wt.wait(bar(PVEMPTY), (jj & 1) ^ 1, SITE_PVE))
-                    break;
-                bool ok = true;
+                }
                 for (int h = 0; h < 2 && ok; ++h) {
-                    const int u = 2 * jj + h, vs = u % VSLOTS;
+                    const int u = 2 * gg + h, vs = u % VSLOTS;
                     if (!wt.wait(bar(VFULL + vs), (u / VSLOTS) & 1, SITE_V)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
                     if (h == 0)
-                        SATTN_TRACE(p, t, 5, jj);
+                        SATTN_TRACE(p, t, 5, j - 1);
                     const uint32_t vb = sb + OFF_V + vs * V_SLOT_BYTES;
                     const uint32_t pb = sb + OFF_P + pbuf * P_BUF_BYTES + h * P_HALF_BYTES;
 #pragma unroll
@@ -292,11 +392,12 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
                 }
                 if (!ok)
                     break;
-                SATTN_TRACE(p, t, 10, jj);
+                SATTN_TRACE(p, t, 10, j - 1);
                 ptx::mma_commit(bar(PVFULL));
                 ptx::mma_commit(bar(PDONE + pbuf));
             }
         }
+        g += t.ntiles;
     }
     // every MMA of this CTA has finished before the TMEM is released
     ptx::mma_commit(bar(MMADONE));
@@ -308,68 +409,79 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
 // 128-byte swizzle); the row max is exchanged through shared memory under a
 // named barrier, so both halves hold the same running max m and alpha.  Half
 // h also owns RO columns [64h, 64h + 64): after writing P_j it folds the
-// partial PV_{j-1} into RO with alpha_{j-1} (both halves keep d).
+// partial PV_{j-1} into RO with alpha_{j-1} (both halves keep d).  Between two
+// items the warps write the next item's Q into TMEM (free once the last QK of
+// the current item has completed) before the last fold and the final
+// conversion, so the next QK overlaps them.
 __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, uint8_t *smem,
-                                             uint32_t tmem, int warp, int lane, const Tile &t,
-                                             const Waiter &wt)
+                                             uint32_t tmem, int warp, int lane, const Waiter &wt)
 {
     auto bar = [sb](int i) { return sb + OFF_BAR + 8u * i; };
     const int half = warp >> 2;                               // 0 or 1
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;                        // query row in the tile = TMEM lane
     const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int i = t.q0 + r;
-
-    // Q codes 64h .. 64h+63 of row i -> FP16 carrier -> TMEM columns [TM_Q + 32h, TM_Q + 32h + 32)
-    {
-        uint32_t h[32];
-        if (i < p.nq32) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                p.q_codes + (static_cast<size_t>(t.b * p.Hq + t.hq) * p.nq32 + i) * HD + 64 * half);
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const uint4 a = src[w];
-                const uint32_t words[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    h[w * 8 + e * 2] = f16x2_of_i8(words[e], 0);
-                    h[w * 8 + e * 2 + 1] = f16x2_of_i8(words[e], 2);
-                }
-            }
-        } else {
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-                h[c] = 0u;
-        }
-        ptx::tmem_st32(taddr + TM_Q + 32 * half, h);
-        ptx::tmem_wait_st();
-    }
-    ptx::tc_fence_before();
-    ptx::mbar_arrive(bar(QFULL));
-
-    const float sq = (i < p.nq32) ? p.q_scales[static_cast<size_t>(t.b * p.Hq + t.hq) * p.nbq + i / kQBlock]
-                                  : 0.0f;
-    const int lim = p.causal ? i + (p.Nkv - p.Nq) : 0x7fffffff;   // last kept key of row i
-    const float *ksc = p.k_scales + static_cast<size_t>(t.b * p.Hkv + t.hk) * p.nbk;
     float *maxx = reinterpret_cast<float *>(smem + OFF_MAXX);
-    uint8_t *prow0 = smem + OFF_P + half * P_HALF_BYTES + r * 128;  // this row's 128 P8 bytes (buffer 0)
+    const float *svs = reinterpret_cast<const float *>(smem + OFF_SV);   // [item % 3][128] V channel scales
     constexpr float kLog2_448 = 8.8073549220576041f;          // log2(448): P is stored as p * 448
-    float m = -INFINITY;
-    float ro[64];
-#pragma unroll
-    for (int c = 0; c < 64; ++c)
-        ro[c] = 0.0f;
-    float d = 0.0f, alpha_prev = 0.0f;
 
-    // RO = RO * alpha + PV partial of tile jj (this half's 64 channels), d likewise
-    auto fold_partial = [&](int jj, float alpha) -> bool {
-        if (!wt.wait(bar(PVFULL), jj & 1, SITE_PV))
+    // Q codes 64h .. 64h+63 of row r of the staged item (16-byte chunk c of
+    // row r sits at chunk c ^ (r % 8)) -> FP16 carrier -> TMEM columns
+    // [TM_Q + 32h, TM_Q + 32h + 32), 8 columns at a time; then QFULL
+    auto store_q = [&](int nq) -> bool {
+        if (!wt.wait(bar(QSTAGE), nq & 1, SITE_QS))
+            return false;
+        const uint8_t *qrow = smem + OFF_QS + r * HD;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(qrow + (((4 * half + w) ^ (r & 7)) << 4));
+            const uint32_t words[4] = {a.x, a.y, a.z, a.w};
+            uint32_t h[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                h[e * 2] = f16x2_of_i8(words[e], 0);
+                h[e * 2 + 1] = f16x2_of_i8(words[e], 2);
+            }
+            ptx::tmem_st8(taddr + TM_Q + 32 * half + 8 * w, h);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(QFULL));
+        return true;
+    };
+    auto qscale = [&](const Tile &tq) {
+        const int i = tq.q0 + r;
+        return i < p.nq32 ? p.q_scales[static_cast<size_t>(tq.b * p.Hq + tq.hq) * p.nbq + i / kQBlock] : 0.0f;
+    };
+    // block scales of this half's four 32-key blocks of tile j of an item
+    auto kscale = [&](const Tile &tk, int j, int c) {
+        const int kb = j * (BN / kQBlock) + 4 * half + c;
+        return kb < p.nbk ? p.k_scales[static_cast<size_t>(tk.b * p.Hkv + tk.hk) * p.nbk + kb] : 0.0f;
+    };
+
+    int it = blockIdx.x;
+    Tile t = item_tile(p, it);
+    if (!store_q(0))
+        return;
+    if (r == 0 && half == 0)
+        SATTN_TRACE(p, t, 38, 1);
+    float sq = qscale(t);
+    float sk[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        sk[c] = kscale(t, 0, c);
+
+    float ro[64];
+    float m, d, alpha_prev;
+    // RO = RO * alpha + PV partial of global tile gg (this half's 64 channels), d likewise
+    auto fold_partial = [&](int gg, int jl, const Tile &tt, float alpha) -> bool {
+        if (!wt.wait(bar(PVFULL), gg & 1, SITE_PV))
             return false;
         ptx::tc_fence_after();
         if (r == 0 && half == 0)
-            SATTN_TRACE(p, t, 6, jj);
+            SATTN_TRACE(p, tt, 6, jl);
 #ifdef SATTN_DEBUG_DUMP
-        if (p.dbg && jj == 0 && t.q0 == 0 && t.hq == 0 && t.b == 0 && half == 0) {
+        if (p.dbg && jl == 0 && tt.q0 == 0 && tt.hq == 0 && tt.b == 0 && half == 0) {
             for (int c = 0; c < static_cast<int>(PV_N); ++c) {
                 uint32_t x;
                 ptx::tmem_ld1(taddr + TM_PV + c, x);
@@ -390,61 +502,90 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
             ro[c] = fmaf(ro[c], alpha, __uint_as_float(part[c >> 5][c & 31]));
         d = fmaf(d, alpha, __uint_as_float(ds));
         if (r == 0 && half == 0)
-            SATTN_TRACE(p, t, 7, jj);
+            SATTN_TRACE(p, tt, 7, jl);
         return true;
     };
 
-    // block scales of this half's four 32-key blocks, one tile ahead
-    auto kscale = [&](int j, int c) {
-        const int kb = j * (BN / kQBlock) + 4 * half + c;
-        return kb < p.nbk ? ksc[kb] : 0.0f;
-    };
-    float sk[4];
+    int g = 0, n = 0;   // KV tiles and items of this CTA before the current item
+    for (;;) {
+        t.g0 = g;
+        const int i = t.q0 + r;
+        const int lim = p.causal ? i + (p.Nkv - p.Nq) : 0x7fffffff;   // last kept key of row i
+        const int nx = it + static_cast<int>(gridDim.x);
+        const bool has_next = nx < p.n_items;
+        // (the next item's tile is recomputed where needed rather than kept live)
+        const float sq_next = has_next ? qscale(item_tile(p, nx)) : 0.0f;
+        m = -INFINITY;
+        d = 0.0f;
+        alpha_prev = 0.0f;
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-        sk[c] = kscale(0, c);
+        for (int c = 0; c < 64; ++c)
+            ro[c] = 0.0f;
 
-    for (int j = 0; j < t.ntiles; ++j) {
-        float sig[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            sig[c] = __fmul_rn(__fmul_rn(sq, sk[c]), p.c0);
-            sk[c] = kscale(j + 1, c);
-        }
-        if (!wt.wait(bar(SFULL), j & 1, SITE_S))
-            return;
-        ptx::tc_fence_after();
         if (r == 0 && half == 0)
-            SATTN_TRACE(p, t, 0, j);
-        uint32_t s[4][32];
+            SATTN_TRACE(p, t, 39, 1);
+        for (int j = 0; j < t.ntiles; ++j) {
+            const int gj = g + j;
+            float sig[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            ptx::tmem_ld32(taddr + TM_S + static_cast<uint32_t>(128 * half + 32 * c), s[c]);
-        ptx::tmem_wait_ld();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(SFREE));                          // S may be overwritten now
-        if (r == 0 && half == 0)
-            SATTN_TRACE(p, t, 1, j);
+            for (int c = 0; c < 4; ++c) {
+                sig[c] = __fmul_rn(__fmul_rn(sq, sk[c]), p.c0);
+                if (j + 1 < t.ntiles)
+                    sk[c] = kscale(t, j + 1, c);
+            }
+            if (j + 1 == t.ntiles && has_next) {
+                const Tile tn = item_tile(p, nx);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    sk[c] = kscale(tn, 0, c);
+            }
+            if (r == 0 && half == 0 && j == 0)
+                SATTN_TRACE(p, t, 40, 1);
+            if (!wt.wait(bar(SFULL), gj & 1, SITE_S))
+                return;
+            ptx::tc_fence_after();
+            if (r == 0 && half == 0)
+                SATTN_TRACE(p, t, 0, j);
+            uint32_t s[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                ptx::tmem_ld32(taddr + TM_S + static_cast<uint32_t>(128 * half + 32 * c), s[c]);
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(SFREE));                          // S may be overwritten now
+            if (r == 0 && half == 0)
+                SATTN_TRACE(p, t, 1, j);
+            if ((r & 31) == 0)
+                SATTN_TRACE(p, t, 29 + 4 * half + (r >> 5), j);
 #ifdef SATTN_DEBUG_DUMP
-        if (p.dbg && j == 0 && t.q0 == 0 && t.hq == 0 && t.b == 0)
-            for (int k = 0; k < 128; ++k)
-                p.dbg[r * BN + 128 * half + k] = __uint_as_float(s[k >> 5][k & 31]);
+            if (p.dbg && j == 0 && t.q0 == 0 && t.hq == 0 && t.b == 0)
+                for (int k = 0; k < 128; ++k)
+                    p.dbg[r * BN + 128 * half + k] = __uint_as_float(s[k >> 5][k & 31]);
 #endif
-        // keys of this half that row i keeps: the first `nvalid` (the mask is a
-        // suffix of the half-tile: keys >= Nkv and, if causal, keys > lim)
-        const bool masked = j >= t.mask_from;
-        int nvalid = 128;
-        if (masked) {
-            const int lo = j * BN + 128 * half;
-            nvalid = max(0, min(128, min(p.Nkv - 1, lim) - lo + 1));
-        }
-        // max of the raw accumulators per 32-key block: the block scale is
-        // positive (or zero), so fl(max(acc) * sig) = max(fl(acc * sig)) exactly
-        float tmax = -INFINITY;
+            // keys of this half that row i keeps are the first `nvalid` (the mask
+            // is a suffix of the half-tile: keys >= Nkv and, if causal, keys >
+            // lim).  Only the last tiles of an item carry masked keys; there the
+            // masked scores are set to -inf before both passes, so one copy of
+            // each pass serves all tiles.  On such tiles the combined scale is
+            // raised to at least FLT_MIN so that -inf * scale stays -inf; a scale
+            // below FLT_MIN moves an integer score by less than 1e-31, which no
+            // later rounding sees.
+            if (j >= t.mask_from) {
+                const int lo = j * BN + 128 * half;
+                const int nvalid = max(0, min(128, min(p.Nkv - 1, lim) - lo + 1));
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float b;
-            if (!masked) {
+                for (int c = 0; c < 4; ++c) {
+                    sig[c] = fmaxf(sig[c], FLT_MIN);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        s[c][k] = (32 * c + k < nvalid) ? s[c][k] : 0xff800000u;
+                }
+            }
+            // max of the raw accumulators per 32-key block: the block scale is
+            // positive (or zero), so fl(max(acc) * sig) = max(fl(acc * sig)) exactly
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
                 // eight independent three-input max chains, then a short tree
                 float q[8];
 #pragma unroll
@@ -454,40 +595,33 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
 #pragma unroll
                 for (int a = 0; a < 8; ++a)
                     q[a] = fmaxf(q[a], __uint_as_float(s[c][a + 24]));
-                b = fmaxf(ptx::fmax3(q[0], q[1], q[2]), ptx::fmax3(q[3], q[4], q[5]));
+                float b = fmaxf(ptx::fmax3(q[0], q[1], q[2]), ptx::fmax3(q[3], q[4], q[5]));
                 b = ptx::fmax3(b, q[6], q[7]);
-            } else {
-                float q[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    q[k & 3] = fmaxf(q[k & 3], 32 * c + k < nvalid ? __uint_as_float(s[c][k]) : -INFINITY);
-                b = fmaxf(fmaxf(q[0], q[1]), fmaxf(q[2], q[3]));
+                tmax = fmaxf(tmax, __fmul_rn(b, sig[c]));
             }
-            tmax = fmaxf(tmax, (b == -INFINITY) ? -INFINITY : __fmul_rn(b, sig[c]));
-        }
-        // exchange the half-row maxima (double-buffered by tile parity)
-        maxx[((j & 1) * 2 + half) * BM + r] = tmax;
-        ptx::named_bar_sync(1, 2 * BM);
-        tmax = fmaxf(tmax, maxx[((j & 1) * 2 + (half ^ 1)) * BM + r]);
-        if (r == 0 && half == 0)
-            SATTN_TRACE(p, t, 2, j);
+            // exchange the half-row maxima (double-buffered by tile parity)
+            maxx[((gj & 1) * 2 + half) * BM + r] = tmax;
+            if ((r & 31) == 0)
+                SATTN_TRACE(p, t, 21 + 4 * half + (r >> 5), j);
+            ptx::named_bar_sync(1, 2 * BM);
+            tmax = fmaxf(tmax, maxx[((gj & 1) * 2 + (half ^ 1)) * BM + r]);
+            if (r == 0 && half == 0)
+                SATTN_TRACE(p, t, 2, j);
 
-        const float mn = fmaxf(m, tmax);
-        const float alpha = (m == -INFINITY) ? 0.0f : ptx::ex2_approx(__fsub_rn(m, mn));
-        const float nb = kLog2_448 - mn;                     // exponent offset of p * 448
+            const float mn = fmaxf(m, tmax);
+            const float alpha = (m == -INFINITY) ? 0.0f : ptx::ex2_approx(__fsub_rn(m, mn));
+            // exponent offset of p * 448; a row with no kept key so far has
+            // mn = -inf and only -inf scores, which any finite offset maps to 0
+            const float nb = (mn == -INFINITY) ? 0.0f : kLog2_448 - mn;
 
-        // P buffer j % 2 is free once PV_{j-2} has read it
-        const int pbuf = j & 1;
-        uint8_t *prow = prow0 + pbuf * P_BUF_BYTES;
-        if (j >= 2 && !wt.wait(bar(PDONE + pbuf), ((j >> 1) - 1) & 1, SITE_PDONE))
-            return;
-        // P8 = E4M3(exp2(acc * sig - m') * 448), four keys per 32-bit word,
-        // stored 32 keys at a time (16-byte chunk c of the row lands at chunk
-        // c ^ (row % 8): the 128-byte swizzle of the K-major operand).  The
-        // masked and unmasked forms are separate copies so that the common,
-        // unmasked tiles carry no per-key select.
-        auto write_p = [&](auto masked_tag) {
-            constexpr bool kMasked = decltype(masked_tag)::value;
+            // P buffer gj % 2 is free once the PV two tiles back has read it
+            const int pbuf = gj & 1;
+            uint8_t *prow = smem + OFF_P + pbuf * P_BUF_BYTES + half * P_HALF_BYTES + r * 128;
+            if (gj >= 2 && !wt.wait(bar(PDONE + pbuf), ((gj >> 1) - 1) & 1, SITE_PDONE))
+                return;
+            // P8 = E4M3(exp2(acc * sig - m') * 448), four keys per 32-bit word,
+            // stored 32 keys at a time (16-byte chunk c of the row lands at chunk
+            // c ^ (row % 8): the 128-byte swizzle of the K-major operand)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t pk[8];
@@ -495,13 +629,8 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
                 for (int w = 0; w < 8; ++w) {
                     float e[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int k = 4 * w + u;
-                        float x = fmaf(__uint_as_float(s[c][k]), sig[c], nb);
-                        if (kMasked)
-                            x = (32 * c + k < nvalid) ? x : -INFINITY;
-                        e[u] = ptx::ex2_approx(x);
-                    }
+                    for (int u = 0; u < 4; ++u)
+                        e[u] = ptx::ex2_approx(fmaf(__uint_as_float(s[c][4 * w + u]), sig[c], nb));
                     pk[w] = ptx::cvt_e4m3x4(e[0], e[1], e[2], e[3]);
                 }
 #ifdef SATTN_DEBUG_DUMP
@@ -514,69 +643,87 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
                 *reinterpret_cast<uint4 *>(prow + (((2 * c + 1) ^ (r & 7)) << 4)) =
                     make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
-        };
-        if (masked)
-            write_p(std::true_type{});
-        else
-            write_p(std::false_type{});
-        ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(bar(PFULL + pbuf));
-        if (r == 0 && half == 0)
-            SATTN_TRACE(p, t, 3, j);
-        if (j >= 1 && !fold_partial(j - 1, alpha_prev))
-            return;
-        alpha_prev = alpha;
-        m = mn;
-    }
-    if (t.ntiles > 0 && !fold_partial(t.ntiles - 1, alpha_prev))
-        return;
-
-    // final conversion: reciprocal of d, per-channel V scale, BF16
-    if (i < p.Nq) {
-        const float rcp = d > 0.0f ? __frcp_rn(d) : 0.0f;
-        const float *sv = p.v_scales + static_cast<size_t>(t.b * p.Hkv + t.hk) * HD + 64 * half;
-        uint4 *dst = reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(t.b * p.Hq + t.hq) * p.Nq + i) * HD +
-                                               64 * half);
-#pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            uint32_t u[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int c = 8 * w + 2 * e;
-                const float o0 = __fmul_rn(__fmul_rn(ro[c], rcp), sv[c]);
-                const float o1 = __fmul_rn(__fmul_rn(ro[c + 1], rcp), sv[c + 1]);
-                const __nv_bfloat162 pr = __floats2bfloat162_rn(o0, o1);
-                memcpy(&u[e], &pr, sizeof(uint32_t));
-            }
-            dst[w] = make_uint4(u[0], u[1], u[2], u[3]);
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(bar(PFULL + pbuf));
+            if (r == 0 && half == 0)
+                SATTN_TRACE(p, t, 3, j);
+            if ((r & 31) == 0)
+                SATTN_TRACE(p, t, 13 + 4 * half + (r >> 5), j);
+            // after the last P of this item its last QK has completed (its S was
+            // read above), so the Q columns of TMEM can take the next item's Q
+            if (j == t.ntiles - 1 && has_next && !store_q(n + 1))
+                return;
+            if (j >= 1 && !fold_partial(gj - 1, j - 1, t, alpha_prev))
+                return;
+            alpha_prev = alpha;
+            m = mn;
         }
+        if (!fold_partial(g + t.ntiles - 1, t.ntiles - 1, t, alpha_prev))
+            return;
+
+        if (r == 0 && half == 0)
+            SATTN_TRACE(p, t, 39, 2);
+        // final conversion: reciprocal of d, per-channel V scale, BF16.  Each
+        // warp stages its 32 rows x 64 channels (4 KB, 16-byte chunk c of row
+        // l at chunk c ^ (l % 8)) in the P buffer of this item's last tile (its
+        // PV has completed) and then writes whole 128-byte row segments, eight
+        // threads per row, instead of one 16-byte piece per row per store.
+        {
+            const float rcp = d > 0.0f ? __frcp_rn(d) : 0.0f;
+            const float *sv = svs + (n % 3) * HD + 64 * half;   // landed with this item's Q
+            uint8_t *stage = smem + OFF_P + ((g + t.ntiles - 1) & 1) * P_BUF_BYTES + (quarter * 2 + half) * 4096;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                uint32_t u[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = 8 * w + 2 * e;
+                    const float o0 = __fmul_rn(__fmul_rn(ro[c], rcp), sv[c]);
+                    const float o1 = __fmul_rn(__fmul_rn(ro[c + 1], rcp), sv[c + 1]);
+                    const __nv_bfloat162 pr = __floats2bfloat162_rn(o0, o1);
+                    memcpy(&u[e], &pr, sizeof(uint32_t));
+                }
+                *reinterpret_cast<uint4 *>(stage + lane * 128 + ((w ^ (lane & 7)) << 4)) =
+                    make_uint4(u[0], u[1], u[2], u[3]);
+            }
+            __syncwarp();
+            const int ch = lane & 7;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int l = 4 * k + (lane >> 3);                     // row of the warp's 32
+                const int row = t.q0 + quarter * 32 + l;
+                const uint4 v = *reinterpret_cast<const uint4 *>(stage + l * 128 + ((ch ^ (l & 7)) << 4));
+                if (row < p.Nq)
+                    *reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(t.b * p.Hq + t.hq) * p.Nq + row) * HD +
+                                               64 * half + 8 * ch) = v;
+            }
+            __syncwarp();
+        }
+        if (r == 0 && half == 0)
+            SATTN_TRACE(p, t, 38, 2);
+        g += t.ntiles;
+        ++n;
+        if (!has_next)
+            break;
+        it = nx;
+        t = item_tile(p, nx);
+        sq = sq_next;
     }
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                    const FwdParams p)
+                    const __grid_constant__ CUtensorMap tm_q, const FwdParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     const uint32_t sb = ptx::smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    Tile t;
-    const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x);   // longest rows first
-    t.hq = blockIdx.y;
-    t.b = blockIdx.z;
-    t.hk = t.hq / p.group;
-    t.q0 = qt * BM;
-    const int off = p.Nkv - p.Nq;
-    int kv_end = p.Nkv;
-    if (p.causal)
-        kv_end = min(p.Nkv, min(t.q0 + BM, p.Nq) + off);
-    t.ntiles = (kv_end + BN - 1) / BN;
-    t.mask_from = p.Nkv / BN;                                  // tiles holding keys >= Nkv
-    if (p.causal)
-        t.mask_from = min(t.mask_from, (t.q0 + off + 1) / BN); // tiles crossing row q0's diagonal
+#ifdef SATTN_DEBUG_DUMP
+    if (p.dbg && threadIdx.x == 0 && blockIdx.x == 0)
+        reinterpret_cast<unsigned long long *>(p.dbg + 61440)[37 * 256 + 0] = clock64();
+#endif
     const Waiter wt{p.status};
     volatile uint32_t *flag = reinterpret_cast<volatile uint32_t *>(smem + OFF_FLAG);
 
@@ -591,6 +738,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ptx::mbar_init(b0 + 8u * (VFULL + s), 1);
             ptx::mbar_init(b0 + 8u * (VEMPTY + s), 1);
         }
+        ptx::mbar_init(b0 + 8u * QSTAGE, 1);
         ptx::mbar_init(b0 + 8u * QFULL, 2 * BM);
         ptx::mbar_init(b0 + 8u * SFULL, 1);
         ptx::mbar_init(b0 + 8u * SFREE, 2 * BM);
@@ -620,18 +768,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + OFF_TMEM_SLOT);
 
-    if (*flag == 0) {
+    if (*flag == 0 && static_cast<int>(blockIdx.x) < p.n_items) {
         if (warp < WARP_PRODUCER) {
             ptx::setmaxnreg_inc<kRegsCompute>();
-            compute_role(p, sb, smem, tmem, warp, lane, t, wt);
+            compute_role(p, sb, smem, tmem, warp, lane, wt);
         } else {
             ptx::setmaxnreg_dec<kRegsOther>();
             if (warp == WARP_PRODUCER) {
                 if (lane == 0)
-                    producer_role(p, &tm_k, &tm_v, sb, t, t.b * p.Hkv + t.hk, wt);
+                    producer_role(p, &tm_k, &tm_v, &tm_q, sb, wt);
             } else if (warp == WARP_MMA) {
                 if (lane == 0)
-                    mma_role(p, sb, tmem, t, wt);
+                    mma_role(p, sb, tmem, wt);
             }
             __syncwarp();
         }
@@ -642,6 +790,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
     }
+#ifdef SATTN_DEBUG_DUMP
+    if (p.dbg && threadIdx.x == 0 && blockIdx.x == 0)
+        reinterpret_cast<unsigned long long *>(p.dbg + 61440)[37 * 256 + 1] = clock64();
+#endif
 }
 
 // INT8 K codes -> FP16 carrier [B*Hkv][Nkv][128]; also clears the status words.
@@ -733,6 +885,19 @@ int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scal
             return 1;
     }
 
+    CUtensorMap tmq;
+    {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(g.nq32),
+                                    static_cast<cuuint64_t>(g.B) * g.Hq};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(g.nq32) * HD};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(HD), static_cast<cuuint32_t>(BM), 1};   // 128 rows x 128 codes
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (encode(&tmq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<int8_t *>(q_codes), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return 1;
+    }
+
     // The per-warpgroup register split only adds up when the kernel is launched
     // with exactly kLaunchRegs registers per thread; refuse to launch otherwise.
     static std::once_flag attr_once;
@@ -756,12 +921,21 @@ int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scal
     prm.v_scales = v_scales;
     prm.out = static_cast<__nv_bfloat16 *>(out);
     prm.status = status;
+    prm.B = g.B;
     prm.Hq = g.Hq;
     prm.Hkv = g.Hkv;
     prm.Nq = g.Nq;
     prm.Nkv = g.Nkv;
     prm.group = g.Hq / g.Hkv;
     prm.n_qtiles = static_cast<int>((g.Nq + BM - 1) / BM);
+    const int64_t n_items = static_cast<int64_t>(prm.n_qtiles) * g.Hq * g.B;
+    if (n_items >= (int64_t(1) << 31))
+        return static_cast<int>(cudaErrorInvalidValue);   // item indices must fit udiv's range
+    prm.n_items = static_cast<int>(n_items);
+    auto recip = [](int d) { return d == 1 ? 0ull : ~0ull / static_cast<unsigned long long>(d) + 1ull; };
+    prm.m_hb = recip(g.Hq * g.B);
+    prm.m_hq = recip(g.Hq);
+    prm.m_group = recip(prm.group);
     prm.causal = g.causal;
     prm.nq32 = static_cast<int>(g.nq32);
     prm.nbq = static_cast<int>(g.nbq);
@@ -772,7 +946,13 @@ int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scal
     prm.dbg = debug_dump_buffer();
 #endif
 
-    attn_fwd_kernel<<<dim3(prm.n_qtiles, g.Hq, g.B), NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, prm);
+    // persistent: one CTA per SM, each walking the items it, it + grid, ...
+    int dev = 0, n_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1)
+        return static_cast<int>(cudaErrorInvalidDevice);
+    const int grid = std::min(prm.n_items, n_sm);
+    attn_fwd_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, prm);
     return static_cast<int>(cudaGetLastError());
 }
 

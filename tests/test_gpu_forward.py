@@ -66,12 +66,23 @@ def test_forward_matches_oracle_sampled_rows(oracle_mod, name):
     (1, 1, 1, 1, 1, False), (1, 1, 1, 1, 1, True), (1, 2, 1, 31, 33, True),
     (1, 1, 1, 127, 129, False), (1, 1, 1, 129, 127, False), (1, 1, 1, 129, 129, True),
     (2, 4, 2, 200, 200, True), (2, 2, 2, 300, 1000, True), (1, 8, 2, 257, 640, False),
-    (1, 2, 2, 1000, 1000, True)])
+    (1, 2, 2, 1000, 1000, True), (1, 2, 1, 100, 356, True), (1, 1, 1, 127, 129, True),
+    (1, 1, 1, 1, 300, True), (1, 2, 2, 260, 520, True)])
 def test_forward_edge_shapes(oracle_mod, shape):
     B, Hq, Hkv, Nq, Nkv, causal = shape
     w = synth.workload("c1", B=B, Hq=Hq, Hkv=Hkv, Nq=Nq, Nkv=Nkv, causal=causal)
     q, k, v = synth.make_inputs(w, seed=2000 + Nq * 3 + Nkv)
     _full(oracle_mod, q, k, v, causal, str(shape))
+
+
+def test_forward_zero_query_block_on_masked_tiles(oracle_mod):
+    # a Q block of zeros has block scale 0, so its rows score 0 against every
+    # key, including on the causal tiles where masked keys must still weigh 0
+    w = synth.workload("c1", B=1, Hq=2, Hkv=1, Nq=300, Nkv=300, causal=True)
+    q, k, v = synth.make_inputs(w, seed=77)
+    q[:, :, 256:288] = 0
+    q[:, 1, 32:64] = 0
+    _full(oracle_mod, q, k, v, True, "zero query block")
 
 
 def test_forward_zero_inputs_give_zero(oracle_mod):
