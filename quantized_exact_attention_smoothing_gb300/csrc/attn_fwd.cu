@@ -4,32 +4,36 @@
 // "Phase 1 State-Ownership Decision": strict tile order, exact FP8 score bytes,
 // per-tile RO rescaling, two-level PV accumulation, final conversion).
 //
-// One CTA computes 128 query rows of one (batch, query head) and visits the
-// KV tiles of 256 keys in increasing order.  Twelve warps:
+// Persistent: one CTA per SM walks work items (128 query rows of one batch and
+// query head) longest first; each item visits its KV tiles of 256 keys in
+// increasing order.  Twelve warps:
 //   warps 0-7   two compute warpgroups, thread = query row = TMEM lane; half h
 //               owns keys [128h, 128h + 128) of every tile and output channels
 //               [64h, 64h + 64): score scaling, masks, running max m (exchanged
 //               between the halves), alpha, the FP8 P bytes (written to shared
-//               memory), then RO = RO * alpha + PV and d = d * alpha + sum p8
-//               for the previous tile, and the final conversion
-//   warp 8      TMA producer: K tiles (FP16 carrier of the INT8 codes) and V
-//               half-tiles (E4M3, channel-major): one K stage (the next tile
-//               loads while PV of the previous one runs) and a ring of four
-//               V half-tile slots
+//               memory), RO = RO * alpha + PV and d = d * alpha + sum p8 for the
+//               previous tile, the final conversion, and the FP16 carrier of
+//               the next item's Q (into TMEM)
+//   warp 8      K loader (TMA): K half-tiles (FP16 carrier of the INT8 codes,
+//               256 keys x 64 channels) into a ring of three slots
 //   warp 9      TMEM allocation and the single MMA-issuing thread:
 //                 S_j  = Q * K_j^T   tcgen05 kind::f16, A = Q from TMEM, N = 256
 //                 PV_j = P_j * V_j   tcgen05 kind::f8f6f4, A = P from shared
 //                                    memory, N = 144: V rows plus a row of ones
 //                                    whose column gives sum_j p8_j
-//   warps 10-11 idle
+//   warp 10     V and Q loader (TMA): V half-tiles (E4M3, channel-major) into
+//               two slots; the next item's INT8 Q tile and V channel scales
+//   warp 11     idle
 // Twelve warps launch at 168 registers each; setmaxnreg then gives the compute
-// warpgroups 232 (128 scores and 64 RO values per thread) and the
-// producer/MMA warpgroup 40.
+// warpgroups 232 (128 scores and 64 RO values per thread) and the loader/MMA
+// warpgroup 40.
 // Tensor memory (512 columns): S [0,256), PV partial [256,400), Q carrier
 // [448,512).  P is double-buffered in shared memory, so the softmax of tile
 // j + 1 never waits for PV of tile j.  A tcgen05.mma instruction costs about
 // the same time for any N up to 256 on this part, hence the 256-key tiles: QK
-// runs at N = 256.
+// runs at N = 256.  The K ring of half-tile slots lets the next tile's K land
+// while the current QK runs; a single full-tile K stage put the whole TMA
+// latency of every tile on the critical path.
 //
 // Exactness of QK: INT8 codes are carried as FP16 values (integers of
 // magnitude <= 127 are exact in FP16); every product is an integer <= 16129 and
@@ -56,9 +60,8 @@ namespace sattn {
 namespace {
 
 constexpr int BM = kQTile, BN = kKvTile, HD = kHeadDim;   // 128 rows x 256 keys
-constexpr int KSTAGES = 1, VSLOTS = 4;
+constexpr int KSLOTS = 3, VSLOTS = 2;                  // K half-tile slots, V half-tile slots
 constexpr uint32_t K_HALF_BYTES = BN * 64 * 2;          // 256 keys x 64 channels, FP16
-constexpr uint32_t K_STAGE_BYTES = 2 * K_HALF_BYTES;    // 64 KB
 constexpr uint32_t PV_N = 144;                          // V rows + ones row + zero rows
 constexpr uint32_t V_SLOT_BYTES = PV_N * 128;           // one 128-key half tile, 18 KB
 constexpr uint32_t V_TMA_BYTES = HD * 128;              // 16 KB loaded per half tile
@@ -68,9 +71,9 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;
 constexpr uint32_t TM_PV = 256;
 constexpr uint32_t TM_Q = 448;
-// warp roles: 0-7 compute (two warpgroups), 8 TMA producer, 9 MMA issuer and
-// TMEM owner, 10-11 idle
-constexpr int WARP_PRODUCER = 8, WARP_MMA = 9;
+// warp roles: 0-7 compute (two warpgroups), 8 K loader, 9 MMA issuer and TMEM
+// owner, 10 V and Q loader, 11 idle
+constexpr int WARP_PRODUCER = 8, WARP_MMA = 9, WARP_VLOAD = 10;
 constexpr int NTHREADS = 12 * 32;
 // Registers: launched at 168 per thread (384 x 168 = 64512), then rebalanced
 // per warpgroup; the shares add up to exactly the launch total.
@@ -83,7 +86,7 @@ constexpr uint64_t TIMEOUT_NS = 1000000000ull;
 
 // shared memory map, offsets from a 1024-byte aligned base
 constexpr uint32_t OFF_K = 0;
-constexpr uint32_t OFF_V = OFF_K + KSTAGES * K_STAGE_BYTES;
+constexpr uint32_t OFF_V = OFF_K + KSLOTS * K_HALF_BYTES;
 constexpr uint32_t OFF_P = OFF_V + VSLOTS * V_SLOT_BYTES;
 constexpr uint32_t OFF_QS = OFF_P + 2 * P_BUF_BYTES;        // INT8 Q tile of the next item (TMA, 128B swizzle)
 constexpr uint32_t QS_BYTES = BM * HD;
@@ -93,8 +96,8 @@ constexpr uint32_t SV_BYTES = HD * 4;
 constexpr uint32_t OFF_BAR = OFF_SV + 3 * SV_BYTES;
 enum Bar : int {
     KFULL = 0,
-    KEMPTY = KFULL + KSTAGES,
-    VFULL = KEMPTY + KSTAGES,
+    KEMPTY = KFULL + KSLOTS,
+    VFULL = KEMPTY + KSLOTS,
     VEMPTY = VFULL + VSLOTS,
     QSTAGE = VEMPTY + VSLOTS,   // INT8 Q codes of an item landed in shared memory
     QFULL = QSTAGE + 1,         // its FP16 carrier is in TMEM
@@ -250,14 +253,51 @@ __device__ __forceinline__ Tile item_tile(const FwdParams &p, int it)
     return t;
 }
 
-// TMA producer.  The K stage and V slot rings run on one tile counter over all
-// items of the CTA, so loads of the next item start as soon as slots free up.
-__device__ __forceinline__ void producer_role(const FwdParams &p, const CUtensorMap *tm_k,
-                                              const CUtensorMap *tm_v, const CUtensorMap *tm_q, uint32_t sb,
-                                              const Waiter &wt)
+// K loader.  Half-tile u = 2 * (tile) + h (channels [64h, 64h + 64) of the
+// tile's 256 keys) goes to slot u % 3; the ring runs on one tile counter over
+// all items of the CTA, so the next tile's halves load while QK of the current
+// one runs (each half slot is released as soon as the four MMAs reading it
+// complete).
+__device__ __forceinline__ void kload_role(const FwdParams &p, const CUtensorMap *tm_k, uint32_t sb,
+                                           const Waiter &wt)
 {
     auto bar = [sb](int i) { return sb + OFF_BAR + 8u * i; };
     ptx::prefetch_tensormap(tm_k);
+    int issued = -1;
+    bool ok = true;
+    int g = 0;   // KV tiles of the earlier items
+    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+        Tile t = item_tile(p, it);
+        t.g0 = g;
+        const int bhk = t.b * p.Hkv + t.hk;
+        for (int j = 0; j < t.ntiles && ok; ++j) {
+            for (int h = 0; h < 2; ++h) {
+                const int u = 2 * (g + j) + h, ks = u % KSLOTS;
+                if (!wt.wait(bar(KEMPTY + ks), ((u / KSLOTS) & 1) ^ 1, SITE_KE)) {
+                    ok = false;
+                    break;
+                }
+                ptx::mbar_arrive_expect_tx(bar(KFULL + ks), K_HALF_BYTES);
+                ptx::tma_load_3d(sb + OFF_K + ks * K_HALF_BYTES, tm_k, bar(KFULL + ks), 64 * h, j * BN, bhk);
+                issued = u;
+            }
+            SATTN_TRACE(p, t, 11, j);
+        }
+        g += t.ntiles;
+    }
+    if (!ok)
+        for (int u = max(0, issued - KSLOTS + 1); u <= issued; ++u)
+            wt.drain(bar(KFULL + u % KSLOTS), (u / KSLOTS) & 1);
+}
+
+// V and Q loader.  V half-tiles (128 keys x 128 channels, E4M3) go to the two
+// V slots; at the first tile of every item, once that item's Q has left the
+// staging buffer (QFULL), the next item's INT8 Q tile and V channel scales are
+// staged.
+__device__ __forceinline__ void vload_role(const FwdParams &p, const CUtensorMap *tm_v,
+                                           const CUtensorMap *tm_q, uint32_t sb, const Waiter &wt)
+{
+    auto bar = [sb](int i) { return sb + OFF_BAR + 8u * i; };
     ptx::prefetch_tensormap(tm_v);
     ptx::prefetch_tensormap(tm_q);
     // INT8 Q tile of item `tq` into the staging buffer, and its V channel
@@ -269,7 +309,7 @@ __device__ __forceinline__ void producer_role(const FwdParams &p, const CUtensor
         ptx::bulk_load(sb + OFF_SV + (nq % 3) * SV_BYTES, p.v_scales + static_cast<size_t>(tq.b * p.Hkv + tq.hk) * HD,
                        SV_BYTES, bar(QSTAGE));
     };
-    int issued_k = -1, issued_v = -1, issued_q = -1;
+    int issued_v = -1, issued_q = -1;
     bool ok = true;
     int g = 0, n = 0;   // KV tiles and items of this CTA before the current item
     for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++n) {
@@ -280,20 +320,9 @@ __device__ __forceinline__ void producer_role(const FwdParams &p, const CUtensor
             load_q(t, 0);
             issued_q = 0;
         }
-        for (int j = 0; j < t.ntiles; ++j) {
-            const int gj = g + j, ks = gj % KSTAGES;
-            if (!wt.wait(bar(KEMPTY + ks), ((gj / KSTAGES) & 1) ^ 1, SITE_KE)) {
-                ok = false;
-                break;
-            }
-            const uint32_t kdst = sb + OFF_K + ks * K_STAGE_BYTES;
-            ptx::mbar_arrive_expect_tx(bar(KFULL + ks), K_STAGE_BYTES);
-            ptx::tma_load_3d(kdst, tm_k, bar(KFULL + ks), 0, j * BN, bhk);
-            ptx::tma_load_3d(kdst + K_HALF_BYTES, tm_k, bar(KFULL + ks), 64, j * BN, bhk);
-            SATTN_TRACE(p, t, 11, j);
-            issued_k = gj;
+        for (int j = 0; j < t.ntiles && ok; ++j) {
             for (int h = 0; h < 2; ++h) {
-                const int u = 2 * gj + h, vs = u % VSLOTS;
+                const int u = 2 * (g + j) + h, vs = u % VSLOTS;
                 if (!wt.wait(bar(VEMPTY + vs), ((u / VSLOTS) & 1) ^ 1, SITE_VE)) {
                     ok = false;
                     break;
@@ -305,8 +334,6 @@ __device__ __forceinline__ void producer_role(const FwdParams &p, const CUtensor
             if (!ok)
                 break;
             SATTN_TRACE(p, t, 12, j);
-            // after the first tile's loads: once this item's Q has left the
-            // staging buffer (QFULL), stage the next item's Q
             const int nx = it + static_cast<int>(gridDim.x);
             if (j == 0 && nx < p.n_items) {
                 if (!wt.wait(bar(QFULL), n & 1, SITE_QE)) {
@@ -320,8 +347,6 @@ __device__ __forceinline__ void producer_role(const FwdParams &p, const CUtensor
         g += t.ntiles;
     }
     if (!ok) {
-        for (int j = max(0, issued_k - KSTAGES + 1); j <= issued_k; ++j)
-            wt.drain(bar(KFULL + j % KSTAGES), (j / KSTAGES) & 1);
         for (int u = max(0, issued_v - VSLOTS + 1); u <= issued_v; ++u)
             wt.drain(bar(VFULL + u % VSLOTS), (u / VSLOTS) & 1);
         if (issued_q >= 0)
@@ -347,22 +372,30 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
         ptx::tc_fence_after();
         for (int j = 0; j <= t.ntiles && ok; ++j) {
             if (j < t.ntiles) {                     // S_j = Q K_j^T (256 keys)
-                const int gj = g + j, ks = gj % KSTAGES;
-                if (!wt.wait(bar(KFULL + ks), (gj / KSTAGES) & 1, SITE_K) ||
-                    (gj >= 1 && !wt.wait(bar(SFREE), (gj - 1) & 1, SITE_SFREE))) {
+                const int gj = g + j;
+                if (gj >= 1 && !wt.wait(bar(SFREE), (gj - 1) & 1, SITE_SFREE)) {
                     ok = false;
                     break;
                 }
-                ptx::tc_fence_after();
-                SATTN_TRACE(p, t, 8, j);
-                const uint32_t kb = sb + OFF_K + ks * K_STAGE_BYTES;
+                for (int h = 0; h < 2; ++h) {       // channels [64h, 64h + 64): four K=16 steps
+                    const int u = 2 * gj + h, ks = u % KSLOTS;
+                    if (!wt.wait(bar(KFULL + ks), (u / KSLOTS) & 1, SITE_K)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    if (h == 0)
+                        SATTN_TRACE(p, t, 8, j);
+                    const uint32_t kb = sb + OFF_K + ks * K_HALF_BYTES;
 #pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    ptx::mma_f16_ts(tmem + TM_S, tmem + TM_Q + 8 * s,
-                                    ptx::sw128_desc(kb + (s >> 2) * K_HALF_BYTES + (s & 3) * 32),
-                                    IDESC_QK, s > 0);
+                    for (int s = 0; s < 4; ++s)
+                        ptx::mma_f16_ts(tmem + TM_S, tmem + TM_Q + 32 * h + 8 * s, ptx::sw128_desc(kb + s * 32),
+                                        IDESC_QK, (h | s) != 0);
+                    ptx::mma_commit(bar(KEMPTY + ks));
+                }
+                if (!ok)
+                    break;
                 SATTN_TRACE(p, t, 9, j);
-                ptx::mma_commit(bar(KEMPTY + ks));
                 ptx::mma_commit(bar(SFULL));
                 SATTN_TRACE(p, t, 4, j);
             }
@@ -407,7 +440,8 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
 // Compute warpgroups.  Half h owns S columns [128h, 128h + 128) of every tile
 // and writes the P8 bytes of those keys into shared-memory half h (K-major,
 // 128-byte swizzle); the row max is exchanged through shared memory under a
-// named barrier, so both halves hold the same running max m and alpha.  Half
+// named barrier of the two warps that share those rows, so both halves hold
+// the same running max m and alpha.  Half
 // h also owns RO columns [64h, 64h + 64): after writing P_j it folds the
 // partial PV_{j-1} into RO with alpha_{j-1} (both halves keep d).  Between two
 // items the warps write the next item's Q into TMEM (free once the last QK of
@@ -599,11 +633,12 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
                 b = ptx::fmax3(b, q[6], q[7]);
                 tmax = fmaxf(tmax, __fmul_rn(b, sig[c]));
             }
-            // exchange the half-row maxima (double-buffered by tile parity)
+            // exchange the half-row maxima (double-buffered by tile parity); only
+            // warps w and w + 4 share rows, so each such pair has its own barrier
             maxx[((gj & 1) * 2 + half) * BM + r] = tmax;
             if ((r & 31) == 0)
                 SATTN_TRACE(p, t, 21 + 4 * half + (r >> 5), j);
-            ptx::named_bar_sync(1, 2 * BM);
+            ptx::named_bar_sync(1 + quarter, 64);
             tmax = fmaxf(tmax, maxx[((gj & 1) * 2 + (half ^ 1)) * BM + r]);
             if (r == 0 && half == 0)
                 SATTN_TRACE(p, t, 2, j);
@@ -622,8 +657,7 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
             // P8 = E4M3(exp2(acc * sig - m') * 448), four keys per 32-bit word,
             // stored 32 keys at a time (16-byte chunk c of the row lands at chunk
             // c ^ (row % 8): the 128-byte swizzle of the K-major operand)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            auto p_block = [&](int c) {
                 uint32_t pk[8];
 #pragma unroll
                 for (int w = 0; w < 8; ++w) {
@@ -642,7 +676,10 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
                     make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 *reinterpret_cast<uint4 *>(prow + (((2 * c + 1) ^ (r & 7)) << 4)) =
                     make_uint4(pk[4], pk[5], pk[6], pk[7]);
-            }
+            };
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                p_block(c);
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(bar(PFULL + pbuf));
             if (r == 0 && half == 0)
@@ -670,16 +707,18 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
         // threads per row, instead of one 16-byte piece per row per store.
         {
             const float rcp = d > 0.0f ? __frcp_rn(d) : 0.0f;
-            const float *sv = svs + (n % 3) * HD + 64 * half;   // landed with this item's Q
+            const float4 *sv4 = reinterpret_cast<const float4 *>(svs + (n % 3) * HD + 64 * half);   // landed with this item's Q
             uint8_t *stage = smem + OFF_P + ((g + t.ntiles - 1) & 1) * P_BUF_BYTES + (quarter * 2 + half) * 4096;
 #pragma unroll
             for (int w = 0; w < 8; ++w) {
+                const float4 va = sv4[2 * w], vb = sv4[2 * w + 1];
+                const float sv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
                 uint32_t u[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int c = 8 * w + 2 * e;
-                    const float o0 = __fmul_rn(__fmul_rn(ro[c], rcp), sv[c]);
-                    const float o1 = __fmul_rn(__fmul_rn(ro[c + 1], rcp), sv[c + 1]);
+                    const float o0 = __fmul_rn(__fmul_rn(ro[c], rcp), sv[2 * e]);
+                    const float o1 = __fmul_rn(__fmul_rn(ro[c + 1], rcp), sv[2 * e + 1]);
                     const __nv_bfloat162 pr = __floats2bfloat162_rn(o0, o1);
                     memcpy(&u[e], &pr, sizeof(uint32_t));
                 }
@@ -730,7 +769,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (threadIdx.x == 0) {
         *flag = *reinterpret_cast<volatile uint32_t *>(p.status);
         const uint32_t b0 = sb + OFF_BAR;
-        for (int s = 0; s < KSTAGES; ++s) {
+        for (int s = 0; s < KSLOTS; ++s) {
             ptx::mbar_init(b0 + 8u * (KFULL + s), 1);
             ptx::mbar_init(b0 + 8u * (KEMPTY + s), 1);
         }
@@ -776,7 +815,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ptx::setmaxnreg_dec<kRegsOther>();
             if (warp == WARP_PRODUCER) {
                 if (lane == 0)
-                    producer_role(p, &tm_k, &tm_v, &tm_q, sb, wt);
+                    kload_role(p, &tm_k, sb, wt);
+            } else if (warp == WARP_VLOAD) {
+                if (lane == 0)
+                    vload_role(p, &tm_v, &tm_q, sb, wt);
             } else if (warp == WARP_MMA) {
                 if (lane == 0)
                     mma_role(p, sb, tmem, wt);
