@@ -447,16 +447,15 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
 // items the warps write the next item's Q into TMEM (free once the last QK of
 // the current item has completed) before the last fold and the final
 // conversion, so the next QK overlaps them.
-__device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, uint8_t *smem,
-                                             uint32_t tmem, int warp, int lane, const Waiter &wt)
+__device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, uint32_t tmem, int warp, int lane,
+                                             const Waiter &wt)
 {
     auto bar = [sb](int i) { return sb + OFF_BAR + 8u * i; };
     const int half = warp >> 2;                               // 0 or 1
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;                        // query row in the tile = TMEM lane
     const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float *maxx = reinterpret_cast<float *>(smem + OFF_MAXX);
-    const float *svs = reinterpret_cast<const float *>(smem + OFF_SV);   // [item % 3][128] V channel scales
+    const uint32_t maxx = sb + OFF_MAXX;                      // [tile parity][half][row] row maxima
     constexpr float kLog2_448 = 8.8073549220576041f;          // log2(448): P is stored as p * 448
 
     // Q codes 64h .. 64h+63 of row r of the staged item (16-byte chunk c of
@@ -465,10 +464,10 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
     auto store_q = [&](int nq) -> bool {
         if (!wt.wait(bar(QSTAGE), nq & 1, SITE_QS))
             return false;
-        const uint8_t *qrow = smem + OFF_QS + r * HD;
+        const uint32_t qrow = sb + OFF_QS + r * HD;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-            const uint4 a = *reinterpret_cast<const uint4 *>(qrow + (((4 * half + w) ^ (r & 7)) << 4));
+            const uint4 a = ptx::ld_shared_v4(qrow + (((4 * half + w) ^ (r & 7)) << 4));
             const uint32_t words[4] = {a.x, a.y, a.z, a.w};
             uint32_t h[8];
 #pragma unroll
@@ -485,12 +484,14 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
     };
     auto qscale = [&](const Tile &tq) {
         const int i = tq.q0 + r;
-        return i < p.nq32 ? p.q_scales[static_cast<size_t>(tq.b * p.Hq + tq.hq) * p.nbq + i / kQBlock] : 0.0f;
+        return i < p.nq32 ? ptx::ld_nc_f32(p.q_scales + static_cast<size_t>(tq.b * p.Hq + tq.hq) * p.nbq + i / kQBlock)
+                          : 0.0f;
     };
     // block scales of this half's four 32-key blocks of tile j of an item
     auto kscale = [&](const Tile &tk, int j, int c) {
         const int kb = j * (BN / kQBlock) + 4 * half + c;
-        return kb < p.nbk ? p.k_scales[static_cast<size_t>(tk.b * p.Hkv + tk.hk) * p.nbk + kb] : 0.0f;
+        // (the load is pinned here: it is consumed one tile later)
+        return kb < p.nbk ? ptx::ld_nc_f32(p.k_scales + static_cast<size_t>(tk.b * p.Hkv + tk.hk) * p.nbk + kb) : 0.0f;
     };
 
     int it = blockIdx.x;
@@ -575,6 +576,8 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
             }
             if (r == 0 && half == 0 && j == 0)
                 SATTN_TRACE(p, t, 40, 1);
+            if (r == 0 && half == 0)
+                SATTN_TRACE(p, t, 41, j);
             if (!wt.wait(bar(SFULL), gj & 1, SITE_S))
                 return;
             ptx::tc_fence_after();
@@ -635,11 +638,11 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
             }
             // exchange the half-row maxima (double-buffered by tile parity); only
             // warps w and w + 4 share rows, so each such pair has its own barrier
-            maxx[((gj & 1) * 2 + half) * BM + r] = tmax;
+            ptx::st_shared_f32(maxx + 4 * (((gj & 1) * 2 + half) * BM + r), tmax);
             if ((r & 31) == 0)
                 SATTN_TRACE(p, t, 21 + 4 * half + (r >> 5), j);
             ptx::named_bar_sync(1 + quarter, 64);
-            tmax = fmaxf(tmax, maxx[((gj & 1) * 2 + (half ^ 1)) * BM + r]);
+            tmax = fmaxf(tmax, ptx::ld_shared_f32(maxx + 4 * (((gj & 1) * 2 + (half ^ 1)) * BM + r)));
             if (r == 0 && half == 0)
                 SATTN_TRACE(p, t, 2, j);
 
@@ -651,7 +654,7 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
 
             // P buffer gj % 2 is free once the PV two tiles back has read it
             const int pbuf = gj & 1;
-            uint8_t *prow = smem + OFF_P + pbuf * P_BUF_BYTES + half * P_HALF_BYTES + r * 128;
+            const uint32_t prow = sb + OFF_P + pbuf * P_BUF_BYTES + half * P_HALF_BYTES + r * 128;
             if (gj >= 2 && !wt.wait(bar(PDONE + pbuf), ((gj >> 1) - 1) & 1, SITE_PDONE))
                 return;
             // P8 = E4M3(exp2(acc * sig - m') * 448), four keys per 32-bit word,
@@ -672,10 +675,8 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
                     for (int w = 0; w < 8; ++w)
                         p.dbg[32768 + r * 64 + 32 * half + 8 * c + w] = __uint_as_float(pk[w]);
 #endif
-                *reinterpret_cast<uint4 *>(prow + (((2 * c) ^ (r & 7)) << 4)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                *reinterpret_cast<uint4 *>(prow + (((2 * c + 1) ^ (r & 7)) << 4)) =
-                    make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                ptx::st_shared_v4(prow + (((2 * c) ^ (r & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+                ptx::st_shared_v4(prow + (((2 * c + 1) ^ (r & 7)) << 4), pk[4], pk[5], pk[6], pk[7]);
             };
 #pragma unroll
             for (int c = 0; c < 4; ++c)
@@ -707,12 +708,14 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
         // threads per row, instead of one 16-byte piece per row per store.
         {
             const float rcp = d > 0.0f ? __frcp_rn(d) : 0.0f;
-            const float4 *sv4 = reinterpret_cast<const float4 *>(svs + (n % 3) * HD + 64 * half);   // landed with this item's Q
-            uint8_t *stage = smem + OFF_P + ((g + t.ntiles - 1) & 1) * P_BUF_BYTES + (quarter * 2 + half) * 4096;
+            const uint32_t sv4 = sb + OFF_SV + (n % 3) * SV_BYTES + 4 * 64 * half;   // landed with this item's Q
+            const uint32_t stage = sb + OFF_P + ((g + t.ntiles - 1) & 1) * P_BUF_BYTES + (quarter * 2 + half) * 4096;
 #pragma unroll
             for (int w = 0; w < 8; ++w) {
-                const float4 va = sv4[2 * w], vb = sv4[2 * w + 1];
-                const float sv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+                const uint4 va = ptx::ld_shared_v4(sv4 + 32 * w), vb = ptx::ld_shared_v4(sv4 + 32 * w + 16);
+                const float sv[8] = {__uint_as_float(va.x), __uint_as_float(va.y), __uint_as_float(va.z),
+                                     __uint_as_float(va.w), __uint_as_float(vb.x), __uint_as_float(vb.y),
+                                     __uint_as_float(vb.z), __uint_as_float(vb.w)};
                 uint32_t u[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -722,8 +725,7 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
                     const __nv_bfloat162 pr = __floats2bfloat162_rn(o0, o1);
                     memcpy(&u[e], &pr, sizeof(uint32_t));
                 }
-                *reinterpret_cast<uint4 *>(stage + lane * 128 + ((w ^ (lane & 7)) << 4)) =
-                    make_uint4(u[0], u[1], u[2], u[3]);
+                ptx::st_shared_v4(stage + lane * 128 + ((w ^ (lane & 7)) << 4), u[0], u[1], u[2], u[3]);
             }
             __syncwarp();
             const int ch = lane & 7;
@@ -731,7 +733,7 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
             for (int k = 0; k < 8; ++k) {
                 const int l = 4 * k + (lane >> 3);                     // row of the warp's 32
                 const int row = t.q0 + quarter * 32 + l;
-                const uint4 v = *reinterpret_cast<const uint4 *>(stage + l * 128 + ((ch ^ (l & 7)) << 4));
+                const uint4 v = ptx::ld_shared_v4(stage + l * 128 + ((ch ^ (l & 7)) << 4));
                 if (row < p.Nq)
                     *reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(t.b * p.Hq + t.hq) * p.Nq + row) * HD +
                                                64 * half + 8 * ch) = v;
@@ -810,7 +812,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (*flag == 0 && static_cast<int>(blockIdx.x) < p.n_items) {
         if (warp < WARP_PRODUCER) {
             ptx::setmaxnreg_inc<kRegsCompute>();
-            compute_role(p, sb, smem, tmem, warp, lane, wt);
+            compute_role(p, sb, tmem, warp, lane, wt);
         } else {
             ptx::setmaxnreg_dec<kRegsOther>();
             if (warp == WARP_PRODUCER) {
