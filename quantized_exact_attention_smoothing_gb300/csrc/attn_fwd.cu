@@ -10,26 +10,29 @@
 //   warps 0-7   two compute warpgroups, thread = query row = TMEM lane; half h
 //               owns keys [128h, 128h + 128) of every tile and output channels
 //               [64h, 64h + 64): score scaling, masks, running max m (exchanged
-//               between the halves), alpha, the FP8 P bytes (written to shared
-//               memory), RO = RO * alpha + PV and d = d * alpha + sum p8 for the
+//               between the halves), alpha, the FP8 P bytes (written to TMEM),
+//               RO = RO * alpha + PV and d = d * alpha + sum p8 for the
 //               previous tile, the final conversion, and the FP16 carrier of
-//               the next item's Q (into TMEM)
+//               the next item's Q (into shared memory)
 //   warp 8      K loader (TMA): K half-tiles (FP16 carrier of the INT8 codes,
 //               256 keys x 64 channels) into a ring of three slots
 //   warp 9      TMEM allocation and the single MMA-issuing thread:
-//                 S_j  = Q * K_j^T   tcgen05 kind::f16, A = Q from TMEM, N = 256
-//                 PV_j = P_j * V_j   tcgen05 kind::f8f6f4, A = P from shared
-//                                    memory, N = 144: V rows plus a row of ones
-//                                    whose column gives sum_j p8_j
+//                 S_j  = Q * K_j^T   tcgen05 kind::f16, A = Q from shared
+//                                    memory, N = 256
+//                 PV_j = P_j * V_j   tcgen05 kind::f8f6f4, A = P from TMEM,
+//                                    N = 144: V rows plus a row of ones whose
+//                                    column gives sum_j p8_j
 //   warp 10     V and Q loader (TMA): V half-tiles (E4M3, channel-major) into
 //               two slots; the next item's INT8 Q tile and V channel scales
 //   warp 11     idle
 // Twelve warps launch at 168 registers each; setmaxnreg then gives the compute
 // warpgroups 232 (128 scores and 64 RO values per thread) and the loader/MMA
 // warpgroup 40.
-// Tensor memory (512 columns): S [0,256), PV partial [256,400), Q carrier
-// [448,512).  P is double-buffered in shared memory, so the softmax of tile
-// j + 1 never waits for PV of tile j.  A tcgen05.mma instruction costs about
+// Tensor memory (512 columns): S [0,256), PV partial [256,400), P8 [448,512)
+// (four E4M3 codes per column).  Writing P with tcgen05.st keeps it off the
+// shared-memory pipe and needs no async-proxy fence; P_j may be written once
+// PV_{j-1} has completed, which in steady state is long before the softmax of
+// tile j reaches it.  A tcgen05.mma instruction costs about
 // the same time for any N up to 256 on this part, hence the 256-key tiles: QK
 // runs at N = 256.  The K ring of half-tile slots lets the next tile's K land
 // while the current QK runs; a single full-tile K stage put the whole TMA
@@ -65,12 +68,12 @@ constexpr uint32_t K_HALF_BYTES = BN * 64 * 2;          // 256 keys x 64 channel
 constexpr uint32_t PV_N = 144;                          // V rows + ones row + zero rows
 constexpr uint32_t V_SLOT_BYTES = PV_N * 128;           // one 128-key half tile, 18 KB
 constexpr uint32_t V_TMA_BYTES = HD * 128;              // 16 KB loaded per half tile
-constexpr uint32_t P_HALF_BYTES = BM * 128;             // 128 rows x 128 keys, E4M3
-constexpr uint32_t P_BUF_BYTES = 2 * P_HALF_BYTES;      // one tile's P (double-buffered)
+constexpr uint32_t Q_HALF_BYTES = BM * 128;             // 128 rows x 64 channels, FP16
+constexpr uint32_t STG_BYTES = BM * HD * 2;             // output tile, BF16
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;
 constexpr uint32_t TM_PV = 256;
-constexpr uint32_t TM_Q = 448;
+constexpr uint32_t TM_P = 448;   // P8 of one tile: 256 keys, four per column
 // warp roles: 0-7 compute (two warpgroups), 8 K loader, 9 MMA issuer and TMEM
 // owner, 10 V and Q loader, 11 idle
 constexpr int WARP_PRODUCER = 8, WARP_MMA = 9, WARP_VLOAD = 10;
@@ -87,8 +90,9 @@ constexpr uint64_t TIMEOUT_NS = 1000000000ull;
 // shared memory map, offsets from a 1024-byte aligned base
 constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_V = OFF_K + KSLOTS * K_HALF_BYTES;
-constexpr uint32_t OFF_P = OFF_V + VSLOTS * V_SLOT_BYTES;
-constexpr uint32_t OFF_QS = OFF_P + 2 * P_BUF_BYTES;        // INT8 Q tile of the next item (TMA, 128B swizzle)
+constexpr uint32_t OFF_Q = OFF_V + VSLOTS * V_SLOT_BYTES;   // FP16 carrier of Q, two 64-channel halves (128B swizzle)
+constexpr uint32_t OFF_STG = OFF_Q + 2 * Q_HALF_BYTES;      // output staging of the final conversion
+constexpr uint32_t OFF_QS = OFF_STG + STG_BYTES;            // INT8 Q tile of the next item (TMA, 128B swizzle)
 constexpr uint32_t QS_BYTES = BM * HD;
 constexpr uint32_t OFF_MAXX = OFF_QS + QS_BYTES;             // [tile parity][half][row] row maxima
 constexpr uint32_t OFF_SV = OFF_MAXX + 4 * BM * 4;          // [item % 3][128] V channel scales
@@ -103,9 +107,9 @@ enum Bar : int {
     QFULL = QSTAGE + 1,         // its FP16 carrier is in TMEM
     SFULL = QFULL + 1,
     SFREE = SFULL + 1,
-    PFULL = SFREE + 1,       // 2 (per P buffer)
-    PDONE = PFULL + 2,       // 2 (per P buffer)
-    PVFULL = PDONE + 2,
+    PFULL = SFREE + 1,
+    PDONE = PFULL + 1,
+    PVFULL = PDONE + 1,
     PVEMPTY = PVFULL + 1,
     MMADONE = PVEMPTY + 1,
     NBARS = MMADONE + 1
@@ -114,7 +118,7 @@ constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBARS * 8;
 constexpr uint32_t OFF_FLAG = OFF_TMEM_SLOT + 4;
 constexpr uint32_t SMEM_BYTES = OFF_FLAG + 4 + 1024;   // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-static_assert(OFF_V % 1024 == 0 && V_SLOT_BYTES % 1024 == 0 && OFF_P % 1024 == 0 && OFF_QS % 1024 == 0,
+static_assert(OFF_V % 1024 == 0 && V_SLOT_BYTES % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_QS % 1024 == 0,
               "swizzle atoms must be 1024-aligned");
 
 // where a wait gave up (second status word)
@@ -389,8 +393,8 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
                     const uint32_t kb = sb + OFF_K + ks * K_HALF_BYTES;
 #pragma unroll
                     for (int s = 0; s < 4; ++s)
-                        ptx::mma_f16_ts(tmem + TM_S, tmem + TM_Q + 32 * h + 8 * s, ptx::sw128_desc(kb + s * 32),
-                                        IDESC_QK, (h | s) != 0);
+                        ptx::mma_f16_ss(tmem + TM_S, ptx::sw128_desc(sb + OFF_Q + h * Q_HALF_BYTES + s * 32),
+                                        ptx::sw128_desc(kb + s * 32), IDESC_QK, (h | s) != 0);
                     ptx::mma_commit(bar(KEMPTY + ks));
                 }
                 if (!ok)
@@ -400,8 +404,8 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
                 SATTN_TRACE(p, t, 4, j);
             }
             if (j >= 1) {                           // PV_{j-1} = P_{j-1} V_{j-1}
-                const int gg = g + j - 1, pbuf = gg & 1;
-                if (!wt.wait(bar(PFULL + pbuf), (gg >> 1) & 1, SITE_P) ||
+                const int gg = g + j - 1;
+                if (!wt.wait(bar(PFULL), gg & 1, SITE_P) ||
                     !wt.wait(bar(PVEMPTY), (gg & 1) ^ 1, SITE_PVE)) {
                     ok = false;
                     break;
@@ -416,10 +420,9 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
                     if (h == 0)
                         SATTN_TRACE(p, t, 5, j - 1);
                     const uint32_t vb = sb + OFF_V + vs * V_SLOT_BYTES;
-                    const uint32_t pb = sb + OFF_P + pbuf * P_BUF_BYTES + h * P_HALF_BYTES;
 #pragma unroll
                     for (int s = 0; s < 4; ++s)
-                        ptx::mma_f8_ss(tmem + TM_PV, ptx::sw128_desc(pb + s * 32), ptx::sw128_desc(vb + s * 32),
+                        ptx::mma_f8_ts(tmem + TM_PV, tmem + TM_P + 32 * h + 8 * s, ptx::sw128_desc(vb + s * 32),
                                        IDESC_PV, (h | s) != 0);
                     ptx::mma_commit(bar(VEMPTY + vs));
                 }
@@ -427,7 +430,7 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
                     break;
                 SATTN_TRACE(p, t, 10, j - 1);
                 ptx::mma_commit(bar(PVFULL));
-                ptx::mma_commit(bar(PDONE + pbuf));
+                ptx::mma_commit(bar(PDONE));
             }
         }
         g += t.ntiles;
@@ -459,8 +462,9 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
     constexpr float kLog2_448 = 8.8073549220576041f;          // log2(448): P is stored as p * 448
 
     // Q codes 64h .. 64h+63 of row r of the staged item (16-byte chunk c of
-    // row r sits at chunk c ^ (r % 8)) -> FP16 carrier -> TMEM columns
-    // [TM_Q + 32h, TM_Q + 32h + 32), 8 columns at a time; then QFULL
+    // row r sits at chunk c ^ (r % 8)) -> FP16 carrier -> row r of the Q half h
+    // in shared memory (the same 128-byte swizzle), 8 channels at a time; then
+    // QFULL
     auto store_q = [&](int nq) -> bool {
         if (!wt.wait(bar(QSTAGE), nq & 1, SITE_QS))
             return false;
@@ -475,10 +479,11 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
                 h[e * 2] = f16x2_of_i8(words[e], 0);
                 h[e * 2 + 1] = f16x2_of_i8(words[e], 2);
             }
-            ptx::tmem_st8(taddr + TM_Q + 32 * half + 8 * w, h);
+            const uint32_t qdst = sb + OFF_Q + half * Q_HALF_BYTES + r * 128;
+            ptx::st_shared_v4(qdst + (((2 * w) ^ (r & 7)) << 4), h[0], h[1], h[2], h[3]);
+            ptx::st_shared_v4(qdst + (((2 * w + 1) ^ (r & 7)) << 4), h[4], h[5], h[6], h[7]);
         }
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
+        ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(bar(QFULL));
         return true;
     };
@@ -652,14 +657,11 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
             // mn = -inf and only -inf scores, which any finite offset maps to 0
             const float nb = (mn == -INFINITY) ? 0.0f : kLog2_448 - mn;
 
-            // P buffer gj % 2 is free once the PV two tiles back has read it
-            const int pbuf = gj & 1;
-            const uint32_t prow = sb + OFF_P + pbuf * P_BUF_BYTES + half * P_HALF_BYTES + r * 128;
-            if (gj >= 2 && !wt.wait(bar(PDONE + pbuf), ((gj >> 1) - 1) & 1, SITE_PDONE))
-                return;
             // P8 = E4M3(exp2(acc * sig - m') * 448), four keys per 32-bit word,
-            // stored 32 keys at a time (16-byte chunk c of the row lands at chunk
-            // c ^ (row % 8): the 128-byte swizzle of the K-major operand)
+            // written 32 keys (8 columns) at a time into TMEM columns
+            // [TM_P + 32h, TM_P + 32h + 32) of this row's lane, where PV reads
+            // them as its A operand; the columns are free once the previous PV
+            // has completed
             auto p_block = [&](int c) {
                 uint32_t pk[8];
 #pragma unroll
@@ -675,14 +677,20 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
                     for (int w = 0; w < 8; ++w)
                         p.dbg[32768 + r * 64 + 32 * half + 8 * c + w] = __uint_as_float(pk[w]);
 #endif
-                ptx::st_shared_v4(prow + (((2 * c) ^ (r & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
-                ptx::st_shared_v4(prow + (((2 * c + 1) ^ (r & 7)) << 4), pk[4], pk[5], pk[6], pk[7]);
+                if (c == 0 && gj >= 1 && !wt.wait(bar(PDONE), (gj - 1) & 1, SITE_PDONE))
+                    return false;
+                ptx::tmem_st8(taddr + TM_P + 32 * half + 8 * c, pk);
+                return true;
             };
+            bool p_ok = true;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-                p_block(c);
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(bar(PFULL + pbuf));
+                p_ok = p_ok && p_block(c);
+            if (!p_ok)
+                return;
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(PFULL));
             if (r == 0 && half == 0)
                 SATTN_TRACE(p, t, 3, j);
             if ((r & 31) == 0)
@@ -702,14 +710,14 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
         if (r == 0 && half == 0)
             SATTN_TRACE(p, t, 39, 2);
         // final conversion: reciprocal of d, per-channel V scale, BF16.  Each
-        // warp stages its 32 rows x 64 channels (4 KB, 16-byte chunk c of row
-        // l at chunk c ^ (l % 8)) in the P buffer of this item's last tile (its
-        // PV has completed) and then writes whole 128-byte row segments, eight
-        // threads per row, instead of one 16-byte piece per row per store.
+        // warp stages its 32 rows x 64 channels (4 KB of its own, 16-byte chunk
+        // c of row l at chunk c ^ (l % 8)) in shared memory and then writes
+        // whole 128-byte row segments, eight threads per row, instead of one
+        // 16-byte piece per row per store.
         {
             const float rcp = d > 0.0f ? __frcp_rn(d) : 0.0f;
             const uint32_t sv4 = sb + OFF_SV + (n % 3) * SV_BYTES + 4 * 64 * half;   // landed with this item's Q
-            const uint32_t stage = sb + OFF_P + ((g + t.ntiles - 1) & 1) * P_BUF_BYTES + (quarter * 2 + half) * 4096;
+            const uint32_t stage = sb + OFF_STG + (quarter * 2 + half) * 4096;
 #pragma unroll
             for (int w = 0; w < 8; ++w) {
                 const uint4 va = ptx::ld_shared_v4(sv4 + 32 * w), vb = ptx::ld_shared_v4(sv4 + 32 * w + 16);
@@ -783,10 +791,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ptx::mbar_init(b0 + 8u * QFULL, 2 * BM);
         ptx::mbar_init(b0 + 8u * SFULL, 1);
         ptx::mbar_init(b0 + 8u * SFREE, 2 * BM);
-        for (int s = 0; s < 2; ++s) {
-            ptx::mbar_init(b0 + 8u * (PFULL + s), 2 * BM);
-            ptx::mbar_init(b0 + 8u * (PDONE + s), 1);
-        }
+        ptx::mbar_init(b0 + 8u * PFULL, 2 * BM);
+        ptx::mbar_init(b0 + 8u * PDONE, 1);
         ptx::mbar_init(b0 + 8u * PVFULL, 1);
         ptx::mbar_init(b0 + 8u * PVEMPTY, 2 * BM);
         ptx::mbar_init(b0 + 8u * MMADONE, 1);
