@@ -293,9 +293,14 @@ def run_ours(args, world, rank, local):
 
     peaks = load_peaks()
     mp = mixed_peak(peaks["bf16_tflops"])
+    # DRAM bytes of one attn_fwd_kernel launch from the ncu capture summarised in
+    # profiles/attn_fwd_c5_b3_full.md (c5 at batch 3: 467.7 MB read + 161.3 MB
+    # written), scaled by the units processed; other workloads were not captured.
+    traffic = 629.03e6 * w.B / 3.0 if w.name == "c5" else None
     achieved = w.algorithmic_ops / (ms_fwd * 1e-3) / 1e12
     prep_bytes = (hq.numel() + hk.numel() + hv.numel()) * 2 + \
         (buf["q_codes"].numel() + buf["k_codes"].numel() + w.B * w.Hkv * 128 * w.Nkv) + \
+        2 * buf["k_carrier"].numel() + \
         4 * (buf["q_scales"].numel() + buf["k_scales"].numel() + buf["k_mean"].numel() + buf["v_scales"].numel())
     result = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -309,9 +314,12 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"replica x{world}"},
         "algorithmic_tops": round(world * w.algorithmic_ops / (ms_step * 1e-3) / 1e12, 3),
         "ms_prepare": round(ms_prep, 5), "ms_forward": round(ms_fwd, 5),
-        "roofline": {"bound": "tensor", "kernel": "sattn_forward (attn_fwd_kernel + K widen)",
+        "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel (the only kernel of sattn_forward)",
                      "achieved": round(achieved, 2), "peak": round(mp["mixed"], 2), "unit": "TFLOP/s",
-                     "frac": round(achieved / mp["mixed"], 4), "traffic": None,
+                     "frac": round(achieved / mp["mixed"], 4),
+                     "traffic": round(traffic) if traffic else None,
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, c5 batch 3, "
+                                       "scaled by batch" if traffic else None,
                      "peak_basis": f"mixed FP16/FP8 roofline from {peaks['source']} bf16 "
                                    f"{peaks['bf16_tflops']} TFLOP/s (burst) x nominal ratios",
                      "frac_of_fp8_dense": round(achieved / mp["fp8"], 4)},
@@ -319,7 +327,8 @@ def run_ours(args, world, rank, local):
                              "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": round(prep_bytes / (ms_prep * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                              "algorithmic_bytes": prep_bytes},
-        "gpu_launches": 7 * K,
+        # per step: 5 prepare kernels + the attention kernel (+ one status memset)
+        "gpu_launches": 6 * K,
         "clocks": clk,
     }
     if e2e is not None:

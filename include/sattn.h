@@ -94,10 +94,11 @@ typedef struct {
     size_t q_codes, q_scales;   /* int8 [B][Hq][Nq32][128], FP32 [B][Hq][Nq32/32] */
     size_t k_codes, k_scales;   /* int8 [B][Hkv][Nkv32][128], FP32 [B][Hkv][Nkv32/32] */
     size_t k_mean;              /* FP32 [B][Hkv][128] */
+    size_t k_carrier;           /* FP16 [B][Hkv][Nkv][128]: the K codes as FP16 values */
     size_t v_codes, v_scales;   /* E4M3 [B][Hkv][128][Nkv128] (channel-major), FP32 [B][Hkv][128] */
     size_t out;                 /* BF16 [B][Hq][Nq][128] */
     size_t prepare_workspace;   /* scratch of sattn_prepare */
-    size_t forward_workspace;   /* scratch of sattn_forward */
+    size_t forward_workspace;   /* scratch of sattn_forward (its status block) */
     size_t arena;               /* one device block holding all of the above,
                                    for sattn_attention_host */
 } sattn_sizes;
@@ -119,6 +120,10 @@ int sattn_query_sizes(const sattn_shape *shape, sattn_sizes *sizes);
  *   k_codes     out: int8 codes of the smoothed K, pad rows 0
  *   k_scales    out: FP32, one per 32-token block
  *   k_mean      out: FP32 per-channel mean of K that was subtracted
+ *   k_carrier   out: FP16 [B][Hkv][Nkv][128], every K code as an FP16 value
+ *               (exact: integers of magnitude <= 127); the operand that the
+ *               forward's tensor cores read, since this part has no INT8
+ *               tensor-core product
  *   v_codes     out: E4M3 bytes, channel-major [B][Hkv][128][Nkv128];
  *               keys Nkv .. Nkv128-1 are 0
  *   v_scales    out: FP32 per channel
@@ -129,25 +134,27 @@ int sattn_query_sizes(const sattn_shape *shape, sattn_sizes *sizes);
  */
 int sattn_prepare(const sattn_shape *shape, const void *q, const void *k, const void *v,
                   int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
-                  float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace,
-                  void *stream);
+                  float *k_mean, void *k_carrier, uint8_t *v_codes, float *v_scales,
+                  void *workspace, void *stream);
 
 /*
  * sattn_forward -- QK traversal, online softmax, FP8 P, two-level PV
  * accumulation, final conversion and ragged tails (page entries "Phase 0
  * Import And Verification" and "Phase 1 State-Ownership Decision").
- *   q_codes .. v_scales  in: as written by sattn_prepare for the same shape
+ *   q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales
+ *               in: as written by sattn_prepare for the same shape
  *   out         out: BF16 [B][Hq][Nq][128]
- *   workspace   scratch, sizes.forward_workspace bytes: holds the K codes
- *               widened to the FP16 carrier of the tensor-core product and a
- *               status word; contents on entry are ignored
+ *   workspace   scratch, sizes.forward_workspace bytes: the status block that
+ *               sattn_check_status reads; contents on entry are ignored
+ * One kernel: a persistent CTA per SM walks the (query tile, head, batch)
+ * items, longest first.
  * Exactness: QK^T is computed from the codes with products and sums that are
  * exact integers; P, PV and the output follow the arithmetic above, with the
  * inner PV sum in the tensor core's FP32 order and exp2 by the hardware
  * approximation.
  */
 int sattn_forward(const sattn_shape *shape, const int8_t *q_codes, const float *q_scales,
-                  const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
+                  const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
                   const float *v_scales, void *out, void *workspace, void *stream);
 
 /*
@@ -204,7 +211,8 @@ int sattn_attention_host(const sattn_shape *shape, const void *q_host, const voi
 #define SATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
 int sattn_prepare_noalloc(const sattn_shape *shape, const void *q, const void *k, const void *v,
                           int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
-                          float *k_mean, uint8_t *v_codes, float *v_scales, void *stream);
+                          float *k_mean, void *k_carrier, uint8_t *v_codes, float *v_scales,
+                          void *stream);
 
 /* A static, human-readable name for a status code. */
 const char *sattn_status_string(int status);

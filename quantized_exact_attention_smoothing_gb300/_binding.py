@@ -20,8 +20,8 @@ QBLOCK = 32
 KV_TILE = 256      # keys per KV tile of the forward pass (part of the numerical contract)
 V_PAD = 128        # V codes are padded to a multiple of 128 keys
 
-_SIZE_FIELDS = ["q", "k", "v", "q_codes", "q_scales", "k_codes", "k_scales", "k_mean", "v_codes",
-                "v_scales", "out", "prepare_workspace", "forward_workspace", "arena"]
+_SIZE_FIELDS = ["q", "k", "v", "q_codes", "q_scales", "k_codes", "k_scales", "k_mean", "k_carrier",
+                "v_codes", "v_scales", "out", "prepare_workspace", "forward_workspace", "arena"]
 
 
 class sattn_shape(ctypes.Structure):
@@ -67,9 +67,9 @@ def load_library(build: bool = True):
     P = ctypes.c_void_p
     SP = ctypes.POINTER(sattn_shape)
     lib.sattn_query_sizes.argtypes = [SP, ctypes.POINTER(sattn_sizes)]
-    lib.sattn_prepare.argtypes = [SP] + [P] * 12
+    lib.sattn_prepare.argtypes = [SP] + [P] * 13
     lib.sattn_forward.argtypes = [SP] + [P] * 9
-    lib.sattn_prepare_noalloc.argtypes = [SP] + [P] * 11
+    lib.sattn_prepare_noalloc.argtypes = [SP] + [P] * 12
     lib.sattn_check_status.argtypes = [P, P]
     lib.sattn_attention_host.argtypes = [SP, P, P, P, P, P, ctypes.c_size_t, P]
     lib.sattn_status_string.argtypes = [ctypes.c_int]
@@ -144,6 +144,7 @@ def prepare_buffers(shape: sattn_shape, device) -> dict:
         k_codes=torch.empty((B, Hkv, nk32, HEAD_DIM), dtype=torch.int8, device=device),
         k_scales=torch.empty((B, Hkv, nk32 // QBLOCK), dtype=torch.float32, device=device),
         k_mean=torch.empty((B, Hkv, HEAD_DIM), dtype=torch.float32, device=device),
+        k_carrier=torch.empty((B, Hkv, Nkv, HEAD_DIM), dtype=torch.float16, device=device),
         v_codes=torch.empty((B, Hkv, HEAD_DIM, nk128), dtype=torch.uint8, device=device),
         v_scales=torch.empty((B, Hkv, HEAD_DIM), dtype=torch.float32, device=device),
         workspace=_empty(z["prepare_workspace"], device),
@@ -160,8 +161,8 @@ def prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fa
     buf = buffers if buffers is not None else prepare_buffers(shape, q.device)
     rc = load_library().sattn_prepare(
         ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(buf["q_codes"]), _ptr(buf["q_scales"]),
-        _ptr(buf["k_codes"]), _ptr(buf["k_scales"]), _ptr(buf["k_mean"]), _ptr(buf["v_codes"]),
-        _ptr(buf["v_scales"]), _ptr(buf["workspace"]), _stream(stream))
+        _ptr(buf["k_codes"]), _ptr(buf["k_scales"]), _ptr(buf["k_mean"]), _ptr(buf["k_carrier"]),
+        _ptr(buf["v_codes"]), _ptr(buf["v_scales"]), _ptr(buf["workspace"]), _stream(stream))
     if rc != 0:
         raise SattnError(rc, "sattn_prepare")
     buf["shape"] = shape
@@ -188,8 +189,8 @@ def prepare_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: b
     buf = buffers if buffers is not None else prepare_buffers(shape, q.device)
     rc = load_library().sattn_prepare_noalloc(
         ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(buf["q_codes"]), _ptr(buf["q_scales"]),
-        _ptr(buf["k_codes"]), _ptr(buf["k_scales"]), _ptr(buf["k_mean"]), _ptr(buf["v_codes"]),
-        _ptr(buf["v_scales"]), _stream(stream))
+        _ptr(buf["k_codes"]), _ptr(buf["k_scales"]), _ptr(buf["k_mean"]), _ptr(buf["k_carrier"]),
+        _ptr(buf["v_codes"]), _ptr(buf["v_scales"]), _stream(stream))
     if rc != 0:
         raise SattnError(rc, "sattn_prepare_noalloc")
     buf["shape"] = shape
@@ -210,7 +211,7 @@ def forward(prep: dict, out: torch.Tensor | None = None, workspace: torch.Tensor
             prep["forward_workspace"] = workspace
     _need_cuda(out, workspace)
     rc = load_library().sattn_forward(
-        ctypes.byref(shape), _ptr(prep["q_codes"]), _ptr(prep["q_scales"]), _ptr(prep["k_codes"]),
+        ctypes.byref(shape), _ptr(prep["q_codes"]), _ptr(prep["q_scales"]), _ptr(prep["k_carrier"]),
         _ptr(prep["k_scales"]), _ptr(prep["v_codes"]), _ptr(prep["v_scales"]), _ptr(out),
         _ptr(workspace), _stream(stream))
     if rc != 0:

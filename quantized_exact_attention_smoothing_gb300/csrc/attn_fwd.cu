@@ -200,19 +200,6 @@ struct Waiter {
     }
 };
 
-// Bytes `byte`, `byte + 1` of `word` (INT8 codes) -> FP16 pair, exactly: with
-// u = x + 128 (the code with its top bit flipped), the FP16 pattern 0x6400 | u
-// is 1024 + u, and subtracting 1152 leaves x.  One byte permute and one packed
-// FP16 subtract per pair, both on the fast pipes (integer-to-FP16 conversion
-// instructions run on the quarter-rate unit).
-__device__ __forceinline__ uint32_t f16x2_of_i8(uint32_t word, int byte)
-{
-    const uint32_t u = __byte_perm(word ^ 0x80808080u, 0x64646464u, byte == 0 ? 0x5140u : 0x7362u);
-    uint32_t h;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h) : "r"(u), "r"(0x64806480u));
-    return h;
-}
-
 struct Tile {
     int b, hq, hk, q0, ntiles, mask_from;
     bool trace;   // debug builds: clock stamps of this CTA's items are recorded
@@ -476,8 +463,8 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
             uint32_t h[8];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                h[e * 2] = f16x2_of_i8(words[e], 0);
-                h[e * 2 + 1] = f16x2_of_i8(words[e], 2);
+                h[e * 2] = ptx::f16x2_of_i8(words[e], 0);
+                h[e * 2 + 1] = ptx::f16x2_of_i8(words[e], 2);
             }
             const uint32_t qdst = sb + OFF_Q + half * Q_HALF_BYTES + r * 128;
             ptx::st_shared_v4(qdst + (((2 * w) ^ (r & 7)) << 4), h[0], h[1], h[2], h[3]);
@@ -846,26 +833,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #endif
 }
 
-// INT8 K codes -> FP16 carrier [B*Hkv][Nkv][128]; also clears the status words.
-__global__ void __launch_bounds__(256) widen_k_kernel(const int8_t *__restrict__ k_codes, int Nkv,
-                                                      int64_t nk32, int64_t n8,
-                                                      __half *__restrict__ carrier,
-                                                      uint32_t *__restrict__ status)
-{
-    if (blockIdx.x == 0 && threadIdx.x < 2)
-        status[threadIdx.x] = 0u;
-    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n8;
-         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t row = idx >> 4;
-        const int g = static_cast<int>(idx & 15);
-        const int64_t bh = row / Nkv, tok = row % Nkv;
-        const uint2 c = *reinterpret_cast<const uint2 *>(k_codes + (bh * nk32 + tok) * HD + g * 8);
-        const uint4 o = make_uint4(f16x2_of_i8(c.x, 0), f16x2_of_i8(c.x, 2), f16x2_of_i8(c.y, 0),
-                                   f16x2_of_i8(c.y, 2));
-        *reinterpret_cast<uint4 *>(carrier + row * HD + g * 8) = o;
-    }
-}
-
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -889,26 +856,22 @@ float *debug_dump_buffer() { return g_debug_dump; }
 extern "C" void sattn_debug_set_dump(float *p) { g_debug_dump = p; }
 #endif
 
-size_t forward_workspace_bytes(const Geometry &g)
+size_t forward_workspace_bytes(const Geometry &)
 {
-    return kStatusBytes + static_cast<size_t>(g.B) * g.Hkv * g.Nkv * HD * sizeof(__half);
+    return kStatusBytes;
 }
 
 int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scales,
-                   const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
+                   const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
                    const float *v_scales, void *out, void *workspace, cudaStream_t stream)
 {
     auto encode = tensor_map_encoder();
     if (!encode)
         return 1;
     uint32_t *status = static_cast<uint32_t *>(workspace);
-    __half *carrier = reinterpret_cast<__half *>(static_cast<char *>(workspace) + kStatusBytes);
     const int bhk = g.B * g.Hkv;
-
-    const int64_t n8 = static_cast<int64_t>(bhk) * g.Nkv * (HD / 8);
-    const int64_t blocks = std::min<int64_t>((n8 + 255) / 256, 152 * 8);
-    widen_k_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(k_codes, g.Nkv, g.nk32, n8,
-                                                                       carrier, status);
+    if (cudaMemsetAsync(status, 0, 2 * sizeof(uint32_t), stream) != cudaSuccess)
+        return static_cast<int>(cudaGetLastError());
 
     CUtensorMap tmk, tmv;
     {
@@ -917,7 +880,7 @@ int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scal
         const cuuint64_t strides[2] = {HD * sizeof(__half), static_cast<cuuint64_t>(g.Nkv) * HD * sizeof(__half)};
         const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BN), 1};   // 256 keys x 64 channels
         const cuuint32_t estr[3] = {1, 1, 1};
-        if (encode(&tmk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, carrier, dims, strides, box, estr,
+        if (encode(&tmk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(k_carrier), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return 1;

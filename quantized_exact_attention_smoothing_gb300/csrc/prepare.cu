@@ -105,12 +105,15 @@ __global__ void __launch_bounds__(128) kv_finalize_kernel(const float *__restric
 }
 
 // One CTA per 32-token block of one head; thread = (token, quarter of the channels).
+// With kSmooth (K), the codes are also written as FP16 values to `carrier`
+// [heads][N][128], the operand of the forward's tensor-core product.
 template <bool kSmooth>
 __global__ void __launch_bounds__(128) quant_int8_kernel(const uint4 *__restrict__ x, int N,
                                                          int64_t npad, int nblk,
                                                          const float *__restrict__ mean,
                                                          int8_t *__restrict__ codes,
-                                                         float *__restrict__ scales)
+                                                         float *__restrict__ scales,
+                                                         uint4 *__restrict__ carrier)
 {
     __shared__ float warp_max[4];
     const int bh = blockIdx.y, blk = blockIdx.x;
@@ -170,6 +173,13 @@ __global__ void __launch_bounds__(128) quant_int8_kernel(const uint4 *__restrict
                                            quarter * 32);
     dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    if (kSmooth && valid) {
+        uint4 *cd = carrier + (static_cast<size_t>(bh) * N + t) * (kHeadDim / 8) + quarter * 4;
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+            cd[w] = make_uint4(ptx::f16x2_of_i8(packed[2 * w], 0), ptx::f16x2_of_i8(packed[2 * w], 2),
+                               ptx::f16x2_of_i8(packed[2 * w + 1], 0), ptx::f16x2_of_i8(packed[2 * w + 1], 2));
+    }
     if (threadIdx.x == 0)
         scales[static_cast<size_t>(bh) * nblk + blk] = s;
 }
@@ -233,8 +243,8 @@ size_t prepare_workspace_bytes(const Geometry &g)
 
 cudaError_t launch_prepare(const Geometry &g, const void *q, const void *k, const void *v,
                            int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
-                           float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace,
-                           cudaStream_t stream)
+                           float *k_mean, void *k_carrier, uint8_t *v_codes, float *v_scales,
+                           void *workspace, cudaStream_t stream)
 {
     const int bhk = g.B * g.Hkv, bhq = g.B * g.Hq;
     float *ksum = static_cast<float *>(workspace);
@@ -248,11 +258,11 @@ cudaError_t launch_prepare(const Geometry &g, const void *q, const void *k, cons
     kv_finalize_kernel<<<bhk, kHeadDim, 0, stream>>>(ksum, vmax, g.Nkv, static_cast<int>(g.nchunks),
                                                      k_mean, v_scales);
     quant_int8_kernel<true><<<dim3(static_cast<unsigned>(g.nbk), bhk), 128, 0, stream>>>(
-        k4, g.Nkv, g.nk32, static_cast<int>(g.nbk), k_mean, k_codes, k_scales);
+        k4, g.Nkv, g.nk32, static_cast<int>(g.nbk), k_mean, k_codes, k_scales, static_cast<uint4 *>(k_carrier));
     quant_v_kernel<<<dim3(static_cast<unsigned>(g.nk128 / kVPad), bhk), 256, 0, stream>>>(
         v4, g.Nkv, g.nk128, v_scales, v_codes);
     quant_int8_kernel<false><<<dim3(static_cast<unsigned>(g.nbq), bhq), 128, 0, stream>>>(
-        q4, g.Nq, g.nq32, static_cast<int>(g.nbq), nullptr, q_codes, q_scales);
+        q4, g.Nq, g.nq32, static_cast<int>(g.nbq), nullptr, q_codes, q_scales, nullptr);
     return cudaGetLastError();
 }
 

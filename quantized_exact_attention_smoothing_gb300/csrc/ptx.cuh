@@ -21,6 +21,19 @@ __device__ __forceinline__ uint64_t globaltimer()
     return t;
 }
 
+// Bytes `byte`, `byte + 1` of `word` (INT8 codes) -> FP16 pair, exactly: with
+// u = x + 128 (the code with its top bit flipped), the FP16 pattern 0x6400 | u
+// is 1024 + u, and subtracting 1152 leaves x.  One byte permute and one packed
+// FP16 subtract per pair, both on the fast pipes (integer-to-FP16 conversion
+// instructions run on the quarter-rate unit).
+__device__ __forceinline__ uint32_t f16x2_of_i8(uint32_t word, int byte)
+{
+    const uint32_t u = __byte_perm(word ^ 0x80808080u, 0x64646464u, byte == 0 ? 0x5140u : 0x7362u);
+    uint32_t h;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h) : "r"(u), "r"(0x64806480u));
+    return h;
+}
+
 // Read-only global load that the compiler may not move: issued where written,
 // so a value needed one loop iteration later hides its latency.
 __device__ __forceinline__ float ld_nc_f32(const float *p)

@@ -65,13 +65,14 @@ void fill_sizes(const Geometry &g, sattn_sizes *z)
     z->k_codes = r16(bhk * g.nk32 * D);
     z->k_scales = r16(bhk * g.nbk * 4);
     z->k_mean = r16(bhk * D * 4);
+    z->k_carrier = r16(bhk * g.Nkv * D * 2);
     z->v_codes = r16(bhk * D * g.nk128);
     z->v_scales = r16(bhk * D * 4);
     z->out = r16(bhq * g.Nq * D * 2);
     z->prepare_workspace = r16(sattn::prepare_workspace_bytes(g));
     z->forward_workspace = r16(sattn::forward_workspace_bytes(g));
     z->arena = r256(z->q) + r256(z->k) + r256(z->v) + r256(z->q_codes) + r256(z->q_scales) +
-               r256(z->k_codes) + r256(z->k_scales) + r256(z->k_mean) + r256(z->v_codes) +
+               r256(z->k_codes) + r256(z->k_scales) + r256(z->k_mean) + r256(z->k_carrier) + r256(z->v_codes) +
                r256(z->v_scales) + r256(z->out) + r256(z->prepare_workspace) +
                r256(z->forward_workspace);
 }
@@ -96,10 +97,11 @@ int check_device()
 }
 
 int prepare_impl(const Geometry &g, const void *q, const void *k, const void *v, int8_t *q_codes,
-                 float *q_scales, int8_t *k_codes, float *k_scales, float *k_mean, uint8_t *v_codes,
-                 float *v_scales, void *workspace, cudaStream_t stream)
+                 float *q_scales, int8_t *k_codes, float *k_scales, float *k_mean, void *k_carrier,
+                 uint8_t *v_codes, float *v_scales, void *workspace, cudaStream_t stream)
 {
-    const void *ptrs[] = {q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes, v_scales, workspace};
+    const void *ptrs[] = {q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes, v_scales,
+                          workspace};
     for (const void *p : ptrs) {
         if (!p)
             return SATTN_ERR_INVALID;
@@ -109,17 +111,17 @@ int prepare_impl(const Geometry &g, const void *q, const void *k, const void *v,
     const int dev = check_device();
     if (dev != SATTN_OK)
         return dev;
-    return sattn::launch_prepare(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes,
+    return sattn::launch_prepare(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes,
                                  v_scales, workspace, stream) == cudaSuccess
                ? SATTN_OK
                : SATTN_ERR_LAUNCH;
 }
 
 int forward_impl(const Geometry &g, const int8_t *q_codes, const float *q_scales,
-                 const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
+                 const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
                  const float *v_scales, void *out, void *workspace, cudaStream_t stream)
 {
-    const void *ptrs[] = {q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, out, workspace};
+    const void *ptrs[] = {q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out, workspace};
     for (const void *p : ptrs) {
         if (!p)
             return SATTN_ERR_INVALID;
@@ -129,7 +131,7 @@ int forward_impl(const Geometry &g, const int8_t *q_codes, const float *q_scales
     const int dev = check_device();
     if (dev != SATTN_OK)
         return dev;
-    const int rc = sattn::launch_forward(g, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales,
+    const int rc = sattn::launch_forward(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales,
                                          out, workspace, stream);
     if (rc == 1)
         return SATTN_ERR_DEVICE;   // no tensor-map encoder in this driver
@@ -154,25 +156,26 @@ int sattn_query_sizes(const sattn_shape *shape, sattn_sizes *sizes)
 
 int sattn_prepare(const sattn_shape *shape, const void *q, const void *k, const void *v,
                   int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
-                  float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace, void *stream)
+                  float *k_mean, void *k_carrier, uint8_t *v_codes, float *v_scales, void *workspace,
+                  void *stream)
 {
     Geometry g;
     const int rc = make_geometry(shape, &g);
     if (rc != SATTN_OK)
         return rc;
-    return prepare_impl(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes, v_scales,
+    return prepare_impl(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes, v_scales,
                         workspace, static_cast<cudaStream_t>(stream));
 }
 
 int sattn_forward(const sattn_shape *shape, const int8_t *q_codes, const float *q_scales,
-                  const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
+                  const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
                   const float *v_scales, void *out, void *workspace, void *stream)
 {
     Geometry g;
     const int rc = make_geometry(shape, &g);
     if (rc != SATTN_OK)
         return rc;
-    return forward_impl(g, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, out, workspace,
+    return forward_impl(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out, workspace,
                         static_cast<cudaStream_t>(stream));
 }
 
@@ -222,6 +225,7 @@ int sattn_attention_host(const sattn_shape *shape, const void *q_host, const voi
     int8_t *k_codes = reinterpret_cast<int8_t *>(take(z.k_codes));
     float *k_scales = reinterpret_cast<float *>(take(z.k_scales));
     float *k_mean = reinterpret_cast<float *>(take(z.k_mean));
+    void *k_carrier = take(z.k_carrier);
     uint8_t *v_codes = reinterpret_cast<uint8_t *>(take(z.v_codes));
     float *v_scales = reinterpret_cast<float *>(take(z.v_scales));
     void *out = take(z.out);
@@ -234,11 +238,11 @@ int sattn_attention_host(const sattn_shape *shape, const void *q_host, const voi
         cudaMemcpyAsync(k, k_host, kb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
         cudaMemcpyAsync(v, v_host, kb, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return SATTN_ERR_LAUNCH;
-    rc = prepare_impl(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes, v_scales,
+    rc = prepare_impl(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes, v_scales,
                       pws, s);
     if (rc != SATTN_OK)
         return rc;
-    rc = forward_impl(g, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, out, fws, s);
+    rc = forward_impl(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out, fws, s);
     if (rc != SATTN_OK)
         return rc;
     if (cudaMemcpyAsync(out_host, out, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
@@ -297,13 +301,13 @@ int prepare_scratch_address(void **out)
 extern "C" int sattn_prepare_noalloc(const sattn_shape *shape, const void *q, const void *k,
                                      const void *v, int8_t *q_codes, float *q_scales,
                                      int8_t *k_codes, float *k_scales, float *k_mean,
-                                     uint8_t *v_codes, float *v_scales, void *stream)
+                                     void *k_carrier, uint8_t *v_codes, float *v_scales, void *stream)
 {
     Geometry g;
     int rc = make_geometry(shape, &g);
     if (rc != SATTN_OK)
         return rc;
-    const void *ptrs[] = {q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes, v_scales};
+    const void *ptrs[] = {q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes, v_scales};
     for (const void *p : ptrs) {
         if (!p)
             return SATTN_ERR_INVALID;
@@ -319,7 +323,7 @@ extern "C" int sattn_prepare_noalloc(const sattn_shape *shape, const void *q, co
     rc = prepare_scratch_address(&scratch);
     if (rc != SATTN_OK)
         return rc;
-    return sattn::launch_prepare(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes,
+    return sattn::launch_prepare(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes,
                                  v_scales, scratch, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? SATTN_OK
                : SATTN_ERR_LAUNCH;

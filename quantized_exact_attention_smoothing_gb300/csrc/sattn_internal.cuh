@@ -30,16 +30,16 @@ struct Geometry {
 size_t prepare_workspace_bytes(const Geometry &g);
 cudaError_t launch_prepare(const Geometry &g, const void *q, const void *k, const void *v,
                            int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
-                           float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace,
-                           cudaStream_t stream);
+                           float *k_mean, void *k_carrier, uint8_t *v_codes, float *v_scales,
+                           void *workspace, cudaStream_t stream);
 
 // ---- forward (attn_fwd.cu) ----
-// Workspace: 256-byte status block, then the FP16 carrier of the K codes [B*Hkv][Nkv][128].
+// Workspace: the 256-byte status block.
 constexpr size_t kStatusBytes = 256;
 size_t forward_workspace_bytes(const Geometry &g);
 // Returns 0 on success, 1 if a tensor map could not be encoded, or a CUDA error.
 int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scales,
-                   const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
+                   const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
                    const float *v_scales, void *out, void *workspace, cudaStream_t stream);
 
 }  // namespace sattn

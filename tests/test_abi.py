@@ -26,7 +26,8 @@ def test_query_sizes_headline_shape():
     assert z["q_codes"] == 4 * 32 * 8192 * 128
     assert z["v_codes"] == 4 * 8 * 128 * 8192
     assert z["q_scales"] == 4 * 32 * 256 * 4
-    assert z["forward_workspace"] == 256 + 4 * 8 * 8192 * 128 * 2
+    assert z["forward_workspace"] == 256
+    assert z["k_carrier"] == 4 * 8 * 8192 * 128 * 2
     assert all(v % 16 == 0 for v in z.values())
 
 
@@ -59,7 +60,7 @@ def test_head_dim_other_than_128_rejected(lib):
 
 def test_null_and_misaligned_pointers_rejected_before_any_device_work(lib):
     s = sattn.make_shape(1, 1, 1, 8, 8)
-    good = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(11)]
+    good = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(12)]
     args = list(good)
     args[3] = None
     assert lib.sattn_prepare(ctypes.byref(s), *args, None) == 1
