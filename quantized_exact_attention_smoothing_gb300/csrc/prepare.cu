@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(256) kv_chunk_stats_kernel(const uint4 *__rest
         s[i] = 0.0f;
         mx[i] = 0.0f;
     }
-#pragma unroll 8
+#pragma unroll 16
     for (int t = t0; t < t1; ++t) {
         const uint4 a = ld_stream(kp);
         const uint4 c = ld_stream(vp);
@@ -95,13 +95,59 @@ __global__ void __launch_bounds__(128) kv_finalize_kernel(const float *__restric
     const float *ks = ksum + static_cast<size_t>(bh) * nchunks * kHeadDim + c;
     const float *vm = vmax + static_cast<size_t>(bh) * nchunks * kHeadDim + c;
     float total = 0.0f, amax = 0.0f;
-#pragma unroll 8
-    for (int ch = 0; ch < nchunks; ++ch) {
+    int ch = 0;
+    for (; ch + 64 <= nchunks; ch += 64) {   // 128 loads in flight, then the ordered sum
+        float a[64], b[64];
+#pragma unroll
+        for (int u = 0; u < 64; ++u) {
+            a[u] = ks[static_cast<size_t>(ch + u) * kHeadDim];
+            b[u] = vm[static_cast<size_t>(ch + u) * kHeadDim];
+        }
+#pragma unroll
+        for (int u = 0; u < 64; ++u) {
+            total = __fadd_rn(total, a[u]);
+            amax = fmaxf(amax, b[u]);
+        }
+    }
+    for (; ch < nchunks; ++ch) {
         total = __fadd_rn(total, ks[static_cast<size_t>(ch) * kHeadDim]);
         amax = fmaxf(amax, vm[static_cast<size_t>(ch) * kHeadDim]);
     }
     k_mean[bh * kHeadDim + c] = __fdiv_rn(total, static_cast<float>(Nkv));
     v_scales[bh * kHeadDim + c] = __fdiv_rn(amax, 448.0f);
+}
+
+// clamp(rint(fl(x / s)), -127, 127) without a division in the common case:
+// q = fl(x * fl(1/s)) lies within 3 ulp of fl(x / s) (two roundings of
+// relative size 2^-24 each, plus that of the quotient), and |q| <= 127 * (1 +
+// 2^-22), so an ulp of q is at most 2^-16.  When q is farther than 2^-14 from
+// the nearest half-integer, fl(x / s) rounds to the same integer as q; only
+// the rare values near a rounding tie take the IEEE division.  Rounding to an
+// integer adds and subtracts 1.5 * 2^23 (exact, ties to even, |q| < 2^22).
+// The code is returned as its two's-complement byte, read from the low bits
+// of k + 1.5 * 2^23 (no float-to-integer conversion instruction).
+__device__ __forceinline__ uint32_t int8_code(float x, float s, float rs)
+{
+    const float q = __fmul_rn(x, rs);
+    float k = __fsub_rn(__fadd_rn(q, 12582912.0f), 12582912.0f);
+    if (!(fabsf(__fsub_rn(q, k)) < 0.49993896484375f))   // 0.5 - 2^-14; false for NaN / inf too
+        k = rintf(__fdiv_rn(x, s));
+    k = fminf(fmaxf(k, -127.0f), 127.0f);
+    return __float_as_uint(__fadd_rn(k, 12582912.0f)) & 0xffu;
+}
+
+// E4M3(fl(v / s)) (round to nearest even, saturating) without a division in
+// the common case: y = fl(v * fl(1/s)) is within 3 ulp (relative 2^-22.4) of
+// fl(v / s), so if y * (1 - 2^-21) and y * (1 + 2^-21) round to the same code
+// (the conversion is monotonic), fl(v / s) does too.  Otherwise (values near a
+// rounding midpoint) the IEEE division decides.  Returns the byte.
+__device__ __forceinline__ uint32_t e4m3_code(float v, float s, float rs)
+{
+    const float y = __fmul_rn(v, rs);
+    const uint32_t two = ptx::cvt_e4m3x2(__fmul_rn(y, 1.0f + 0x1p-21f), __fmul_rn(y, 1.0f - 0x1p-21f));
+    if ((two & 0xffu) == (two >> 8))
+        return two & 0xffu;
+    return ptx::cvt_e4m3x2(0.0f, __fdiv_rn(v, s)) & 0xffu;
 }
 
 // One CTA per 32-token block of one head; thread = (token, quarter of the channels).
@@ -154,20 +200,19 @@ __global__ void __launch_bounds__(128) quant_int8_kernel(const uint4 *__restrict
     __syncthreads();
     const float amax = fmaxf(fmaxf(warp_max[0], warp_max[1]), fmaxf(warp_max[2], warp_max[3]));
     const float s = __fdiv_rn(amax, 127.0f);
+    const float rs = s > 0.0f ? __frcp_rn(s) : 0.0f;
     uint32_t packed[8];
+    if (valid && s > 0.0f) {
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-        uint32_t word = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            int code = 0;
-            if (valid && s > 0.0f) {
-                const float q = rintf(__fdiv_rn(val[w * 4 + b], s));
-                code = static_cast<int>(fminf(fmaxf(q, -127.0f), 127.0f));
-            }
-            word |= (static_cast<uint32_t>(code) & 0xffu) << (8 * b);
+        for (int w = 0; w < 8; ++w) {
+            const uint32_t lo = __byte_perm(int8_code(val[w * 4], s, rs), int8_code(val[w * 4 + 1], s, rs), 0x0040u);
+            const uint32_t hi = __byte_perm(int8_code(val[w * 4 + 2], s, rs), int8_code(val[w * 4 + 3], s, rs), 0x0040u);
+            packed[w] = __byte_perm(lo, hi, 0x5410u);
         }
-        packed[w] = word;
+    } else {
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+            packed[w] = 0u;
     }
     uint4 *dst = reinterpret_cast<uint4 *>(codes + (static_cast<size_t>(bh) * npad + t) * kHeadDim +
                                            quarter * 32);
@@ -184,53 +229,69 @@ __global__ void __launch_bounds__(128) quant_int8_kernel(const uint4 *__restrict
         scales[static_cast<size_t>(bh) * nblk + blk] = s;
 }
 
-// One CTA per 128-token tile of one KV head: E4M3 codes staged in shared
-// memory as [channel][token] and written out channel-major.
-constexpr int kVRow = 144;   // shared row stride in bytes (16-byte multiple)
-
+// One CTA per 128-token tile of one KV head.  Phase 1: coalesced 16-byte
+// loads of 8 channels of one token, E4M3 codes written token-major into
+// shared memory (8 bytes per store).  Phase 2: each thread gathers 16
+// consecutive tokens of one channel and writes them channel-major (16-byte
+// stores).  Word j of token row t is stored at word j ^ (2 * ((t >> 4) & 7)),
+// so the 16-token gathers of one warp hit eight distinct banks.
 __global__ void __launch_bounds__(256) quant_v_kernel(const uint4 *__restrict__ v, int Nkv,
                                                       int64_t nk128,
                                                       const float *__restrict__ v_scales,
                                                       uint8_t *__restrict__ vcodes)
 {
-    __shared__ __align__(16) uint8_t tile[kHeadDim * kVRow];
-    __shared__ float sv[kHeadDim];
+    __shared__ __align__(16) uint32_t tile[kVPad * 32];   // [token][32 words]
+    __shared__ float sv[kHeadDim], rv[kHeadDim];
     const int bh = blockIdx.y;
     const int t0 = blockIdx.x * kVPad;
-    if (threadIdx.x < kHeadDim)
-        sv[threadIdx.x] = v_scales[bh * kHeadDim + threadIdx.x];
+    if (threadIdx.x < kHeadDim) {
+        const float x = v_scales[bh * kHeadDim + threadIdx.x];
+        sv[threadIdx.x] = x;
+        rv[threadIdx.x] = x > 0.0f ? __frcp_rn(x) : 0.0f;
+    }
     __syncthreads();
+    const int g = threadIdx.x & 15;                        // this thread's 8 channels, every item
+    float s8[8], r8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        s8[i] = sv[g * 8 + i];
+        r8[i] = rv[g * 8 + i];
+    }
 #pragma unroll 2
     for (int it = 0; it < 8; ++it) {
-        const int item = threadIdx.x + it * 256;
-        const int row = item >> 4, g = item & 15;
+        const int row = (threadIdx.x + it * 256) >> 4;
         const int t = t0 + row;
-        float f[8];
-        if (t < Nkv)
+        uint32_t w0 = 0, w1 = 0;
+        if (t < Nkv) {
+            float f[8];
+            uint32_t cd[8];
             unpack8(ld_stream(v + (static_cast<size_t>(bh) * Nkv + t) * 16 + g), f);
 #pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-            const int c = g * 8 + i;
-            float y0 = 0.0f, y1 = 0.0f;
-            if (t < Nkv) {
-                if (sv[c] > 0.0f)
-                    y0 = __fdiv_rn(f[i], sv[c]);
-                if (sv[c + 1] > 0.0f)
-                    y1 = __fdiv_rn(f[i + 1], sv[c + 1]);
-            }
-            const uint32_t two = ptx::cvt_e4m3x2(y1, y0);
-            tile[c * kVRow + row] = static_cast<uint8_t>(two & 0xffu);
-            tile[(c + 1) * kVRow + row] = static_cast<uint8_t>(two >> 8);
+            for (int i = 0; i < 8; ++i)
+                cd[i] = s8[i] > 0.0f ? e4m3_code(f[i], s8[i], r8[i]) : 0u;
+            w0 = __byte_perm(__byte_perm(cd[0], cd[1], 0x0040u), __byte_perm(cd[2], cd[3], 0x0040u), 0x5410u);
+            w1 = __byte_perm(__byte_perm(cd[4], cd[5], 0x0040u), __byte_perm(cd[6], cd[7], 0x0040u), 0x5410u);
         }
+        const int sw = ((row >> 4) & 7) << 1;
+        *reinterpret_cast<uint2 *>(&tile[row * 32 + ((2 * g) ^ sw)]) = make_uint2(w0, w1);
     }
     __syncthreads();
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
         const int idx = threadIdx.x + it * 256;
-        const int c = idx >> 3, w = idx & 7;
-        const uint4 val = *reinterpret_cast<const uint4 *>(tile + c * kVRow + w * 16);
-        *reinterpret_cast<uint4 *>(vcodes + (static_cast<size_t>(bh) * kHeadDim + c) * nk128 + t0 +
-                                   w * 16) = val;
+        const int c = idx >> 3, w = idx & 7;               // channel, 16-token group
+        const int word = (c >> 2) ^ (2 * w);
+        const uint32_t sel = (c & 3) | ((4 + (c & 3)) << 4);   // byte c % 4 of each of two words
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t *rowp = tile + (16 * w + 4 * q) * 32 + word;
+            const uint32_t ab = __byte_perm(rowp[0], rowp[32], sel);
+            const uint32_t cdw = __byte_perm(rowp[64], rowp[96], sel);
+            o[q] = __byte_perm(ab, cdw, 0x5410u);
+        }
+        *reinterpret_cast<uint4 *>(vcodes + (static_cast<size_t>(bh) * kHeadDim + c) * nk128 + t0 + w * 16) =
+            make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
