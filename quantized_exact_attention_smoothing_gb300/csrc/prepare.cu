@@ -150,47 +150,56 @@ __device__ __forceinline__ uint32_t e4m3_code(float v, float s, float rs)
     return ptx::cvt_e4m3x2(0.0f, __fdiv_rn(v, s)) & 0xffu;
 }
 
-// One CTA per 32-token block of one head; thread = (token, quarter of the channels).
-// With kSmooth (K), the codes are also written as FP16 values to `carrier`
-// [heads][N][128], the operand of the forward's tensor-core product.
+// One CTA per 32-token block of one head; thread = (token, eighth of the
+// channels: 16 values), so a thread holds few registers and many CTAs stay
+// resident to keep loads in flight.  With kSmooth (K), the codes are also
+// written as FP16 values to `carrier` [heads][N][128], the operand of the
+// forward's tensor-core product.
 template <bool kSmooth>
-__global__ void __launch_bounds__(128) quant_int8_kernel(const uint4 *__restrict__ x, int N,
+__global__ void __launch_bounds__(256) quant_int8_kernel(const uint4 *__restrict__ x, int N,
                                                          int64_t npad, int nblk,
                                                          const float *__restrict__ mean,
                                                          int8_t *__restrict__ codes,
                                                          float *__restrict__ scales,
                                                          uint4 *__restrict__ carrier)
 {
-    __shared__ float warp_max[4];
+    __shared__ float warp_max[8];
     const int bh = blockIdx.y, blk = blockIdx.x;
-    const int r = threadIdx.x >> 2, quarter = threadIdx.x & 3;
+    const int r = threadIdx.x >> 3, part = threadIdx.x & 7;
     const int t = blk * kQBlock + r;
     const bool valid = t < N;
-    float val[32];
+    float val[16];
     if (valid) {
-        const uint4 *src = x + (static_cast<size_t>(bh) * N + t) * 16 + quarter * 4;
+        const uint4 *src = x + (static_cast<size_t>(bh) * N + t) * 16 + part * 2;
+        const uint4 a = ld_stream(src), b = ld_stream(src + 1);
+        float f[8];
+        unpack8(a, f);
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            float f[8];
-            unpack8(ld_stream(src + w), f);
+        for (int i = 0; i < 8; ++i)
+            val[i] = f[i];
+        unpack8(b, f);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                val[w * 8 + i] = f[i];
-        }
+        for (int i = 0; i < 8; ++i)
+            val[8 + i] = f[i];
         if (kSmooth) {
-            const float *mu = mean + bh * kHeadDim + quarter * 32;
+            const float4 *mu = reinterpret_cast<const float4 *>(mean + bh * kHeadDim + part * 16);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                val[i] = __fsub_rn(val[i], mu[i]);
+            for (int w = 0; w < 4; ++w) {
+                const float4 m4 = mu[w];
+                val[4 * w] = __fsub_rn(val[4 * w], m4.x);
+                val[4 * w + 1] = __fsub_rn(val[4 * w + 1], m4.y);
+                val[4 * w + 2] = __fsub_rn(val[4 * w + 2], m4.z);
+                val[4 * w + 3] = __fsub_rn(val[4 * w + 3], m4.w);
+            }
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 16; ++i)
             val[i] = 0.0f;
     }
     float am = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 16; ++i)
         am = fmaxf(am, fabsf(val[i]));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
@@ -198,30 +207,31 @@ __global__ void __launch_bounds__(128) quant_int8_kernel(const uint4 *__restrict
     if ((threadIdx.x & 31) == 0)
         warp_max[threadIdx.x >> 5] = am;
     __syncthreads();
-    const float amax = fmaxf(fmaxf(warp_max[0], warp_max[1]), fmaxf(warp_max[2], warp_max[3]));
+    float amax = warp_max[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w)
+        amax = fmaxf(amax, warp_max[w]);
     const float s = __fdiv_rn(amax, 127.0f);
     const float rs = s > 0.0f ? __frcp_rn(s) : 0.0f;
-    uint32_t packed[8];
+    uint32_t packed[4];
     if (valid && s > 0.0f) {
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
+        for (int w = 0; w < 4; ++w) {
             const uint32_t lo = __byte_perm(int8_code(val[w * 4], s, rs), int8_code(val[w * 4 + 1], s, rs), 0x0040u);
             const uint32_t hi = __byte_perm(int8_code(val[w * 4 + 2], s, rs), int8_code(val[w * 4 + 3], s, rs), 0x0040u);
             packed[w] = __byte_perm(lo, hi, 0x5410u);
         }
     } else {
 #pragma unroll
-        for (int w = 0; w < 8; ++w)
+        for (int w = 0; w < 4; ++w)
             packed[w] = 0u;
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(codes + (static_cast<size_t>(bh) * npad + t) * kHeadDim +
-                                           quarter * 32);
-    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    *reinterpret_cast<uint4 *>(codes + (static_cast<size_t>(bh) * npad + t) * kHeadDim + part * 16) =
+        make_uint4(packed[0], packed[1], packed[2], packed[3]);
     if (kSmooth && valid) {
-        uint4 *cd = carrier + (static_cast<size_t>(bh) * N + t) * (kHeadDim / 8) + quarter * 4;
+        uint4 *cd = carrier + (static_cast<size_t>(bh) * N + t) * (kHeadDim / 8) + part * 2;
 #pragma unroll
-        for (int w = 0; w < 4; ++w)
+        for (int w = 0; w < 2; ++w)
             cd[w] = make_uint4(ptx::f16x2_of_i8(packed[2 * w], 0), ptx::f16x2_of_i8(packed[2 * w], 2),
                                ptx::f16x2_of_i8(packed[2 * w + 1], 0), ptx::f16x2_of_i8(packed[2 * w + 1], 2));
     }
@@ -318,11 +328,11 @@ cudaError_t launch_prepare(const Geometry &g, const void *q, const void *k, cons
                             stream>>>(k4, v4, g.Nkv, static_cast<int>(g.nchunks), ksum, vmax);
     kv_finalize_kernel<<<bhk, kHeadDim, 0, stream>>>(ksum, vmax, g.Nkv, static_cast<int>(g.nchunks),
                                                      k_mean, v_scales);
-    quant_int8_kernel<true><<<dim3(static_cast<unsigned>(g.nbk), bhk), 128, 0, stream>>>(
+    quant_int8_kernel<true><<<dim3(static_cast<unsigned>(g.nbk), bhk), 256, 0, stream>>>(
         k4, g.Nkv, g.nk32, static_cast<int>(g.nbk), k_mean, k_codes, k_scales, static_cast<uint4 *>(k_carrier));
     quant_v_kernel<<<dim3(static_cast<unsigned>(g.nk128 / kVPad), bhk), 256, 0, stream>>>(
         v4, g.Nkv, g.nk128, v_scales, v_codes);
-    quant_int8_kernel<false><<<dim3(static_cast<unsigned>(g.nbq), bhq), 128, 0, stream>>>(
+    quant_int8_kernel<false><<<dim3(static_cast<unsigned>(g.nbq), bhq), 256, 0, stream>>>(
         q4, g.Nq, g.nq32, static_cast<int>(g.nbq), nullptr, q_codes, q_scales, nullptr);
     return cudaGetLastError();
 }
