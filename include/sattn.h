@@ -158,6 +158,19 @@ int sattn_forward(const sattn_shape *shape, const int8_t *q_codes, const float *
                   const float *v_scales, void *out, void *workspace, void *stream);
 
 /*
+ * sattn_test_forward_withhold_v -- test hook for failure detection, not part
+ * of the computation (the page has no counterpart).  Same arguments as
+ * sattn_forward; the launch loads no V tile, so the MMA thread's wait for V
+ * runs out after about one second, the other roles stop at their own bounded
+ * waits, every CTA releases its tensor memory and the kernel ends.
+ * sattn_check_status then returns SATTN_ERR_TIMEOUT; `out` is undefined.  The
+ * CUDA context stays usable: a following sattn_forward computes normally.
+ */
+int sattn_test_forward_withhold_v(const sattn_shape *shape, const int8_t *q_codes, const float *q_scales,
+                                  const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
+                                  const float *v_scales, void *out, void *workspace, void *stream);
+
+/*
  * sattn_check_status -- synchronise `stream` and read the status word that
  * sattn_forward left in `forward_workspace`.  Returns SATTN_OK, or
  * SATTN_ERR_TIMEOUT if a bounded device wait ran out, or SATTN_ERR_DEVICE if

@@ -69,6 +69,7 @@ def load_library(build: bool = True):
     lib.sattn_query_sizes.argtypes = [SP, ctypes.POINTER(sattn_sizes)]
     lib.sattn_prepare.argtypes = [SP] + [P] * 13
     lib.sattn_forward.argtypes = [SP] + [P] * 9
+    lib.sattn_test_forward_withhold_v.argtypes = [SP] + [P] * 9
     lib.sattn_prepare_noalloc.argtypes = [SP] + [P] * 12
     lib.sattn_check_status.argtypes = [P, P]
     lib.sattn_attention_host.argtypes = [SP, P, P, P, P, P, ctypes.c_size_t, P]
@@ -216,6 +217,30 @@ def forward(prep: dict, out: torch.Tensor | None = None, workspace: torch.Tensor
         _ptr(workspace), _stream(stream))
     if rc != 0:
         raise SattnError(rc, "sattn_forward")
+    return out
+
+
+def forward_withhold_v_for_test(prep: dict, out: torch.Tensor | None = None,
+                                workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """sattn_test_forward_withhold_v: a forward launch that loads no V tile, so
+    its bounded waits run out (about one second) and check_status() reports
+    SATTN_ERR_TIMEOUT.  Test hook for failure detection; `out` is undefined."""
+    shape = prep["shape"]
+    dev = prep["q_codes"].device
+    if out is None:
+        out = torch.empty((shape.B, shape.Hq, shape.Nq, HEAD_DIM), dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        workspace = prep.get("forward_workspace")
+        if workspace is None:
+            workspace = _empty(query_sizes(shape)["forward_workspace"], dev)
+            prep["forward_workspace"] = workspace
+    _need_cuda(out, workspace)
+    rc = load_library().sattn_test_forward_withhold_v(
+        ctypes.byref(shape), _ptr(prep["q_codes"]), _ptr(prep["q_scales"]), _ptr(prep["k_carrier"]),
+        _ptr(prep["k_scales"]), _ptr(prep["v_codes"]), _ptr(prep["v_scales"]), _ptr(out),
+        _ptr(workspace), _stream(stream))
+    if rc != 0:
+        raise SattnError(rc, "sattn_test_forward_withhold_v")
     return out
 
 

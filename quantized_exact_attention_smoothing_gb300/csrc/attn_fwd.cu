@@ -116,7 +116,8 @@ enum Bar : int {
 };
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBARS * 8;
 constexpr uint32_t OFF_FLAG = OFF_TMEM_SLOT + 4;
-constexpr uint32_t SMEM_BYTES = OFF_FLAG + 4 + 1024;   // + alignment slack
+constexpr uint32_t OFF_ABORT = OFF_FLAG + 4;          // set by a compute warp that gave up
+constexpr uint32_t SMEM_BYTES = OFF_ABORT + 4 + 1024;   // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(OFF_V % 1024 == 0 && V_SLOT_BYTES % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_QS % 1024 == 0,
               "swizzle atoms must be 1024-aligned");
@@ -133,6 +134,7 @@ struct FwdParams {
     __nv_bfloat16 *out;
     uint32_t *status;
     int B, Hq, Hkv, Nq, Nkv, group, n_qtiles, n_items, causal;
+    int withhold_v;   // test hook: the V loader stages the first Q tile and loads no V
     // reciprocals for exact division by Hq * B, Hq and group (see udiv)
     unsigned long long m_hb, m_hq, m_group;
     int nq32, nbq, nbk;
@@ -300,6 +302,11 @@ __device__ __forceinline__ void vload_role(const FwdParams &p, const CUtensorMap
         ptx::bulk_load(sb + OFF_SV + (nq % 3) * SV_BYTES, p.v_scales + static_cast<size_t>(tq.b * p.Hkv + tq.hk) * HD,
                        SV_BYTES, bar(QSTAGE));
     };
+    if (p.withhold_v) {   // test hook: the MMA thread's wait for V runs out
+        load_q(item_tile(p, blockIdx.x), 0);
+        wt.drain(bar(QSTAGE), 0);
+        return;
+    }
     int issued_v = -1, issued_q = -1;
     bool ok = true;
     int g = 0, n = 0;   // KV tiles and items of this CTA before the current item
@@ -437,7 +444,7 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
 // items the warps write the next item's Q into TMEM (free once the last QK of
 // the current item has completed) before the last fold and the final
 // conversion, so the next QK overlaps them.
-__device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, uint32_t tmem, int warp, int lane,
+__device__ __forceinline__ bool compute_loop(const FwdParams &p, uint32_t sb, uint32_t tmem, int warp, int lane,
                                              const Waiter &wt)
 {
     auto bar = [sb](int i) { return sb + OFF_BAR + 8u * i; };
@@ -489,7 +496,7 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
     int it = blockIdx.x;
     Tile t = item_tile(p, it);
     if (!store_q(0))
-        return;
+        return false;
     if (r == 0 && half == 0)
         SATTN_TRACE(p, t, 38, 1);
     float sq = qscale(t);
@@ -571,7 +578,7 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
             if (r == 0 && half == 0)
                 SATTN_TRACE(p, t, 41, j);
             if (!wt.wait(bar(SFULL), gj & 1, SITE_S))
-                return;
+                return false;
             ptx::tc_fence_after();
             if (r == 0 && half == 0)
                 SATTN_TRACE(p, t, 0, j);
@@ -633,6 +640,8 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
             ptx::st_shared_f32(maxx + 4 * (((gj & 1) * 2 + half) * BM + r), tmax);
             if ((r & 31) == 0)
                 SATTN_TRACE(p, t, 21 + 4 * half + (r >> 5), j);
+            if (ptx::ld_shared_u32(sb + OFF_ABORT) != 0)   // a warp gave up: leave, do not wait for it
+                return false;
             ptx::named_bar_sync(1 + quarter, 64);
             tmax = fmaxf(tmax, ptx::ld_shared_f32(maxx + 4 * (((gj & 1) * 2 + (half ^ 1)) * BM + r)));
             if (r == 0 && half == 0)
@@ -674,7 +683,7 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
             for (int c = 0; c < 4; ++c)
                 p_ok = p_ok && p_block(c);
             if (!p_ok)
-                return;
+                return false;
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(PFULL));
@@ -685,14 +694,14 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
             // after the last P of this item its last QK has completed (its S was
             // read above), so the Q columns of TMEM can take the next item's Q
             if (j == t.ntiles - 1 && has_next && !store_q(n + 1))
-                return;
+                return false;
             if (j >= 1 && !fold_partial(gj - 1, j - 1, t, alpha_prev))
-                return;
+                return false;
             alpha_prev = alpha;
             m = mn;
         }
         if (!fold_partial(g + t.ntiles - 1, t.ntiles - 1, t, alpha_prev))
-            return;
+            return false;
 
         if (r == 0 && half == 0)
             SATTN_TRACE(p, t, 39, 2);
@@ -745,6 +754,21 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
         t = item_tile(p, nx);
         sq = sq_next;
     }
+    return true;
+}
+
+// A compute warp that gave up (a bounded wait ran out, or another role
+// reported a failure) marks the CTA as aborting and arrives once on its pair's
+// exchange barrier: a partner already waiting there is released, and every
+// compute warp checks the mark before that barrier, so none waits for a warp
+// that has left.
+__device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, uint32_t tmem, int warp, int lane,
+                                             const Waiter &wt)
+{
+    if (!compute_loop(p, sb, tmem, warp, lane, wt)) {
+        asm volatile("st.shared.u32 [%0], 1;" ::"r"(sb + OFF_ABORT) : "memory");
+        ptx::named_bar_arrive(1 + (warp & 3), 64);
+    }
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -765,6 +789,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     if (threadIdx.x == 0) {
         *flag = *reinterpret_cast<volatile uint32_t *>(p.status);
+        *reinterpret_cast<volatile uint32_t *>(smem + OFF_ABORT) = 0u;
         const uint32_t b0 = sb + OFF_BAR;
         for (int s = 0; s < KSLOTS; ++s) {
             ptx::mbar_init(b0 + 8u * (KFULL + s), 1);
@@ -863,7 +888,7 @@ size_t forward_workspace_bytes(const Geometry &)
 
 int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scales,
                    const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
-                   const float *v_scales, void *out, void *workspace, cudaStream_t stream)
+                   const float *v_scales, void *out, void *workspace, cudaStream_t stream, bool withhold_v)
 {
     auto encode = tensor_map_encoder();
     if (!encode)
@@ -934,6 +959,7 @@ int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scal
     prm.v_scales = v_scales;
     prm.out = static_cast<__nv_bfloat16 *>(out);
     prm.status = status;
+    prm.withhold_v = withhold_v ? 1 : 0;
     prm.B = g.B;
     prm.Hq = g.Hq;
     prm.Hkv = g.Hkv;

@@ -119,7 +119,8 @@ int prepare_impl(const Geometry &g, const void *q, const void *k, const void *v,
 
 int forward_impl(const Geometry &g, const int8_t *q_codes, const float *q_scales,
                  const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
-                 const float *v_scales, void *out, void *workspace, cudaStream_t stream)
+                 const float *v_scales, void *out, void *workspace, cudaStream_t stream,
+                 bool withhold_v = false)
 {
     const void *ptrs[] = {q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out, workspace};
     for (const void *p : ptrs) {
@@ -132,7 +133,7 @@ int forward_impl(const Geometry &g, const int8_t *q_codes, const float *q_scales
     if (dev != SATTN_OK)
         return dev;
     const int rc = sattn::launch_forward(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales,
-                                         out, workspace, stream);
+                                         out, workspace, stream, withhold_v);
     if (rc == 1)
         return SATTN_ERR_DEVICE;   // no tensor-map encoder in this driver
     return rc == 0 ? SATTN_OK : SATTN_ERR_LAUNCH;
@@ -177,6 +178,18 @@ int sattn_forward(const sattn_shape *shape, const int8_t *q_codes, const float *
         return rc;
     return forward_impl(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out, workspace,
                         static_cast<cudaStream_t>(stream));
+}
+
+int sattn_test_forward_withhold_v(const sattn_shape *shape, const int8_t *q_codes, const float *q_scales,
+                                  const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
+                                  const float *v_scales, void *out, void *workspace, void *stream)
+{
+    Geometry g;
+    const int rc = make_geometry(shape, &g);
+    if (rc != SATTN_OK)
+        return rc;
+    return forward_impl(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out, workspace,
+                        static_cast<cudaStream_t>(stream), true);
 }
 
 int sattn_check_status(const void *forward_workspace, void *stream)

@@ -38,8 +38,11 @@ cudaError_t launch_prepare(const Geometry &g, const void *q, const void *k, cons
 constexpr size_t kStatusBytes = 256;
 size_t forward_workspace_bytes(const Geometry &g);
 // Returns 0 on success, 1 if a tensor map could not be encoded, or a CUDA error.
+// withhold_v (test hook): no V tile is loaded, so the launch ends through its
+// bounded waits and reports a timeout in the status block.
 int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scales,
                    const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
-                   const float *v_scales, void *out, void *workspace, cudaStream_t stream);
+                   const float *v_scales, void *out, void *workspace, cudaStream_t stream,
+                   bool withhold_v = false);
 
 }  // namespace sattn
