@@ -24,7 +24,9 @@
 //                                    column gives sum_j p8_j
 //   warp 10     V and Q loader (TMA): V half-tiles (E4M3, channel-major) into
 //               two slots; the next item's INT8 Q tile and V channel scales
-//   warp 11     idle
+//   warp 11     Q converter: the staged INT8 Q tile of the next item -> its
+//               FP16 carrier in shared memory, as soon as the current item's
+//               last QK has completed
 // Twelve warps launch at 168 registers each; setmaxnreg then gives the compute
 // warpgroups 232 (128 scores and 64 RO values per thread) and the loader/MMA
 // warpgroup 40.
@@ -75,8 +77,8 @@ constexpr uint32_t TM_S = 0;
 constexpr uint32_t TM_PV = 256;
 constexpr uint32_t TM_P = 448;   // P8 of one tile: 256 keys, four per column
 // warp roles: 0-7 compute (two warpgroups), 8 K loader, 9 MMA issuer and TMEM
-// owner, 10 V and Q loader, 11 idle
-constexpr int WARP_PRODUCER = 8, WARP_MMA = 9, WARP_VLOAD = 10;
+// owner, 10 V and Q loader, 11 Q converter
+constexpr int WARP_PRODUCER = 8, WARP_MMA = 9, WARP_VLOAD = 10, WARP_QCONV = 11;
 constexpr int NTHREADS = 12 * 32;
 // Registers: launched at 168 per thread (384 x 168 = 64512), then rebalanced
 // per warpgroup; the shares add up to exactly the launch total.
@@ -104,8 +106,9 @@ enum Bar : int {
     VFULL = KEMPTY + KSLOTS,
     VEMPTY = VFULL + VSLOTS,
     QSTAGE = VEMPTY + VSLOTS,   // INT8 Q codes of an item landed in shared memory
-    QFULL = QSTAGE + 1,         // its FP16 carrier is in TMEM
-    SFULL = QFULL + 1,
+    QFULL = QSTAGE + 1,         // its FP16 carrier is in shared memory
+    QEMPTY = QFULL + 1,         // the item's last QK has completed: the Q carrier may be replaced
+    SFULL = QEMPTY + 1,
     SFREE = SFULL + 1,
     PFULL = SFREE + 1,
     PDONE = PFULL + 1,
@@ -125,7 +128,7 @@ static_assert(OFF_V % 1024 == 0 && V_SLOT_BYTES % 1024 == 0 && OFF_Q % 1024 == 0
 // where a wait gave up (second status word)
 enum Site : uint32_t {
     SITE_KE = 1, SITE_VE, SITE_Q, SITE_K, SITE_P, SITE_V, SITE_PVE, SITE_DONE, SITE_S,
-    SITE_PV, SITE_DRAIN, SITE_SFREE, SITE_PDONE, SITE_QS, SITE_QE
+    SITE_PV, SITE_DRAIN, SITE_SFREE, SITE_PDONE, SITE_QS, SITE_QE, SITE_QEMPTY
 };
 
 struct FwdParams {
@@ -395,6 +398,8 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
                     break;
                 SATTN_TRACE(p, t, 9, j);
                 ptx::mma_commit(bar(SFULL));
+                if (j == t.ntiles - 1)
+                    ptx::mma_commit(bar(QEMPTY));   // the item's Q carrier is no longer read
                 SATTN_TRACE(p, t, 4, j);
             }
             if (j >= 1) {                           // PV_{j-1} = P_{j-1} V_{j-1}
@@ -434,6 +439,40 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
     wt.drain(bar(MMADONE), 0);
 }
 
+// Q converter (one warp): for every item of the CTA, the staged INT8 Q tile
+// (16-byte chunk c of row r at chunk c ^ (r % 8)) becomes the FP16 carrier in
+// the two 64-channel halves of the Q buffer (same 128-byte swizzle); for items
+// after the first it waits until the previous item's last QK has completed.
+// Thread l converts rows l, l + 32, l + 64, l + 96, so the 16-byte accesses
+// of a warp instruction spread over all banks.
+__device__ __forceinline__ void qconv_role(const FwdParams &p, uint32_t sb, int lane, const Waiter &wt)
+{
+    auto bar = [sb](int i) { return sb + OFF_BAR + 8u * i; };
+    int n = 0;
+    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x, ++n) {
+        if ((n >= 1 && !wt.wait(bar(QEMPTY), (n - 1) & 1, SITE_QEMPTY)) ||
+            !wt.wait(bar(QSTAGE), n & 1, SITE_QS))
+            return;
+#pragma unroll 1
+        for (int i = 0; i < 4; ++i) {
+            const int r = lane + 32 * i;
+            const uint32_t src = sb + OFF_QS + r * HD;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {   // codes 16c .. 16c + 15 -> channels of half c / 4
+                const uint4 a = ptx::ld_shared_v4(src + ((c ^ (r & 7)) << 4));
+                const uint32_t dst = sb + OFF_Q + (c >> 2) * Q_HALF_BYTES + r * 128;
+                const int w = 2 * (c & 3);  // FP16 chunk (8 channels) within the half row
+                ptx::st_shared_v4(dst + ((w ^ (r & 7)) << 4), ptx::f16x2_of_i8(a.x, 0), ptx::f16x2_of_i8(a.x, 2),
+                                  ptx::f16x2_of_i8(a.y, 0), ptx::f16x2_of_i8(a.y, 2));
+                ptx::st_shared_v4(dst + (((w + 1) ^ (r & 7)) << 4), ptx::f16x2_of_i8(a.z, 0),
+                                  ptx::f16x2_of_i8(a.z, 2), ptx::f16x2_of_i8(a.w, 0), ptx::f16x2_of_i8(a.w, 2));
+            }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(bar(QFULL));
+    }
+}
+
 // Compute warpgroups.  Half h owns S columns [128h, 128h + 128) of every tile
 // and writes the P8 bytes of those keys into shared-memory half h (K-major,
 // 128-byte swizzle); the row max is exchanged through shared memory under a
@@ -455,32 +494,6 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, uint32_t sb, ui
     const uint32_t maxx = sb + OFF_MAXX;                      // [tile parity][half][row] row maxima
     constexpr float kLog2_448 = 8.8073549220576041f;          // log2(448): P is stored as p * 448
 
-    // Q codes 64h .. 64h+63 of row r of the staged item (16-byte chunk c of
-    // row r sits at chunk c ^ (r % 8)) -> FP16 carrier -> row r of the Q half h
-    // in shared memory (the same 128-byte swizzle), 8 channels at a time; then
-    // QFULL
-    auto store_q = [&](int nq) -> bool {
-        if (!wt.wait(bar(QSTAGE), nq & 1, SITE_QS))
-            return false;
-        const uint32_t qrow = sb + OFF_QS + r * HD;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const uint4 a = ptx::ld_shared_v4(qrow + (((4 * half + w) ^ (r & 7)) << 4));
-            const uint32_t words[4] = {a.x, a.y, a.z, a.w};
-            uint32_t h[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                h[e * 2] = ptx::f16x2_of_i8(words[e], 0);
-                h[e * 2 + 1] = ptx::f16x2_of_i8(words[e], 2);
-            }
-            const uint32_t qdst = sb + OFF_Q + half * Q_HALF_BYTES + r * 128;
-            ptx::st_shared_v4(qdst + (((2 * w) ^ (r & 7)) << 4), h[0], h[1], h[2], h[3]);
-            ptx::st_shared_v4(qdst + (((2 * w + 1) ^ (r & 7)) << 4), h[4], h[5], h[6], h[7]);
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(bar(QFULL));
-        return true;
-    };
     auto qscale = [&](const Tile &tq) {
         const int i = tq.q0 + r;
         return i < p.nq32 ? ptx::ld_nc_f32(p.q_scales + static_cast<size_t>(tq.b * p.Hq + tq.hq) * p.nbq + i / kQBlock)
@@ -495,8 +508,6 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, uint32_t sb, ui
 
     int it = blockIdx.x;
     Tile t = item_tile(p, it);
-    if (!store_q(0))
-        return false;
     if (r == 0 && half == 0)
         SATTN_TRACE(p, t, 38, 1);
     float sq = qscale(t);
@@ -691,10 +702,6 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, uint32_t sb, ui
                 SATTN_TRACE(p, t, 3, j);
             if ((r & 31) == 0)
                 SATTN_TRACE(p, t, 13 + 4 * half + (r >> 5), j);
-            // after the last P of this item its last QK has completed (its S was
-            // read above), so the Q columns of TMEM can take the next item's Q
-            if (j == t.ntiles - 1 && has_next && !store_q(n + 1))
-                return false;
             if (j >= 1 && !fold_partial(gj - 1, j - 1, t, alpha_prev))
                 return false;
             alpha_prev = alpha;
@@ -800,7 +807,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ptx::mbar_init(b0 + 8u * (VEMPTY + s), 1);
         }
         ptx::mbar_init(b0 + 8u * QSTAGE, 1);
-        ptx::mbar_init(b0 + 8u * QFULL, 2 * BM);
+        ptx::mbar_init(b0 + 8u * QFULL, 32);
+        ptx::mbar_init(b0 + 8u * QEMPTY, 1);
         ptx::mbar_init(b0 + 8u * SFULL, 1);
         ptx::mbar_init(b0 + 8u * SFREE, 2 * BM);
         ptx::mbar_init(b0 + 8u * PFULL, 2 * BM);
@@ -842,6 +850,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             } else if (warp == WARP_MMA) {
                 if (lane == 0)
                     mma_role(p, sb, tmem, wt);
+            } else if (warp == WARP_QCONV) {
+                qconv_role(p, sb, lane, wt);
             }
             __syncwarp();
         }
