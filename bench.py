@@ -263,6 +263,9 @@ def run_ours(args, world, rank, local):
     ms_total = max_over_ranks(start.elapsed_time(end), world, dev)
     ms_prep = sum(e[0].elapsed_time(e[1]) for e in evs) / K
     ms_fwd = sum(e[1].elapsed_time(e[2]) for e in evs) / K
+    per_step = [e[0].elapsed_time(e[2]) for e in evs]
+    step_median = statistics.median(per_step)
+    step_cv = statistics.pstdev(per_step) / statistics.fmean(per_step) if K > 1 else 0.0
     ms_step = ms_total / K
     value = world * w.literal_ops / (ms_step * 1e-3) / 1e12
 
@@ -314,6 +317,7 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"replica x{world}"},
         "algorithmic_tops": round(world * w.algorithmic_ops / (ms_step * 1e-3) / 1e12, 3),
         "ms_prepare": round(ms_prep, 5), "ms_forward": round(ms_fwd, 5),
+        "ms_per_step_median": round(step_median, 5), "step_cv": round(step_cv, 4),
         "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel (the only kernel of sattn_forward)",
                      "achieved": round(achieved, 2), "peak": round(mp["mixed"], 2), "unit": "TFLOP/s",
                      "frac": round(achieved / mp["mixed"], 4),
