@@ -33,12 +33,12 @@ def cosine(a: np.ndarray, b: np.ndarray) -> float:
     return float(a @ b / (na * nb))
 
 
-def assert_close_output(gpu_bits: np.ndarray, ref_bits: np.ndarray, what=""):
+def assert_close_output(gpu_bits: np.ndarray, ref_bits: np.ndarray, what="", tol_maxabs=TOL_MAXABS):
     g, r = as_f64(gpu_bits), as_f64(ref_bits)
     assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
     maxabs = float(np.abs(g - r).max()) if g.size else 0.0
     cos = cosine(g, r)
-    assert maxabs <= TOL_MAXABS and cos >= TOL_COS, f"{what}: max-abs {maxabs:.3g}, cosine {cos:.8f}"
+    assert maxabs <= tol_maxabs and cos >= TOL_COS, f"{what}: max-abs {maxabs:.3g}, cosine {cos:.8f}"
     return maxabs, cos
 
 

@@ -11,7 +11,7 @@ import torch
 
 import quantized_exact_attention_smoothing_gb300 as sattn
 import synth
-from helpers import assert_close_output, bf16_bits, to_device_bf16
+from helpers import TOL_MAXABS, assert_close_output, bf16_bits, to_device_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -129,3 +129,34 @@ def test_host_entry_point_matches_device_path():
     torch.cuda.synchronize()
     dev = sattn.attention(tq.cuda(), tk.cuda(), tv.cuda(), causal=True)
     assert torch.equal(out_h.view(torch.int16), dev.cpu().view(torch.int16))
+
+
+@pytest.mark.parametrize("sm_scale", [0.03, 0.2])
+def test_forward_explicit_softmax_scale(oracle_mod, sm_scale):
+    # A scale other than 1/sqrt(128) changes c0 = sm_scale * log2(e) on both
+    # sides.  The 4e-3 figure is stated for the default scale.  At 0.03 the
+    # softmax is nearly flat: a row of ~120 kept keys gives each key ~1/120 of
+    # the weight.  The kernel forms the exponent argument with one fused
+    # multiply-add and ex2.approx; the oracle rounds the score first.  So a
+    # P8 value within an FP32 ulp of an E4M3 tie (here 400.00006, between 384
+    # and 416) can take the other code.  That one step (32 of 448) on one key,
+    # times an outlier value, moves one output by 4.15e-3 on these inputs.
+    # A CPU emulation of the kernel's rounding path gives the same figure.
+    # The bound allows two such flips; the cosine bound is unchanged.
+    w = synth.workload("c1", B=1, Hq=2, Hkv=1, Nq=200, Nkv=300, causal=True)
+    q, k, v = synth.make_inputs(w, seed=91)
+    prep = sattn.prepare(to_device_bf16(q), to_device_bf16(k), to_device_bf16(v), True, sm_scale=sm_scale)
+    got = bf16_bits(sattn.forward(prep))
+    assert sattn.check_status(prep["forward_workspace"]) == 0
+    ref = oracle_mod.prepare(q, k, v)
+    rb, _ = oracle_mod.forward(ref, w.Nq, w.Nkv, True, sm_scale=sm_scale)
+    assert_close_output(got, rb, f"sm_scale {sm_scale}", tol_maxabs=2 * TOL_MAXABS)
+
+
+@pytest.mark.parametrize("heads", [(16, 2), (8, 1), (3, 3)])
+def test_forward_gqa_groups(oracle_mod, heads):
+    # query head h reads KV head h / (Hq / Hkv): groups of 8, all heads on one, and plain MHA
+    Hq, Hkv = heads
+    w = synth.workload("c1", B=2, Hq=Hq, Hkv=Hkv, Nq=160, Nkv=416, causal=False)
+    q, k, v = synth.make_inputs(w, seed=97 + Hq)
+    _full(oracle_mod, q, k, v, False, f"GQA {Hq}/{Hkv}")
