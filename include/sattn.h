@@ -158,6 +158,34 @@ int sattn_forward(const sattn_shape *shape, const int8_t *q_codes, const float *
                   const float *v_scales, void *out, void *workspace, void *stream);
 
 /*
+ * sattn_prepare_kv -- the K and V part of sattn_prepare (K smoothing, INT8
+ * K, FP8 V; same page entry), for sattn_forward_q_bf16, which quantises Q
+ * itself.  Arguments as in sattn_prepare without q, q_codes and q_scales;
+ * the outputs are byte for byte those of sattn_prepare.
+ */
+int sattn_prepare_kv(const sattn_shape *shape, const void *k, const void *v, int8_t *k_codes,
+                     float *k_scales, float *k_mean, void *k_carrier, uint8_t *v_codes,
+                     float *v_scales, void *workspace, void *stream);
+
+/*
+ * sattn_forward_q_bf16 -- sattn_forward with the Q stage of the preparation
+ * (the INT8 block quantiser of sattn_prepare) moved into the kernel: each
+ * work item's 128 x 128 BF16 Q tile is quantised in shared memory while the
+ * previous item computes.  No Q codes or scales reach device memory.
+ *   q           in: BF16 [B][Hq][Nq][128], contiguous, 16-byte aligned
+ *   k_carrier, k_scales, v_codes, v_scales
+ *               in: as written by sattn_prepare_kv (or sattn_prepare)
+ *   out, workspace
+ *               as in sattn_forward
+ * The codes and block scales are the ones sattn_prepare would write, so the
+ * output equals, byte for byte, sattn_forward's on sattn_prepare's outputs.
+ * Errors as sattn_forward.
+ */
+int sattn_forward_q_bf16(const sattn_shape *shape, const void *q, const void *k_carrier,
+                         const float *k_scales, const uint8_t *v_codes, const float *v_scales,
+                         void *out, void *workspace, void *stream);
+
+/*
  * sattn_test_forward_withhold_v -- test hook for failure detection, not part
  * of the computation (the page has no counterpart).  Same arguments as
  * sattn_forward; the launch loads no V tile, so the MMA thread's wait for V
@@ -169,6 +197,19 @@ int sattn_forward(const sattn_shape *shape, const int8_t *q_codes, const float *
 int sattn_test_forward_withhold_v(const sattn_shape *shape, const int8_t *q_codes, const float *q_scales,
                                   const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
                                   const float *v_scales, void *out, void *workspace, void *stream);
+
+/*
+ * sattn_test_int8_quantiser -- test hook, not part of the computation: checks
+ * the INT8 block quantiser that sattn_prepare and sattn_forward_q_bf16 use
+ * (clamp(rint(x / s), -127, 127), s = amax / 127, computed without a
+ * division) against the IEEE division, for every positive finite BF16 amax
+ * whose bit pattern lies in [amax_lo, amax_hi) (1 <= amax_lo < amax_hi <=
+ * 0x7f80) and every BF16 x with |x| <= amax.
+ *   result   out: device array of three uint64: mismatching codes, values
+ *            that took the division-free tie decision, and the last mismatch
+ *            (amax bits << 16 | x bits); valid after the stream synchronises
+ */
+int sattn_test_int8_quantiser(uint32_t amax_lo, uint32_t amax_hi, unsigned long long *result, void *stream);
 
 /*
  * sattn_check_status -- synchronise `stream` and read the status word that

@@ -71,12 +71,16 @@ def load_library(build: bool = True):
     lib.sattn_forward.argtypes = [SP] + [P] * 9
     lib.sattn_test_forward_withhold_v.argtypes = [SP] + [P] * 9
     lib.sattn_prepare_noalloc.argtypes = [SP] + [P] * 12
+    lib.sattn_prepare_kv.argtypes = [SP] + [P] * 10
+    lib.sattn_forward_q_bf16.argtypes = [SP] + [P] * 8
     lib.sattn_check_status.argtypes = [P, P]
+    lib.sattn_test_int8_quantiser.argtypes = [ctypes.c_uint32, ctypes.c_uint32, P, P]
     lib.sattn_attention_host.argtypes = [SP, P, P, P, P, P, ctypes.c_size_t, P]
     lib.sattn_status_string.argtypes = [ctypes.c_int]
     lib.sattn_status_string.restype = ctypes.c_char_p
     for name in ("sattn_query_sizes", "sattn_prepare", "sattn_forward", "sattn_check_status",
-                 "sattn_attention_host", "sattn_prepare_noalloc"):
+                 "sattn_attention_host", "sattn_prepare_noalloc", "sattn_prepare_kv", "sattn_forward_q_bf16",
+                 "sattn_test_int8_quantiser"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -132,16 +136,15 @@ def _empty(nbytes: int, device, dtype=torch.uint8) -> torch.Tensor:
     return torch.empty(n, dtype=dtype, device=device)
 
 
-def prepare_buffers(shape: sattn_shape, device) -> dict:
-    """Device buffers for sattn_prepare's outputs, shaped as documented."""
+def prepare_buffers(shape: sattn_shape, device, with_q: bool = True) -> dict:
+    """Device buffers for sattn_prepare's outputs (without the Q codes and
+    scales when with_q is false: sattn_prepare_kv), shaped as documented."""
     B, Hq, Hkv, Nq, Nkv = shape.B, shape.Hq, shape.Hkv, shape.Nq, shape.Nkv
     nq32 = -(-Nq // QBLOCK) * QBLOCK
     nk32 = -(-Nkv // QBLOCK) * QBLOCK
     nk128 = -(-Nkv // V_PAD) * V_PAD
     z = query_sizes(shape)
-    return dict(
-        q_codes=torch.empty((B, Hq, nq32, HEAD_DIM), dtype=torch.int8, device=device),
-        q_scales=torch.empty((B, Hq, nq32 // QBLOCK), dtype=torch.float32, device=device),
+    buf = dict(
         k_codes=torch.empty((B, Hkv, nk32, HEAD_DIM), dtype=torch.int8, device=device),
         k_scales=torch.empty((B, Hkv, nk32 // QBLOCK), dtype=torch.float32, device=device),
         k_mean=torch.empty((B, Hkv, HEAD_DIM), dtype=torch.float32, device=device),
@@ -150,6 +153,10 @@ def prepare_buffers(shape: sattn_shape, device) -> dict:
         v_scales=torch.empty((B, Hkv, HEAD_DIM), dtype=torch.float32, device=device),
         workspace=_empty(z["prepare_workspace"], device),
     )
+    if with_q:
+        buf["q_codes"] = torch.empty((B, Hq, nq32, HEAD_DIM), dtype=torch.int8, device=device)
+        buf["q_scales"] = torch.empty((B, Hq, nq32 // QBLOCK), dtype=torch.float32, device=device)
+    return buf
 
 
 def prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
@@ -220,6 +227,55 @@ def forward(prep: dict, out: torch.Tensor | None = None, workspace: torch.Tensor
     return out
 
 
+def prepare_kv(k: torch.Tensor, v: torch.Tensor, Hq: int, Nq: int, causal: bool = False,
+               sm_scale: float = 0.0, buffers: dict | None = None, stream=None) -> dict:
+    """sattn_prepare_kv: the K and V part of prepare(), for forward_q_bf16.
+
+    The shape needs the query side too (Hq, Nq): it is checked here and
+    kept with the buffers for the forward call.  The Q entries of the
+    returned buffers are absent.
+    """
+    _need_cuda(k, v)
+    B, Hkv, Nkv, _ = k.shape
+    shape = make_shape(B, Hq, Hkv, Nq, Nkv, causal, sm_scale)
+    if buffers is None:
+        buffers = prepare_buffers(shape, k.device, with_q=False)
+    rc = load_library().sattn_prepare_kv(
+        ctypes.byref(shape), _ptr(k), _ptr(v), _ptr(buffers["k_codes"]), _ptr(buffers["k_scales"]),
+        _ptr(buffers["k_mean"]), _ptr(buffers["k_carrier"]), _ptr(buffers["v_codes"]),
+        _ptr(buffers["v_scales"]), _ptr(buffers["workspace"]), _stream(stream))
+    if rc != 0:
+        raise SattnError(rc, "sattn_prepare_kv")
+    buffers["shape"] = shape
+    return buffers
+
+
+def forward_q_bf16(q: torch.Tensor, prep: dict, out: torch.Tensor | None = None,
+                   workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """sattn_forward_q_bf16: the forward pass that quantises the BF16 Q itself,
+    on the K/V buffers of prepare_kv() (or prepare()).  Same output bytes as
+    forward() on prepare()'s codes."""
+    shape = prep["shape"]
+    _need_cuda(q)
+    if tuple(q.shape) != (shape.B, shape.Hq, shape.Nq, HEAD_DIM) or q.dtype != torch.bfloat16:
+        raise ValueError("q must be BF16 [B, Hq, Nq, 128] of the prepared shape")
+    dev = q.device
+    if out is None:
+        out = torch.empty((shape.B, shape.Hq, shape.Nq, HEAD_DIM), dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        workspace = prep.get("forward_workspace")
+        if workspace is None:
+            workspace = _empty(query_sizes(shape)["forward_workspace"], dev)
+            prep["forward_workspace"] = workspace
+    _need_cuda(out, workspace)
+    rc = load_library().sattn_forward_q_bf16(
+        ctypes.byref(shape), _ptr(q), _ptr(prep["k_carrier"]), _ptr(prep["k_scales"]), _ptr(prep["v_codes"]),
+        _ptr(prep["v_scales"]), _ptr(out), _ptr(workspace), _stream(stream))
+    if rc != 0:
+        raise SattnError(rc, "sattn_forward_q_bf16")
+    return out
+
+
 def forward_withhold_v_for_test(prep: dict, out: torch.Tensor | None = None,
                                 workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """sattn_test_forward_withhold_v: a forward launch that loads no V tile, so
@@ -244,13 +300,25 @@ def forward_withhold_v_for_test(prep: dict, out: torch.Tensor | None = None,
     return out
 
 
+def int8_quantiser_sweep_for_test(amax_lo: int = 1, amax_hi: int = 0x7f80, device="cuda") -> tuple[int, int, int]:
+    """sattn_test_int8_quantiser: (mismatches, tie decisions, last mismatch) of
+    the INT8 quantiser against IEEE division over BF16 blocks (test hook)."""
+    res = torch.zeros(4, dtype=torch.int64, device=device)
+    rc = load_library().sattn_test_int8_quantiser(amax_lo, amax_hi, _ptr(res), _stream(None))
+    if rc != 0:
+        raise SattnError(rc, "sattn_test_int8_quantiser")
+    bad, near, last = (int(v) for v in res[:3].cpu())
+    return bad, near, last
+
+
 def check_status(workspace: torch.Tensor, stream=None) -> int:
     """sattn_check_status: synchronises the stream, returns the status code."""
     return int(load_library().sattn_check_status(_ptr(workspace), _stream(stream)))
 
 
 def attention(q, k, v, causal=False, sm_scale=0.0, stream=None) -> torch.Tensor:
-    """prepare + forward on device tensors."""
+    """prepare + forward on device tensors (the faster of the two paths on
+    GB300; prepare_kv + forward_q_bf16 give the same bytes)."""
     return forward(prepare(q, k, v, causal, sm_scale, stream=stream), stream=stream)
 
 

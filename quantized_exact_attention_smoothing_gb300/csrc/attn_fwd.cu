@@ -59,6 +59,7 @@
 #include <cudaTypedefs.h>
 
 #include "ptx.cuh"
+#include "quant.cuh"
 #include "sattn_internal.cuh"
 
 namespace sattn {
@@ -99,7 +100,8 @@ constexpr uint32_t QS_BYTES = BM * HD;
 constexpr uint32_t OFF_MAXX = OFF_QS + QS_BYTES;             // [tile parity][half][row] row maxima
 constexpr uint32_t OFF_SV = OFF_MAXX + 4 * BM * 4;          // [item % 3][128] V channel scales
 constexpr uint32_t SV_BYTES = HD * 4;
-constexpr uint32_t OFF_BAR = OFF_SV + 3 * SV_BYTES;
+constexpr uint32_t OFF_SQ = OFF_SV + 3 * SV_BYTES;          // [item % 2][4] Q block scales (in-kernel Q quantisation)
+constexpr uint32_t OFF_BAR = OFF_SQ + 2 * 4 * 4;
 enum Bar : int {
     KFULL = 0,
     KEMPTY = KFULL + KSLOTS,
@@ -115,7 +117,10 @@ enum Bar : int {
     PVFULL = PDONE + 1,
     PVEMPTY = PVFULL + 1,
     MMADONE = PVEMPTY + 1,
-    NBARS = MMADONE + 1
+    QBF = MMADONE + 1,          // in-kernel Q quantisation: the BF16 Q tile landed in the staging buffer
+    QQDONE = QBF + 1,           // its codes and block scales are written; the staging buffer is free
+    STGFREE = QQDONE + 1,       // an item's final conversion has left the staging buffer
+    NBARS = STGFREE + 1
 };
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBARS * 8;
 constexpr uint32_t OFF_FLAG = OFF_TMEM_SLOT + 4;
@@ -128,7 +133,7 @@ static_assert(OFF_V % 1024 == 0 && V_SLOT_BYTES % 1024 == 0 && OFF_Q % 1024 == 0
 // where a wait gave up (second status word)
 enum Site : uint32_t {
     SITE_KE = 1, SITE_VE, SITE_Q, SITE_K, SITE_P, SITE_V, SITE_PVE, SITE_DONE, SITE_S,
-    SITE_PV, SITE_DRAIN, SITE_SFREE, SITE_PDONE, SITE_QS, SITE_QE, SITE_QEMPTY
+    SITE_PV, SITE_DRAIN, SITE_SFREE, SITE_PDONE, SITE_QS, SITE_QE, SITE_QEMPTY, SITE_QBF, SITE_QQ, SITE_STG
 };
 
 struct FwdParams {
@@ -288,20 +293,23 @@ __device__ __forceinline__ void kload_role(const FwdParams &p, const CUtensorMap
 
 // V and Q loader.  V half-tiles (128 keys x 128 channels, E4M3) go to the two
 // V slots; at the first tile of every item, once that item's Q has left the
-// staging buffer (QFULL), the next item's INT8 Q tile and V channel scales are
-// staged.
+// staging buffer (QFULL), the next item's INT8 Q tile (prepared codes only)
+// and V channel scales are staged.
+template <bool kFuseQ>
 __device__ __forceinline__ void vload_role(const FwdParams &p, const CUtensorMap *tm_v,
                                            const CUtensorMap *tm_q, uint32_t sb, const Waiter &wt)
 {
     auto bar = [sb](int i) { return sb + OFF_BAR + 8u * i; };
     ptx::prefetch_tensormap(tm_v);
-    ptx::prefetch_tensormap(tm_q);
+    if (!kFuseQ)
+        ptx::prefetch_tensormap(tm_q);
     // INT8 Q tile of item `tq` into the staging buffer, and its V channel
     // scales into slot nq % 3 (the final conversion of item nq - 3, the last
     // reader of that slot, ends before QFULL of item nq - 1 is arrived)
     auto load_q = [&](const Tile &tq, int nq) {
-        ptx::mbar_arrive_expect_tx(bar(QSTAGE), QS_BYTES + SV_BYTES);
-        ptx::tma_load_3d(sb + OFF_QS, tm_q, bar(QSTAGE), 0, tq.q0, tq.b * p.Hq + tq.hq);
+        ptx::mbar_arrive_expect_tx(bar(QSTAGE), (kFuseQ ? 0u : QS_BYTES) + SV_BYTES);
+        if (!kFuseQ)
+            ptx::tma_load_3d(sb + OFF_QS, tm_q, bar(QSTAGE), 0, tq.q0, tq.b * p.Hq + tq.hq);
         ptx::bulk_load(sb + OFF_SV + (nq % 3) * SV_BYTES, p.v_scales + static_cast<size_t>(tq.b * p.Hkv + tq.hk) * HD,
                        SV_BYTES, bar(QSTAGE));
     };
@@ -439,15 +447,88 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
     wt.drain(bar(MMADONE), 0);
 }
 
+// In-kernel Q quantisation (the preparation's block quantiser applied to the
+// item's BF16 Q tile).  The tile (128 rows x 128 channels, rows >= Nq read as
+// zeros) has landed by TMA in the output staging buffer, 256 bytes per row.
+// For each 32-row block: amax -> s = fl(amax / 127), rs = fl(1 / s), and the
+// INT8 codes go to the INT8 staging buffer in the layout the prepared codes
+// arrive in by TMA (16-byte chunk c of row r at chunk c ^ (r % 8)); s goes to
+// Q scale slot `slot`.  Thread l reads chunk l % 16 of row 2i + l / 16, so
+// each warp instruction reads two whole rows without bank conflicts.
+__device__ __forceinline__ void quantize_q_tile(uint32_t sb, int lane, int slot)
+{
+    const int k = lane & 15, rh = lane >> 4;
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+        uint32_t am2 = 0u;   // max |x| of this thread's values, two BF16 lanes
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+            const uint4 a = ptx::ld_shared_v4(sb + OFF_STG + (32 * blk + 2 * i + rh) * 256 + 16 * k);
+            am2 = ptx::bf16x2_max(am2, ptx::bf16x2_max(ptx::bf16x2_max(a.x & 0x7fff7fffu, a.y & 0x7fff7fffu),
+                                                      ptx::bf16x2_max(a.z & 0x7fff7fffu, a.w & 0x7fff7fffu)));
+        }
+        float am = fmaxf(bf16_lo(am2), bf16_hi(am2));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        const float s = __fdiv_rn(am, 127.0f);
+        const float rs = s > 0.0f ? __frcp_rn(s) : 0.0f;   // s = 0: every value is 0 and so is its code
+#pragma unroll 2
+        for (int i = 0; i < 16; ++i) {
+            const int row = 32 * blk + 2 * i + rh;
+            const uint2 c = int8_codes8(ptx::ld_shared_v4(sb + OFF_STG + row * 256 + 16 * k), s, rs);
+            ptx::st_shared_v2(sb + OFF_QS + row * 128 + (((k >> 1) ^ (row & 7)) << 4) + 8 * (k & 1), c.x, c.y);
+        }
+        if (lane == 0)
+            ptx::st_shared_f32(sb + OFF_SQ + 16 * slot + 4 * blk, s);
+    }
+}
+
 // Q converter (one warp): for every item of the CTA, the staged INT8 Q tile
 // (16-byte chunk c of row r at chunk c ^ (r % 8)) becomes the FP16 carrier in
 // the two 64-channel halves of the Q buffer (same 128-byte swizzle); for items
 // after the first it waits until the previous item's last QK has completed.
 // Thread l converts rows l, l + 32, l + 64, l + 96, so the 16-byte accesses
 // of a warp instruction spread over all banks.
-__device__ __forceinline__ void qconv_role(const FwdParams &p, uint32_t sb, int lane, const Waiter &wt)
+//
+// With kFuseQ the INT8 tile is this warp's own.  The first item's tile is
+// quantised before the loop (QQDONE phase 0).  Right after the carrier of
+// item n is handed over (QFULL), the BF16 Q tile of item n + 1 is staged in
+// the output staging buffer and quantised into the INT8 staging buffer and
+// the scale slot of its parity (QQDONE phase n + 1), once STGFREE phase n has
+// completed: for n = 0 the compute warps have read the first scales, for
+// n >= 1 the final conversion of item n - 1 has left the staging buffer.  The
+// compute warps wait for QQDONE phase n + 1 before the final conversion of
+// item n and only then arrive on STGFREE phase n + 1, so neither barrier runs
+// more than one phase ahead of its waiter.
+template <bool kFuseQ>
+__device__ __forceinline__ void qconv_role(const FwdParams &p, const CUtensorMap *tm_q, uint32_t sb, int lane,
+                                           const Waiter &wt)
 {
     auto bar = [sb](int i) { return sb + OFF_BAR + 8u * i; };
+    // stage and quantise the BF16 Q tile of item `itq`, the CTA's item number nq
+    auto quantize_item = [&](int itq, int nq) -> bool {
+        if (lane == 0) {
+            const Tile tq = item_tile(p, itq);
+            ptx::mbar_arrive_expect_tx(bar(QBF), STG_BYTES);
+            ptx::tma_load_3d(sb + OFF_STG, tm_q, bar(QBF), 0, tq.q0, tq.b * p.Hq + tq.hq);
+        }
+        if (!wt.wait(bar(QBF), nq & 1, SITE_QBF)) {
+            wt.drain(bar(QBF), nq & 1);   // the copy lands before the CTA may leave
+            return false;
+        }
+        quantize_q_tile(sb, lane, nq & 1);
+        __syncwarp();
+        if (lane == 0)
+            ptx::mbar_arrive(bar(QQDONE));
+        return true;
+    };
+    if (kFuseQ) {
+        if (lane == 0)
+            ptx::prefetch_tensormap(tm_q);
+        if (!quantize_item(blockIdx.x, 0))
+            return;
+    }
     int n = 0;
     for (int it = blockIdx.x; it < p.n_items; it += gridDim.x, ++n) {
         if ((n >= 1 && !wt.wait(bar(QEMPTY), (n - 1) & 1, SITE_QEMPTY)) ||
@@ -470,19 +551,26 @@ __device__ __forceinline__ void qconv_role(const FwdParams &p, uint32_t sb, int 
         }
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(bar(QFULL));
+        if (kFuseQ) {
+            const int nx = it + static_cast<int>(gridDim.x);
+            if (nx < p.n_items) {
+                __syncwarp();   // every lane has read the INT8 tile before it is rewritten
+                if (!wt.wait(bar(STGFREE), n & 1, SITE_STG) || !quantize_item(nx, n + 1))
+                    return;
+            }
+        }
     }
 }
 
 // Compute warpgroups.  Half h owns S columns [128h, 128h + 128) of every tile
-// and writes the P8 bytes of those keys into shared-memory half h (K-major,
-// 128-byte swizzle); the row max is exchanged through shared memory under a
+// and writes the P8 bytes of those keys into TMEM columns [TM_P + 32h,
+// TM_P + 32h + 32); the row max is exchanged through shared memory under a
 // named barrier of the two warps that share those rows, so both halves hold
-// the same running max m and alpha.  Half
-// h also owns RO columns [64h, 64h + 64): after writing P_j it folds the
-// partial PV_{j-1} into RO with alpha_{j-1} (both halves keep d).  Between two
-// items the warps write the next item's Q into TMEM (free once the last QK of
-// the current item has completed) before the last fold and the final
-// conversion, so the next QK overlaps them.
+// the same running max m and alpha.  Half h also owns RO columns [64h, 64h +
+// 64): after writing P_j it folds the partial PV_{j-1} into RO with
+// alpha_{j-1} (both halves keep d).  The Q block scale of a row comes from
+// q_scales, or with kFuseQ from the scale slot the Q converter fills (QQDONE).
+template <bool kFuseQ>
 __device__ __forceinline__ bool compute_loop(const FwdParams &p, uint32_t sb, uint32_t tmem, int warp, int lane,
                                              const Waiter &wt)
 {
@@ -510,7 +598,17 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, uint32_t sb, ui
     Tile t = item_tile(p, it);
     if (r == 0 && half == 0)
         SATTN_TRACE(p, t, 38, 1);
-    float sq = qscale(t);
+    float sq;
+    if (kFuseQ) {
+        if (!wt.wait(bar(QQDONE), 0, SITE_QQ))
+            return false;
+        sq = ptx::ld_shared_f32(sb + OFF_SQ + 4 * quarter);
+        __syncwarp();
+        if (lane == 0)   // STGFREE phase 0: the first scales have been read
+            ptx::mbar_arrive(bar(STGFREE));
+    } else {
+        sq = qscale(t);
+    }
     float sk[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c)
@@ -559,7 +657,7 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, uint32_t sb, ui
         const int nx = it + static_cast<int>(gridDim.x);
         const bool has_next = nx < p.n_items;
         // (the next item's tile is recomputed where needed rather than kept live)
-        const float sq_next = has_next ? qscale(item_tile(p, nx)) : 0.0f;
+        float sq_next = (!kFuseQ && has_next) ? qscale(item_tile(p, nx)) : 0.0f;
         m = -INFINITY;
         d = 0.0f;
         alpha_prev = 0.0f;
@@ -712,6 +810,11 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, uint32_t sb, ui
 
         if (r == 0 && half == 0)
             SATTN_TRACE(p, t, 39, 2);
+        if (kFuseQ && has_next) {   // the next item's Q scales are written and the staging buffer is free
+            if (!wt.wait(bar(QQDONE), (n + 1) & 1, SITE_QQ))
+                return false;
+            sq_next = ptx::ld_shared_f32(sb + OFF_SQ + 16 * ((n + 1) & 1) + 4 * quarter);
+        }
         // final conversion: reciprocal of d, per-channel V scale, BF16.  Each
         // warp stages its 32 rows x 64 channels (4 KB of its own, 16-byte chunk
         // c of row l at chunk c ^ (l % 8)) in shared memory and then writes
@@ -750,6 +853,11 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, uint32_t sb, ui
                                                64 * half + 8 * ch) = v;
             }
             __syncwarp();
+            if (kFuseQ) {   // STGFREE phase n + 1: the Q converter stages the item after next here (TMA)
+                ptx::fence_proxy_async_smem();
+                if (lane == 0)
+                    ptx::mbar_arrive(bar(STGFREE));
+            }
         }
         if (r == 0 && half == 0)
             SATTN_TRACE(p, t, 38, 2);
@@ -769,15 +877,17 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, uint32_t sb, ui
 // exchange barrier: a partner already waiting there is released, and every
 // compute warp checks the mark before that barrier, so none waits for a warp
 // that has left.
+template <bool kFuseQ>
 __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, uint32_t tmem, int warp, int lane,
                                              const Waiter &wt)
 {
-    if (!compute_loop(p, sb, tmem, warp, lane, wt)) {
+    if (!compute_loop<kFuseQ>(p, sb, tmem, warp, lane, wt)) {
         asm volatile("st.shared.u32 [%0], 1;" ::"r"(sb + OFF_ABORT) : "memory");
         ptx::named_bar_arrive(1 + (warp & 3), 64);
     }
 }
 
+template <bool kFuseQ>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_q, const FwdParams p)
@@ -816,6 +926,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ptx::mbar_init(b0 + 8u * PVFULL, 1);
         ptx::mbar_init(b0 + 8u * PVEMPTY, 2 * BM);
         ptx::mbar_init(b0 + 8u * MMADONE, 1);
+        ptx::mbar_init(b0 + 8u * QBF, 1);
+        ptx::mbar_init(b0 + 8u * QQDONE, 1);
+        ptx::mbar_init(b0 + 8u * STGFREE, 8);
         ptx::fence_mbar_init();
     }
     // constant rows of every V slot: row 128 holds E4M3 1.0 (0x38), rows 129..143 hold 0
@@ -838,7 +951,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (*flag == 0 && static_cast<int>(blockIdx.x) < p.n_items) {
         if (warp < WARP_PRODUCER) {
             ptx::setmaxnreg_inc<kRegsCompute>();
-            compute_role(p, sb, tmem, warp, lane, wt);
+            compute_role<kFuseQ>(p, sb, tmem, warp, lane, wt);
         } else {
             ptx::setmaxnreg_dec<kRegsOther>();
             if (warp == WARP_PRODUCER) {
@@ -846,12 +959,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     kload_role(p, &tm_k, sb, wt);
             } else if (warp == WARP_VLOAD) {
                 if (lane == 0)
-                    vload_role(p, &tm_v, &tm_q, sb, wt);
+                    vload_role<kFuseQ>(p, &tm_v, &tm_q, sb, wt);
             } else if (warp == WARP_MMA) {
                 if (lane == 0)
                     mma_role(p, sb, tmem, wt);
             } else if (warp == WARP_QCONV) {
-                qconv_role(p, sb, lane, wt);
+                qconv_role<kFuseQ>(p, &tm_q, sb, lane, wt);
             }
             __syncwarp();
         }
@@ -896,9 +1009,14 @@ size_t forward_workspace_bytes(const Geometry &)
     return kStatusBytes;
 }
 
-int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scales,
-                   const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
-                   const float *v_scales, void *out, void *workspace, cudaStream_t stream, bool withhold_v)
+namespace {
+
+// q: INT8 codes [B, Hq, nq32, 128] with q_scales, or with kFuseQ the BF16 Q
+// [B, Hq, Nq, 128] itself (q_scales unused)
+template <bool kFuseQ>
+int launch_impl(const Geometry &g, const void *q, const float *q_scales, const void *k_carrier,
+                const float *k_scales, const uint8_t *v_codes, const float *v_scales, void *out,
+                void *workspace, cudaStream_t stream, bool withhold_v)
 {
     auto encode = tensor_map_encoder();
     if (!encode)
@@ -934,13 +1052,23 @@ int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scal
     }
 
     CUtensorMap tmq;
-    {
+    if (kFuseQ) {   // BF16 Q, 128 rows x 128 channels (32 KB, 256-byte rows), rows >= Nq read as zeros
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(g.Nq),
+                                    static_cast<cuuint64_t>(g.B) * g.Hq};
+        const cuuint64_t strides[2] = {HD * 2, static_cast<cuuint64_t>(g.Nq) * HD * 2};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(HD), static_cast<cuuint32_t>(BM), 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (encode(&tmq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return 1;
+    } else {
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(g.nq32),
                                     static_cast<cuuint64_t>(g.B) * g.Hq};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(g.nq32) * HD};
         const cuuint32_t box[3] = {static_cast<cuuint32_t>(HD), static_cast<cuuint32_t>(BM), 1};   // 128 rows x 128 codes
         const cuuint32_t estr[3] = {1, 1, 1};
-        if (encode(&tmq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<int8_t *>(q_codes), dims, strides, box,
+        if (encode(&tmq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(q), dims, strides, box,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return 1;
@@ -952,18 +1080,18 @@ int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scal
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
         cudaFuncAttributes fa;
-        attr_err = cudaFuncGetAttributes(&fa, attn_fwd_kernel);
+        attr_err = cudaFuncGetAttributes(&fa, attn_fwd_kernel<kFuseQ>);
         if (attr_err == cudaSuccess && fa.numRegs != kLaunchRegs)
             attr_err = cudaErrorInvalidConfiguration;
         if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            attr_err = cudaFuncSetAttribute(attn_fwd_kernel<kFuseQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             static_cast<int>(SMEM_BYTES));
     });
     if (attr_err != cudaSuccess)
         return static_cast<int>(attr_err);
 
     FwdParams prm;
-    prm.q_codes = q_codes;
+    prm.q_codes = kFuseQ ? nullptr : static_cast<const int8_t *>(q);
     prm.q_scales = q_scales;
     prm.k_scales = k_scales;
     prm.v_scales = v_scales;
@@ -1001,8 +1129,25 @@ int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scal
         cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1)
         return static_cast<int>(cudaErrorInvalidDevice);
     const int grid = std::min(prm.n_items, n_sm);
-    attn_fwd_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, prm);
+    attn_fwd_kernel<kFuseQ><<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, prm);
     return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace
+
+int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scales,
+                   const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
+                   const float *v_scales, void *out, void *workspace, cudaStream_t stream, bool withhold_v)
+{
+    return launch_impl<false>(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out, workspace, stream,
+                              withhold_v);
+}
+
+int launch_forward_q_bf16(const Geometry &g, const void *q, const void *k_carrier, const float *k_scales,
+                          const uint8_t *v_codes, const float *v_scales, void *out, void *workspace,
+                          cudaStream_t stream)
+{
+    return launch_impl<true>(g, q, nullptr, k_carrier, k_scales, v_codes, v_scales, out, workspace, stream, false);
 }
 
 }  // namespace sattn

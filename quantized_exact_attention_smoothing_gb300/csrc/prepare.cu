@@ -15,13 +15,11 @@
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
+#include "quant.cuh"
 #include "sattn_internal.cuh"
 
 namespace sattn {
 namespace {
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 __device__ __forceinline__ void unpack8(const uint4 &a, float (&f)[8])
 {
@@ -115,25 +113,6 @@ __global__ void __launch_bounds__(128) kv_finalize_kernel(const float *__restric
     }
     k_mean[bh * kHeadDim + c] = __fdiv_rn(total, static_cast<float>(Nkv));
     v_scales[bh * kHeadDim + c] = __fdiv_rn(amax, 448.0f);
-}
-
-// clamp(rint(fl(x / s)), -127, 127) without a division in the common case:
-// q = fl(x * fl(1/s)) lies within 3 ulp of fl(x / s) (two roundings of
-// relative size 2^-24 each, plus that of the quotient), and |q| <= 127 * (1 +
-// 2^-22), so an ulp of q is at most 2^-16.  When q is farther than 2^-14 from
-// the nearest half-integer, fl(x / s) rounds to the same integer as q; only
-// the rare values near a rounding tie take the IEEE division.  Rounding to an
-// integer adds and subtracts 1.5 * 2^23 (exact, ties to even, |q| < 2^22).
-// The code is returned as its two's-complement byte, read from the low bits
-// of k + 1.5 * 2^23 (no float-to-integer conversion instruction).
-__device__ __forceinline__ uint32_t int8_code(float x, float s, float rs)
-{
-    const float q = __fmul_rn(x, rs);
-    float k = __fsub_rn(__fadd_rn(q, 12582912.0f), 12582912.0f);
-    if (!(fabsf(__fsub_rn(q, k)) < 0.49993896484375f))   // 0.5 - 2^-14; false for NaN / inf too
-        k = rintf(__fdiv_rn(x, s));
-    k = fminf(fmaxf(k, -127.0f), 127.0f);
-    return __float_as_uint(__fadd_rn(k, 12582912.0f)) & 0xffu;
 }
 
 // E4M3(fl(v / s)) (round to nearest even, saturating) without a division in
@@ -305,6 +284,42 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint4 *__restrict__ 
     }
 }
 
+// Test kernel: every BF16 x with |x| <= amax against the INT8 quantiser of
+// one block whose amax has BF16 bits blockIdx.x + amax_lo.  result[0] counts
+// codes that differ from clamp(rint(fl(x / s))) by IEEE division, result[1]
+// the values that took the tie decision, result[2] the last mismatch seen
+// (amax bits << 16 | x bits).
+__global__ void __launch_bounds__(256) int8_quantiser_sweep_kernel(uint32_t amax_lo, unsigned long long *result)
+{
+    const uint32_t a = amax_lo + blockIdx.x;
+    const float amax = __uint_as_float(a << 16);
+    const float s = __fdiv_rn(amax, 127.0f);
+    const float rs = __frcp_rn(s);
+    unsigned long long bad = 0, near = 0;
+    for (uint32_t xb = threadIdx.x; xb < 0x10000u; xb += blockDim.x) {
+        if ((xb & 0x7fffu) > a)
+            continue;
+        const float x = __uint_as_float(xb << 16);
+        const float q = __fmul_rn(x, rs);
+        near += isfinite(q) && !(fabsf(__fsub_rn(q, __fsub_rn(__fadd_rn(q, kRoundMagic), kRoundMagic))) < kTieMargin);
+        if (int8_code(x, s, rs) != int8_code_div(x, s)) {
+            ++bad;
+            result[2] = (static_cast<unsigned long long>(a) << 16) | xb;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        bad += __shfl_xor_sync(0xffffffffu, bad, o);
+        near += __shfl_xor_sync(0xffffffffu, near, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        if (bad)
+            atomicAdd(result, bad);
+        if (near)
+            atomicAdd(result + 1, near);
+    }
+}
+
 }  // namespace
 
 size_t prepare_workspace_bytes(const Geometry &g)
@@ -332,8 +347,18 @@ cudaError_t launch_prepare(const Geometry &g, const void *q, const void *k, cons
         k4, g.Nkv, g.nk32, static_cast<int>(g.nbk), k_mean, k_codes, k_scales, static_cast<uint4 *>(k_carrier));
     quant_v_kernel<<<dim3(static_cast<unsigned>(g.nk128 / kVPad), bhk), 256, 0, stream>>>(
         v4, g.Nkv, g.nk128, v_scales, v_codes);
-    quant_int8_kernel<false><<<dim3(static_cast<unsigned>(g.nbq), bhq), 256, 0, stream>>>(
-        q4, g.Nq, g.nq32, static_cast<int>(g.nbq), nullptr, q_codes, q_scales, nullptr);
+    if (q)   // without Q, K and V only (the forward quantises Q itself)
+        quant_int8_kernel<false><<<dim3(static_cast<unsigned>(g.nbq), bhq), 256, 0, stream>>>(
+            q4, g.Nq, g.nq32, static_cast<int>(g.nbq), nullptr, q_codes, q_scales, nullptr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_int8_quantiser_sweep(uint32_t amax_lo, uint32_t amax_hi, unsigned long long *result,
+                                        cudaStream_t stream)
+{
+    if (cudaMemsetAsync(result, 0, 3 * sizeof(unsigned long long), stream) != cudaSuccess)
+        return cudaGetLastError();
+    int8_quantiser_sweep_kernel<<<amax_hi - amax_lo, 256, 0, stream>>>(amax_lo, result);
     return cudaGetLastError();
 }
 

@@ -100,8 +100,10 @@ int prepare_impl(const Geometry &g, const void *q, const void *k, const void *v,
                  float *q_scales, int8_t *k_codes, float *k_scales, float *k_mean, void *k_carrier,
                  uint8_t *v_codes, float *v_scales, void *workspace, cudaStream_t stream)
 {
-    const void *ptrs[] = {q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes, v_scales,
-                          workspace};
+    // q, q_codes and q_scales are all null for the K/V-only preparation
+    const bool with_q = q != nullptr;
+    const void *ptrs[] = {k, v, k_codes, k_scales, k_mean, k_carrier, v_codes, v_scales, workspace,
+                          with_q ? q : k, with_q ? q_codes : k, with_q ? q_scales : k};
     for (const void *p : ptrs) {
         if (!p)
             return SATTN_ERR_INVALID;
@@ -117,12 +119,15 @@ int prepare_impl(const Geometry &g, const void *q, const void *k, const void *v,
                : SATTN_ERR_LAUNCH;
 }
 
+// q_bf16 non-null: the forward that quantises Q itself (q_codes, q_scales unused)
 int forward_impl(const Geometry &g, const int8_t *q_codes, const float *q_scales,
                  const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
                  const float *v_scales, void *out, void *workspace, cudaStream_t stream,
-                 bool withhold_v = false)
+                 bool withhold_v = false, const void *q_bf16 = nullptr)
 {
-    const void *ptrs[] = {q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out, workspace};
+    const bool fused = q_bf16 != nullptr;
+    const void *ptrs[] = {fused ? q_bf16 : q_codes, fused ? q_bf16 : q_scales, k_carrier, k_scales, v_codes,
+                          v_scales, out, workspace};
     for (const void *p : ptrs) {
         if (!p)
             return SATTN_ERR_INVALID;
@@ -132,8 +137,10 @@ int forward_impl(const Geometry &g, const int8_t *q_codes, const float *q_scales
     const int dev = check_device();
     if (dev != SATTN_OK)
         return dev;
-    const int rc = sattn::launch_forward(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales,
-                                         out, workspace, stream, withhold_v);
+    const int rc = fused ? sattn::launch_forward_q_bf16(g, q_bf16, k_carrier, k_scales, v_codes, v_scales, out,
+                                                        workspace, stream)
+                         : sattn::launch_forward(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales,
+                                                 out, workspace, stream, withhold_v);
     if (rc == 1)
         return SATTN_ERR_DEVICE;   // no tensor-map encoder in this driver
     return rc == 0 ? SATTN_OK : SATTN_ERR_LAUNCH;
@@ -164,6 +171,8 @@ int sattn_prepare(const sattn_shape *shape, const void *q, const void *k, const 
     const int rc = make_geometry(shape, &g);
     if (rc != SATTN_OK)
         return rc;
+    if (!q || !q_codes || !q_scales)
+        return SATTN_ERR_INVALID;
     return prepare_impl(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes, v_scales,
                         workspace, static_cast<cudaStream_t>(stream));
 }
@@ -180,6 +189,29 @@ int sattn_forward(const sattn_shape *shape, const int8_t *q_codes, const float *
                         static_cast<cudaStream_t>(stream));
 }
 
+int sattn_prepare_kv(const sattn_shape *shape, const void *k, const void *v, int8_t *k_codes,
+                     float *k_scales, float *k_mean, void *k_carrier, uint8_t *v_codes, float *v_scales,
+                     void *workspace, void *stream)
+{
+    Geometry g;
+    const int rc = make_geometry(shape, &g);
+    if (rc != SATTN_OK)
+        return rc;
+    return prepare_impl(g, nullptr, k, v, nullptr, nullptr, k_codes, k_scales, k_mean, k_carrier, v_codes,
+                        v_scales, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int sattn_forward_q_bf16(const sattn_shape *shape, const void *q, const void *k_carrier, const float *k_scales,
+                         const uint8_t *v_codes, const float *v_scales, void *out, void *workspace, void *stream)
+{
+    Geometry g;
+    const int rc = make_geometry(shape, &g);
+    if (rc != SATTN_OK)
+        return rc;
+    return forward_impl(g, nullptr, nullptr, k_carrier, k_scales, v_codes, v_scales, out, workspace,
+                        static_cast<cudaStream_t>(stream), false, q);
+}
+
 int sattn_test_forward_withhold_v(const sattn_shape *shape, const int8_t *q_codes, const float *q_scales,
                                   const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
                                   const float *v_scales, void *out, void *workspace, void *stream)
@@ -190,6 +222,21 @@ int sattn_test_forward_withhold_v(const sattn_shape *shape, const int8_t *q_code
         return rc;
     return forward_impl(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out, workspace,
                         static_cast<cudaStream_t>(stream), true);
+}
+
+int sattn_test_int8_quantiser(uint32_t amax_lo, uint32_t amax_hi, unsigned long long *result, void *stream)
+{
+    if (!result || amax_lo < 1 || amax_hi > 0x7f80u || amax_lo >= amax_hi)
+        return SATTN_ERR_INVALID;
+    if (!aligned16(result))
+        return SATTN_ERR_MISALIGNED;
+    const int dev = check_device();
+    if (dev != SATTN_OK)
+        return dev;
+    return sattn::launch_int8_quantiser_sweep(amax_lo, amax_hi, result, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? SATTN_OK
+               : SATTN_ERR_LAUNCH;
 }
 
 int sattn_check_status(const void *forward_workspace, void *stream)

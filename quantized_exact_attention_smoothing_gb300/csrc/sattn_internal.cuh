@@ -28,6 +28,11 @@ struct Geometry {
 // ---- prepare (prepare.cu) ----
 // Workspace: [B*Hkv][nchunks][128] FP32 K column sums, then the same for V max |v|.
 size_t prepare_workspace_bytes(const Geometry &g);
+// Test hook: the INT8 quantiser against IEEE division over BF16 blocks whose
+// amax has BF16 bits in [amax_lo, amax_hi) (device result[3], see prepare.cu).
+cudaError_t launch_int8_quantiser_sweep(uint32_t amax_lo, uint32_t amax_hi, unsigned long long *result,
+                                        cudaStream_t stream);
+// q = nullptr skips the Q part (q_codes, q_scales unused).
 cudaError_t launch_prepare(const Geometry &g, const void *q, const void *k, const void *v,
                            int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
                            float *k_mean, void *k_carrier, uint8_t *v_codes, float *v_scales,
@@ -44,5 +49,12 @@ int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scal
                    const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
                    const float *v_scales, void *out, void *workspace, cudaStream_t stream,
                    bool withhold_v = false);
+
+// The forward pass with Q quantised inside the kernel: q is the BF16 Q
+// [B, Hq, Nq, 128]; the codes and block scales are those launch_prepare
+// writes, and the output is launch_forward's on them, byte for byte.
+int launch_forward_q_bf16(const Geometry &g, const void *q, const void *k_carrier, const float *k_scales,
+                          const uint8_t *v_codes, const float *v_scales, void *out, void *workspace,
+                          cudaStream_t stream);
 
 }  // namespace sattn

@@ -77,3 +77,38 @@ def test_status_strings(lib):
     for code in range(6):
         assert lib.sattn_status_string(code)
     assert lib.sattn_status_string(99) == b"unknown status"
+
+
+def test_kv_prepare_and_fused_forward_check_pointers_first(lib):
+    s = sattn.make_shape(1, 1, 1, 8, 8)
+    kv = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(9)]
+    args = list(kv)
+    args[2] = None                                   # k_codes
+    assert lib.sattn_prepare_kv(ctypes.byref(s), *args, None) == 1
+    args = list(kv)
+    args[0] = ctypes.c_void_p(0x1001)                # k
+    assert lib.sattn_prepare_kv(ctypes.byref(s), *args, None) == 2
+    fwd = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(7)]
+    args = list(fwd)
+    args[0] = None                                   # q
+    assert lib.sattn_forward_q_bf16(ctypes.byref(s), *args, None) == 1
+    args = list(fwd)
+    args[5] = ctypes.c_void_p(0x3008)                # out
+    assert lib.sattn_forward_q_bf16(ctypes.byref(s), *args, None) == 2
+    bad = sattn.make_shape(1, 3, 2, 8, 8)            # Hq % Hkv != 0
+    assert lib.sattn_forward_q_bf16(ctypes.byref(bad), *fwd, None) == 1
+
+
+def test_full_prepare_still_requires_q(lib):
+    s = sattn.make_shape(1, 1, 1, 8, 8)
+    args = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(12)]
+    args[0] = None                                   # q
+    assert lib.sattn_prepare(ctypes.byref(s), *args, None) == 1
+
+
+def test_quantiser_sweep_hook_checks_arguments(lib):
+    assert lib.sattn_test_int8_quantiser(0, 10, ctypes.c_void_p(0x1000), None) == 1
+    assert lib.sattn_test_int8_quantiser(1, 0x7f81, ctypes.c_void_p(0x1000), None) == 1
+    assert lib.sattn_test_int8_quantiser(5, 5, ctypes.c_void_p(0x1000), None) == 1
+    assert lib.sattn_test_int8_quantiser(1, 10, None, None) == 1
+    assert lib.sattn_test_int8_quantiser(1, 10, ctypes.c_void_p(0x1008), None) == 2

@@ -66,3 +66,12 @@ def test_prepare_repeatable(oracle_mod):
     torch.cuda.synchronize()
     for n, t in first.items():
         assert torch.equal(t, a[n]), n
+
+
+def test_int8_quantiser_exhaustive_over_bf16():
+    # every positive finite BF16 amax and every BF16 x with |x| <= amax: the
+    # division-free quantiser (including its exact tie decision) gives the
+    # code of clamp(rint(fl(x / s))) with IEEE division, s = fl(amax / 127)
+    bad, near, last = sattn.int8_quantiser_sweep_for_test()
+    assert bad == 0, f"{bad} mismatches, last amax bits {last >> 16:#x} x bits {last & 0xffff:#x}"
+    assert near > 100000   # the tie decision was exercised
