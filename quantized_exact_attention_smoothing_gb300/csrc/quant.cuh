@@ -35,7 +35,9 @@ __device__ __forceinline__ uint32_t int8_code_div(float x, float s)
 // division.  BF16 inputs make them common (x / s = 127 x / amax often lands
 // within an ulp of a half-integer: a few per thousand values of Gaussian
 // data), so the branch is per value: a warp pays for the division only at
-// the positions where one of its lanes needs it.
+// the positions where one of its lanes needs it.  (Division-free exact tie
+// decisions measured slower: short enough to be predicated, they are paid by
+// every value.)
 __device__ __forceinline__ uint32_t int8_code(float x, float s, float rs)
 {
     const float q = __fmul_rn(x, rs);
