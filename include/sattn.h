@@ -221,14 +221,26 @@ int sattn_check_status(const void *forward_workspace, void *stream);
 
 /*
  * sattn_attention_host -- the whole path from host buffers: copies q, k, v
- * from host memory to the device, runs sattn_prepare and sattn_forward, and
- * copies the BF16 output back to host memory, all enqueued on `stream`.
+ * from host memory to the device, runs the preparation and the forward pass,
+ * and copies the BF16 output back to host memory.
  *   q_host, k_host, v_host   in:  BF16 host arrays (pinned memory lets the
- *                                 copies run asynchronously)
- *   out_host                 out: BF16 host array, valid after the stream
+ *                                 copies overlap the kernels)
+ *   out_host                 out: BF16 host array, valid after `stream`
  *                                 has been synchronised
  *   arena                    device scratch of sizes.arena bytes (holds the
- *                            inputs, codes, scales, workspaces and output)
+ *                            inputs, codes, scales, two preparation
+ *                            workspaces, the status block and the output)
+ * The (batch, KV head) units are independent problems, so large shapes are
+ * cut into up to eight chunks of contiguous units, each with at least two
+ * forward work items per SM.  Each chunk's copies, preparation, forward and
+ * copy back run in order on `stream` or on a helper stream of the library
+ * (created once per device).  The chunks alternate between the two, so the
+ * copies of one overlap the kernels of the other.  The helper stream waits
+ * for `stream` at the start, and `stream` waits for it at the end, so all
+ * work is ordered on `stream` as seen by the caller.  The output bytes equal
+ * sattn_prepare + sattn_forward on the whole shape.  Every chunk's forward
+ * reports into the arena's status block, cleared once per call.
+ * Calls on one device serialise their enqueueing (not their execution).
  */
 int sattn_attention_host(const sattn_shape *shape, const void *q_host, const void *k_host,
                          const void *v_host, void *out_host, void *arena, size_t arena_bytes,

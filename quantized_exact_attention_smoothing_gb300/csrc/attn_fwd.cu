@@ -1016,14 +1016,14 @@ namespace {
 template <bool kFuseQ>
 int launch_impl(const Geometry &g, const void *q, const float *q_scales, const void *k_carrier,
                 const float *k_scales, const uint8_t *v_codes, const float *v_scales, void *out,
-                void *workspace, cudaStream_t stream, bool withhold_v)
+                void *workspace, cudaStream_t stream, bool withhold_v, bool reset_status)
 {
     auto encode = tensor_map_encoder();
     if (!encode)
         return 1;
     uint32_t *status = static_cast<uint32_t *>(workspace);
     const int bhk = g.B * g.Hkv;
-    if (cudaMemsetAsync(status, 0, 2 * sizeof(uint32_t), stream) != cudaSuccess)
+    if (reset_status && cudaMemsetAsync(status, 0, 2 * sizeof(uint32_t), stream) != cudaSuccess)
         return static_cast<int>(cudaGetLastError());
 
     CUtensorMap tmk, tmv;
@@ -1137,17 +1137,19 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const v
 
 int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scales,
                    const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
-                   const float *v_scales, void *out, void *workspace, cudaStream_t stream, bool withhold_v)
+                   const float *v_scales, void *out, void *workspace, cudaStream_t stream, bool withhold_v,
+                   bool reset_status)
 {
     return launch_impl<false>(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out, workspace, stream,
-                              withhold_v);
+                              withhold_v, reset_status);
 }
 
 int launch_forward_q_bf16(const Geometry &g, const void *q, const void *k_carrier, const float *k_scales,
                           const uint8_t *v_codes, const float *v_scales, void *out, void *workspace,
                           cudaStream_t stream)
 {
-    return launch_impl<true>(g, q, nullptr, k_carrier, k_scales, v_codes, v_scales, out, workspace, stream, false);
+    return launch_impl<true>(g, q, nullptr, k_carrier, k_scales, v_codes, v_scales, out, workspace, stream, false,
+                             true);
 }
 
 }  // namespace sattn

@@ -73,7 +73,7 @@ void fill_sizes(const Geometry &g, sattn_sizes *z)
     z->forward_workspace = r16(sattn::forward_workspace_bytes(g));
     z->arena = r256(z->q) + r256(z->k) + r256(z->v) + r256(z->q_codes) + r256(z->q_scales) +
                r256(z->k_codes) + r256(z->k_scales) + r256(z->k_mean) + r256(z->k_carrier) + r256(z->v_codes) +
-               r256(z->v_scales) + r256(z->out) + r256(z->prepare_workspace) +
+               r256(z->v_scales) + r256(z->out) + 2 * r256(z->prepare_workspace) +
                r256(z->forward_workspace);
 }
 
@@ -144,6 +144,121 @@ int forward_impl(const Geometry &g, const int8_t *q_codes, const float *q_scales
     if (rc == 1)
         return SATTN_ERR_DEVICE;   // no tensor-map encoder in this driver
     return rc == 0 ? SATTN_OK : SATTN_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
+// The host-buffer path, pipelined: the (batch, KV head) units are independent
+// problems (their K mean and V scales are their own), so the units are cut
+// into contiguous chunks, each a problem of one batch and several KV heads
+// whose tensors are contiguous slices of the whole ones.  Chunks alternate
+// between the caller's stream and one helper stream of the library, so the
+// copies of one chunk overlap the kernels of the other.  Every chunk's
+// forward reports into the one status block, cleared once before the fork.
+// ---------------------------------------------------------------------------
+struct HostBuffers {
+    void *q, *k, *v, *out, *k_carrier, *pws[2], *fws;
+    int8_t *q_codes, *k_codes;
+    float *q_scales, *k_scales, *k_mean, *v_scales;
+    uint8_t *v_codes;
+};
+
+constexpr int kMaxHostChunks = 8;
+
+// Chunks for the pipeline: at most kMaxHostChunks, and each with at least two
+// work items of the forward per SM (smaller chunks would leave SMs idle).
+int host_chunks(const Geometry &g, int n_sm)
+{
+    const int64_t units = static_cast<int64_t>(g.B) * g.Hkv;
+    const int64_t items_per_unit = (g.Nq + sattn::kQTile - 1) / sattn::kQTile * (g.Hq / g.Hkv);
+    int64_t c = units < kMaxHostChunks ? units : kMaxHostChunks;
+    while (c > 1 && (units / c) * items_per_unit < 2 * static_cast<int64_t>(n_sm))
+        --c;
+    return static_cast<int>(c);
+}
+
+struct HelperStreams {
+    std::mutex mu;
+    cudaStream_t helper[64] = {};
+    cudaEvent_t fork[64] = {}, join[64] = {};
+};
+
+HelperStreams &helpers()
+{
+    static HelperStreams h;
+    return h;
+}
+
+int attention_host_pipelined(const Geometry &g, const sattn_shape &shape, const void *q_host, const void *k_host,
+                             const void *v_host, void *out_host, const HostBuffers &hb, cudaStream_t s0)
+{
+    int dev = 0, n_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return SATTN_ERR_DEVICE;
+    const int nc = host_chunks(g, n_sm);
+    const int grp = g.Hq / g.Hkv;
+    const int64_t units = static_cast<int64_t>(g.B) * g.Hkv;
+    const size_t D = sattn::kHeadDim;
+
+    HelperStreams &h = helpers();
+    std::lock_guard<std::mutex> lock(h.mu);   // the fork and join events are shared by the calls on a device
+    if (nc > 1 && !h.helper[dev]) {
+        if (cudaStreamCreateWithFlags(&h.helper[dev], cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&h.fork[dev], cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&h.join[dev], cudaEventDisableTiming) != cudaSuccess)
+            return SATTN_ERR_DEVICE;
+    }
+    if (cudaMemsetAsync(hb.fws, 0, 2 * sizeof(uint32_t), s0) != cudaSuccess)
+        return SATTN_ERR_LAUNCH;
+    cudaStream_t s1 = nc > 1 ? h.helper[dev] : s0;
+    if (nc > 1 && (cudaEventRecord(h.fork[dev], s0) != cudaSuccess ||
+                   cudaStreamWaitEvent(s1, h.fork[dev], 0) != cudaSuccess))
+        return SATTN_ERR_LAUNCH;
+
+    for (int c = 0; c < nc; ++c) {
+        const int64_t u0 = units * c / nc, u1 = units * (c + 1) / nc, nu = u1 - u0;
+        cudaStream_t st = (c & 1) ? s1 : s0;
+        sattn_shape cs = shape;                 // one batch of nu KV heads
+        cs.B = 1;
+        cs.Hkv = static_cast<int32_t>(nu);
+        cs.Hq = static_cast<int32_t>(nu * grp);
+        Geometry gc;
+        if (make_geometry(&cs, &gc) != SATTN_OK)
+            return SATTN_ERR_INVALID;
+        const size_t qh = static_cast<size_t>(u0) * grp, kh = static_cast<size_t>(u0);   // first q / kv head
+        const size_t qb = static_cast<size_t>(nu) * grp * g.Nq * D * 2, kb = static_cast<size_t>(nu) * g.Nkv * D * 2;
+        auto at = [](const void *base, size_t off) { return static_cast<const char *>(base) + off; };
+        auto atw = [](void *base, size_t off) { return static_cast<char *>(base) + off; };
+        void *q = atw(hb.q, qh * g.Nq * D * 2), *k = atw(hb.k, kh * g.Nkv * D * 2), *v = atw(hb.v, kh * g.Nkv * D * 2);
+        void *out = atw(hb.out, qh * g.Nq * D * 2);
+        int8_t *q_codes = hb.q_codes + qh * g.nq32 * D;
+        float *q_scales = hb.q_scales + qh * g.nbq;
+        int8_t *k_codes = hb.k_codes + kh * g.nk32 * D;
+        float *k_scales = hb.k_scales + kh * g.nbk;
+        float *k_mean = hb.k_mean + kh * D;
+        void *k_carrier = atw(hb.k_carrier, kh * g.Nkv * D * 2);
+        uint8_t *v_codes = hb.v_codes + kh * D * g.nk128;
+        float *v_scales = hb.v_scales + kh * D;
+        if (cudaMemcpyAsync(q, at(q_host, qh * g.Nq * D * 2), qb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+            cudaMemcpyAsync(k, at(k_host, kh * g.Nkv * D * 2), kb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+            cudaMemcpyAsync(v, at(v_host, kh * g.Nkv * D * 2), kb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return SATTN_ERR_LAUNCH;
+        if (sattn::launch_prepare(gc, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes,
+                                  v_scales, hb.pws[c & 1], st) != cudaSuccess)
+            return SATTN_ERR_LAUNCH;
+        const int frc = sattn::launch_forward(gc, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out,
+                                              hb.fws, st, false, false);
+        if (frc == 1)
+            return SATTN_ERR_DEVICE;
+        if (frc != 0)
+            return SATTN_ERR_LAUNCH;
+        if (cudaMemcpyAsync(atw(out_host, qh * g.Nq * D * 2), out, qb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+            return SATTN_ERR_LAUNCH;
+    }
+    if (nc > 1 && (cudaEventRecord(h.join[dev], s1) != cudaSuccess ||
+                   cudaStreamWaitEvent(s0, h.join[dev], 0) != cudaSuccess))
+        return SATTN_ERR_LAUNCH;
+    return SATTN_OK;
 }
 
 }  // namespace
@@ -279,35 +394,24 @@ int sattn_attention_host(const sattn_shape *shape, const void *q_host, const voi
         p += r256(n);
         return r;
     };
-    void *q = take(z.q), *k = take(z.k), *v = take(z.v);
-    int8_t *q_codes = reinterpret_cast<int8_t *>(take(z.q_codes));
-    float *q_scales = reinterpret_cast<float *>(take(z.q_scales));
-    int8_t *k_codes = reinterpret_cast<int8_t *>(take(z.k_codes));
-    float *k_scales = reinterpret_cast<float *>(take(z.k_scales));
-    float *k_mean = reinterpret_cast<float *>(take(z.k_mean));
-    void *k_carrier = take(z.k_carrier);
-    uint8_t *v_codes = reinterpret_cast<uint8_t *>(take(z.v_codes));
-    float *v_scales = reinterpret_cast<float *>(take(z.v_scales));
-    void *out = take(z.out);
-    void *pws = take(z.prepare_workspace);
-    void *fws = take(z.forward_workspace);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t qb = static_cast<size_t>(g.B) * g.Hq * g.Nq * sattn::kHeadDim * 2;
-    const size_t kb = static_cast<size_t>(g.B) * g.Hkv * g.Nkv * sattn::kHeadDim * 2;
-    if (cudaMemcpyAsync(q, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(k, k_host, kb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(v, v_host, kb, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return SATTN_ERR_LAUNCH;
-    rc = prepare_impl(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes, v_scales,
-                      pws, s);
-    if (rc != SATTN_OK)
-        return rc;
-    rc = forward_impl(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out, fws, s);
-    if (rc != SATTN_OK)
-        return rc;
-    if (cudaMemcpyAsync(out_host, out, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return SATTN_ERR_LAUNCH;
-    return SATTN_OK;
+    HostBuffers hb;
+    hb.q = take(z.q);
+    hb.k = take(z.k);
+    hb.v = take(z.v);
+    hb.q_codes = reinterpret_cast<int8_t *>(take(z.q_codes));
+    hb.q_scales = reinterpret_cast<float *>(take(z.q_scales));
+    hb.k_codes = reinterpret_cast<int8_t *>(take(z.k_codes));
+    hb.k_scales = reinterpret_cast<float *>(take(z.k_scales));
+    hb.k_mean = reinterpret_cast<float *>(take(z.k_mean));
+    hb.k_carrier = take(z.k_carrier);
+    hb.v_codes = reinterpret_cast<uint8_t *>(take(z.v_codes));
+    hb.v_scales = reinterpret_cast<float *>(take(z.v_scales));
+    hb.out = take(z.out);
+    hb.pws[0] = take(z.prepare_workspace);
+    hb.pws[1] = take(z.prepare_workspace);
+    hb.fws = take(z.forward_workspace);
+    return attention_host_pipelined(g, *shape, q_host, k_host, v_host, out_host, hb,
+                                    static_cast<cudaStream_t>(stream));
 }
 
 const char *sattn_status_string(int status)

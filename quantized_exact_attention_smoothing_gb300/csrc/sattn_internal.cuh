@@ -44,11 +44,12 @@ constexpr size_t kStatusBytes = 256;
 size_t forward_workspace_bytes(const Geometry &g);
 // Returns 0 on success, 1 if a tensor map could not be encoded, or a CUDA error.
 // withhold_v (test hook): no V tile is loaded, so the launch ends through its
-// bounded waits and reports a timeout in the status block.
+// bounded waits and reports a timeout in the status block.  With reset_status false
+// the status block is not cleared first (several launches report into one).
 int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scales,
                    const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
                    const float *v_scales, void *out, void *workspace, cudaStream_t stream,
-                   bool withhold_v = false);
+                   bool withhold_v = false, bool reset_status = true);
 
 // The forward pass with Q quantised inside the kernel: q is the BF16 Q
 // [B, Hq, Nq, 128]; the codes and block scales are those launch_prepare

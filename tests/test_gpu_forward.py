@@ -121,13 +121,22 @@ def test_forward_repeatable_byte_identical():
         assert torch.equal(first.view(torch.int16), again.view(torch.int16))
 
 
-def test_host_entry_point_matches_device_path():
-    w = synth.workload("c2", Hq=4, Hkv=2, causal=True)
+@pytest.mark.parametrize("name, overrides", [
+    ("c2", dict(Hq=4, Hkv=2, causal=True)),                        # one chunk
+    ("c1", dict(B=2, Hq=16, Hkv=4, Nq=4096, Nkv=4096, causal=True)),  # three chunks of 2, 3, 3 KV heads
+    ("c5", {})])                                                    # the benchmark's workload: eight chunks
+def test_host_entry_point_matches_device_path(name, overrides):
+    # the host-buffer path cuts the (batch, KV head) units into chunks that it
+    # pipelines over two streams; its output must equal the one-pass device path
+    w = synth.workload(name, **overrides)
     q, k, v = synth.make_inputs(w)
     tq, tk, tv = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (q, k, v))
-    out_h = sattn.attention_host(tq, tk, tv, causal=True)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        out_h = sattn.attention_host(tq, tk, tv, causal=w.causal, stream=stream)
+    stream.synchronize()
+    dev = sattn.attention(tq.cuda(), tk.cuda(), tv.cuda(), causal=w.causal)
     torch.cuda.synchronize()
-    dev = sattn.attention(tq.cuda(), tk.cuda(), tv.cuda(), causal=True)
     assert torch.equal(out_h.view(torch.int16), dev.cpu().view(torch.int16))
 
 
