@@ -232,12 +232,14 @@ int sattn_check_status(const void *forward_workspace, void *stream);
  *                            workspaces, the status block and the output)
  * The (batch, KV head) units are independent problems, so large shapes are
  * cut into up to eight chunks of contiguous units, each with at least two
- * forward work items per SM.  Each chunk's copies, preparation, forward and
- * copy back run in order on `stream` or on a helper stream of the library
- * (created once per device).  The chunks alternate between the two, so the
- * copies of one overlap the kernels of the other.  The helper stream waits
- * for `stream` at the start, and `stream` waits for it at the end, so all
- * work is ordered on `stream` as seen by the caller.  The output bytes equal
+ * forward work items per SM.  The host-to-device copies run back to back on
+ * one helper stream of the library, each chunk's preparation and forward on
+ * `stream` or a second helper stream (alternating, so the end of one chunk's
+ * forward overlaps the start of the next), and the copies back on a third.
+ * Events hand each chunk from stage to stage.  The helper streams and events
+ * are created once per device.  The helpers wait for `stream` at the start,
+ * and `stream` waits for the last copy back, so all work is ordered on
+ * `stream` as seen by the caller.  The output bytes equal
  * sattn_prepare + sattn_forward on the whole shape.  Every chunk's forward
  * reports into the arena's status block, cleared once per call.
  * Calls on one device serialise their enqueueing (not their execution).

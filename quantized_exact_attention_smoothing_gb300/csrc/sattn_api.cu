@@ -150,10 +150,13 @@ int forward_impl(const Geometry &g, const int8_t *q_codes, const float *q_scales
 // The host-buffer path, pipelined: the (batch, KV head) units are independent
 // problems (their K mean and V scales are their own), so the units are cut
 // into contiguous chunks, each a problem of one batch and several KV heads
-// whose tensors are contiguous slices of the whole ones.  Chunks alternate
-// between the caller's stream and one helper stream of the library, so the
-// copies of one chunk overlap the kernels of the other.  Every chunk's
-// forward reports into the one status block, cleared once before the fork.
+// whose tensors are contiguous slices of the whole ones.  Three helper
+// streams of the library carry the stages: the host-to-device copies run back
+// to back on one, the chunks' kernels alternate between the caller's stream
+// and a second one (so one chunk's forward tail overlaps the next chunk's
+// start), and the copies back run on a third; events hand each chunk from
+// stage to stage.  Every chunk's forward reports into the one status block,
+// cleared once before the fork.
 // ---------------------------------------------------------------------------
 struct HostBuffers {
     void *q, *k, *v, *out, *k_carrier, *pws[2], *fws;
@@ -176,16 +179,37 @@ int host_chunks(const Geometry &g, int n_sm)
     return static_cast<int>(c);
 }
 
+struct DeviceStreams {
+    cudaStream_t h2d = nullptr, compute = nullptr, d2h = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, in[kMaxHostChunks] = {}, done[kMaxHostChunks] = {};
+};
+
 struct HelperStreams {
     std::mutex mu;
-    cudaStream_t helper[64] = {};
-    cudaEvent_t fork[64] = {}, join[64] = {};
+    DeviceStreams dev[64];
 };
 
 HelperStreams &helpers()
 {
     static HelperStreams h;
     return h;
+}
+
+bool create_streams(DeviceStreams &d)
+{
+    if (d.h2d)
+        return true;
+    bool ok = cudaStreamCreateWithFlags(&d.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&d.compute, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&d.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming) == cudaSuccess;
+    for (int c = 0; c < kMaxHostChunks && ok; ++c)
+        ok = cudaEventCreateWithFlags(&d.in[c], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&d.done[c], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok)
+        d.h2d = nullptr;   // retried on the next call
+    return ok;
 }
 
 int attention_host_pipelined(const Geometry &g, const sattn_shape &shape, const void *q_host, const void *k_host,
@@ -201,23 +225,47 @@ int attention_host_pipelined(const Geometry &g, const sattn_shape &shape, const 
     const size_t D = sattn::kHeadDim;
 
     HelperStreams &h = helpers();
-    std::lock_guard<std::mutex> lock(h.mu);   // the fork and join events are shared by the calls on a device
-    if (nc > 1 && !h.helper[dev]) {
-        if (cudaStreamCreateWithFlags(&h.helper[dev], cudaStreamNonBlocking) != cudaSuccess ||
-            cudaEventCreateWithFlags(&h.fork[dev], cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&h.join[dev], cudaEventDisableTiming) != cudaSuccess)
-            return SATTN_ERR_DEVICE;
-    }
+    std::lock_guard<std::mutex> lock(h.mu);   // the events are shared by the calls on a device
+    DeviceStreams &ds = h.dev[dev];
+    if (nc > 1 && !create_streams(ds))
+        return SATTN_ERR_DEVICE;
     if (cudaMemsetAsync(hb.fws, 0, 2 * sizeof(uint32_t), s0) != cudaSuccess)
         return SATTN_ERR_LAUNCH;
-    cudaStream_t s1 = nc > 1 ? h.helper[dev] : s0;
-    if (nc > 1 && (cudaEventRecord(h.fork[dev], s0) != cudaSuccess ||
-                   cudaStreamWaitEvent(s1, h.fork[dev], 0) != cudaSuccess))
-        return SATTN_ERR_LAUNCH;
-
+    // single chunk: every stage on the caller's stream
+    cudaStream_t s_in = nc > 1 ? ds.h2d : s0, s_out = nc > 1 ? ds.d2h : s0;
+    cudaStream_t s_c[2] = {s0, nc > 1 ? ds.compute : s0};
+    if (nc > 1) {
+        if (cudaEventRecord(ds.fork, s0) != cudaSuccess || cudaStreamWaitEvent(ds.h2d, ds.fork, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(ds.compute, ds.fork, 0) != cudaSuccess ||
+            cudaStreamWaitEvent(ds.d2h, ds.fork, 0) != cudaSuccess)
+            return SATTN_ERR_LAUNCH;
+    }
+    auto at = [](const void *base, size_t off) { return static_cast<const char *>(base) + off; };
+    auto atw = [](void *base, size_t off) { return static_cast<char *>(base) + off; };
+    auto chunk_units = [&](int c, int64_t &u0, int64_t &nu) {
+        u0 = units * c / nc;
+        nu = units * (c + 1) / nc - u0;
+    };
+    // stage 1: host-to-device copies, back to back
     for (int c = 0; c < nc; ++c) {
-        const int64_t u0 = units * c / nc, u1 = units * (c + 1) / nc, nu = u1 - u0;
-        cudaStream_t st = (c & 1) ? s1 : s0;
+        int64_t u0, nu;
+        chunk_units(c, u0, nu);
+        const size_t qo = static_cast<size_t>(u0) * grp * g.Nq * D * 2, ko = static_cast<size_t>(u0) * g.Nkv * D * 2;
+        const size_t qb = static_cast<size_t>(nu) * grp * g.Nq * D * 2, kb = static_cast<size_t>(nu) * g.Nkv * D * 2;
+        if (cudaMemcpyAsync(atw(hb.q, qo), at(q_host, qo), qb, cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
+            cudaMemcpyAsync(atw(hb.k, ko), at(k_host, ko), kb, cudaMemcpyHostToDevice, s_in) != cudaSuccess ||
+            cudaMemcpyAsync(atw(hb.v, ko), at(v_host, ko), kb, cudaMemcpyHostToDevice, s_in) != cudaSuccess)
+            return SATTN_ERR_LAUNCH;
+        if (nc > 1 && cudaEventRecord(ds.in[c], s_in) != cudaSuccess)
+            return SATTN_ERR_LAUNCH;
+    }
+    // stage 2: preparation and forward of each chunk, alternating between two streams
+    for (int c = 0; c < nc; ++c) {
+        int64_t u0, nu;
+        chunk_units(c, u0, nu);
+        cudaStream_t st = s_c[c & 1];
+        if (nc > 1 && cudaStreamWaitEvent(st, ds.in[c], 0) != cudaSuccess)
+            return SATTN_ERR_LAUNCH;
         sattn_shape cs = shape;                 // one batch of nu KV heads
         cs.B = 1;
         cs.Hkv = static_cast<int32_t>(nu);
@@ -226,9 +274,6 @@ int attention_host_pipelined(const Geometry &g, const sattn_shape &shape, const 
         if (make_geometry(&cs, &gc) != SATTN_OK)
             return SATTN_ERR_INVALID;
         const size_t qh = static_cast<size_t>(u0) * grp, kh = static_cast<size_t>(u0);   // first q / kv head
-        const size_t qb = static_cast<size_t>(nu) * grp * g.Nq * D * 2, kb = static_cast<size_t>(nu) * g.Nkv * D * 2;
-        auto at = [](const void *base, size_t off) { return static_cast<const char *>(base) + off; };
-        auto atw = [](void *base, size_t off) { return static_cast<char *>(base) + off; };
         void *q = atw(hb.q, qh * g.Nq * D * 2), *k = atw(hb.k, kh * g.Nkv * D * 2), *v = atw(hb.v, kh * g.Nkv * D * 2);
         void *out = atw(hb.out, qh * g.Nq * D * 2);
         int8_t *q_codes = hb.q_codes + qh * g.nq32 * D;
@@ -239,10 +284,6 @@ int attention_host_pipelined(const Geometry &g, const sattn_shape &shape, const 
         void *k_carrier = atw(hb.k_carrier, kh * g.Nkv * D * 2);
         uint8_t *v_codes = hb.v_codes + kh * D * g.nk128;
         float *v_scales = hb.v_scales + kh * D;
-        if (cudaMemcpyAsync(q, at(q_host, qh * g.Nq * D * 2), qb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-            cudaMemcpyAsync(k, at(k_host, kh * g.Nkv * D * 2), kb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-            cudaMemcpyAsync(v, at(v_host, kh * g.Nkv * D * 2), kb, cudaMemcpyHostToDevice, st) != cudaSuccess)
-            return SATTN_ERR_LAUNCH;
         if (sattn::launch_prepare(gc, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes,
                                   v_scales, hb.pws[c & 1], st) != cudaSuccess)
             return SATTN_ERR_LAUNCH;
@@ -252,11 +293,22 @@ int attention_host_pipelined(const Geometry &g, const sattn_shape &shape, const 
             return SATTN_ERR_DEVICE;
         if (frc != 0)
             return SATTN_ERR_LAUNCH;
-        if (cudaMemcpyAsync(atw(out_host, qh * g.Nq * D * 2), out, qb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        if (nc > 1 && cudaEventRecord(ds.done[c], st) != cudaSuccess)
             return SATTN_ERR_LAUNCH;
     }
-    if (nc > 1 && (cudaEventRecord(h.join[dev], s1) != cudaSuccess ||
-                   cudaStreamWaitEvent(s0, h.join[dev], 0) != cudaSuccess))
+    // stage 3: device-to-host copies as each chunk's output is complete
+    for (int c = 0; c < nc; ++c) {
+        int64_t u0, nu;
+        chunk_units(c, u0, nu);
+        const size_t qo = static_cast<size_t>(u0) * grp * g.Nq * D * 2;
+        const size_t qb = static_cast<size_t>(nu) * grp * g.Nq * D * 2;
+        if (nc > 1 && cudaStreamWaitEvent(s_out, ds.done[c], 0) != cudaSuccess)
+            return SATTN_ERR_LAUNCH;
+        if (cudaMemcpyAsync(atw(out_host, qo), at(hb.out, qo), qb, cudaMemcpyDeviceToHost, s_out) != cudaSuccess)
+            return SATTN_ERR_LAUNCH;
+    }
+    // join: the copies back wait for every chunk, so their end is the end of the call
+    if (nc > 1 && (cudaEventRecord(ds.join, ds.d2h) != cudaSuccess || cudaStreamWaitEvent(s0, ds.join, 0) != cudaSuccess))
         return SATTN_ERR_LAUNCH;
     return SATTN_OK;
 }
