@@ -232,7 +232,9 @@ int sattn_check_status(const void *forward_workspace, void *stream);
  *                            workspaces, the status block and the output)
  * The (batch, KV head) units are independent problems, so large shapes are
  * cut into up to eight chunks of contiguous units, each with at least two
- * forward work items per SM.  The host-to-device copies run back to back on
+ * forward work items per SM, sized as a ramp (small first and last chunks,
+ * whose copies and kernels nothing else overlaps) when the ends stay that
+ * large, else equal.  The host-to-device copies run back to back on
  * one helper stream of the library, each chunk's preparation and forward on
  * `stream` or a second helper stream (alternating, so the end of one chunk's
  * forward overlaps the start of the next), and the copies back on a third.

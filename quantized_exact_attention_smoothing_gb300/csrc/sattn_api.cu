@@ -167,16 +167,46 @@ struct HostBuffers {
 
 constexpr int kMaxHostChunks = 8;
 
-// Chunks for the pipeline: at most kMaxHostChunks, and each with at least two
-// work items of the forward per SM (smaller chunks would leave SMs idle).
-int host_chunks(const Geometry &g, int n_sm)
+// Chunk plan for the pipeline: at most kMaxHostChunks chunks, each of at
+// least two work items of the forward per SM (smaller chunks would leave SMs
+// idle), sized like a ramp (weights 1, 2, 3, ..., 3, 2, 1): the first chunk's
+// copy in and the last chunk's kernels and copy back are the parts of the
+// pipeline that nothing overlaps, so those chunks are the small ones.
+// bound[c] .. bound[c + 1] are the units of chunk c; returns the chunk count.
+int host_chunks(const Geometry &g, int n_sm, int64_t (&bound)[kMaxHostChunks + 1])
 {
     const int64_t units = static_cast<int64_t>(g.B) * g.Hkv;
     const int64_t items_per_unit = (g.Nq + sattn::kQTile - 1) / sattn::kQTile * (g.Hq / g.Hkv);
-    int64_t c = units < kMaxHostChunks ? units : kMaxHostChunks;
-    while (c > 1 && (units / c) * items_per_unit < 2 * static_cast<int64_t>(n_sm))
-        --c;
-    return static_cast<int>(c);
+    const int64_t min_units = (2 * static_cast<int64_t>(n_sm) + items_per_unit - 1) / items_per_unit;
+    int nc = static_cast<int>(units / min_units < kMaxHostChunks ? units / min_units : kMaxHostChunks);
+    if (nc < 1)
+        nc = 1;
+    for (; nc > 1; --nc) {
+        int64_t wsum = 0, w[kMaxHostChunks];
+        for (int c = 0; c < nc; ++c)
+            wsum += w[c] = (c + 1 < nc - c ? c + 1 : nc - c);
+        int64_t acc = 0;
+        bool ok = true;
+        bound[0] = 0;
+        for (int c = 0; c < nc; ++c) {
+            acc += w[c];
+            bound[c + 1] = (units * acc + wsum / 2) / wsum;
+            ok = ok && bound[c + 1] - bound[c] >= min_units;
+        }
+        if (ok)
+            return nc;
+        // the ramp leaves an end chunk too small: equal chunks if they fit
+        bool eq = true;
+        for (int c = 0; c <= nc; ++c)
+            bound[c] = units * c / nc;
+        for (int c = 0; c < nc; ++c)
+            eq = eq && bound[c + 1] - bound[c] >= min_units;
+        if (eq)
+            return nc;
+    }
+    bound[0] = 0;
+    bound[1] = units;
+    return 1;
 }
 
 struct DeviceStreams {
@@ -219,9 +249,9 @@ int attention_host_pipelined(const Geometry &g, const sattn_shape &shape, const 
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 ||
         cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return SATTN_ERR_DEVICE;
-    const int nc = host_chunks(g, n_sm);
+    int64_t bound[kMaxHostChunks + 1];
+    const int nc = host_chunks(g, n_sm, bound);
     const int grp = g.Hq / g.Hkv;
-    const int64_t units = static_cast<int64_t>(g.B) * g.Hkv;
     const size_t D = sattn::kHeadDim;
 
     HelperStreams &h = helpers();
@@ -243,8 +273,8 @@ int attention_host_pipelined(const Geometry &g, const sattn_shape &shape, const 
     auto at = [](const void *base, size_t off) { return static_cast<const char *>(base) + off; };
     auto atw = [](void *base, size_t off) { return static_cast<char *>(base) + off; };
     auto chunk_units = [&](int c, int64_t &u0, int64_t &nu) {
-        u0 = units * c / nc;
-        nu = units * (c + 1) / nc - u0;
+        u0 = bound[c];
+        nu = bound[c + 1] - u0;
     };
     // stage 1: host-to-device copies, back to back
     for (int c = 0; c < nc; ++c) {

@@ -123,8 +123,9 @@ def test_forward_repeatable_byte_identical():
 
 @pytest.mark.parametrize("name, overrides", [
     ("c2", dict(Hq=4, Hkv=2, causal=True)),                        # one chunk
-    ("c1", dict(B=2, Hq=16, Hkv=4, Nq=4096, Nkv=4096, causal=True)),  # three chunks of 2, 3, 3 KV heads
-    ("c5", {})])                                                    # the benchmark's workload: eight chunks
+    ("c1", dict(B=2, Hq=16, Hkv=4, Nq=4096, Nkv=4096, causal=True)),  # two chunks of 4 KV heads
+    ("c3", dict(B=1, Hq=32, Hkv=32)),                              # equal chunks (ramp ends too small)
+    ("c5", {})])                                                    # ramp of 2, 3, 5, 6, 6, 5, 3, 2 KV heads
 def test_host_entry_point_matches_device_path(name, overrides):
     # the host-buffer path cuts the (batch, KV head) units into chunks that it
     # pipelines over two streams; its output must equal the one-pass device path
