@@ -284,6 +284,34 @@ int sattn_prepare_noalloc(const sattn_shape *shape, const void *q, const void *k
                           float *k_mean, void *k_carrier, uint8_t *v_codes, float *v_scales,
                           void *stream);
 
+/*
+ * sattn_graph_create / sattn_graph_launch / sattn_graph_destroy -- the
+ * preparation and the forward pass on fixed buffers, recorded once as a CUDA
+ * graph and replayed with one launch per step.  This is the small-shape
+ * latency path: at the sizes where the seven launches of a step cost more on
+ * the host than the kernels on the GPU, one graph launch replaces them.
+ *   create   arguments as sattn_prepare followed by sattn_forward's out and
+ *            workspace; the buffers are recorded by address and must stay
+ *            allocated until the graph is destroyed.  Each launch reads
+ *            whatever q, k, v hold when it runs, and writes every output
+ *            sattn_prepare and sattn_forward write.  *graph receives an
+ *            opaque handle (NULL on failure).  Capture runs on a private
+ *            stream of the call; nothing is executed.
+ *   launch   enqueues one replay on `stream`; sattn_check_status on the
+ *            forward workspace reads its status after the stream synchronises
+ *   destroy  releases the graph (after its last launch has completed)
+ * The output of a launch equals sattn_prepare + sattn_forward, byte for byte.
+ * Errors as those two calls; launch and destroy return SATTN_ERR_INVALID for a
+ * NULL handle.
+ */
+typedef struct sattn_graph sattn_graph;
+int sattn_graph_create(const sattn_shape *shape, const void *q, const void *k, const void *v,
+                       int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
+                       float *k_mean, void *k_carrier, uint8_t *v_codes, float *v_scales,
+                       void *prepare_workspace, void *out, void *forward_workspace, sattn_graph **graph);
+int sattn_graph_launch(sattn_graph *graph, void *stream);
+int sattn_graph_destroy(sattn_graph *graph);
+
 /* A static, human-readable name for a status code. */
 const char *sattn_status_string(int status);
 

@@ -75,12 +75,15 @@ def load_library(build: bool = True):
     lib.sattn_forward_q_bf16.argtypes = [SP] + [P] * 8
     lib.sattn_check_status.argtypes = [P, P]
     lib.sattn_test_int8_quantiser.argtypes = [ctypes.c_uint32, ctypes.c_uint32, P, P]
+    lib.sattn_graph_create.argtypes = [SP] + [P] * 14 + [ctypes.POINTER(ctypes.c_void_p)]
+    lib.sattn_graph_launch.argtypes = [P, P]
+    lib.sattn_graph_destroy.argtypes = [P]
     lib.sattn_attention_host.argtypes = [SP, P, P, P, P, P, ctypes.c_size_t, P]
     lib.sattn_status_string.argtypes = [ctypes.c_int]
     lib.sattn_status_string.restype = ctypes.c_char_p
     for name in ("sattn_query_sizes", "sattn_prepare", "sattn_forward", "sattn_check_status",
                  "sattn_attention_host", "sattn_prepare_noalloc", "sattn_prepare_kv", "sattn_forward_q_bf16",
-                 "sattn_test_int8_quantiser"):
+                 "sattn_test_int8_quantiser", "sattn_graph_create", "sattn_graph_launch", "sattn_graph_destroy"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -309,6 +312,55 @@ def int8_quantiser_sweep_for_test(amax_lo: int = 1, amax_hi: int = 0x7f80, devic
         raise SattnError(rc, "sattn_test_int8_quantiser")
     bad, near, last = (int(v) for v in res[:3].cpu())
     return bad, near, last
+
+
+class Graph:
+    """sattn_graph_*: prepare + forward on fixed buffers recorded as one CUDA
+    graph (the small-shape latency path).  q, k, v are the device tensors the
+    graph reads: fill them in place and call launch() for each step.  The
+    preparation buffers (``buffers``, as from prepare_buffers), ``out`` and
+    ``workspace`` are allocated here unless given."""
+
+    def __init__(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                 sm_scale: float = 0.0, buffers: dict | None = None, out: torch.Tensor | None = None,
+                 workspace: torch.Tensor | None = None):
+        _need_cuda(q, k, v)
+        B, Hq, Nq, _ = q.shape
+        shape = make_shape(B, Hq, k.shape[1], Nq, k.shape[2], causal, sm_scale)
+        dev = q.device
+        prep = buffers if buffers is not None else prepare_buffers(shape, dev)
+        self.out = out if out is not None else torch.empty((B, Hq, Nq, HEAD_DIM), dtype=torch.bfloat16, device=dev)
+        self.workspace = workspace if workspace is not None else _empty(query_sizes(shape)["forward_workspace"], dev)
+        self.buffers = prep
+        self._keep = (q, k, v)   # the graph holds their addresses
+        self.shape = shape
+        handle = ctypes.c_void_p()
+        rc = load_library().sattn_graph_create(
+            ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(prep["q_codes"]), _ptr(prep["q_scales"]),
+            _ptr(prep["k_codes"]), _ptr(prep["k_scales"]), _ptr(prep["k_mean"]), _ptr(prep["k_carrier"]),
+            _ptr(prep["v_codes"]), _ptr(prep["v_scales"]), _ptr(prep["workspace"]), _ptr(self.out),
+            _ptr(self.workspace), ctypes.byref(handle))
+        if rc != 0:
+            raise SattnError(rc, "sattn_graph_create")
+        self._handle = handle
+
+    def launch(self, stream=None) -> torch.Tensor:
+        rc = load_library().sattn_graph_launch(self._handle, _stream(stream))
+        if rc != 0:
+            raise SattnError(rc, "sattn_graph_launch")
+        return self.out
+
+    def close(self):
+        if getattr(self, "_handle", None):
+            torch.cuda.synchronize()
+            load_library().sattn_graph_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # interpreter shutdown: the process releases the graph
+            pass
 
 
 def check_status(workspace: torch.Tensor, stream=None) -> int:

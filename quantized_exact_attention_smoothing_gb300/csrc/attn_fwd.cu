@@ -1011,6 +1011,26 @@ size_t forward_workspace_bytes(const Geometry &)
 
 namespace {
 
+// The per-warpgroup register split only adds up when the kernel is launched
+// with exactly kLaunchRegs registers per thread; refuse to launch otherwise.
+// Also raises the kernel's dynamic shared-memory limit.  Once per process.
+template <bool kFuseQ>
+cudaError_t kernel_attributes()
+{
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        cudaFuncAttributes fa;
+        attr_err = cudaFuncGetAttributes(&fa, attn_fwd_kernel<kFuseQ>);
+        if (attr_err == cudaSuccess && fa.numRegs != kLaunchRegs)
+            attr_err = cudaErrorInvalidConfiguration;
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(attn_fwd_kernel<kFuseQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(SMEM_BYTES));
+    });
+    return attr_err;
+}
+
 // q: INT8 codes [B, Hq, nq32, 128] with q_scales, or with kFuseQ the BF16 Q
 // [B, Hq, Nq, 128] itself (q_scales unused)
 template <bool kFuseQ>
@@ -1074,19 +1094,7 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const v
             return 1;
     }
 
-    // The per-warpgroup register split only adds up when the kernel is launched
-    // with exactly kLaunchRegs registers per thread; refuse to launch otherwise.
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        cudaFuncAttributes fa;
-        attr_err = cudaFuncGetAttributes(&fa, attn_fwd_kernel<kFuseQ>);
-        if (attr_err == cudaSuccess && fa.numRegs != kLaunchRegs)
-            attr_err = cudaErrorInvalidConfiguration;
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(attn_fwd_kernel<kFuseQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            static_cast<int>(SMEM_BYTES));
-    });
+    const cudaError_t attr_err = kernel_attributes<kFuseQ>();
     if (attr_err != cudaSuccess)
         return static_cast<int>(attr_err);
 
@@ -1142,6 +1150,14 @@ int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scal
 {
     return launch_impl<false>(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out, workspace, stream,
                               withhold_v, reset_status);
+}
+
+int forward_init()
+{
+    if (!tensor_map_encoder())
+        return 1;
+    const cudaError_t a = kernel_attributes<false>(), b = kernel_attributes<true>();
+    return a != cudaSuccess ? static_cast<int>(a) : static_cast<int>(b);
 }
 
 int launch_forward_q_bf16(const Geometry &g, const void *q, const void *k_carrier, const float *k_scales,

@@ -496,6 +496,87 @@ int sattn_attention_host(const sattn_shape *shape, const void *q_host, const voi
                                     static_cast<cudaStream_t>(stream));
 }
 
+struct sattn_graph {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+};
+
+int sattn_graph_create(const sattn_shape *shape, const void *q, const void *k, const void *v, int8_t *q_codes,
+                       float *q_scales, int8_t *k_codes, float *k_scales, float *k_mean, void *k_carrier,
+                       uint8_t *v_codes, float *v_scales, void *prepare_workspace, void *out,
+                       void *forward_workspace, sattn_graph **graph)
+{
+    if (!graph)
+        return SATTN_ERR_INVALID;
+    *graph = nullptr;
+    Geometry g;
+    int rc = make_geometry(shape, &g);
+    if (rc != SATTN_OK)
+        return rc;
+    const void *ptrs[] = {q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes, v_scales,
+                          prepare_workspace, out, forward_workspace};
+    for (const void *ptr : ptrs) {
+        if (!ptr)
+            return SATTN_ERR_INVALID;
+        if (!aligned16(ptr))
+            return SATTN_ERR_MISALIGNED;
+    }
+    rc = check_device();
+    if (rc != SATTN_OK)
+        return rc;
+    const int init = sattn::forward_init();   // no one-time setup calls inside the capture
+    if (init == 1)
+        return SATTN_ERR_DEVICE;
+    if (init != 0)
+        return SATTN_ERR_LAUNCH;
+    cudaStream_t cs = nullptr;
+    if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess)
+        return SATTN_ERR_DEVICE;
+    sattn_graph *gr = new sattn_graph;
+    rc = SATTN_OK;
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        rc = SATTN_ERR_LAUNCH;
+    } else {
+        rc = prepare_impl(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes, v_scales,
+                          prepare_workspace, cs);
+        if (rc == SATTN_OK)
+            rc = forward_impl(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out, forward_workspace,
+                              cs);
+        const cudaError_t end = cudaStreamEndCapture(cs, &gr->graph);   // ends the capture in every case
+        if (rc == SATTN_OK && end != cudaSuccess)
+            rc = SATTN_ERR_LAUNCH;
+    }
+    if (rc == SATTN_OK && cudaGraphInstantiate(&gr->exec, gr->graph, 0) != cudaSuccess)
+        rc = SATTN_ERR_LAUNCH;
+    cudaStreamDestroy(cs);
+    if (rc != SATTN_OK) {
+        sattn_graph_destroy(gr);
+        return rc;
+    }
+    *graph = gr;
+    return SATTN_OK;
+}
+
+int sattn_graph_launch(sattn_graph *graph, void *stream)
+{
+    if (!graph || !graph->exec)
+        return SATTN_ERR_INVALID;
+    return cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SATTN_OK
+                                                                                          : SATTN_ERR_LAUNCH;
+}
+
+int sattn_graph_destroy(sattn_graph *graph)
+{
+    if (!graph)
+        return SATTN_ERR_INVALID;
+    if (graph->exec)
+        cudaGraphExecDestroy(graph->exec);
+    if (graph->graph)
+        cudaGraphDestroy(graph->graph);
+    delete graph;
+    return SATTN_OK;
+}
+
 const char *sattn_status_string(int status)
 {
     switch (status) {

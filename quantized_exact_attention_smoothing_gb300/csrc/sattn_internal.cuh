@@ -51,6 +51,11 @@ int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scal
                    const float *v_scales, void *out, void *workspace, cudaStream_t stream,
                    bool withhold_v = false, bool reset_status = true);
 
+// One-time host setup of the forward kernels (tensor-map encoder, register
+// check, shared-memory limit), so that launches captured into a CUDA graph
+// make no such calls.  Returns 0, 1 without an encoder, or a CUDA error.
+int forward_init();
+
 // The forward pass with Q quantised inside the kernel: q is the BF16 Q
 // [B, Hq, Nq, 128]; the codes and block scales are those launch_prepare
 // writes, and the output is launch_forward's on them, byte for byte.

@@ -112,3 +112,19 @@ def test_quantiser_sweep_hook_checks_arguments(lib):
     assert lib.sattn_test_int8_quantiser(5, 5, ctypes.c_void_p(0x1000), None) == 1
     assert lib.sattn_test_int8_quantiser(1, 10, None, None) == 1
     assert lib.sattn_test_int8_quantiser(1, 10, ctypes.c_void_p(0x1008), None) == 2
+
+
+def test_graph_entry_points_check_arguments(lib):
+    s = sattn.make_shape(1, 1, 1, 8, 8)
+    bufs = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(14)]
+    h = ctypes.c_void_p()
+    assert lib.sattn_graph_create(ctypes.byref(s), *bufs, None) == 1          # no handle pointer
+    args = list(bufs)
+    args[12] = None                                                          # out
+    assert lib.sattn_graph_create(ctypes.byref(s), *args, ctypes.byref(h)) == 1
+    assert h.value is None
+    args = list(bufs)
+    args[0] = ctypes.c_void_p(0x1002)                                        # q misaligned
+    assert lib.sattn_graph_create(ctypes.byref(s), *args, ctypes.byref(h)) == 2
+    assert lib.sattn_graph_launch(None, None) == 1
+    assert lib.sattn_graph_destroy(None) == 1
