@@ -571,8 +571,8 @@ __device__ __forceinline__ void qconv_role(const FwdParams &p, const CUtensorMap
 // alpha_{j-1} (both halves keep d).  The Q block scale of a row comes from
 // q_scales, or with kFuseQ from the scale slot the Q converter fills (QQDONE).
 template <bool kFuseQ>
-__device__ __forceinline__ bool compute_loop(const FwdParams &p, uint32_t sb, uint32_t tmem, int warp, int lane,
-                                             const Waiter &wt)
+__device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorMap *tm_o, uint32_t sb, uint32_t tmem,
+                                             int warp, int lane, const Waiter &wt)
 {
     auto bar = [sb](int i) { return sb + OFF_BAR + 8u * i; };
     const int half = warp >> 2;                               // 0 or 1
@@ -817,10 +817,14 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, uint32_t sb, ui
         }
         // final conversion: reciprocal of d, per-channel V scale, BF16.  Each
         // warp stages its 32 rows x 64 channels (4 KB of its own, 16-byte chunk
-        // c of row l at chunk c ^ (l % 8)) in shared memory and then writes
-        // whole 128-byte row segments, eight threads per row, instead of one
-        // 16-byte piece per row per store.
+        // c of row l at chunk c ^ (l % 8): the 128-byte swizzle) in shared
+        // memory, and one thread stores the tile with TMA (rows >= Nq are
+        // clipped by the tensor map).  The previous item's store has long
+        // finished reading the staging buffer; the wait only confirms it.
         {
+            if (lane == 0)
+                ptx::bulk_wait_read();
+            __syncwarp();
             const float rcp = d > 0.0f ? __frcp_rn(d) : 0.0f;
             const uint32_t sv4 = sb + OFF_SV + (n % 3) * SV_BYTES + 4 * 64 * half;   // landed with this item's Q
             const uint32_t stage = sb + OFF_STG + (quarter * 2 + half) * 4096;
@@ -841,23 +845,17 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, uint32_t sb, ui
                 }
                 ptx::st_shared_v4(stage + lane * 128 + ((w ^ (lane & 7)) << 4), u[0], u[1], u[2], u[3]);
             }
+            ptx::fence_proxy_async_smem();   // the TMA store reads what the threads wrote
             __syncwarp();
-            const int ch = lane & 7;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int l = 4 * k + (lane >> 3);                     // row of the warp's 32
-                const int row = t.q0 + quarter * 32 + l;
-                const uint4 v = ptx::ld_shared_v4(stage + l * 128 + ((ch ^ (l & 7)) << 4));
-                if (row < p.Nq)
-                    *reinterpret_cast<uint4 *>(p.out + (static_cast<size_t>(t.b * p.Hq + t.hq) * p.Nq + row) * HD +
-                                               64 * half + 8 * ch) = v;
+            if (lane == 0) {
+                ptx::tma_store_3d(tm_o, stage, 64 * half, t.q0 + quarter * 32, t.b * p.Hq + t.hq);
+                ptx::bulk_commit();
+                if (kFuseQ)   // the Q converter stages the item after next here: the store must have read it
+                    ptx::bulk_wait_read();
             }
             __syncwarp();
-            if (kFuseQ) {   // STGFREE phase n + 1: the Q converter stages the item after next here (TMA)
-                ptx::fence_proxy_async_smem();
-                if (lane == 0)
-                    ptx::mbar_arrive(bar(STGFREE));
-            }
+            if (kFuseQ && lane == 0)   // STGFREE phase n + 1
+                ptx::mbar_arrive(bar(STGFREE));
         }
         if (r == 0 && half == 0)
             SATTN_TRACE(p, t, 38, 2);
@@ -878,10 +876,13 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, uint32_t sb, ui
 // compute warp checks the mark before that barrier, so none waits for a warp
 // that has left.
 template <bool kFuseQ>
-__device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, uint32_t tmem, int warp, int lane,
-                                             const Waiter &wt)
+__device__ __forceinline__ void compute_role(const FwdParams &p, const CUtensorMap *tm_o, uint32_t sb, uint32_t tmem,
+                                             int warp, int lane, const Waiter &wt)
 {
-    if (!compute_loop<kFuseQ>(p, sb, tmem, warp, lane, wt)) {
+    const bool ok = compute_loop<kFuseQ>(p, tm_o, sb, tmem, warp, lane, wt);
+    if (lane == 0)
+        ptx::bulk_wait_all();   // output stores complete before the CTA's shared memory is released
+    if (!ok) {
         asm volatile("st.shared.u32 [%0], 1;" ::"r"(sb + OFF_ABORT) : "memory");
         ptx::named_bar_arrive(1 + (warp & 3), 64);
     }
@@ -890,7 +891,8 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, uint32_t sb, ui
 template <bool kFuseQ>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_q, const FwdParams p)
+                    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
+                    const FwdParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -951,7 +953,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (*flag == 0 && static_cast<int>(blockIdx.x) < p.n_items) {
         if (warp < WARP_PRODUCER) {
             ptx::setmaxnreg_inc<kRegsCompute>();
-            compute_role<kFuseQ>(p, sb, tmem, warp, lane, wt);
+            compute_role<kFuseQ>(p, &tm_o, sb, tmem, warp, lane, wt);
         } else {
             ptx::setmaxnreg_dec<kRegsOther>();
             if (warp == WARP_PRODUCER) {
@@ -1046,7 +1048,18 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const v
     if (reset_status && cudaMemsetAsync(status, 0, 2 * sizeof(uint32_t), stream) != cudaSuccess)
         return static_cast<int>(cudaGetLastError());
 
-    CUtensorMap tmk, tmv;
+    CUtensorMap tmk, tmv, tmo;
+    {   // BF16 output, stored per warp as 32 rows x 64 channels (128-byte swizzle); rows >= Nq are clipped
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(g.Nq),
+                                    static_cast<cuuint64_t>(g.B) * g.Hq};
+        const cuuint64_t strides[2] = {HD * 2, static_cast<cuuint64_t>(g.Nq) * HD * 2};
+        const cuuint32_t box[3] = {64, 32, 1};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        if (encode(&tmo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return 1;
+    }
     {
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(g.Nkv),
                                     static_cast<cuuint64_t>(bhk)};
@@ -1137,7 +1150,7 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const v
         cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1)
         return static_cast<int>(cudaErrorInvalidDevice);
     const int grid = std::min(prm.n_items, n_sm);
-    attn_fwd_kernel<kFuseQ><<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, prm);
+    attn_fwd_kernel<kFuseQ><<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, tmo, prm);
     return static_cast<int>(cudaGetLastError());
 }
 
