@@ -297,9 +297,9 @@ def run_ours(args, world, rank, local):
     peaks = load_peaks()
     mp = mixed_peak(peaks["bf16_tflops"])
     # DRAM bytes of one attn_fwd_kernel launch from the ncu capture summarised in
-    # profiles/attn_fwd_c5_b3_full.md (c5 at batch 3: 490.5 MB read + 159.9 MB
+    # profiles/attn_fwd_c5_b3_full.md (c5 at batch 3: 495.3 MB read + 159.7 MB
     # written), scaled by the units processed; other workloads were not captured.
-    traffic = 650.49e6 * w.B / 3.0 if w.name == "c5" else None
+    traffic = 655.01e6 * w.B / 3.0 if w.name == "c5" else None
     achieved = w.algorithmic_ops / (ms_fwd * 1e-3) / 1e12
     prep_bytes = (hq.numel() + hk.numel() + hv.numel()) * 2 + \
         (buf["q_codes"].numel() + buf["k_codes"].numel() + w.B * w.Hkv * 128 * w.Nkv) + \
