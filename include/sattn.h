@@ -131,6 +131,11 @@ int sattn_query_sizes(const sattn_shape *shape, sattn_sizes *sizes);
  *               are ignored
  * Codes and scales are bit-exact functions of the inputs (the arithmetic is
  * fixed above, including the summation order of the mean).
+ * Q's quantisation runs on a helper stream of the library (created once per
+ * device) concurrently with the K/V kernels on `stream`, and V's beside K's
+ * on a second one after the shared K/V statistics; `stream` waits for both
+ * before the call's work ends, so everything is ordered on `stream` as the
+ * caller sees it (and a CUDA graph capture of the call records the branches).
  */
 int sattn_prepare(const sattn_shape *shape, const void *q, const void *k, const void *v,
                   int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,

@@ -353,6 +353,45 @@ cudaError_t launch_prepare(const Geometry &g, const void *q, const void *k, cons
     return cudaGetLastError();
 }
 
+cudaError_t launch_prepare_kv_split(const Geometry &g, const void *k, const void *v, int8_t *k_codes,
+                                    float *k_scales, float *k_mean, void *k_carrier, uint8_t *v_codes,
+                                    float *v_scales, void *workspace, cudaStream_t stream, cudaStream_t v_stream,
+                                    cudaEvent_t fork, cudaEvent_t join)
+{
+    const int bhk = g.B * g.Hkv;
+    float *ksum = static_cast<float *>(workspace);
+    float *vmax = ksum + static_cast<size_t>(bhk) * g.nchunks * kHeadDim;
+    const uint4 *k4 = static_cast<const uint4 *>(k);
+    const uint4 *v4 = static_cast<const uint4 *>(v);
+    kv_chunk_stats_kernel<<<dim3(static_cast<unsigned>((g.nchunks + 15) / 16), bhk), 256, 0,
+                            stream>>>(k4, v4, g.Nkv, static_cast<int>(g.nchunks), ksum, vmax);
+    kv_finalize_kernel<<<bhk, kHeadDim, 0, stream>>>(ksum, vmax, g.Nkv, static_cast<int>(g.nchunks),
+                                                     k_mean, v_scales);
+    cudaError_t e = cudaEventRecord(fork, stream);
+    if (e == cudaSuccess)
+        e = cudaStreamWaitEvent(v_stream, fork, 0);
+    if (e != cudaSuccess)
+        return e;
+    quant_v_kernel<<<dim3(static_cast<unsigned>(g.nk128 / kVPad), bhk), 256, 0, v_stream>>>(
+        v4, g.Nkv, g.nk128, v_scales, v_codes);
+    if ((e = cudaEventRecord(join, v_stream)) != cudaSuccess)
+        return e;
+    quant_int8_kernel<true><<<dim3(static_cast<unsigned>(g.nbk), bhk), 256, 0, stream>>>(
+        k4, g.Nkv, g.nk32, static_cast<int>(g.nbk), k_mean, k_codes, k_scales, static_cast<uint4 *>(k_carrier));
+    if ((e = cudaStreamWaitEvent(stream, join, 0)) != cudaSuccess)
+        return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prepare_q(const Geometry &g, const void *q, int8_t *q_codes, float *q_scales,
+                             cudaStream_t stream)
+{
+    quant_int8_kernel<false><<<dim3(static_cast<unsigned>(g.nbq), static_cast<unsigned>(g.B * g.Hq)), 256, 0,
+                               stream>>>(static_cast<const uint4 *>(q), g.Nq, g.nq32, static_cast<int>(g.nbq), nullptr,
+                                         q_codes, q_scales, nullptr);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_int8_quantiser_sweep(uint32_t amax_lo, uint32_t amax_hi, unsigned long long *result,
                                         cudaStream_t stream)
 {

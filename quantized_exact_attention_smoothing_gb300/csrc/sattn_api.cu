@@ -96,6 +96,60 @@ int check_device()
     return verdict[dev] == 1 ? SATTN_OK : SATTN_ERR_DEVICE;
 }
 
+constexpr int kMaxHostChunks = 8;
+
+// Helper streams and events of the library, created once per device: the
+// host-buffer pipeline's three stage streams, and the stream on which the
+// preparation quantises Q while the K/V kernels run on the caller's stream.
+struct DeviceStreams {
+    cudaStream_t h2d = nullptr, compute = nullptr, d2h = nullptr, qprep = nullptr, vprep = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, in[kMaxHostChunks] = {}, done[kMaxHostChunks] = {};
+    cudaEvent_t qfork = nullptr, qjoin = nullptr, vfork = nullptr, vjoin = nullptr;
+};
+
+struct HelperStreams {
+    std::mutex mu;
+    DeviceStreams dev[64];
+};
+
+HelperStreams &helpers()
+{
+    static HelperStreams h;
+    return h;
+}
+
+bool create_streams(DeviceStreams &d)
+{
+    if (d.h2d)
+        return true;
+    bool ok = cudaStreamCreateWithFlags(&d.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&d.compute, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&d.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming) == cudaSuccess;
+    for (int c = 0; c < kMaxHostChunks && ok; ++c)
+        ok = cudaEventCreateWithFlags(&d.in[c], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&d.done[c], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok)
+        d.h2d = nullptr;   // retried on the next call
+    return ok;
+}
+
+bool create_qprep_stream(DeviceStreams &d)
+{
+    if (d.qprep)
+        return true;
+    const bool ok = cudaStreamCreateWithFlags(&d.qprep, cudaStreamNonBlocking) == cudaSuccess &&
+                    cudaStreamCreateWithFlags(&d.vprep, cudaStreamNonBlocking) == cudaSuccess &&
+                    cudaEventCreateWithFlags(&d.qfork, cudaEventDisableTiming) == cudaSuccess &&
+                    cudaEventCreateWithFlags(&d.qjoin, cudaEventDisableTiming) == cudaSuccess &&
+                    cudaEventCreateWithFlags(&d.vfork, cudaEventDisableTiming) == cudaSuccess &&
+                    cudaEventCreateWithFlags(&d.vjoin, cudaEventDisableTiming) == cudaSuccess;
+    if (!ok)
+        d.qprep = nullptr;   // retried on the next call
+    return ok;
+}
+
 int prepare_impl(const Geometry &g, const void *q, const void *k, const void *v, int8_t *q_codes,
                  float *q_scales, int8_t *k_codes, float *k_scales, float *k_mean, void *k_carrier,
                  uint8_t *v_codes, float *v_scales, void *workspace, cudaStream_t stream)
@@ -110,13 +164,33 @@ int prepare_impl(const Geometry &g, const void *q, const void *k, const void *v,
         if (!aligned16(p))
             return SATTN_ERR_MISALIGNED;
     }
-    const int dev = check_device();
-    if (dev != SATTN_OK)
-        return dev;
-    return sattn::launch_prepare(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes,
-                                 v_scales, workspace, stream) == cudaSuccess
-               ? SATTN_OK
-               : SATTN_ERR_LAUNCH;
+    const int dc = check_device();
+    if (dc != SATTN_OK)
+        return dc;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return SATTN_ERR_DEVICE;
+    // Q's quantisation depends on nothing the K/V kernels compute: it runs on
+    // a helper stream, concurrently with them on `stream`; after the K/V
+    // statistics, V's quantisation runs on a second helper stream beside K's.
+    // `stream` waits for both at the end (all work stays ordered on `stream`
+    // for the caller).
+    HelperStreams &h = helpers();
+    std::lock_guard<std::mutex> lock(h.mu);
+    DeviceStreams &ds = h.dev[dev];
+    if (!with_q || !create_qprep_stream(ds))
+        return sattn::launch_prepare(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes,
+                                     v_scales, workspace, stream) == cudaSuccess
+                   ? SATTN_OK
+                   : SATTN_ERR_LAUNCH;
+    if (cudaEventRecord(ds.qfork, stream) != cudaSuccess || cudaStreamWaitEvent(ds.qprep, ds.qfork, 0) != cudaSuccess ||
+        sattn::launch_prepare_q(g, q, q_codes, q_scales, ds.qprep) != cudaSuccess ||
+        cudaEventRecord(ds.qjoin, ds.qprep) != cudaSuccess ||
+        sattn::launch_prepare_kv_split(g, k, v, k_codes, k_scales, k_mean, k_carrier, v_codes, v_scales, workspace,
+                                       stream, ds.vprep, ds.vfork, ds.vjoin) != cudaSuccess ||
+        cudaStreamWaitEvent(stream, ds.qjoin, 0) != cudaSuccess)
+        return SATTN_ERR_LAUNCH;
+    return SATTN_OK;
 }
 
 // q_bf16 non-null: the forward that quantises Q itself (q_codes, q_scales unused)
@@ -165,8 +239,6 @@ struct HostBuffers {
     uint8_t *v_codes;
 };
 
-constexpr int kMaxHostChunks = 8;
-
 // Chunk plan for the pipeline: at most kMaxHostChunks chunks, each of at
 // least two work items of the forward per SM (smaller chunks would leave SMs
 // idle), sized like a ramp (weights 1, 2, 3, ..., 3, 2, 1): the first chunk's
@@ -207,39 +279,6 @@ int host_chunks(const Geometry &g, int n_sm, int64_t (&bound)[kMaxHostChunks + 1
     bound[0] = 0;
     bound[1] = units;
     return 1;
-}
-
-struct DeviceStreams {
-    cudaStream_t h2d = nullptr, compute = nullptr, d2h = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr, in[kMaxHostChunks] = {}, done[kMaxHostChunks] = {};
-};
-
-struct HelperStreams {
-    std::mutex mu;
-    DeviceStreams dev[64];
-};
-
-HelperStreams &helpers()
-{
-    static HelperStreams h;
-    return h;
-}
-
-bool create_streams(DeviceStreams &d)
-{
-    if (d.h2d)
-        return true;
-    bool ok = cudaStreamCreateWithFlags(&d.h2d, cudaStreamNonBlocking) == cudaSuccess &&
-              cudaStreamCreateWithFlags(&d.compute, cudaStreamNonBlocking) == cudaSuccess &&
-              cudaStreamCreateWithFlags(&d.d2h, cudaStreamNonBlocking) == cudaSuccess &&
-              cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming) == cudaSuccess &&
-              cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming) == cudaSuccess;
-    for (int c = 0; c < kMaxHostChunks && ok; ++c)
-        ok = cudaEventCreateWithFlags(&d.in[c], cudaEventDisableTiming) == cudaSuccess &&
-             cudaEventCreateWithFlags(&d.done[c], cudaEventDisableTiming) == cudaSuccess;
-    if (!ok)
-        d.h2d = nullptr;   // retried on the next call
-    return ok;
 }
 
 int attention_host_pipelined(const Geometry &g, const sattn_shape &shape, const void *q_host, const void *k_host,

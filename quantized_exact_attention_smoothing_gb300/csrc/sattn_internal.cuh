@@ -28,6 +28,16 @@ struct Geometry {
 // ---- prepare (prepare.cu) ----
 // Workspace: [B*Hkv][nchunks][128] FP32 K column sums, then the same for V max |v|.
 size_t prepare_workspace_bytes(const Geometry &g);
+// The K/V part of launch_prepare with V's quantisation on v_stream: after the
+// K/V statistics `fork` is recorded on `stream` and waited by v_stream; `join`
+// is recorded on v_stream after V's kernel and waited by `stream` at the end.
+cudaError_t launch_prepare_kv_split(const Geometry &g, const void *k, const void *v, int8_t *k_codes,
+                                    float *k_scales, float *k_mean, void *k_carrier, uint8_t *v_codes,
+                                    float *v_scales, void *workspace, cudaStream_t stream, cudaStream_t v_stream,
+                                    cudaEvent_t fork, cudaEvent_t join);
+// The Q part of launch_prepare alone (INT8 codes and block scales of Q).
+cudaError_t launch_prepare_q(const Geometry &g, const void *q, int8_t *q_codes, float *q_scales,
+                             cudaStream_t stream);
 // Test hook: the INT8 quantiser against IEEE division over BF16 blocks whose
 // amax has BF16 bits in [amax_lo, amax_hi) (device result[3], see prepare.cu).
 cudaError_t launch_int8_quantiser_sweep(uint32_t amax_lo, uint32_t amax_hi, unsigned long long *result,
