@@ -568,6 +568,15 @@ int sattn_graph_create(const sattn_shape *shape, const void *q, const void *k, c
         return SATTN_ERR_DEVICE;
     if (init != 0)
         return SATTN_ERR_LAUNCH;
+    {   // nor the creation of the preparation's helper streams
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+            return SATTN_ERR_DEVICE;
+        HelperStreams &h = helpers();
+        std::lock_guard<std::mutex> lock(h.mu);
+        if (!create_qprep_stream(h.dev[dev]))
+            return SATTN_ERR_DEVICE;
+    }
     cudaStream_t cs = nullptr;
     if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess)
         return SATTN_ERR_DEVICE;

@@ -33,3 +33,30 @@ def test_graph_replay_equals_direct_calls(name, overrides):
             assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), f"seed {seed}"
     finally:
         g.close()
+
+
+def test_graph_as_the_first_call_of_a_process(tmp_path):
+    # a fresh process whose first library call is sattn_graph_create: the
+    # helper streams and kernel attributes are set up before the capture
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    script = tmp_path / "graph_first.py"
+    script.write_text(
+        "import sys, torch\n"
+        f"sys.path.insert(0, {root!r}); sys.path.insert(0, {os.path.join(root, 'tests')!r})\n"
+        "import synth, quantized_exact_attention_smoothing_gb300 as sattn\n"
+        "from helpers import to_device_bf16\n"
+        "w = synth.workload('c1', causal=True)\n"
+        "q, k, v = (to_device_bf16(x) for x in synth.make_inputs(w, seed=5))\n"
+        "g = sattn.Graph(q, k, v, causal=True)\n"
+        "got = g.launch().clone()\n"
+        "assert sattn.check_status(g.workspace) == 0\n"
+        "ref = sattn.forward(sattn.prepare(q, k, v, True))\n"
+        "torch.cuda.synchronize()\n"
+        "assert torch.equal(got.view(torch.int16), ref.view(torch.int16))\n"
+        "g.close()\n"
+        "print('ok')\n")
+    r = subprocess.run([sys.executable, str(script)], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
