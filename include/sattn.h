@@ -41,10 +41,16 @@
  *
  * Ownership and synchronisation: the caller allocates every buffer (device
  * memory unless stated otherwise) and owns the stream.  Calls only enqueue
- * work on `stream` (a cudaStream_t; NULL is the legacy default stream) and
- * return; they never allocate, free or synchronise, except
- * sattn_check_status which synchronises the stream by design.  All device
- * pointers must be 16-byte aligned.  Buffers of one call must not overlap.
+ * work and return: on `stream` (a cudaStream_t; NULL is the legacy default
+ * stream), and for sattn_prepare and sattn_attention_host also on helper
+ * streams of the library that fork from `stream` and join back into it with
+ * events, so the caller sees all of a call's work ordered on `stream`.  The
+ * helper streams and events are created once per device and kept for the
+ * life of the process.  Calls never allocate device memory, free or
+ * synchronise, except sattn_check_status, which synchronises the stream by
+ * design, and sattn_graph_create, which builds a CUDA graph (released by
+ * sattn_graph_destroy).  All device pointers must be 16-byte aligned.
+ * Buffers of one call must not overlap.
  *
  * Errors: every entry point returns an sattn_status; no exception crosses
  * the ABI.  Argument checks happen before anything is enqueued; a failing
