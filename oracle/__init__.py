@@ -76,6 +76,8 @@ def _load():
     lib.oracle_forward_rows.argtypes = [i, i, i, i, i, i, ctypes.c_float, i,
                                         P, P, P, P, P, P, ctypes.c_long, P, P, P, i]
     lib.oracle_forward_rows.restype = i
+    lib.oracle_first_tile.argtypes = [i, i, i, i, i, i, ctypes.c_float, i, P, P, P, P, P, P, i, i, i, P, P, P]
+    lib.oracle_first_tile.restype = i
     lib.oracle_forward_exact.argtypes = [i, i, i, i, i, i, ctypes.c_double, i,
                                          P, P, P, i, P]
     lib.oracle_forward_exact.restype = i
@@ -183,6 +185,26 @@ def forward(prep: dict, Nq: int, Nkv: int, causal: bool, sm_scale: float = 0.0, 
     if rc != 0:
         raise ValueError("oracle_forward: invalid shape or rows")
     return ob, of
+
+
+def first_tile(prep: dict, Nq: int, Nkv: int, causal: bool, b: int = 0, h: int = 0, q0: int = 0,
+               sm_scale: float = 0.0, tile: int = 256):
+    """Intermediates of the first KV tile for query rows q0 .. q0 + 127 of
+    (b, h): exact int32 QK accumulators [128, tile], P8 bytes [128, tile] and
+    the tile's PV partial with its weight sum in column 128 [128, 129]."""
+    lib = _load()
+    B, Hq = prep["q_codes"].shape[:2]
+    Hkv = prep["k_codes"].shape[1]
+    acc = np.empty((128, tile), np.int32)
+    p8 = np.empty((128, tile), np.uint8)
+    part = np.empty((128, HEAD_DIM + 1), np.float32)
+    rc = lib.oracle_first_tile(B, Hq, Hkv, Nq, Nkv, int(bool(causal)), float(sm_scale), tile,
+                               _ptr(prep["q_codes"]), _ptr(prep["q_scales"]), _ptr(prep["k_codes"]),
+                               _ptr(prep["k_scales"]), _ptr(prep["v_codes"]), _ptr(prep["v_scales"]),
+                               b, h, q0, _ptr(acc), _ptr(p8), _ptr(part))
+    if rc != 0:
+        raise ValueError("oracle_first_tile: invalid shape or position")
+    return acc, p8, part
 
 
 def forward_exact(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool, smooth: bool,

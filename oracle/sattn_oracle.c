@@ -393,6 +393,76 @@ int oracle_forward(int B, int Hq, int Hkv, int Nq, int Nkv, int causal, float sm
     return 0;
 }
 
+/* oracle_first_tile: the checked intermediates of the first KV tile (entry
+ * "Phase 2B Fixed Aligned Numerical Prototype": QK, m, FP8 probability, PV)
+ * for the query rows q0 .. q0 + 127 of (batch b, query head h).  For row r
+ * (query q0 + r; rows >= Nq stay zero) and key j < tile:
+ *   acc[r][j]        the exact int32 dot product of the codes (0 for j >= Nkv),
+ *                    masked or not
+ *   p8[r][j]         the E4M3 byte of exp2(s2 - m) * 448, m the row's maximum
+ *                    score over the tile's kept keys (0 for masked keys)
+ *   part[r][c]       sum over j of p8_j * v8_j,c in ascending j (FP32), c < 128
+ *   part[r][128]     sum over j of p8_j (the tile's contribution to d)
+ * These are the first iteration of attend_row's loop (m = -inf before it, so
+ * alpha = 0 and RO = part, d = part[128] after it); with Nkv <= tile they are
+ * the whole recurrence. */
+int oracle_first_tile(int B, int Hq, int Hkv, int Nq, int Nkv, int causal, float sm_scale, int tile,
+                      const int8_t *q_codes, const float *q_scales, const int8_t *k_codes,
+                      const float *k_scales, const uint8_t *v_codes, const float *v_scales, int b,
+                      int h, int q0, int32_t *acc, uint8_t *p8, float *part)
+{
+    if (check_shape(B, Hq, Hkv, Nq, Nkv, causal, tile) || b < 0 || b >= B || h < 0 || h >= Hq ||
+        q0 < 0 || q0 >= Nq)
+        return -1;
+    ctx_t cx;
+    setup_quant(&cx, B, Hq, Hkv, Nq, Nkv, causal, sm_scale, tile, q_codes, q_scales, k_codes,
+                k_scales, v_codes, v_scales);
+    const int hk = h / (Hq / Hkv);
+    const int n = Nkv < tile ? Nkv : tile;
+    memset(acc, 0, sizeof(int32_t) * 128 * (size_t)tile);
+    memset(p8, 0, (size_t)128 * tile);
+    memset(part, 0, sizeof(float) * 128 * (HEAD_DIM + 1));
+    for (int r = 0; r < 128 && q0 + r < Nq; ++r) {
+        const int i = q0 + r;
+        int last = Nkv - 1;
+        if (causal && i + (Nkv - Nq) < last)
+            last = i + (Nkv - Nq);
+        const int8_t *qi = cx.qc + ((size_t)(b * Hq + h) * cx.Nq_pad + i) * HEAD_DIM;
+        float m = -INFINITY;
+        for (int j = 0; j < n; ++j) {
+            const int8_t *kj = cx.kc + ((size_t)(b * Hkv + hk) * cx.Nkv_pad + j) * HEAD_DIM;
+            int32_t a = 0;
+            for (int c = 0; c < HEAD_DIM; ++c)
+                a += (int32_t)qi[c] * (int32_t)kj[c];
+            acc[(size_t)r * tile + j] = a;
+            if (j <= last) {
+                const float s2 = score_q(&cx, b, h, hk, i, j);
+                if (s2 > m)
+                    m = s2;
+            }
+        }
+        float w[MAX_TILE], tsum = 0;
+        for (int j = 0; j < n; ++j) {
+            w[j] = 0;
+            if (j <= last) {
+                const uint8_t code = oracle_f32_to_e4m3(exp2_f32(score_q(&cx, b, h, hk, i, j) - m) * 448.0f);
+                p8[(size_t)r * tile + j] = code;
+                w[j] = oracle_e4m3_to_f32(code);
+            }
+        }
+        for (int j = 0; j < n; ++j)
+            tsum = tsum + w[j];
+        for (int c = 0; c < HEAD_DIM; ++c) {
+            float s = 0;
+            for (int j = 0; j < n; ++j)
+                s = s + w[j] * value_q(&cx, b, hk, j, c);
+            part[(size_t)r * (HEAD_DIM + 1) + c] = s;
+        }
+        part[(size_t)r * (HEAD_DIM + 1) + HEAD_DIM] = tsum;
+    }
+    return 0;
+}
+
 /* oracle_forward_rows: as oracle_forward, for the listed rows only.
  * rows[r] = (b * Hq + h) * Nq + i; outputs are [nrows][128]. */
 int oracle_forward_rows(int B, int Hq, int Hkv, int Nq, int Nkv, int causal, float sm_scale,

@@ -40,23 +40,35 @@ def _inputs() -> list[str]:
                                                                  os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+DEBUG_DIR = os.path.join(OUT_DIR, "debug")
+DEBUG_LIB_PATH = os.path.join(DEBUG_DIR, "libsattn_dbg.so")
+
+
+def up_to_date(lib_path: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib_path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    if not force and up_to_date():
-        return LIB_PATH
+def build_debug(force: bool = False, verbose: bool = False) -> str:
+    """The same library built with SATTN_DEBUG_DUMP: the forward kernel can write
+    the intermediates of its first tile (raw QK accumulators, P8 bytes, the
+    first PV partial) to a buffer set with sattn_debug_set_dump.  For tests."""
+    return build(force, verbose, ["-DSATTN_DEBUG_DUMP"], out_dir=DEBUG_DIR, lib_path=DEBUG_LIB_PATH)
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          out_dir: str = OUT_DIR, lib_path: str = LIB_PATH) -> str:
+    if not force and up_to_date(lib_path):
+        return lib_path
     nvcc = _nvcc()
-    os.makedirs(OUT_DIR, exist_ok=True)
+    os.makedirs(out_dir, exist_ok=True)
     flags = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC",
              "-I", os.path.join(ROOT, "include"), *(extra_flags or [])]
     procs, objs = [], []
     for src in sources():
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *flags, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
@@ -71,12 +83,12 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
             failed.append(src)
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(failed))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-Xlinker",
            "-rpath," + _cuda_lib_dir(nvcc), *objs, "-o", tmp]
     subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

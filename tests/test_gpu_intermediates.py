@@ -1,0 +1,98 @@
+"""GPU parity of the forward kernel's intermediates against the oracle, for the
+first KV tile of query tile 0 of (batch 0, head 0): the raw QK accumulators,
+the FP8 P bytes and the first PV partial.
+
+A build with SATTN_DEBUG_DUMP (quantized_exact_attention_smoothing_gb300.build
+.build_debug) makes the kernel write them to a buffer set with
+sattn_debug_set_dump.  The accumulators must equal the oracle's exact int32
+dot products.  P8 must equal the oracle's bytes, except that a value within
+rounding distance of an E4M3 tie may take the neighbouring code (the kernel
+forms exp2's argument with one FMA and uses ex2.approx).  The PV partial
+must equal the sum of the kernel's own P8 values times the V codes, up to
+FP32 summation order.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from quantized_exact_attention_smoothing_gb300 import _binding as bnd
+from quantized_exact_attention_smoothing_gb300 import build as B
+import synth
+from helpers import to_device_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dbg_lib():
+    lib = ctypes.CDLL(B.build_debug())
+    P, SP = ctypes.c_void_p, ctypes.POINTER(bnd.sattn_shape)
+    lib.sattn_prepare.argtypes = [SP] + [P] * 13
+    lib.sattn_forward.argtypes = [SP] + [P] * 9
+    lib.sattn_debug_set_dump.argtypes = [P]
+    return lib
+
+
+def _run_dump(lib, q, k, v, causal):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    dq, dk, dv = to_device_bf16(q), to_device_bf16(k), to_device_bf16(v)
+    Bn, Hq, Nq, _ = q.shape
+    shape = bnd.make_shape(Bn, Hq, k.shape[1], Nq, k.shape[2], causal)
+    buf = bnd.prepare_buffers(shape, dq.device)
+    out = torch.empty((Bn, Hq, Nq, 128), dtype=torch.bfloat16, device="cuda")
+    fws = torch.zeros(64, dtype=torch.int32, device="cuda")
+    dump = torch.zeros(98304, dtype=torch.float32, device="cuda")
+    s = bnd._stream(None)
+    p = bnd._ptr
+    assert lib.sattn_prepare(ctypes.byref(shape), p(dq), p(dk), p(dv), p(buf["q_codes"]), p(buf["q_scales"]),
+                             p(buf["k_codes"]), p(buf["k_scales"]), p(buf["k_mean"]), p(buf["k_carrier"]),
+                             p(buf["v_codes"]), p(buf["v_scales"]), p(buf["workspace"]), s) == 0
+    lib.sattn_debug_set_dump(ctypes.c_void_p(dump.data_ptr()))
+    try:
+        assert lib.sattn_forward(ctypes.byref(shape), p(buf["q_codes"]), p(buf["q_scales"]), p(buf["k_carrier"]),
+                                 p(buf["k_scales"]), p(buf["v_codes"]), p(buf["v_scales"]), p(out), p(fws), s) == 0
+        torch.cuda.synchronize()
+    finally:
+        lib.sattn_debug_set_dump(None)
+    assert int(fws[0]) == 0
+    d = dump.cpu().numpy()
+    s_acc = d[:32768].reshape(128, 256)
+    p8 = d[32768:40960].view(np.uint32).reshape(128, 64).view(np.uint8).reshape(128, 256)
+    part = d[40960:40960 + 128 * 144].reshape(128, 144)
+    return s_acc, p8, part
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 1, 1, 128, 192, False),    # c1: 192 kept keys of 256, every row
+    (1, 1, 1, 128, 512, False),    # a full first tile
+    (1, 2, 1, 256, 256, True),     # the causal diagonal runs through the tile
+    (1, 1, 1, 100, 300, True)])    # ragged rows, bottom-right causal offset
+def test_first_tile_intermediates_match_the_oracle(oracle_mod, dbg_lib, shape):
+    Bn, Hq, Hkv, Nq, Nkv, causal = shape
+    w = synth.workload("c1", B=Bn, Hq=Hq, Hkv=Hkv, Nq=Nq, Nkv=Nkv, causal=causal)
+    q, k, v = synth.make_inputs(w, seed=500 + Nkv)
+    s_acc, p8, part = _run_dump(dbg_lib, q, k, v, causal)
+    ref = oracle_mod.prepare(q, k, v)
+    acc_o, p8_o, _ = oracle_mod.first_tile(ref, Nq, Nkv, causal)
+    rows, n = min(Nq, 128), min(Nkv, 256)
+
+    # QK: exact integers, every key of the tile (pad keys read zero codes)
+    assert np.array_equal(s_acc[:rows], acc_o[:rows].astype(np.float32))
+
+    # P8: bytes equal but for rare one-code steps at E4M3 ties
+    diff = p8[:rows].astype(np.int16) - p8_o[:rows].astype(np.int16)
+    assert np.abs(diff).max() <= 1, "P8 differs by more than one code"
+    assert np.count_nonzero(diff) <= max(2, rows * n // 1000), f"{np.count_nonzero(diff)} P8 codes differ"
+
+    # PV: the kernel's partial from its own P8 and the V codes (FP64 reference)
+    pv = oracle_mod.e4m3_to_f32(p8[:rows].reshape(-1)).reshape(rows, 256).astype(np.float64)
+    vv = np.zeros((256, 128))
+    vv[:n] = oracle_mod.e4m3_to_f32(ref["v_codes"][0, 0, :n].reshape(-1)).reshape(n, 128)
+    want = pv @ vv
+    got = part[:rows, :128].astype(np.float64)
+    scale = np.abs(pv) @ np.abs(vv) + 1e-30
+    assert np.all(np.abs(got - want) <= 4e-6 * scale), "PV partial off beyond FP32 summation order"
+    assert np.allclose(part[:rows, 128], pv.sum(axis=1), rtol=1e-6, atol=0)   # the ones row: sum of p8
+    assert not part[:rows, 129:].any()

@@ -197,3 +197,45 @@ def test_forward_rejects_bad_shapes(oracle_mod):
         oracle_mod.forward(p, 9, 8, causal=True)       # causal needs Nq <= Nkv
     with pytest.raises(ValueError):
         oracle_mod.forward(p, 9, 8, causal=False, tile=0)
+
+
+# --- first-tile intermediates (QK, m, FP8 P, PV of one tile) ----------------
+
+@pytest.mark.parametrize("shape", [(1, 1, 1, 128, 192, False), (1, 2, 1, 100, 200, True),
+                                   (2, 2, 2, 160, 256, True), (1, 1, 1, 128, 600, False)])
+def test_first_tile_accumulators_are_exact_dot_products(oracle_mod, shape):
+    B, Hq, Hkv, Nq, Nkv, causal = shape
+    w = synth.workload("c1", B=B, Hq=Hq, Hkv=Hkv, Nq=Nq, Nkv=Nkv, causal=causal)
+    q, k, v = synth.make_inputs(w, seed=300 + Nkv)
+    prep = oracle_mod.prepare(q, k, v)
+    b, h = B - 1, Hq - 1
+    acc, p8, _ = oracle_mod.first_tile(prep, Nq, Nkv, causal, b=b, h=h)
+    hk = h // (Hq // Hkv)
+    n, rows = min(Nkv, 256), min(Nq, 128)
+    ref = prep["q_codes"][b, h, :rows].astype(np.int64) @ prep["k_codes"][b, hk, :n].astype(np.int64).T
+    assert np.array_equal(acc[:rows, :n], ref)
+    assert not acc[:, n:].any() and not acc[rows:].any()
+    # every row's largest kept weight is exp2(0) * 448 = 448 (byte 0x7e); masked keys carry 0
+    last = np.arange(rows)[:, None] + (Nkv - Nq) if causal else np.full((rows, 1), Nkv - 1)
+    kept = np.arange(256)[None, :] <= np.minimum(last, n - 1)
+    assert np.all(p8[:rows].max(axis=1) == 0x7E)
+    assert not p8[:rows][~kept].any()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_single_tile_intermediates_reproduce_the_forward(oracle_mod, causal):
+    # with Nkv <= 256 the first tile is the whole recurrence: RO = partial,
+    # d = its weight sum, out = bf16((RO * (1/d)) * s_v), equal to forward()
+    w = synth.workload("c1", B=1, Hq=2, Hkv=1, Nq=200, Nkv=240, causal=causal)
+    q, k, v = synth.make_inputs(w, seed=17)
+    prep = oracle_mod.prepare(q, k, v)
+    rb, _ = oracle_mod.forward(prep, w.Nq, w.Nkv, causal)
+    for h in range(2):
+        for q0 in (0, 128):
+            _, _, part = oracle_mod.first_tile(prep, w.Nq, w.Nkv, causal, h=h, q0=q0)
+            rows = min(128, w.Nq - q0)
+            d = part[:rows, 128]
+            r = (np.float32(1) / d).astype(np.float32)
+            o = ((part[:rows, :128] * r[:, None]).astype(np.float32) * prep["v_scales"][0, 0][None, :]).astype(np.float32)
+            got = oracle_mod.f32_to_bf16(o).reshape(rows, 128)
+            assert np.array_equal(got, rb[0, h, q0:q0 + rows]), (h, q0)
