@@ -121,6 +121,25 @@ def test_forward_repeatable_byte_identical():
         assert torch.equal(first.view(torch.int16), again.view(torch.int16))
 
 
+def test_thousand_launches_byte_identical():
+    # determinism gate: 1000 back-to-back preparations and forward passes
+    # (causal GQA, ragged) must all give the same bytes; mismatches are
+    # counted on the device so the loop stays asynchronous
+    w = synth.workload("c1", B=2, Hq=8, Hkv=2, Nq=700, Nkv=900, causal=True)
+    q, k, v = synth.make_inputs(w, seed=41)
+    dq, dk, dv = to_device_bf16(q), to_device_bf16(k), to_device_bf16(v)
+    prep = sattn.prepare(dq, dk, dv, True)
+    out = sattn.forward(prep)
+    first = out.clone()
+    bad = torch.zeros((), dtype=torch.int64, device="cuda")
+    for _ in range(1000):
+        sattn.prepare(dq, dk, dv, True, buffers=prep)
+        sattn.forward(prep, out=out)
+        bad += (out.view(torch.int16) != first.view(torch.int16)).sum()
+    assert sattn.check_status(prep["forward_workspace"]) == 0
+    assert int(bad) == 0
+
+
 @pytest.mark.parametrize("name, overrides", [
     ("c2", dict(Hq=4, Hkv=2, causal=True)),                        # one chunk
     ("c1", dict(B=2, Hq=16, Hkv=4, Nq=4096, Nkv=4096, causal=True)),  # two chunks of 4 KV heads
