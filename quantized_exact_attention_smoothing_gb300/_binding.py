@@ -134,6 +134,19 @@ def _need_cuda(*ts: torch.Tensor):
             raise ValueError("tensors must be contiguous")
 
 
+def _need_inputs(q: torch.Tensor | None, k: torch.Tensor, v: torch.Tensor):
+    """BF16 [B, H, N, 128] inputs of one problem: q [B, Hq, Nq, 128] (if given),
+    k and v [B, Hkv, Nkv, 128] with the same shape."""
+    ts = (k, v) if q is None else (q, k, v)
+    for t in ts:
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or t.shape[-1] != HEAD_DIM:
+            raise ValueError("inputs must be BF16 tensors of shape [B, H, N, 128]")
+    if k.shape != v.shape:
+        raise ValueError("k and v must have the same shape")
+    if q is not None and (q.shape[0] != k.shape[0] or q.shape[1] % k.shape[1] != 0):
+        raise ValueError("q [B, Hq, Nq, 128] must share B with k, and Hq must be a multiple of Hkv")
+
+
 def _empty(nbytes: int, device, dtype=torch.uint8) -> torch.Tensor:
     n = max(1, nbytes // torch.empty(0, dtype=dtype).element_size())
     return torch.empty(n, dtype=dtype, device=device)
@@ -166,6 +179,7 @@ def prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fa
             sm_scale: float = 0.0, buffers: dict | None = None, stream=None) -> dict:
     """sattn_prepare on BF16 device tensors q [B,Hq,Nq,128], k/v [B,Hkv,Nkv,128]."""
     _need_cuda(q, k, v)
+    _need_inputs(q, k, v)
     B, Hq, Nq, _ = q.shape
     Hkv, Nkv = k.shape[1], k.shape[2]
     shape = make_shape(B, Hq, Hkv, Nq, Nkv, causal, sm_scale)
@@ -194,6 +208,7 @@ def prepare_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: b
     the caller's; without them this wrapper allocates them with PyTorch.
     """
     _need_cuda(q, k, v)
+    _need_inputs(q, k, v)
     B, Hq, Nq, _ = q.shape
     Hkv, Nkv = k.shape[1], k.shape[2]
     shape = make_shape(B, Hq, Hkv, Nq, Nkv, causal, sm_scale)
@@ -239,6 +254,7 @@ def prepare_kv(k: torch.Tensor, v: torch.Tensor, Hq: int, Nq: int, causal: bool 
     returned buffers are absent.
     """
     _need_cuda(k, v)
+    _need_inputs(None, k, v)
     B, Hkv, Nkv, _ = k.shape
     shape = make_shape(B, Hq, Hkv, Nq, Nkv, causal, sm_scale)
     if buffers is None:
@@ -325,6 +341,7 @@ class Graph:
                  sm_scale: float = 0.0, buffers: dict | None = None, out: torch.Tensor | None = None,
                  workspace: torch.Tensor | None = None):
         _need_cuda(q, k, v)
+        _need_inputs(q, k, v)
         B, Hq, Nq, _ = q.shape
         shape = make_shape(B, Hq, k.shape[1], Nq, k.shape[2], causal, sm_scale)
         dev = q.device
@@ -386,6 +403,7 @@ def attention_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal=Fal
     for t in (q, k, v):
         if t.is_cuda or not t.is_contiguous():
             raise ValueError("attention_host takes contiguous host tensors")
+    _need_inputs(q, k, v)
     B, Hq, Nq, _ = q.shape
     Hkv, Nkv = k.shape[1], k.shape[2]
     shape = make_shape(B, Hq, Hkv, Nq, Nkv, causal, sm_scale)

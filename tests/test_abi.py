@@ -128,3 +128,19 @@ def test_graph_entry_points_check_arguments(lib):
     assert lib.sattn_graph_create(ctypes.byref(s), *args, ctypes.byref(h)) == 2
     assert lib.sattn_graph_launch(None, None) == 1
     assert lib.sattn_graph_destroy(None) == 1
+
+
+def test_binding_rejects_wrong_input_dtypes_and_shapes():
+    # host tensors reach the shape checks of attention_host before any device work
+    import torch
+    q = torch.zeros((1, 2, 8, 128), dtype=torch.bfloat16)
+    k = torch.zeros((1, 1, 8, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        sattn.attention_host(q.float(), k, k)
+    with pytest.raises(ValueError):
+        sattn.attention_host(q, k, torch.zeros((1, 1, 9, 128), dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        sattn.attention_host(torch.zeros((1, 3, 8, 128), dtype=torch.bfloat16), torch.zeros((1, 2, 8, 128), dtype=torch.bfloat16),
+                             torch.zeros((1, 2, 8, 128), dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        sattn.attention_host(torch.zeros((1, 2, 8, 64), dtype=torch.bfloat16), k, k)
