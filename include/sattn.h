@@ -223,6 +223,17 @@ int sattn_test_forward_withhold_v(const sattn_shape *shape, const int8_t *q_code
 int sattn_test_int8_quantiser(uint32_t amax_lo, uint32_t amax_hi, unsigned long long *result, void *stream);
 
 /*
+ * sattn_test_host_chunks -- test hook, not part of the computation: the
+ * chunk plan sattn_attention_host uses for `shape` on a device with `n_sm`
+ * SMs.  Pure host function.
+ *   bounds   out: host array of at least 9 int64; chunk c covers the
+ *            (batch, KV head) units bounds[c] .. bounds[c + 1] - 1, with units
+ *            numbered b * Hkv + kv_head
+ *   nchunks  out: the number of chunks (1 to 8)
+ */
+int sattn_test_host_chunks(const sattn_shape *shape, int n_sm, int64_t *bounds, int *nchunks);
+
+/*
  * sattn_check_status -- synchronise `stream` and read the status word that
  * sattn_forward left in `forward_workspace`.  Returns SATTN_OK, or
  * SATTN_ERR_TIMEOUT if a bounded device wait ran out, or SATTN_ERR_DEVICE if

@@ -76,6 +76,8 @@ def load_library(build: bool = True):
     lib.sattn_check_status.argtypes = [P, P]
     lib.sattn_test_int8_quantiser.argtypes = [ctypes.c_uint32, ctypes.c_uint32, P, P]
     lib.sattn_graph_create.argtypes = [SP] + [P] * 14 + [ctypes.POINTER(ctypes.c_void_p)]
+    lib.sattn_test_host_chunks.argtypes = [SP, ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
+                                           ctypes.POINTER(ctypes.c_int)]
     lib.sattn_graph_launch.argtypes = [P, P]
     lib.sattn_graph_destroy.argtypes = [P]
     lib.sattn_attention_host.argtypes = [SP, P, P, P, P, P, ctypes.c_size_t, P]
@@ -83,7 +85,8 @@ def load_library(build: bool = True):
     lib.sattn_status_string.restype = ctypes.c_char_p
     for name in ("sattn_query_sizes", "sattn_prepare", "sattn_forward", "sattn_check_status",
                  "sattn_attention_host", "sattn_prepare_noalloc", "sattn_prepare_kv", "sattn_forward_q_bf16",
-                 "sattn_test_int8_quantiser", "sattn_graph_create", "sattn_graph_launch", "sattn_graph_destroy"):
+                 "sattn_test_int8_quantiser", "sattn_graph_create", "sattn_graph_launch", "sattn_graph_destroy",
+                 "sattn_test_host_chunks"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib

@@ -475,6 +475,21 @@ int sattn_test_int8_quantiser(uint32_t amax_lo, uint32_t amax_hi, unsigned long 
                : SATTN_ERR_LAUNCH;
 }
 
+int sattn_test_host_chunks(const sattn_shape *shape, int n_sm, int64_t *bounds, int *nchunks)
+{
+    Geometry g;
+    const int rc = make_geometry(shape, &g);
+    if (rc != SATTN_OK)
+        return rc;
+    if (!bounds || !nchunks || n_sm < 1)
+        return SATTN_ERR_INVALID;
+    int64_t b[kMaxHostChunks + 1];
+    *nchunks = host_chunks(g, n_sm, b);
+    for (int c = 0; c <= *nchunks; ++c)
+        bounds[c] = b[c];
+    return SATTN_OK;
+}
+
 int sattn_check_status(const void *forward_workspace, void *stream)
 {
     if (!forward_workspace)

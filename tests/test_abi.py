@@ -144,3 +144,42 @@ def test_binding_rejects_wrong_input_dtypes_and_shapes():
                              torch.zeros((1, 2, 8, 128), dtype=torch.bfloat16))
     with pytest.raises(ValueError):
         sattn.attention_host(torch.zeros((1, 2, 8, 64), dtype=torch.bfloat16), k, k)
+
+
+def _chunks(lib, shape, n_sm=152):
+    bounds = (ctypes.c_int64 * 9)()
+    n = ctypes.c_int()
+    assert lib.sattn_test_host_chunks(ctypes.byref(shape), n_sm, bounds, ctypes.byref(n)) == 0
+    b = list(bounds)[:n.value + 1]
+    return [b[c + 1] - b[c] for c in range(n.value)], b
+
+
+@pytest.mark.parametrize("dims, want", [
+    ((4, 32, 8, 8192, 8192, True), [2, 3, 5, 6, 6, 5, 3, 2]),        # c5: ramp
+    ((1, 16, 16, 32760, 32760, False), [2] * 8),                   # c4: ramp ends too small -> equal
+    ((2, 32, 32, 4000, 4000, True), [10, 11, 11, 10, 11, 11]),     # c3: equal chunks of >= 10 heads
+    ((1, 8, 8, 1024, 1024, False), [8]),                           # c2: too small to cut
+    ((1, 1, 1, 128, 192, False), [1])])                            # c1
+def test_host_chunk_plan(lib, dims, want):
+    sizes, bounds = _chunks(lib, sattn.make_shape(*dims))
+    assert sizes == want
+    B, Hq, Hkv, Nq = dims[:4]
+    units = B * Hkv
+    assert bounds[0] == 0 and bounds[-1] == units and all(x > 0 for x in sizes)
+    if len(sizes) > 1:   # every chunk holds at least two forward work items per SM
+        items_per_unit = -(-Nq // 128) * (Hq // Hkv)
+        assert min(sizes) * items_per_unit >= 2 * 152
+
+
+def test_host_chunk_plan_properties_over_many_shapes(lib):
+    rng = __import__("random").Random(3)
+    for _ in range(300):
+        Hkv = rng.choice([1, 2, 4, 8, 16, 32])
+        g = rng.choice([1, 2, 4, 8])
+        B, N = rng.randint(1, 6), rng.randint(1, 40000)
+        for n_sm in (8, 152):
+            sizes, bounds = _chunks(lib, sattn.make_shape(B, Hkv * g, Hkv, N, N, True), n_sm)
+            assert 1 <= len(sizes) <= 8 and bounds[0] == 0 and bounds[-1] == B * Hkv
+            assert all(x > 0 for x in sizes)
+            if len(sizes) > 1:
+                assert min(sizes) * (-(-N // 128) * g) >= 2 * n_sm
