@@ -12,8 +12,8 @@
 //               [64h, 64h + 64): score scaling, masks, running max m (exchanged
 //               between the halves), alpha, the FP8 P bytes (written to TMEM),
 //               RO = RO * alpha + PV and d = d * alpha + sum p8 for the
-//               previous tile, the final conversion, and the FP16 carrier of
-//               the next item's Q (into shared memory)
+//               previous tile, and the final conversion (each warp's 32 x 64
+//               BF16 tile staged in shared memory, then one TMA store)
 //   warp 8      K loader (TMA): K half-tiles (FP16 carrier of the INT8 codes,
 //               256 keys x 64 channels) into a ring of three slots
 //   warp 9      TMEM allocation and the single MMA-issuing thread:
@@ -26,7 +26,8 @@
 //               two slots; the next item's INT8 Q tile and V channel scales
 //   warp 11     Q converter: the staged INT8 Q tile of the next item -> its
 //               FP16 carrier in shared memory, as soon as the current item's
-//               last QK has completed
+//               last QK has completed (with kFuseQ it also quantises each
+//               item's BF16 Q tile itself, staged in the output buffer)
 // Twelve warps launch at 168 registers each; setmaxnreg then gives the compute
 // warpgroups 232 (128 scores and 64 RO values per thread) and the loader/MMA
 // warpgroup 40.
