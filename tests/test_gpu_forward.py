@@ -170,7 +170,8 @@ def test_forward_explicit_softmax_scale(oracle_mod, sm_scale):
     # P8 value within an FP32 ulp of an E4M3 tie (here 400.00006, between 384
     # and 416) can take the other code.  That one step (32 of 448) on one key,
     # times an outlier value, moves one output by 4.15e-3 on these inputs.
-    # A CPU emulation of the kernel's rounding path gives the same figure.
+    # A CPU model of the kernel's rounding path gives the same figure
+    # (test_oracle_forward.py::test_flat_softmax_tie_explains_the_explicit_scale_bound).
     # The bound allows two such flips; the cosine bound is unchanged.
     w = synth.workload("c1", B=1, Hq=2, Hkv=1, Nq=200, Nkv=300, causal=True)
     q, k, v = synth.make_inputs(w, seed=91)
