@@ -303,7 +303,6 @@ def run_ours(args, world, rank, local):
     achieved = w.algorithmic_ops / (ms_fwd * 1e-3) / 1e12
     prep_bytes = (hq.numel() + hk.numel() + hv.numel()) * 2 + \
         (buf["q_codes"].numel() + buf["k_codes"].numel() + w.B * w.Hkv * 128 * w.Nkv) + \
-        2 * buf["k_carrier"].numel() + \
         4 * (buf["q_scales"].numel() + buf["k_scales"].numel() + buf["k_mean"].numel() + buf["v_scales"].numel())
     result = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": K,

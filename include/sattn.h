@@ -46,7 +46,13 @@
  * streams of the library that fork from `stream` and join back into it with
  * events, so the caller sees all of a call's work ordered on `stream`.  The
  * helper streams and events are created once per device and kept for the
- * life of the process.  Calls never allocate device memory, free or
+ * life of the process.  The helper streams are shared by every caller on a
+ * device, so two sattn_prepare calls enqueued on unrelated caller streams are
+ * ordered behind each other's helper work (each call's Q and V branches wait
+ * for the previous call's branches on the same device); callers that need
+ * independent streams to stay independent should use sattn_prepare_noalloc or
+ * the graph entry points, which keep the serial order on the caller's
+ * stream.  Calls never allocate device memory, free or
  * synchronise, except sattn_check_status, which synchronises the stream by
  * design, and sattn_graph_create, which builds a CUDA graph (released by
  * sattn_graph_destroy).  All device pointers must be 16-byte aligned.
@@ -100,11 +106,12 @@ typedef struct {
     size_t q_codes, q_scales;   /* int8 [B][Hq][Nq32][128], FP32 [B][Hq][Nq32/32] */
     size_t k_codes, k_scales;   /* int8 [B][Hkv][Nkv32][128], FP32 [B][Hkv][Nkv32/32] */
     size_t k_mean;              /* FP32 [B][Hkv][128] */
-    size_t k_carrier;           /* FP16 [B][Hkv][Nkv][128]: the K codes as FP16 values */
     size_t v_codes, v_scales;   /* E4M3 [B][Hkv][128][Nkv128] (channel-major), FP32 [B][Hkv][128] */
     size_t out;                 /* BF16 [B][Hq][Nq][128] */
     size_t prepare_workspace;   /* scratch of sattn_prepare */
-    size_t forward_workspace;   /* scratch of sattn_forward (its status block) */
+    size_t forward_workspace;   /* scratch of sattn_forward: a 256-byte status block,
+                                   then the FP16 copy of the K codes that the
+                                   tensor cores read (B * Hkv * Nkv * 256 bytes) */
     size_t arena;               /* one device block holding all of the above,
                                    for sattn_attention_host */
 } sattn_sizes;
@@ -126,10 +133,6 @@ int sattn_query_sizes(const sattn_shape *shape, sattn_sizes *sizes);
  *   k_codes     out: int8 codes of the smoothed K, pad rows 0
  *   k_scales    out: FP32, one per 32-token block
  *   k_mean      out: FP32 per-channel mean of K that was subtracted
- *   k_carrier   out: FP16 [B][Hkv][Nkv][128], every K code as an FP16 value
- *               (exact: integers of magnitude <= 127); the operand that the
- *               forward's tensor cores read, since this part has no INT8
- *               tensor-core product
  *   v_codes     out: E4M3 bytes, channel-major [B][Hkv][128][Nkv128];
  *               keys Nkv .. Nkv128-1 are 0
  *   v_scales    out: FP32 per channel
@@ -145,27 +148,30 @@ int sattn_query_sizes(const sattn_shape *shape, sattn_sizes *sizes);
  */
 int sattn_prepare(const sattn_shape *shape, const void *q, const void *k, const void *v,
                   int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
-                  float *k_mean, void *k_carrier, uint8_t *v_codes, float *v_scales,
-                  void *workspace, void *stream);
+                  float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace, void *stream);
 
 /*
  * sattn_forward -- QK traversal, online softmax, FP8 P, two-level PV
  * accumulation, final conversion and ragged tails (page entries "Phase 0
  * Import And Verification" and "Phase 1 State-Ownership Decision").
- *   q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales
+ *   q_codes, q_scales, k_codes, k_scales, v_codes, v_scales
  *               in: as written by sattn_prepare for the same shape
  *   out         out: BF16 [B][Hq][Nq][128]
  *   workspace   scratch, sizes.forward_workspace bytes: the status block that
- *               sattn_check_status reads; contents on entry are ignored
- * One kernel: a persistent CTA per SM walks the (query tile, head, batch)
- * items, longest first.
+ *               sattn_check_status reads, then the FP16 copy of the K codes
+ *               (every INT8 code as the same integer in FP16, exact) that the
+ *               tensor cores read, since this part has no INT8 tensor-core
+ *               product; contents on entry are ignored
+ * Two kernels: the K codes are copied to FP16 into the workspace (bound by
+ * HBM bandwidth), then a persistent CTA per SM walks the (query tile, head,
+ * batch) items, longest first.
  * Exactness: QK^T is computed from the codes with products and sums that are
  * exact integers; P, PV and the output follow the arithmetic above, with the
  * inner PV sum in the tensor core's FP32 order and exp2 by the hardware
  * approximation.
  */
 int sattn_forward(const sattn_shape *shape, const int8_t *q_codes, const float *q_scales,
-                  const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
+                  const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
                   const float *v_scales, void *out, void *workspace, void *stream);
 
 /*
@@ -175,7 +181,7 @@ int sattn_forward(const sattn_shape *shape, const int8_t *q_codes, const float *
  * the outputs are byte for byte those of sattn_prepare.
  */
 int sattn_prepare_kv(const sattn_shape *shape, const void *k, const void *v, int8_t *k_codes,
-                     float *k_scales, float *k_mean, void *k_carrier, uint8_t *v_codes,
+                     float *k_scales, float *k_mean, uint8_t *v_codes,
                      float *v_scales, void *workspace, void *stream);
 
 /*
@@ -184,7 +190,7 @@ int sattn_prepare_kv(const sattn_shape *shape, const void *k, const void *v, int
  * work item's 128 x 128 BF16 Q tile is quantised in shared memory while the
  * previous item computes.  No Q codes or scales reach device memory.
  *   q           in: BF16 [B][Hq][Nq][128], contiguous, 16-byte aligned
- *   k_carrier, k_scales, v_codes, v_scales
+ *   k_codes, k_scales, v_codes, v_scales
  *               in: as written by sattn_prepare_kv (or sattn_prepare)
  *   out, workspace
  *               as in sattn_forward
@@ -192,7 +198,7 @@ int sattn_prepare_kv(const sattn_shape *shape, const void *k, const void *v, int
  * output equals, byte for byte, sattn_forward's on sattn_prepare's outputs.
  * Errors as sattn_forward.
  */
-int sattn_forward_q_bf16(const sattn_shape *shape, const void *q, const void *k_carrier,
+int sattn_forward_q_bf16(const sattn_shape *shape, const void *q, const int8_t *k_codes,
                          const float *k_scales, const uint8_t *v_codes, const float *v_scales,
                          void *out, void *workspace, void *stream);
 
@@ -206,7 +212,7 @@ int sattn_forward_q_bf16(const sattn_shape *shape, const void *q, const void *k_
  * CUDA context stays usable: a following sattn_forward computes normally.
  */
 int sattn_test_forward_withhold_v(const sattn_shape *shape, const int8_t *q_codes, const float *q_scales,
-                                  const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
+                                  const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
                                   const float *v_scales, void *out, void *workspace, void *stream);
 
 /*
@@ -251,7 +257,8 @@ int sattn_check_status(const void *forward_workspace, void *stream);
  *                                 has been synchronised
  *   arena                    device scratch of sizes.arena bytes (holds the
  *                            inputs, codes, scales, two preparation
- *                            workspaces, the status block and the output)
+ *                            workspaces, the status block, two FP16 copies
+ *                            of the K codes and the output)
  * The (batch, KV head) units are independent problems, so large shapes are
  * cut into up to eight chunks of contiguous units, each with at least two
  * forward work items per SM, sized as a ramp (small first and last chunks,
@@ -293,7 +300,10 @@ int sattn_attention_host(const sattn_shape *shape, const void *q_host, const voi
  *
  * Set-up: the first call on each device (with that device current) looks up
  * the array's device address once (cudaGetSymbolAddress) and caches it; make
- * that first call before any stream capture begins on that device.
+ * that first call before any stream capture begins on that device.  The
+ * cached address belongs to the device's context at that time: after a
+ * cudaDeviceReset (or any teardown of the primary context) the entry point
+ * must not be called again in the same process.
  *
  * Concurrency: all calls on one device share the one array, so calls whose
  * kernels may overlap on the GPU (different streams without ordering between
@@ -303,7 +313,7 @@ int sattn_attention_host(const sattn_shape *shape, const void *q_host, const voi
 #define SATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
 int sattn_prepare_noalloc(const sattn_shape *shape, const void *q, const void *k, const void *v,
                           int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
-                          float *k_mean, void *k_carrier, uint8_t *v_codes, float *v_scales,
+                          float *k_mean, uint8_t *v_codes, float *v_scales,
                           void *stream);
 
 /*
@@ -329,7 +339,7 @@ int sattn_prepare_noalloc(const sattn_shape *shape, const void *q, const void *k
 typedef struct sattn_graph sattn_graph;
 int sattn_graph_create(const sattn_shape *shape, const void *q, const void *k, const void *v,
                        int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
-                       float *k_mean, void *k_carrier, uint8_t *v_codes, float *v_scales,
+                       float *k_mean, uint8_t *v_codes, float *v_scales,
                        void *prepare_workspace, void *out, void *forward_workspace, sattn_graph **graph);
 int sattn_graph_launch(sattn_graph *graph, void *stream);
 int sattn_graph_destroy(sattn_graph *graph);

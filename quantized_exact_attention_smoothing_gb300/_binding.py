@@ -20,7 +20,7 @@ QBLOCK = 32
 KV_TILE = 256      # keys per KV tile of the forward pass (part of the numerical contract)
 V_PAD = 128        # V codes are padded to a multiple of 128 keys
 
-_SIZE_FIELDS = ["q", "k", "v", "q_codes", "q_scales", "k_codes", "k_scales", "k_mean", "k_carrier",
+_SIZE_FIELDS = ["q", "k", "v", "q_codes", "q_scales", "k_codes", "k_scales", "k_mean",
                 "v_codes", "v_scales", "out", "prepare_workspace", "forward_workspace", "arena"]
 
 
@@ -67,15 +67,15 @@ def load_library(build: bool = True):
     P = ctypes.c_void_p
     SP = ctypes.POINTER(sattn_shape)
     lib.sattn_query_sizes.argtypes = [SP, ctypes.POINTER(sattn_sizes)]
-    lib.sattn_prepare.argtypes = [SP] + [P] * 13
+    lib.sattn_prepare.argtypes = [SP] + [P] * 12
     lib.sattn_forward.argtypes = [SP] + [P] * 9
     lib.sattn_test_forward_withhold_v.argtypes = [SP] + [P] * 9
-    lib.sattn_prepare_noalloc.argtypes = [SP] + [P] * 12
-    lib.sattn_prepare_kv.argtypes = [SP] + [P] * 10
+    lib.sattn_prepare_noalloc.argtypes = [SP] + [P] * 11
+    lib.sattn_prepare_kv.argtypes = [SP] + [P] * 9
     lib.sattn_forward_q_bf16.argtypes = [SP] + [P] * 8
     lib.sattn_check_status.argtypes = [P, P]
     lib.sattn_test_int8_quantiser.argtypes = [ctypes.c_uint32, ctypes.c_uint32, P, P]
-    lib.sattn_graph_create.argtypes = [SP] + [P] * 14 + [ctypes.POINTER(ctypes.c_void_p)]
+    lib.sattn_graph_create.argtypes = [SP] + [P] * 13 + [ctypes.POINTER(ctypes.c_void_p)]
     lib.sattn_test_host_chunks.argtypes = [SP, ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
                                            ctypes.POINTER(ctypes.c_int)]
     lib.sattn_graph_launch.argtypes = [P, P]
@@ -167,7 +167,6 @@ def prepare_buffers(shape: sattn_shape, device, with_q: bool = True) -> dict:
         k_codes=torch.empty((B, Hkv, nk32, HEAD_DIM), dtype=torch.int8, device=device),
         k_scales=torch.empty((B, Hkv, nk32 // QBLOCK), dtype=torch.float32, device=device),
         k_mean=torch.empty((B, Hkv, HEAD_DIM), dtype=torch.float32, device=device),
-        k_carrier=torch.empty((B, Hkv, Nkv, HEAD_DIM), dtype=torch.float16, device=device),
         v_codes=torch.empty((B, Hkv, HEAD_DIM, nk128), dtype=torch.uint8, device=device),
         v_scales=torch.empty((B, Hkv, HEAD_DIM), dtype=torch.float32, device=device),
         workspace=_empty(z["prepare_workspace"], device),
@@ -189,7 +188,7 @@ def prepare(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = Fa
     buf = buffers if buffers is not None else prepare_buffers(shape, q.device)
     rc = load_library().sattn_prepare(
         ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(buf["q_codes"]), _ptr(buf["q_scales"]),
-        _ptr(buf["k_codes"]), _ptr(buf["k_scales"]), _ptr(buf["k_mean"]), _ptr(buf["k_carrier"]),
+        _ptr(buf["k_codes"]), _ptr(buf["k_scales"]), _ptr(buf["k_mean"]),
         _ptr(buf["v_codes"]), _ptr(buf["v_scales"]), _ptr(buf["workspace"]), _stream(stream))
     if rc != 0:
         raise SattnError(rc, "sattn_prepare")
@@ -218,7 +217,7 @@ def prepare_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: b
     buf = buffers if buffers is not None else prepare_buffers(shape, q.device)
     rc = load_library().sattn_prepare_noalloc(
         ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(buf["q_codes"]), _ptr(buf["q_scales"]),
-        _ptr(buf["k_codes"]), _ptr(buf["k_scales"]), _ptr(buf["k_mean"]), _ptr(buf["k_carrier"]),
+        _ptr(buf["k_codes"]), _ptr(buf["k_scales"]), _ptr(buf["k_mean"]),
         _ptr(buf["v_codes"]), _ptr(buf["v_scales"]), _stream(stream))
     if rc != 0:
         raise SattnError(rc, "sattn_prepare_noalloc")
@@ -240,7 +239,7 @@ def forward(prep: dict, out: torch.Tensor | None = None, workspace: torch.Tensor
             prep["forward_workspace"] = workspace
     _need_cuda(out, workspace)
     rc = load_library().sattn_forward(
-        ctypes.byref(shape), _ptr(prep["q_codes"]), _ptr(prep["q_scales"]), _ptr(prep["k_carrier"]),
+        ctypes.byref(shape), _ptr(prep["q_codes"]), _ptr(prep["q_scales"]), _ptr(prep["k_codes"]),
         _ptr(prep["k_scales"]), _ptr(prep["v_codes"]), _ptr(prep["v_scales"]), _ptr(out),
         _ptr(workspace), _stream(stream))
     if rc != 0:
@@ -264,7 +263,7 @@ def prepare_kv(k: torch.Tensor, v: torch.Tensor, Hq: int, Nq: int, causal: bool 
         buffers = prepare_buffers(shape, k.device, with_q=False)
     rc = load_library().sattn_prepare_kv(
         ctypes.byref(shape), _ptr(k), _ptr(v), _ptr(buffers["k_codes"]), _ptr(buffers["k_scales"]),
-        _ptr(buffers["k_mean"]), _ptr(buffers["k_carrier"]), _ptr(buffers["v_codes"]),
+        _ptr(buffers["k_mean"]), _ptr(buffers["v_codes"]),
         _ptr(buffers["v_scales"]), _ptr(buffers["workspace"]), _stream(stream))
     if rc != 0:
         raise SattnError(rc, "sattn_prepare_kv")
@@ -291,7 +290,7 @@ def forward_q_bf16(q: torch.Tensor, prep: dict, out: torch.Tensor | None = None,
             prep["forward_workspace"] = workspace
     _need_cuda(out, workspace)
     rc = load_library().sattn_forward_q_bf16(
-        ctypes.byref(shape), _ptr(q), _ptr(prep["k_carrier"]), _ptr(prep["k_scales"]), _ptr(prep["v_codes"]),
+        ctypes.byref(shape), _ptr(q), _ptr(prep["k_codes"]), _ptr(prep["k_scales"]), _ptr(prep["v_codes"]),
         _ptr(prep["v_scales"]), _ptr(out), _ptr(workspace), _stream(stream))
     if rc != 0:
         raise SattnError(rc, "sattn_forward_q_bf16")
@@ -314,7 +313,7 @@ def forward_withhold_v_for_test(prep: dict, out: torch.Tensor | None = None,
             prep["forward_workspace"] = workspace
     _need_cuda(out, workspace)
     rc = load_library().sattn_test_forward_withhold_v(
-        ctypes.byref(shape), _ptr(prep["q_codes"]), _ptr(prep["q_scales"]), _ptr(prep["k_carrier"]),
+        ctypes.byref(shape), _ptr(prep["q_codes"]), _ptr(prep["q_scales"]), _ptr(prep["k_codes"]),
         _ptr(prep["k_scales"]), _ptr(prep["v_codes"]), _ptr(prep["v_scales"]), _ptr(out),
         _ptr(workspace), _stream(stream))
     if rc != 0:
@@ -357,7 +356,7 @@ class Graph:
         handle = ctypes.c_void_p()
         rc = load_library().sattn_graph_create(
             ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(prep["q_codes"]), _ptr(prep["q_scales"]),
-            _ptr(prep["k_codes"]), _ptr(prep["k_scales"]), _ptr(prep["k_mean"]), _ptr(prep["k_carrier"]),
+            _ptr(prep["k_codes"]), _ptr(prep["k_scales"]), _ptr(prep["k_mean"]),
             _ptr(prep["v_codes"]), _ptr(prep["v_scales"]), _ptr(prep["workspace"]), _ptr(self.out),
             _ptr(self.workspace), ctypes.byref(handle))
         if rc != 0:

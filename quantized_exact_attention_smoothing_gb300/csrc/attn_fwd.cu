@@ -984,6 +984,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #endif
 }
 
+// The K codes [B*Hkv][nk32][128] (INT8) -> their FP16 carrier [B*Hkv][Nkv][128],
+// the operand of QK^T on the tensor cores (this part has no INT8 tensor-core
+// product; integers of magnitude <= 127 are exact in FP16).  Thread = 16
+// codes (one 16-byte load, two 16-byte stores), kCarrierUnroll chunks per
+// thread; grid y = KV head.  Bound by HBM bandwidth: 128 bytes read and 256
+// written per key.
+constexpr int kCarrierUnroll = 4;
+__global__ void __launch_bounds__(256) k_carrier_kernel(const uint4 *__restrict__ codes, int Nkv, int64_t nk32,
+                                                        uint4 *__restrict__ carrier)
+{
+    const int64_t bh = blockIdx.y;
+    const int64_t n = static_cast<int64_t>(Nkv) * (HD / 16);   // 16-code chunks of this head
+    const uint4 *src = codes + bh * nk32 * (HD / 16);
+    uint4 *dst = carrier + bh * Nkv * static_cast<int64_t>(HD / 8);
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * (256 * kCarrierUnroll) + threadIdx.x;
+    uint4 a[kCarrierUnroll];
+#pragma unroll
+    for (int u = 0; u < kCarrierUnroll; ++u)
+        if (c0 + 256 * u < n)
+            a[u] = __ldg(src + c0 + 256 * u);
+#pragma unroll
+    for (int u = 0; u < kCarrierUnroll; ++u) {
+        const int64_t c = c0 + 256 * u;
+        if (c < n) {
+            dst[2 * c] = make_uint4(ptx::f16x2_of_i8(a[u].x, 0), ptx::f16x2_of_i8(a[u].x, 2),
+                                    ptx::f16x2_of_i8(a[u].y, 0), ptx::f16x2_of_i8(a[u].y, 2));
+            dst[2 * c + 1] = make_uint4(ptx::f16x2_of_i8(a[u].z, 0), ptx::f16x2_of_i8(a[u].z, 2),
+                                        ptx::f16x2_of_i8(a[u].w, 0), ptx::f16x2_of_i8(a[u].w, 2));
+        }
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1007,9 +1039,14 @@ float *debug_dump_buffer() { return g_debug_dump; }
 extern "C" void sattn_debug_set_dump(float *p) { g_debug_dump = p; }
 #endif
 
-size_t forward_workspace_bytes(const Geometry &)
+size_t carrier_bytes(const Geometry &g)
 {
-    return kStatusBytes;
+    return static_cast<size_t>(g.B) * g.Hkv * g.Nkv * HD * sizeof(__half);
+}
+
+size_t forward_workspace_bytes(const Geometry &g)
+{
+    return kStatusBytes + carrier_bytes(g);
 }
 
 namespace {
@@ -1037,14 +1074,14 @@ cudaError_t kernel_attributes()
 // q: INT8 codes [B, Hq, nq32, 128] with q_scales, or with kFuseQ the BF16 Q
 // [B, Hq, Nq, 128] itself (q_scales unused)
 template <bool kFuseQ>
-int launch_impl(const Geometry &g, const void *q, const float *q_scales, const void *k_carrier,
+int launch_impl(const Geometry &g, const void *q, const float *q_scales, const int8_t *k_codes,
                 const float *k_scales, const uint8_t *v_codes, const float *v_scales, void *out,
-                void *workspace, cudaStream_t stream, bool withhold_v, bool reset_status)
+                void *status_block, void *k_carrier, cudaStream_t stream, bool withhold_v, bool reset_status)
 {
     auto encode = tensor_map_encoder();
     if (!encode)
         return 1;
-    uint32_t *status = static_cast<uint32_t *>(workspace);
+    uint32_t *status = static_cast<uint32_t *>(status_block);
     const int bhk = g.B * g.Hkv;
     if (reset_status && cudaMemsetAsync(status, 0, 2 * sizeof(uint32_t), stream) != cudaSuccess)
         return static_cast<int>(cudaGetLastError());
@@ -1112,6 +1149,14 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const v
     if (attr_err != cudaSuccess)
         return static_cast<int>(attr_err);
 
+    {   // the FP16 carrier of the K codes, read by the attention kernel's K loader
+        const int64_t nchunk = static_cast<int64_t>(g.Nkv) * (HD / 16);
+        const dim3 grid(static_cast<unsigned>((nchunk + 256 * kCarrierUnroll - 1) / (256 * kCarrierUnroll)),
+                        static_cast<unsigned>(bhk));
+        k_carrier_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4 *>(k_codes), g.Nkv, g.nk32,
+                                                    static_cast<uint4 *>(k_carrier));
+    }
+
     FwdParams prm;
     prm.q_codes = kFuseQ ? nullptr : static_cast<const int8_t *>(q);
     prm.q_scales = q_scales;
@@ -1158,12 +1203,12 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const v
 }  // namespace
 
 int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scales,
-                   const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
-                   const float *v_scales, void *out, void *workspace, cudaStream_t stream, bool withhold_v,
-                   bool reset_status)
+                   const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
+                   const float *v_scales, void *out, void *status, void *carrier, cudaStream_t stream,
+                   bool withhold_v, bool reset_status)
 {
-    return launch_impl<false>(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out, workspace, stream,
-                              withhold_v, reset_status);
+    return launch_impl<false>(g, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, out, status, carrier,
+                              stream, withhold_v, reset_status);
 }
 
 int forward_init()
@@ -1174,12 +1219,12 @@ int forward_init()
     return a != cudaSuccess ? static_cast<int>(a) : static_cast<int>(b);
 }
 
-int launch_forward_q_bf16(const Geometry &g, const void *q, const void *k_carrier, const float *k_scales,
-                          const uint8_t *v_codes, const float *v_scales, void *out, void *workspace,
+int launch_forward_q_bf16(const Geometry &g, const void *q, const int8_t *k_codes, const float *k_scales,
+                          const uint8_t *v_codes, const float *v_scales, void *out, void *status, void *carrier,
                           cudaStream_t stream)
 {
-    return launch_impl<true>(g, q, nullptr, k_carrier, k_scales, v_codes, v_scales, out, workspace, stream, false,
-                             true);
+    return launch_impl<true>(g, q, nullptr, k_codes, k_scales, v_codes, v_scales, out, status, carrier, stream,
+                             false, true);
 }
 
 }  // namespace sattn

@@ -131,16 +131,14 @@ __device__ __forceinline__ uint32_t e4m3_code(float v, float s, float rs)
 
 // One CTA per 32-token block of one head; thread = (token, eighth of the
 // channels: 16 values), so a thread holds few registers and many CTAs stay
-// resident to keep loads in flight.  With kSmooth (K), the codes are also
-// written as FP16 values to `carrier` [heads][N][128], the operand of the
-// forward's tensor-core product.
+// resident to keep loads in flight.  With kSmooth (K), the per-channel mean
+// is subtracted first.
 template <bool kSmooth>
 __global__ void __launch_bounds__(256) quant_int8_kernel(const uint4 *__restrict__ x, int N,
                                                          int64_t npad, int nblk,
                                                          const float *__restrict__ mean,
                                                          int8_t *__restrict__ codes,
-                                                         float *__restrict__ scales,
-                                                         uint4 *__restrict__ carrier)
+                                                         float *__restrict__ scales)
 {
     __shared__ float warp_max[8];
     const int bh = blockIdx.y, blk = blockIdx.x;
@@ -207,13 +205,6 @@ __global__ void __launch_bounds__(256) quant_int8_kernel(const uint4 *__restrict
     }
     *reinterpret_cast<uint4 *>(codes + (static_cast<size_t>(bh) * npad + t) * kHeadDim + part * 16) =
         make_uint4(packed[0], packed[1], packed[2], packed[3]);
-    if (kSmooth && valid) {
-        uint4 *cd = carrier + (static_cast<size_t>(bh) * N + t) * (kHeadDim / 8) + part * 2;
-#pragma unroll
-        for (int w = 0; w < 2; ++w)
-            cd[w] = make_uint4(ptx::f16x2_of_i8(packed[2 * w], 0), ptx::f16x2_of_i8(packed[2 * w], 2),
-                               ptx::f16x2_of_i8(packed[2 * w + 1], 0), ptx::f16x2_of_i8(packed[2 * w + 1], 2));
-    }
     if (threadIdx.x == 0)
         scales[static_cast<size_t>(bh) * nblk + blk] = s;
 }
@@ -329,8 +320,8 @@ size_t prepare_workspace_bytes(const Geometry &g)
 
 cudaError_t launch_prepare(const Geometry &g, const void *q, const void *k, const void *v,
                            int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
-                           float *k_mean, void *k_carrier, uint8_t *v_codes, float *v_scales,
-                           void *workspace, cudaStream_t stream)
+                           float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace,
+                           cudaStream_t stream)
 {
     const int bhk = g.B * g.Hkv, bhq = g.B * g.Hq;
     float *ksum = static_cast<float *>(workspace);
@@ -344,18 +335,18 @@ cudaError_t launch_prepare(const Geometry &g, const void *q, const void *k, cons
     kv_finalize_kernel<<<bhk, kHeadDim, 0, stream>>>(ksum, vmax, g.Nkv, static_cast<int>(g.nchunks),
                                                      k_mean, v_scales);
     quant_int8_kernel<true><<<dim3(static_cast<unsigned>(g.nbk), bhk), 256, 0, stream>>>(
-        k4, g.Nkv, g.nk32, static_cast<int>(g.nbk), k_mean, k_codes, k_scales, static_cast<uint4 *>(k_carrier));
+        k4, g.Nkv, g.nk32, static_cast<int>(g.nbk), k_mean, k_codes, k_scales);
     quant_v_kernel<<<dim3(static_cast<unsigned>(g.nk128 / kVPad), bhk), 256, 0, stream>>>(
         v4, g.Nkv, g.nk128, v_scales, v_codes);
     if (q)   // without Q, K and V only (the forward quantises Q itself)
         quant_int8_kernel<false><<<dim3(static_cast<unsigned>(g.nbq), bhq), 256, 0, stream>>>(
-            q4, g.Nq, g.nq32, static_cast<int>(g.nbq), nullptr, q_codes, q_scales, nullptr);
+            q4, g.Nq, g.nq32, static_cast<int>(g.nbq), nullptr, q_codes, q_scales);
     return cudaGetLastError();
 }
 
 cudaError_t launch_prepare_kv_split(const Geometry &g, const void *k, const void *v, int8_t *k_codes,
-                                    float *k_scales, float *k_mean, void *k_carrier, uint8_t *v_codes,
-                                    float *v_scales, void *workspace, cudaStream_t stream, cudaStream_t v_stream,
+                                    float *k_scales, float *k_mean, uint8_t *v_codes, float *v_scales,
+                                    void *workspace, cudaStream_t stream, cudaStream_t v_stream,
                                     cudaEvent_t fork, cudaEvent_t join)
 {
     const int bhk = g.B * g.Hkv;
@@ -377,7 +368,7 @@ cudaError_t launch_prepare_kv_split(const Geometry &g, const void *k, const void
     if ((e = cudaEventRecord(join, v_stream)) != cudaSuccess)
         return e;
     quant_int8_kernel<true><<<dim3(static_cast<unsigned>(g.nbk), bhk), 256, 0, stream>>>(
-        k4, g.Nkv, g.nk32, static_cast<int>(g.nbk), k_mean, k_codes, k_scales, static_cast<uint4 *>(k_carrier));
+        k4, g.Nkv, g.nk32, static_cast<int>(g.nbk), k_mean, k_codes, k_scales);
     if ((e = cudaStreamWaitEvent(stream, join, 0)) != cudaSuccess)
         return e;
     return cudaGetLastError();
@@ -388,7 +379,7 @@ cudaError_t launch_prepare_q(const Geometry &g, const void *q, int8_t *q_codes, 
 {
     quant_int8_kernel<false><<<dim3(static_cast<unsigned>(g.nbq), static_cast<unsigned>(g.B * g.Hq)), 256, 0,
                                stream>>>(static_cast<const uint4 *>(q), g.Nq, g.nq32, static_cast<int>(g.nbq), nullptr,
-                                         q_codes, q_scales, nullptr);
+                                         q_codes, q_scales);
     return cudaGetLastError();
 }
 

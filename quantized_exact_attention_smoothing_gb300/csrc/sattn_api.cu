@@ -65,16 +65,15 @@ void fill_sizes(const Geometry &g, sattn_sizes *z)
     z->k_codes = r16(bhk * g.nk32 * D);
     z->k_scales = r16(bhk * g.nbk * 4);
     z->k_mean = r16(bhk * D * 4);
-    z->k_carrier = r16(bhk * g.Nkv * D * 2);
     z->v_codes = r16(bhk * D * g.nk128);
     z->v_scales = r16(bhk * D * 4);
     z->out = r16(bhq * g.Nq * D * 2);
     z->prepare_workspace = r16(sattn::prepare_workspace_bytes(g));
     z->forward_workspace = r16(sattn::forward_workspace_bytes(g));
     z->arena = r256(z->q) + r256(z->k) + r256(z->v) + r256(z->q_codes) + r256(z->q_scales) +
-               r256(z->k_codes) + r256(z->k_scales) + r256(z->k_mean) + r256(z->k_carrier) + r256(z->v_codes) +
-               r256(z->v_scales) + r256(z->out) + 2 * r256(z->prepare_workspace) +
-               r256(z->forward_workspace);
+               r256(z->k_codes) + r256(z->k_scales) + r256(z->k_mean) + r256(z->v_codes) + r256(z->v_scales) +
+               r256(z->out) + 2 * r256(z->prepare_workspace) + r256(sattn::kStatusBytes) +
+               2 * r256(sattn::carrier_bytes(g));
 }
 
 // The current device must be compute capability 10.3; the answer is cached per device.
@@ -151,12 +150,12 @@ bool create_qprep_stream(DeviceStreams &d)
 }
 
 int prepare_impl(const Geometry &g, const void *q, const void *k, const void *v, int8_t *q_codes,
-                 float *q_scales, int8_t *k_codes, float *k_scales, float *k_mean, void *k_carrier,
-                 uint8_t *v_codes, float *v_scales, void *workspace, cudaStream_t stream)
+                 float *q_scales, int8_t *k_codes, float *k_scales, float *k_mean, uint8_t *v_codes,
+                 float *v_scales, void *workspace, cudaStream_t stream)
 {
     // q, q_codes and q_scales are all null for the K/V-only preparation
     const bool with_q = q != nullptr;
-    const void *ptrs[] = {k, v, k_codes, k_scales, k_mean, k_carrier, v_codes, v_scales, workspace,
+    const void *ptrs[] = {k, v, k_codes, k_scales, k_mean, v_codes, v_scales, workspace,
                           with_q ? q : k, with_q ? q_codes : k, with_q ? q_scales : k};
     for (const void *p : ptrs) {
         if (!p)
@@ -179,28 +178,31 @@ int prepare_impl(const Geometry &g, const void *q, const void *k, const void *v,
     std::lock_guard<std::mutex> lock(h.mu);
     DeviceStreams &ds = h.dev[dev];
     if (!with_q || !create_qprep_stream(ds))
-        return sattn::launch_prepare(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes,
-                                     v_scales, workspace, stream) == cudaSuccess
+        return sattn::launch_prepare(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes, v_scales,
+                                     workspace, stream) == cudaSuccess
                    ? SATTN_OK
                    : SATTN_ERR_LAUNCH;
     if (cudaEventRecord(ds.qfork, stream) != cudaSuccess || cudaStreamWaitEvent(ds.qprep, ds.qfork, 0) != cudaSuccess ||
         sattn::launch_prepare_q(g, q, q_codes, q_scales, ds.qprep) != cudaSuccess ||
         cudaEventRecord(ds.qjoin, ds.qprep) != cudaSuccess ||
-        sattn::launch_prepare_kv_split(g, k, v, k_codes, k_scales, k_mean, k_carrier, v_codes, v_scales, workspace,
-                                       stream, ds.vprep, ds.vfork, ds.vjoin) != cudaSuccess ||
+        sattn::launch_prepare_kv_split(g, k, v, k_codes, k_scales, k_mean, v_codes, v_scales, workspace, stream,
+                                       ds.vprep, ds.vfork, ds.vjoin) != cudaSuccess ||
         cudaStreamWaitEvent(stream, ds.qjoin, 0) != cudaSuccess)
         return SATTN_ERR_LAUNCH;
     return SATTN_OK;
 }
 
+// The forward workspace: the status block, then the FP16 carrier of the K codes.
+void *carrier_of(void *workspace) { return static_cast<char *>(workspace) + sattn::kStatusBytes; }
+
 // q_bf16 non-null: the forward that quantises Q itself (q_codes, q_scales unused)
 int forward_impl(const Geometry &g, const int8_t *q_codes, const float *q_scales,
-                 const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
+                 const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
                  const float *v_scales, void *out, void *workspace, cudaStream_t stream,
                  bool withhold_v = false, const void *q_bf16 = nullptr)
 {
     const bool fused = q_bf16 != nullptr;
-    const void *ptrs[] = {fused ? q_bf16 : q_codes, fused ? q_bf16 : q_scales, k_carrier, k_scales, v_codes,
+    const void *ptrs[] = {fused ? q_bf16 : q_codes, fused ? q_bf16 : q_scales, k_codes, k_scales, v_codes,
                           v_scales, out, workspace};
     for (const void *p : ptrs) {
         if (!p)
@@ -211,10 +213,10 @@ int forward_impl(const Geometry &g, const int8_t *q_codes, const float *q_scales
     const int dev = check_device();
     if (dev != SATTN_OK)
         return dev;
-    const int rc = fused ? sattn::launch_forward_q_bf16(g, q_bf16, k_carrier, k_scales, v_codes, v_scales, out,
-                                                        workspace, stream)
-                         : sattn::launch_forward(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales,
-                                                 out, workspace, stream, withhold_v);
+    const int rc = fused ? sattn::launch_forward_q_bf16(g, q_bf16, k_codes, k_scales, v_codes, v_scales, out,
+                                                        workspace, carrier_of(workspace), stream)
+                         : sattn::launch_forward(g, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales,
+                                                 out, workspace, carrier_of(workspace), stream, withhold_v);
     if (rc == 1)
         return SATTN_ERR_DEVICE;   // no tensor-map encoder in this driver
     return rc == 0 ? SATTN_OK : SATTN_ERR_LAUNCH;
@@ -233,7 +235,7 @@ int forward_impl(const Geometry &g, const int8_t *q_codes, const float *q_scales
 // cleared once before the fork.
 // ---------------------------------------------------------------------------
 struct HostBuffers {
-    void *q, *k, *v, *out, *k_carrier, *pws[2], *fws;
+    void *q, *k, *v, *out, *carrier[2], *pws[2], *fws;
     int8_t *q_codes, *k_codes;
     float *q_scales, *k_scales, *k_mean, *v_scales;
     uint8_t *v_codes;
@@ -350,14 +352,13 @@ int attention_host_pipelined(const Geometry &g, const sattn_shape &shape, const 
         int8_t *k_codes = hb.k_codes + kh * g.nk32 * D;
         float *k_scales = hb.k_scales + kh * g.nbk;
         float *k_mean = hb.k_mean + kh * D;
-        void *k_carrier = atw(hb.k_carrier, kh * g.Nkv * D * 2);
         uint8_t *v_codes = hb.v_codes + kh * D * g.nk128;
         float *v_scales = hb.v_scales + kh * D;
-        if (sattn::launch_prepare(gc, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes,
-                                  v_scales, hb.pws[c & 1], st) != cudaSuccess)
+        if (sattn::launch_prepare(gc, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes, v_scales,
+                                  hb.pws[c & 1], st) != cudaSuccess)
             return SATTN_ERR_LAUNCH;
-        const int frc = sattn::launch_forward(gc, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out,
-                                              hb.fws, st, false, false);
+        const int frc = sattn::launch_forward(gc, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, out,
+                                              hb.fws, hb.carrier[c & 1], st, false, false);
         if (frc == 1)
             return SATTN_ERR_DEVICE;
         if (frc != 0)
@@ -400,8 +401,7 @@ int sattn_query_sizes(const sattn_shape *shape, sattn_sizes *sizes)
 
 int sattn_prepare(const sattn_shape *shape, const void *q, const void *k, const void *v,
                   int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
-                  float *k_mean, void *k_carrier, uint8_t *v_codes, float *v_scales, void *workspace,
-                  void *stream)
+                  float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace, void *stream)
 {
     Geometry g;
     const int rc = make_geometry(shape, &g);
@@ -409,54 +409,54 @@ int sattn_prepare(const sattn_shape *shape, const void *q, const void *k, const 
         return rc;
     if (!q || !q_codes || !q_scales)
         return SATTN_ERR_INVALID;
-    return prepare_impl(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes, v_scales,
-                        workspace, static_cast<cudaStream_t>(stream));
+    return prepare_impl(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes, v_scales, workspace,
+                        static_cast<cudaStream_t>(stream));
 }
 
 int sattn_forward(const sattn_shape *shape, const int8_t *q_codes, const float *q_scales,
-                  const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
+                  const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
                   const float *v_scales, void *out, void *workspace, void *stream)
 {
     Geometry g;
     const int rc = make_geometry(shape, &g);
     if (rc != SATTN_OK)
         return rc;
-    return forward_impl(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out, workspace,
+    return forward_impl(g, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, out, workspace,
                         static_cast<cudaStream_t>(stream));
 }
 
 int sattn_prepare_kv(const sattn_shape *shape, const void *k, const void *v, int8_t *k_codes,
-                     float *k_scales, float *k_mean, void *k_carrier, uint8_t *v_codes, float *v_scales,
-                     void *workspace, void *stream)
+                     float *k_scales, float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace,
+                     void *stream)
 {
     Geometry g;
     const int rc = make_geometry(shape, &g);
     if (rc != SATTN_OK)
         return rc;
-    return prepare_impl(g, nullptr, k, v, nullptr, nullptr, k_codes, k_scales, k_mean, k_carrier, v_codes,
-                        v_scales, workspace, static_cast<cudaStream_t>(stream));
+    return prepare_impl(g, nullptr, k, v, nullptr, nullptr, k_codes, k_scales, k_mean, v_codes, v_scales,
+                        workspace, static_cast<cudaStream_t>(stream));
 }
 
-int sattn_forward_q_bf16(const sattn_shape *shape, const void *q, const void *k_carrier, const float *k_scales,
+int sattn_forward_q_bf16(const sattn_shape *shape, const void *q, const int8_t *k_codes, const float *k_scales,
                          const uint8_t *v_codes, const float *v_scales, void *out, void *workspace, void *stream)
 {
     Geometry g;
     const int rc = make_geometry(shape, &g);
     if (rc != SATTN_OK)
         return rc;
-    return forward_impl(g, nullptr, nullptr, k_carrier, k_scales, v_codes, v_scales, out, workspace,
+    return forward_impl(g, nullptr, nullptr, k_codes, k_scales, v_codes, v_scales, out, workspace,
                         static_cast<cudaStream_t>(stream), false, q);
 }
 
 int sattn_test_forward_withhold_v(const sattn_shape *shape, const int8_t *q_codes, const float *q_scales,
-                                  const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
+                                  const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
                                   const float *v_scales, void *out, void *workspace, void *stream)
 {
     Geometry g;
     const int rc = make_geometry(shape, &g);
     if (rc != SATTN_OK)
         return rc;
-    return forward_impl(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out, workspace,
+    return forward_impl(g, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, out, workspace,
                         static_cast<cudaStream_t>(stream), true);
 }
 
@@ -539,13 +539,14 @@ int sattn_attention_host(const sattn_shape *shape, const void *q_host, const voi
     hb.k_codes = reinterpret_cast<int8_t *>(take(z.k_codes));
     hb.k_scales = reinterpret_cast<float *>(take(z.k_scales));
     hb.k_mean = reinterpret_cast<float *>(take(z.k_mean));
-    hb.k_carrier = take(z.k_carrier);
     hb.v_codes = reinterpret_cast<uint8_t *>(take(z.v_codes));
     hb.v_scales = reinterpret_cast<float *>(take(z.v_scales));
     hb.out = take(z.out);
     hb.pws[0] = take(z.prepare_workspace);
     hb.pws[1] = take(z.prepare_workspace);
-    hb.fws = take(z.forward_workspace);
+    hb.fws = take(sattn::kStatusBytes);
+    hb.carrier[0] = take(sattn::carrier_bytes(g));
+    hb.carrier[1] = take(sattn::carrier_bytes(g));
     return attention_host_pipelined(g, *shape, q_host, k_host, v_host, out_host, hb,
                                     static_cast<cudaStream_t>(stream));
 }
@@ -556,9 +557,9 @@ struct sattn_graph {
 };
 
 int sattn_graph_create(const sattn_shape *shape, const void *q, const void *k, const void *v, int8_t *q_codes,
-                       float *q_scales, int8_t *k_codes, float *k_scales, float *k_mean, void *k_carrier,
-                       uint8_t *v_codes, float *v_scales, void *prepare_workspace, void *out,
-                       void *forward_workspace, sattn_graph **graph)
+                       float *q_scales, int8_t *k_codes, float *k_scales, float *k_mean, uint8_t *v_codes,
+                       float *v_scales, void *prepare_workspace, void *out, void *forward_workspace,
+                       sattn_graph **graph)
 {
     if (!graph)
         return SATTN_ERR_INVALID;
@@ -567,7 +568,7 @@ int sattn_graph_create(const sattn_shape *shape, const void *q, const void *k, c
     int rc = make_geometry(shape, &g);
     if (rc != SATTN_OK)
         return rc;
-    const void *ptrs[] = {q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes, v_scales,
+    const void *ptrs[] = {q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes, v_scales,
                           prepare_workspace, out, forward_workspace};
     for (const void *ptr : ptrs) {
         if (!ptr)
@@ -600,10 +601,10 @@ int sattn_graph_create(const sattn_shape *shape, const void *q, const void *k, c
     if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
         rc = SATTN_ERR_LAUNCH;
     } else {
-        rc = prepare_impl(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes, v_scales,
+        rc = prepare_impl(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes, v_scales,
                           prepare_workspace, cs);
         if (rc == SATTN_OK)
-            rc = forward_impl(g, q_codes, q_scales, k_carrier, k_scales, v_codes, v_scales, out, forward_workspace,
+            rc = forward_impl(g, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, out, forward_workspace,
                               cs);
         const cudaError_t end = cudaStreamEndCapture(cs, &gr->graph);   // ends the capture in every case
         if (rc == SATTN_OK && end != cudaSuccess)
@@ -691,13 +692,13 @@ int prepare_scratch_address(void **out)
 extern "C" int sattn_prepare_noalloc(const sattn_shape *shape, const void *q, const void *k,
                                      const void *v, int8_t *q_codes, float *q_scales,
                                      int8_t *k_codes, float *k_scales, float *k_mean,
-                                     void *k_carrier, uint8_t *v_codes, float *v_scales, void *stream)
+                                     uint8_t *v_codes, float *v_scales, void *stream)
 {
     Geometry g;
     int rc = make_geometry(shape, &g);
     if (rc != SATTN_OK)
         return rc;
-    const void *ptrs[] = {q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes, v_scales};
+    const void *ptrs[] = {q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes, v_scales};
     for (const void *p : ptrs) {
         if (!p)
             return SATTN_ERR_INVALID;
@@ -713,8 +714,8 @@ extern "C" int sattn_prepare_noalloc(const sattn_shape *shape, const void *q, co
     rc = prepare_scratch_address(&scratch);
     if (rc != SATTN_OK)
         return rc;
-    return sattn::launch_prepare(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, k_carrier, v_codes,
-                                 v_scales, scratch, static_cast<cudaStream_t>(stream)) == cudaSuccess
+    return sattn::launch_prepare(g, q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes, v_scales,
+                                 scratch, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? SATTN_OK
                : SATTN_ERR_LAUNCH;
 }

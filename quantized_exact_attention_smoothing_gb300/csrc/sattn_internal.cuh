@@ -32,8 +32,8 @@ size_t prepare_workspace_bytes(const Geometry &g);
 // K/V statistics `fork` is recorded on `stream` and waited by v_stream; `join`
 // is recorded on v_stream after V's kernel and waited by `stream` at the end.
 cudaError_t launch_prepare_kv_split(const Geometry &g, const void *k, const void *v, int8_t *k_codes,
-                                    float *k_scales, float *k_mean, void *k_carrier, uint8_t *v_codes,
-                                    float *v_scales, void *workspace, cudaStream_t stream, cudaStream_t v_stream,
+                                    float *k_scales, float *k_mean, uint8_t *v_codes, float *v_scales,
+                                    void *workspace, cudaStream_t stream, cudaStream_t v_stream,
                                     cudaEvent_t fork, cudaEvent_t join);
 // The Q part of launch_prepare alone (INT8 codes and block scales of Q).
 cudaError_t launch_prepare_q(const Geometry &g, const void *q, int8_t *q_codes, float *q_scales,
@@ -45,20 +45,25 @@ cudaError_t launch_int8_quantiser_sweep(uint32_t amax_lo, uint32_t amax_hi, unsi
 // q = nullptr skips the Q part (q_codes, q_scales unused).
 cudaError_t launch_prepare(const Geometry &g, const void *q, const void *k, const void *v,
                            int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
-                           float *k_mean, void *k_carrier, uint8_t *v_codes, float *v_scales,
-                           void *workspace, cudaStream_t stream);
+                           float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace,
+                           cudaStream_t stream);
 
 // ---- forward (attn_fwd.cu) ----
-// Workspace: the 256-byte status block.
+// Workspace: the 256-byte status block, then the FP16 carrier of the K codes
+// ([B][Hkv][Nkv][128], the tensor-core operand of QK^T, written by the forward
+// pass itself from the INT8 codes).
 constexpr size_t kStatusBytes = 256;
+size_t carrier_bytes(const Geometry &g);
 size_t forward_workspace_bytes(const Geometry &g);
 // Returns 0 on success, 1 if a tensor map could not be encoded, or a CUDA error.
+// `status` is the status block, `carrier` the carrier's scratch (both inside
+// the forward workspace for the public entry points).
 // withhold_v (test hook): no V tile is loaded, so the launch ends through its
 // bounded waits and reports a timeout in the status block.  With reset_status false
 // the status block is not cleared first (several launches report into one).
 int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scales,
-                   const void *k_carrier, const float *k_scales, const uint8_t *v_codes,
-                   const float *v_scales, void *out, void *workspace, cudaStream_t stream,
+                   const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
+                   const float *v_scales, void *out, void *status, void *carrier, cudaStream_t stream,
                    bool withhold_v = false, bool reset_status = true);
 
 // One-time host setup of the forward kernels (tensor-map encoder, register
@@ -69,8 +74,8 @@ int forward_init();
 // The forward pass with Q quantised inside the kernel: q is the BF16 Q
 // [B, Hq, Nq, 128]; the codes and block scales are those launch_prepare
 // writes, and the output is launch_forward's on them, byte for byte.
-int launch_forward_q_bf16(const Geometry &g, const void *q, const void *k_carrier, const float *k_scales,
-                          const uint8_t *v_codes, const float *v_scales, void *out, void *workspace,
-                          cudaStream_t stream);
+int launch_forward_q_bf16(const Geometry &g, const void *q, const int8_t *k_codes, const float *k_scales,
+                          const uint8_t *v_codes, const float *v_scales, void *out, void *status,
+                          void *carrier, cudaStream_t stream);
 
 }  // namespace sattn

@@ -26,8 +26,9 @@ def test_query_sizes_headline_shape():
     assert z["q_codes"] == 4 * 32 * 8192 * 128
     assert z["v_codes"] == 4 * 8 * 128 * 8192
     assert z["q_scales"] == 4 * 32 * 256 * 4
-    assert z["forward_workspace"] == 256
-    assert z["k_carrier"] == 4 * 8 * 8192 * 128 * 2
+    # status block, then the FP16 copy of the K codes the tensor cores read
+    assert z["forward_workspace"] == 256 + 4 * 8 * 8192 * 128 * 2
+    assert "k_carrier" not in z
     assert all(v % 16 == 0 for v in z.values())
 
 
@@ -60,7 +61,7 @@ def test_head_dim_other_than_128_rejected(lib):
 
 def test_null_and_misaligned_pointers_rejected_before_any_device_work(lib):
     s = sattn.make_shape(1, 1, 1, 8, 8)
-    good = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(12)]
+    good = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(11)]
     args = list(good)
     args[3] = None
     assert lib.sattn_prepare(ctypes.byref(s), *args, None) == 1
@@ -81,7 +82,7 @@ def test_status_strings(lib):
 
 def test_kv_prepare_and_fused_forward_check_pointers_first(lib):
     s = sattn.make_shape(1, 1, 1, 8, 8)
-    kv = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(9)]
+    kv = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(8)]
     args = list(kv)
     args[2] = None                                   # k_codes
     assert lib.sattn_prepare_kv(ctypes.byref(s), *args, None) == 1
@@ -101,7 +102,7 @@ def test_kv_prepare_and_fused_forward_check_pointers_first(lib):
 
 def test_full_prepare_still_requires_q(lib):
     s = sattn.make_shape(1, 1, 1, 8, 8)
-    args = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(12)]
+    args = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(11)]
     args[0] = None                                   # q
     assert lib.sattn_prepare(ctypes.byref(s), *args, None) == 1
 
@@ -116,11 +117,11 @@ def test_quantiser_sweep_hook_checks_arguments(lib):
 
 def test_graph_entry_points_check_arguments(lib):
     s = sattn.make_shape(1, 1, 1, 8, 8)
-    bufs = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(14)]
+    bufs = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(13)]
     h = ctypes.c_void_p()
     assert lib.sattn_graph_create(ctypes.byref(s), *bufs, None) == 1          # no handle pointer
     args = list(bufs)
-    args[12] = None                                                          # out
+    args[11] = None                                                          # out
     assert lib.sattn_graph_create(ctypes.byref(s), *args, ctypes.byref(h)) == 1
     assert h.value is None
     args = list(bufs)

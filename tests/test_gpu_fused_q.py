@@ -17,7 +17,7 @@ from helpers import assert_close_output, bf16_bits, to_device_bf16
 
 pytestmark = pytest.mark.gpu
 
-KV_NAMES = ("k_codes", "k_scales", "k_mean", "k_carrier", "v_codes", "v_scales")
+KV_NAMES = ("k_codes", "k_scales", "k_mean", "v_codes", "v_scales")
 
 
 def _both(q, k, v, causal, sm_scale=0.0):

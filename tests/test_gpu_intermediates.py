@@ -29,7 +29,7 @@ pytestmark = pytest.mark.gpu
 def dbg_lib():
     lib = ctypes.CDLL(B.build_debug())
     P, SP = ctypes.c_void_p, ctypes.POINTER(bnd.sattn_shape)
-    lib.sattn_prepare.argtypes = [SP] + [P] * 13
+    lib.sattn_prepare.argtypes = [SP] + [P] * 12
     lib.sattn_forward.argtypes = [SP] + [P] * 9
     lib.sattn_debug_set_dump.argtypes = [P]
     return lib
@@ -42,16 +42,16 @@ def _run_dump(lib, q, k, v, causal):
     shape = bnd.make_shape(Bn, Hq, k.shape[1], Nq, k.shape[2], causal)
     buf = bnd.prepare_buffers(shape, dq.device)
     out = torch.empty((Bn, Hq, Nq, 128), dtype=torch.bfloat16, device="cuda")
-    fws = torch.zeros(64, dtype=torch.int32, device="cuda")
+    fws = torch.zeros(bnd.query_sizes(shape)["forward_workspace"] // 4, dtype=torch.int32, device="cuda")
     dump = torch.zeros(98304, dtype=torch.float32, device="cuda")
     s = bnd._stream(None)
     p = bnd._ptr
     assert lib.sattn_prepare(ctypes.byref(shape), p(dq), p(dk), p(dv), p(buf["q_codes"]), p(buf["q_scales"]),
-                             p(buf["k_codes"]), p(buf["k_scales"]), p(buf["k_mean"]), p(buf["k_carrier"]),
+                             p(buf["k_codes"]), p(buf["k_scales"]), p(buf["k_mean"]),
                              p(buf["v_codes"]), p(buf["v_scales"]), p(buf["workspace"]), s) == 0
     lib.sattn_debug_set_dump(ctypes.c_void_p(dump.data_ptr()))
     try:
-        assert lib.sattn_forward(ctypes.byref(shape), p(buf["q_codes"]), p(buf["q_scales"]), p(buf["k_carrier"]),
+        assert lib.sattn_forward(ctypes.byref(shape), p(buf["q_codes"]), p(buf["q_scales"]), p(buf["k_codes"]),
                                  p(buf["k_scales"]), p(buf["v_codes"]), p(buf["v_scales"]), p(out), p(fws), s) == 0
         torch.cuda.synchronize()
     finally:

@@ -19,7 +19,7 @@ from helpers import to_device_bf16
 
 pytestmark = pytest.mark.gpu
 
-NAMES = ("q_codes", "q_scales", "k_codes", "k_scales", "k_mean", "k_carrier", "v_codes", "v_scales")
+NAMES = ("q_codes", "q_scales", "k_codes", "k_scales", "k_mean", "v_codes", "v_scales")
 
 
 def _inputs(w):
@@ -52,5 +52,5 @@ def test_noalloc_scratch_limit_is_reported():
     import ctypes
     p = ctypes.c_void_p(z.data_ptr())
     rc = lib.sattn_prepare_noalloc(ctypes.byref(shape), ctypes.c_void_p(q.data_ptr()), p, p, p, p, p,
-                                   p, p, p, p, p, None)
+                                   p, p, p, p, None)
     assert rc == 6, rc
