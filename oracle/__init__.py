@@ -19,6 +19,10 @@ Parity status of each function (what pins it, see tests/test_oracle_*.py):
                       invariance of K smoothing
   forward             pinned: constant V, one-hot key, tile-size invariance,
                       accuracy against forward_exact, shares the pinned skeleton
+  p8_codes            pinned: exhaustive E4M3 midpoints against exact rational
+                      arithmetic, monotonicity, saturation, zeros
+  tile_state          pinned: its last-tile state reproduces forward's output;
+                      shares the per-row recurrence with forward
 """
 from __future__ import annotations
 
@@ -81,6 +85,12 @@ def _load():
     lib.oracle_forward_exact.argtypes = [i, i, i, i, i, i, ctypes.c_double, i,
                                          P, P, P, i, P]
     lib.oracle_forward_exact.restype = i
+    lib.oracle_p8_codes.argtypes = [ctypes.c_long, P, P, P, P]
+    lib.oracle_p8_codes.restype = i
+    lib.oracle_exp2_rn.argtypes = [ctypes.c_long, P, P]
+    lib.oracle_exp2_rn.restype = i
+    lib.oracle_tile_state.argtypes = [i, i, i, i, i, i, ctypes.c_float, i, P, P, P, P, P, P, i, i, i, i, P, P]
+    lib.oracle_tile_state.restype = i
     _lib = lib
     return lib
 
@@ -205,6 +215,50 @@ def first_tile(prep: dict, Nq: int, Nkv: int, causal: bool, b: int = 0, h: int =
     if rc != 0:
         raise ValueError("oracle_first_tile: invalid shape or position")
     return acc, p8, part
+
+
+def p8_codes(acc, sig, m) -> np.ndarray:
+    """FP8 P bytes of elementwise (acc, sig, m): E4M3(fl(fl(exp2(fl(fl(acc * sig)
+    - m))) * 448)) with a correctly rounded exp2 (the forward's P step)."""
+    lib = _load()
+    acc, sig, m = np.broadcast_arrays(np.asarray(acc, np.float32), np.asarray(sig, np.float32),
+                                      np.asarray(m, np.float32))
+    shape = acc.shape
+    acc, sig, m = (np.ascontiguousarray(x.reshape(-1)) for x in (acc, sig, m))
+    out = np.empty(acc.size, np.uint8)
+    if lib.oracle_p8_codes(acc.size, _ptr(acc), _ptr(sig), _ptr(m), _ptr(out)) != 0:
+        raise ValueError("oracle_p8_codes")
+    return out.reshape(shape)
+
+
+def exp2_rn(x) -> np.ndarray:
+    """FP32 2^x, correctly rounded (the exp2 of the P step)."""
+    lib = _load()
+    x = np.ascontiguousarray(np.asarray(x, np.float32))
+    out = np.empty_like(x)
+    if lib.oracle_exp2_rn(x.size, _ptr(x), _ptr(out)) != 0:
+        raise ValueError("oracle_exp2_rn")
+    return out
+
+
+def tile_state(prep: dict, Nq: int, Nkv: int, causal: bool, which: int, b: int = 0, h: int = 0, q0: int = 0,
+               sm_scale: float = 0.0, tile: int = 256) -> dict:
+    """Running state after KV tile ``which`` for query rows q0 .. q0 + 127 of
+    (b, h): m, the tile's alpha, d and RO after it, the final d and 1/d, and
+    whether each row visited that tile (arrays of 128 rows, RO [128, 128])."""
+    lib = _load()
+    B, Hq = prep["q_codes"].shape[:2]
+    Hkv = prep["k_codes"].shape[1]
+    st = np.zeros((128, 6), np.float64)
+    ro = np.zeros((128, HEAD_DIM), np.float64)
+    rc = lib.oracle_tile_state(B, Hq, Hkv, Nq, Nkv, int(bool(causal)), float(sm_scale), tile,
+                               _ptr(prep["q_codes"]), _ptr(prep["q_scales"]), _ptr(prep["k_codes"]),
+                               _ptr(prep["k_scales"]), _ptr(prep["v_codes"]), _ptr(prep["v_scales"]),
+                               b, h, q0, which, _ptr(st), _ptr(ro))
+    if rc != 0:
+        raise ValueError("oracle_tile_state: invalid shape or position")
+    return dict(m=st[:, 0], alpha=st[:, 1], d=st[:, 2], d_final=st[:, 3], rcp=st[:, 4],
+                visited=st[:, 5] > 0, ro=ro)
 
 
 def forward_exact(q: np.ndarray, k: np.ndarray, v: np.ndarray, causal: bool, smooth: bool,

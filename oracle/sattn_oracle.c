@@ -118,7 +118,28 @@ uint8_t oracle_f32_to_e4m3(float x)
     return s | (uint8_t)(biased << 3) | (uint8_t)mant;
 }
 
-static float exp2_f32(float x) { return (float)exp2((double)x); }
+/* exp2 of an FP32 value, correctly rounded to FP32 (round to nearest even).
+ * The double-precision exp2 of the C library is within about one double ulp
+ * of 2^x, so rounding it to FP32 gives the correctly rounded value unless 2^x
+ * lies within a few double ulps of a point halfway between two FP32 values.
+ * Those rare cases are decided again from exp2l (extended or quadruple
+ * precision, depending on the platform).  2^x of an FP32 x that is not an
+ * integer is irrational, so it never equals a halfway point. */
+static float exp2_rn(float x)
+{
+    const double d = exp2((double)x);
+    const float f = (float)d;
+    if (!(d > 0.0) || isinf(d) || d < 0x1p-126)
+        return f;
+    /* distance from d to the nearest halfway point between FP32 neighbours */
+    const double lo = (double)nextafterf(f, 0.0f), hi = (double)nextafterf(f, INFINITY);
+    const double mid_lo = 0.5 * ((double)f + lo), mid_hi = 0.5 * ((double)f + hi);
+    const double gap = fmin(fabs(d - mid_lo), fabs(d - mid_hi));
+    if (gap > 0x1p-45 * d)
+        return f;
+    const long double e = exp2l((long double)x);
+    return (float)e;
+}
 
 /* ------------------------------------------------------------------------- */
 /* preparation: K smoothing, INT8 Q/K, FP8 V                                 */
@@ -260,6 +281,13 @@ typedef struct {
     double scale_log2;                      /* sm_scale * log2(e), FP64 */
 } ctx_t;
 
+/* State of one row's recurrence after a chosen KV tile, and at the end. */
+typedef struct {
+    int tile, reached;
+    double m, alpha, d, ro[HEAD_DIM];
+    double d_final, rcp;
+} row_rec_t;
+
 static inline float score_q(const ctx_t *cx, int b, int h, int hk, int i, int j)
 {
     const int8_t *qi = cx->qc + ((size_t)(b * cx->Hq + h) * cx->Nq_pad + i) * HEAD_DIM;
@@ -271,6 +299,15 @@ static inline float score_q(const ctx_t *cx, int b, int h, int hk, int i, int j)
     const float sk = cx->ks[(size_t)(b * cx->Hkv + hk) * cx->nbk + j / QBLK];
     const float sigma = (sq * sk) * cx->c0;
     return (float)acc * sigma;
+}
+
+/* FP8 P: the E4M3 byte of exp2(s2 - m) * 448, every step rounded to FP32:
+ * dd = fl(s2 - m), p = fl(exp2(dd)) (correctly rounded), y = fl(p * 448). */
+static inline uint8_t p8_of(float s2, float m)
+{
+    const float dd = s2 - m;
+    const float p = exp2_rn(dd);
+    return oracle_f32_to_e4m3(p * 448.0f);
 }
 
 static inline float prob_q(float p) { return oracle_e4m3_to_f32(oracle_f32_to_e4m3(p * 448.0f)); }
@@ -303,7 +340,7 @@ static inline double value_x(const ctx_t *cx, int b, int hk, int j, int c)
 
 #define ROW_FN attend_row_quant
 #define REAL float
-#define EXP2(x) exp2_f32(x)
+#define EXP2(x) exp2_rn(x)
 #define SCORE(cx, b, h, hk, i, j) score_q(cx, b, h, hk, i, j)
 #define PROB(p) prob_q(p)
 #define VALUE(cx, b, hk, j, c) value_q(cx, b, hk, j, c)
@@ -382,7 +419,7 @@ int oracle_forward(int B, int Hq, int Hkv, int Nq, int Nkv, int causal, float sm
     for (long row = 0; row < nrows; ++row) {
         const int i = (int)(row % Nq), bh = (int)(row / Nq);
         float o[HEAD_DIM];
-        attend_row_quant(&cx, bh / Hq, bh % Hq, i, o);
+        attend_row_quant(&cx, bh / Hq, bh % Hq, i, o, NULL);
         for (int c = 0; c < HEAD_DIM; ++c) {
             if (out_f32)
                 out_f32[row * HEAD_DIM + c] = o[c];
@@ -445,7 +482,7 @@ int oracle_first_tile(int B, int Hq, int Hkv, int Nq, int Nkv, int causal, float
         for (int j = 0; j < n; ++j) {
             w[j] = 0;
             if (j <= last) {
-                const uint8_t code = oracle_f32_to_e4m3(exp2_f32(score_q(&cx, b, h, hk, i, j) - m) * 448.0f);
+                const uint8_t code = p8_of(score_q(&cx, b, h, hk, i, j), m);
                 p8[(size_t)r * tile + j] = code;
                 w[j] = oracle_e4m3_to_f32(code);
             }
@@ -490,7 +527,7 @@ int oracle_forward_rows(int B, int Hq, int Hkv, int Nq, int Nkv, int causal, flo
         const int64_t row = rows[r];
         const int i = (int)(row % Nq), bh = (int)(row / Nq);
         float o[HEAD_DIM];
-        attend_row_quant(&cx, bh / Hq, bh % Hq, i, o);
+        attend_row_quant(&cx, bh / Hq, bh % Hq, i, o, NULL);
         for (int c = 0; c < HEAD_DIM; ++c) {
             if (out_f32)
                 out_f32[r * HEAD_DIM + c] = o[c];
@@ -538,8 +575,80 @@ int oracle_forward_exact(int B, int Hq, int Hkv, int Nq, int Nkv, int causal, do
 #pragma omp parallel for schedule(dynamic, 16)
     for (long row = 0; row < nrows; ++row) {
         const int i = (int)(row % Nq), bh = (int)(row / Nq);
-        attend_row_exact(&cx, bh / Hq, bh % Hq, i, out + row * HEAD_DIM);
+        attend_row_exact(&cx, bh / Hq, bh % Hq, i, out + row * HEAD_DIM, NULL);
     }
     free(mean);
+    return 0;
+}
+
+/*
+ * oracle_p8_codes: the FP8 P byte of n (acc, sig, m) triples, as the forward
+ * computes it (entry "Phase 1 State-Ownership Decision": exact FP8 score
+ * bytes): s2 = fl(acc * sig), then E4M3(fl(fl(exp2(fl(s2 - m))) * 448)) with
+ * a correctly rounded exp2.  acc holds exact integers (as FP32 values), sig
+ * the block scale product, m the running maximum after the tile.
+ */
+int oracle_p8_codes(long n, const float *acc, const float *sig, const float *m, uint8_t *out)
+{
+    if (n < 0)
+        return -1;
+#pragma omp parallel for schedule(static)
+    for (long e = 0; e < n; ++e)
+        out[e] = p8_of(acc[e] * sig[e], m[e]);
+    return 0;
+}
+
+/*
+ * oracle_tile_state: the checked intermediates after KV tile `tile` (entry
+ * "Phase 2B Fixed Aligned Numerical Prototype": m, rescale, d, FP32 RO,
+ * reciprocal) for the query rows q0 .. q0 + 127 of (batch b, query head h),
+ * from the same per-row recurrence as oracle_forward.  Per row r (query
+ * q0 + r; rows >= Nq stay zero):
+ *   st[r][0] = m after the tile, st[r][1] = the tile's alpha,
+ *   st[r][2] = d after the tile, st[r][3] = d after the last tile,
+ *   st[r][4] = the final reciprocal 1 / d, st[r][5] = 1 if the row visited
+ *              the tile (rows whose kept keys end earlier do not)
+ *   ro[r][c] = RO after the tile.
+ */
+int oracle_tile_state(int B, int Hq, int Hkv, int Nq, int Nkv, int causal, float sm_scale, int tile,
+                      const int8_t *q_codes, const float *q_scales, const int8_t *k_codes,
+                      const float *k_scales, const uint8_t *v_codes, const float *v_scales, int b,
+                      int h, int q0, int which, double *st, double *ro)
+{
+    if (check_shape(B, Hq, Hkv, Nq, Nkv, causal, tile) || b < 0 || b >= B || h < 0 || h >= Hq ||
+        q0 < 0 || q0 >= Nq || which < 0)
+        return -1;
+    ctx_t cx;
+    setup_quant(&cx, B, Hq, Hkv, Nq, Nkv, causal, sm_scale, tile, q_codes, q_scales, k_codes,
+                k_scales, v_codes, v_scales);
+    memset(st, 0, sizeof(double) * 128 * 6);
+    memset(ro, 0, sizeof(double) * 128 * HEAD_DIM);
+    for (int r = 0; r < 128 && q0 + r < Nq; ++r) {
+        row_rec_t rec;
+        memset(&rec, 0, sizeof rec);
+        rec.tile = which;
+        float o[HEAD_DIM];
+        attend_row_quant(&cx, b, h, q0 + r, o, &rec);
+        st[r * 6 + 0] = rec.m;
+        st[r * 6 + 1] = rec.alpha;
+        st[r * 6 + 2] = rec.d;
+        st[r * 6 + 3] = rec.d_final;
+        st[r * 6 + 4] = rec.rcp;
+        st[r * 6 + 5] = rec.reached;
+        for (int c = 0; c < HEAD_DIM; ++c)
+            ro[(size_t)r * HEAD_DIM + c] = rec.ro[c];
+    }
+    return 0;
+}
+
+/* oracle_exp2_rn: FP32 2^x correctly rounded (the exp2 of the P step), for
+ * n values. */
+int oracle_exp2_rn(long n, const float *x, float *out)
+{
+    if (n < 0)
+        return -1;
+#pragma omp parallel for schedule(static)
+    for (long e = 0; e < n; ++e)
+        out[e] = exp2_rn(x[e]);
     return 0;
 }
