@@ -229,6 +229,28 @@ int sattn_test_forward_withhold_v(const sattn_shape *shape, const int8_t *q_code
 int sattn_test_int8_quantiser(uint32_t amax_lo, uint32_t amax_hi, unsigned long long *result, void *stream);
 
 /*
+ * sattn_test_p8_codes -- test hook, not part of the computation: the FP8 P
+ * bytes that sattn_forward writes for n_groups groups of 32 keys, through the
+ * forward kernel's own per-block function.  Group i has raw QK accumulators
+ * acc[32i .. 32i + 31] (FP32 values; any finite value or -inf, not only the
+ * integers the forward produces), block scale product sig[i] and running
+ * maximum m[i] (finite).  Byte 32i + k of `out` is
+ * E4M3(fl(fl(2^fl(fl(acc * sig) - m)) * 448)) with a correctly rounded 2^x
+ * (the P step of the arithmetic above).  Device arrays; acc and out 16-byte
+ * aligned; results valid after the stream synchronises.
+ */
+int sattn_test_p8_codes(int n_groups, const float *acc, const float *sig, const float *m, uint8_t *out,
+                        void *stream);
+
+/*
+ * sattn_test_exp2 -- test hook, not part of the computation: the correctly
+ * rounded FP32 2^x that sattn_forward uses for the rare FP8 P bytes its fast
+ * path cannot decide, elementwise over n device floats (x <= 0.5; x <= -40
+ * gives 0).  Results valid after the stream synchronises.
+ */
+int sattn_test_exp2(int n, const float *x, float *out, void *stream);
+
+/*
  * sattn_test_host_chunks -- test hook, not part of the computation: the
  * chunk plan sattn_attention_host uses for `shape` on a device with `n_sm`
  * SMs.  Pure host function.

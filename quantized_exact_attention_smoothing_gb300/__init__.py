@@ -4,13 +4,13 @@ The computation lives in libsattn.so (hand-written sm_103a CUDA kernels behind
 the C ABI of include/sattn.h); this package is its Python binding.
 """
 from ._binding import (HEAD_DIM, KV_TILE, NOALLOC_SCRATCH_BYTES, QBLOCK, STATUS, Graph, SattnError, attention,
-                       attention_host, check_status, declared_functions, forward, forward_q_bf16,
+                       attention_host, check_status, declared_functions, exp2_for_test, forward, forward_q_bf16,
                        forward_withhold_v_for_test, int8_quantiser_sweep_for_test, library_path, load_library,
-                       make_shape, prepare, prepare_buffers, prepare_kv, prepare_noalloc, query_sizes, sattn_shape,
-                       sattn_sizes)
+                       make_shape, p8_codes_for_test, prepare, prepare_buffers, prepare_kv, prepare_noalloc,
+                       query_sizes, sattn_shape, sattn_sizes)
 
 __all__ = ["HEAD_DIM", "KV_TILE", "NOALLOC_SCRATCH_BYTES", "QBLOCK", "STATUS", "Graph", "SattnError", "attention",
-           "attention_host", "check_status", "declared_functions", "forward", "forward_q_bf16",
+           "attention_host", "check_status", "declared_functions", "exp2_for_test", "forward", "forward_q_bf16",
            "forward_withhold_v_for_test", "int8_quantiser_sweep_for_test", "library_path", "load_library",
-           "make_shape", "prepare", "prepare_buffers", "prepare_kv", "prepare_noalloc", "query_sizes",
-           "sattn_shape", "sattn_sizes"]
+           "make_shape", "p8_codes_for_test", "prepare", "prepare_buffers", "prepare_kv", "prepare_noalloc",
+           "query_sizes", "sattn_shape", "sattn_sizes"]

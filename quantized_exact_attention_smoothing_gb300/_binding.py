@@ -75,6 +75,8 @@ def load_library(build: bool = True):
     lib.sattn_forward_q_bf16.argtypes = [SP] + [P] * 8
     lib.sattn_check_status.argtypes = [P, P]
     lib.sattn_test_int8_quantiser.argtypes = [ctypes.c_uint32, ctypes.c_uint32, P, P]
+    lib.sattn_test_p8_codes.argtypes = [ctypes.c_int, P, P, P, P, P]
+    lib.sattn_test_exp2.argtypes = [ctypes.c_int, P, P, P]
     lib.sattn_graph_create.argtypes = [SP] + [P] * 13 + [ctypes.POINTER(ctypes.c_void_p)]
     lib.sattn_test_host_chunks.argtypes = [SP, ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
                                            ctypes.POINTER(ctypes.c_int)]
@@ -86,7 +88,7 @@ def load_library(build: bool = True):
     for name in ("sattn_query_sizes", "sattn_prepare", "sattn_forward", "sattn_check_status",
                  "sattn_attention_host", "sattn_prepare_noalloc", "sattn_prepare_kv", "sattn_forward_q_bf16",
                  "sattn_test_int8_quantiser", "sattn_graph_create", "sattn_graph_launch", "sattn_graph_destroy",
-                 "sattn_test_host_chunks"):
+                 "sattn_test_host_chunks", "sattn_test_p8_codes", "sattn_test_exp2"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -330,6 +332,32 @@ def int8_quantiser_sweep_for_test(amax_lo: int = 1, amax_hi: int = 0x7f80, devic
         raise SattnError(rc, "sattn_test_int8_quantiser")
     bad, near, last = (int(v) for v in res[:3].cpu())
     return bad, near, last
+
+
+def p8_codes_for_test(acc: torch.Tensor, sig: torch.Tensor, m: torch.Tensor) -> torch.Tensor:
+    """sattn_test_p8_codes: the forward's FP8 P bytes for groups of 32 keys
+    (acc [G, 32], sig [G], m [G], FP32 CUDA tensors); returns uint8 [G, 32]."""
+    _need_cuda(acc, sig, m)
+    G = acc.shape[0]
+    if acc.dtype != torch.float32 or tuple(acc.shape) != (G, 32) or sig.shape != (G,) or m.shape != (G,):
+        raise ValueError("acc [G, 32], sig [G], m [G] FP32")
+    out = torch.empty((G, 32), dtype=torch.uint8, device=acc.device)
+    rc = load_library().sattn_test_p8_codes(G, _ptr(acc), _ptr(sig), _ptr(m), _ptr(out), _stream(None))
+    if rc != 0:
+        raise SattnError(rc, "sattn_test_p8_codes")
+    return out
+
+
+def exp2_for_test(x: torch.Tensor) -> torch.Tensor:
+    """sattn_test_exp2: the forward's correctly rounded 2^x (FP32 CUDA tensor)."""
+    _need_cuda(x)
+    if x.dtype != torch.float32:
+        raise ValueError("x must be FP32")
+    out = torch.empty_like(x)
+    rc = load_library().sattn_test_exp2(x.numel(), _ptr(x), _ptr(out), _stream(None))
+    if rc != 0:
+        raise SattnError(rc, "sattn_test_exp2")
+    return out
 
 
 class Graph:

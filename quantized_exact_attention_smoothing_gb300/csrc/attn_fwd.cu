@@ -46,6 +46,16 @@
 // every partial sum an integer below 2^21, so the FP32 accumulator holds the
 // exact int32 dot product.
 //
+// Exactness of P: the FP8 byte of a key is E4M3(fl(fl(2^dd) * 448)) with
+// dd = fl(fl(acc * sig) - m), s2 and dd rounded exactly as stated (packed FP32
+// pairs), and 2^dd from ex2.approx, whose relative error is below 2^-22.7 over
+// the range used (measured for every FP32 input).  The byte is taken from
+// 2^dd * 448 * (1 + 2^-20) and 2^dd * 448 * (1 - 2^-20): the bracket holds the
+// exact value, so when both give the same byte (rounding is monotonic) that is
+// the byte.  Otherwise (within 2^-20 of an E4M3 rounding midpoint, about
+// 3e-5 of the keys) the byte is recomputed with a correctly rounded exp2,
+// after the tile's P pass (see the compute warpgroups).
+//
 // Every mbarrier wait is bounded: after about a second, or as soon as another
 // CTA has reported a failure, the thread records the failure in the status
 // word, stops, waits for its own copies and MMAs in flight, and the CTA frees
@@ -139,6 +149,8 @@ enum Site : uint32_t {
 
 struct FwdParams {
     const int8_t *q_codes;
+    const __nv_bfloat16 *q_bf16;   // in-kernel Q quantisation: the BF16 Q [B*Hq][Nq][128]
+    const int8_t *k_codes;   // INT8 K codes [B*Hkv][nk32][128] (the rare exact path recomputes a score from them)
     const float *q_scales, *k_scales, *v_scales;
     __nv_bfloat16 *out;
     uint32_t *status;
@@ -146,7 +158,7 @@ struct FwdParams {
     int withhold_v;   // test hook: the V loader stages the first Q tile and loads no V
     // reciprocals for exact division by Hq * B, Hq and group (see udiv)
     unsigned long long m_hb, m_hq, m_group;
-    int nq32, nbq, nbk;
+    int nq32, nbq, nbk, nk32;
     float c0;
 #ifdef SATTN_DEBUG_DUMP
     // intermediates of query tile 0 of (batch 0, head 0), KV tile 0:
@@ -158,6 +170,11 @@ struct FwdParams {
 };
 
 #ifdef SATTN_DEBUG_DUMP
+// Debug dump: KV tile 0 of query tile 0 of (batch 0, head 0) as described in
+// FwdParams; the state after KV tile 1 of the same item (running maximum,
+// alpha, d after the outer update, [128] each, and RO after it [128][128]);
+// d and its reciprocal at the end of the item [128] each.
+constexpr int DBG_M1 = 83000, DBG_A1 = 83128, DBG_D1 = 83256, DBG_RO1 = 83384, DBG_DF = 99768, DBG_RCP = 99896;
 // Debug builds only: SM clock stamps of one CTA (the first in launch order:
 // the last query tile, batch 0, head 0), event `id` of KV tile `j`.
 #define SATTN_TRACE(p, t, id, j)                                                                 \
@@ -253,6 +270,247 @@ __device__ __forceinline__ Tile item_tile(const FwdParams &p, int it)
     t.trace = (blockIdx.x == 0);
     t.g0 = 0;
     return t;
+}
+
+// ---------------------------------------------------------------- the P step
+//
+// 2^x correctly rounded to FP32, for the rare keys whose FP8 byte the bracket
+// of the fast path cannot decide.  Written from the Taylor series of e^t with
+// t = r ln 2, x = n + r (n the nearest integer, |r| <= 1/2, both exact), in
+// "float-float" arithmetic: each quantity is an unevaluated sum of two FP32
+// values, products split exactly with a fused multiply-add (Dekker) and sums
+// renormalised with the fast two-sum (Dekker; Knuth).  Terms up to t^7 / 7!
+// are carried in float-float, the tail from t^8 / 8! to t^12 / 12! in FP32
+// (its weight t^8 <= 2^-12 keeps its rounding below 2^-47); the result is
+// within about 2^-44 of 2^r, so its FP32 rounding is the correctly rounded one
+// unless 2^x lies that close to a point halfway between two FP32 values.
+// The constants are ln 2 and 1/k! split into FP32 high and low parts.
+// x <= -40 (and -inf) gives 0, which every FP8 byte of 448 * 2^x agrees with.
+__device__ __forceinline__ void fast_two_sum(float a, float b, float &s, float &e)
+{
+    s = __fadd_rn(a, b);
+    e = __fadd_rn(b, __fsub_rn(a, s));
+}
+
+// (ph, pl) <- (ch, cl) + (th, tl) * (ph, pl), for |c| > |t * p|
+__device__ __forceinline__ void ff_horner_step(float &ph, float &pl, float th, float tl, float ch, float cl)
+{
+    const float mh = __fmul_rn(ph, th);
+    float ml = __fmaf_rn(ph, th, -mh);
+    ml = __fmaf_rn(ph, tl, ml);
+    ml = __fmaf_rn(pl, th, ml);
+    float s, e;
+    fast_two_sum(ch, mh, s, e);
+    e = __fadd_rn(e, __fadd_rn(ml, cl));
+    fast_two_sum(s, e, ph, pl);
+}
+
+__device__ __forceinline__ float exp2_rn(float x)
+{
+    if (!(x > -40.0f))
+        return 0.0f;
+    const float n = rintf(x);
+    const float r = __fsub_rn(x, n);
+    const float L1 = 0x1.62e430p-1f, L2 = -0x1.05c610p-29f;   // ln 2 = L1 + L2 + O(2^-54)
+    float th = __fmul_rn(r, L1);
+    float tl = __fmaf_rn(r, L1, -th);
+    tl = __fmaf_rn(r, L2, tl);
+    fast_two_sum(th, tl, th, tl);
+    // tail sum_{k=8..12} t^(k-8) / k!
+    float q = 0x1.1eed8ep-29f;               // 1/12!
+    q = __fmaf_rn(q, th, 0x1.ae6456p-26f);   // 1/11!
+    q = __fmaf_rn(q, th, 0x1.27e4fcp-22f);   // 1/10!
+    q = __fmaf_rn(q, th, 0x1.71de3ap-19f);   // 1/9!
+    q = __fmaf_rn(q, th, 0x1.a01a02p-16f);   // 1/8!
+    float ph = q, pl = 0.0f;
+    ff_horner_step(ph, pl, th, tl, 0x1.a01a02p-13f, -0x1.7f97fap-39f);   // 1/7!
+    ff_horner_step(ph, pl, th, tl, 0x1.6c16c2p-10f, -0x1.27d27ep-35f);   // 1/6!
+    ff_horner_step(ph, pl, th, tl, 0x1.111112p-7f, -0x1.dddddep-32f);    // 1/5!
+    ff_horner_step(ph, pl, th, tl, 0x1.555556p-5f, -0x1.555556p-30f);    // 1/4!
+    ff_horner_step(ph, pl, th, tl, 0x1.555556p-3f, -0x1.555556p-28f);    // 1/3!
+    ff_horner_step(ph, pl, th, tl, 0.5f, 0.0f);                           // 1/2!
+    ff_horner_step(ph, pl, th, tl, 1.0f, 0.0f);                           // 1/1!
+    ff_horner_step(ph, pl, th, tl, 1.0f, 0.0f);                           // 1/0!
+    // ph = RN(ph + pl) after the renormalisation; scale by 2^n (exact, n >= -40)
+    return __fmul_rn(ph, __int_as_float((static_cast<int>(n) + 127) << 23));
+}
+
+// The FP8 byte of one key, every step in the stated order (the slow path).
+__device__ __forceinline__ uint32_t p8_exact(float acc, float sig, float mu)
+{
+    const float dd = __fsub_rn(__fmul_rn(acc, sig), mu);
+    return ptx::cvt_e4m3x2(0.0f, __fmul_rn(exp2_rn(dd), 448.0f)) & 0xffu;
+}
+
+constexpr float kP8Hi = 448.0f * (1.0f + 0x1p-20f), kP8Lo = 448.0f * (1.0f - 0x1p-20f);   // both exact in FP32
+
+// FP8 P bytes of 32 keys (one block of the tile: raw accumulators x as FP32
+// bit patterns, -inf for masked keys) with block scale product sig and running
+// maximum mu (finite), four bytes per word, key 4w + u in byte u of word w.
+// s2 = fl(x * sig), dd = fl(s2 - mu) in packed pairs; the bytes of
+// 2^dd * 448 * (1 + 2^-20) (the result) and of 2^dd * 448 * (1 - 2^-20)
+// (compared, not kept); keys whose two bytes differ are recomputed with
+// p8_exact (per lane, rare), after recomputing the lower bytes of the block.
+__device__ __forceinline__ void p8_words4(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3, uint64_t sg2,
+                                          uint64_t m2, uint32_t &hi, uint32_t &lo)
+{
+    const uint64_t hi2 = ptx::f32x2(kP8Hi, kP8Hi), lo2 = ptx::f32x2(kP8Lo, kP8Lo);
+    const uint64_t d01 = ptx::sub_f32x2(ptx::mul_f32x2(ptx::f32x2(__uint_as_float(x0), __uint_as_float(x1)), sg2), m2);
+    const uint64_t d23 = ptx::sub_f32x2(ptx::mul_f32x2(ptx::f32x2(__uint_as_float(x2), __uint_as_float(x3)), sg2), m2);
+    const uint64_t e01 = ptx::f32x2(ptx::ex2_approx(ptx::f32x2_lo(d01)), ptx::ex2_approx(ptx::f32x2_hi(d01)));
+    const uint64_t e23 = ptx::f32x2(ptx::ex2_approx(ptx::f32x2_lo(d23)), ptx::ex2_approx(ptx::f32x2_hi(d23)));
+    const uint64_t p01 = ptx::mul_f32x2(e01, hi2), p23 = ptx::mul_f32x2(e23, hi2);
+    const uint64_t n01 = ptx::mul_f32x2(e01, lo2), n23 = ptx::mul_f32x2(e23, lo2);
+    hi = ptx::cvt_e4m3x4(ptx::f32x2_lo(p01), ptx::f32x2_hi(p01), ptx::f32x2_lo(p23), ptx::f32x2_hi(p23));
+    lo = ptx::cvt_e4m3x4(ptx::f32x2_lo(n01), ptx::f32x2_hi(n01), ptx::f32x2_lo(n23), ptx::f32x2_hi(n23));
+}
+
+__device__ __forceinline__ void p8_words(const uint32_t (&x)[32], int w, uint64_t sg2, uint64_t m2, uint32_t &hi,
+                                         uint32_t &lo)
+{
+    p8_words4(x[4 * w], x[4 * w + 1], x[4 * w + 2], x[4 * w + 3], sg2, m2, hi, lo);
+}
+
+// Fast path of one block: the result bytes (upper bracket) in `out`; the
+// return value is nonzero if any key's two brackets differ.
+__device__ __forceinline__ uint32_t p8_block_fast(const uint32_t (&x)[32], float sig, float mu, uint32_t (&out)[8])
+{
+    const uint64_t sg2 = ptx::f32x2(sig, sig), m2 = ptx::f32x2(mu, mu);
+    uint32_t diff = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        uint32_t lo;
+        p8_words(x, w, sg2, m2, out[w], lo);
+        diff |= out[w] ^ lo;
+    }
+    return diff;
+}
+
+// Fix-up of one block (rare): the bytes again, with the undecided keys
+// recomputed by p8_exact.
+__device__ __forceinline__ void p8_block_fix(const uint32_t (&x)[32], float sig, float mu, uint32_t (&out)[8])
+{
+    const uint64_t sg2 = ptx::f32x2(sig, sig), m2 = ptx::f32x2(mu, mu);
+    uint32_t flags = 0;   // bit 4w + u: byte u of word w undecided
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        uint32_t lo;
+        p8_words(x, w, sg2, m2, out[w], lo);
+        const uint32_t dw = out[w] ^ lo;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            flags |= (((dw >> (8 * u)) & 0xffu) != 0u ? 1u : 0u) << (4 * w + u);
+    }
+    while (flags != 0u) {
+        const int k = __ffs(flags) - 1;
+        flags &= flags - 1u;
+        uint32_t xk = 0;
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            xk = (e == k) ? x[e] : xk;
+        const uint32_t code = p8_exact(__uint_as_float(xk), sig, mu);
+        const uint32_t sh = 8u * static_cast<uint32_t>(k & 3);
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+            if ((k >> 2) == w)
+                out[w] = (out[w] & ~(0xffu << sh)) | (code << sh);
+    }
+}
+
+// Fix-up of one block whose 32 accumulators lie in shared memory at `slot`
+// (value e at slot + 16 * ((e / 4) ^ (lane % 8)) + 4 * (e % 4)); the words
+// of the block as written by the fast path are in `out`, and are rewritten
+// with the undecided keys recomputed by p8_exact.
+__device__ void p8_block_fix_smem(uint32_t slot, int lane, float sig, float mu, uint32_t (&out)[8])
+{
+    const uint64_t sg2 = ptx::f32x2(sig, sig), m2 = ptx::f32x2(mu, mu);
+#pragma unroll 1
+    for (int w = 0; w < 8; ++w) {
+        const uint4 a = ptx::ld_shared_v4(slot + 16u * static_cast<uint32_t>(w ^ (lane & 7)));
+        uint32_t hi, lo;
+        p8_words4(a.x, a.y, a.z, a.w, sg2, m2, hi, lo);
+        uint32_t dw = hi ^ lo, word = hi;
+        const uint32_t xs[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (((dw >> (8 * u)) & 0xffu) != 0u)
+                word = (word & ~(0xffu << (8 * u))) | (p8_exact(__uint_as_float(xs[u]), sig, mu) << (8 * u));
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+            if (v == w)
+                out[v] = word;
+    }
+}
+
+// The raw QK accumulator (exact int32 dot product of the codes) of key `key`
+// for query row r of the item: K from the INT8 codes in global memory; Q from
+// the prepared INT8 codes, or, with in-kernel Q quantisation, quantised again
+// from the BF16 Q with the row's block scale sq by the preparation's own
+// quantiser (the Q carrier in shared memory may already hold the next item).
+__device__ int dot_row_key(const FwdParams &p, const Tile &t, int r, int key, float sq)
+{
+    const uint4 *kr = reinterpret_cast<const uint4 *>(p.k_codes +
+                                                      (static_cast<size_t>(t.b * p.Hkv + t.hk) * p.nk32 + key) * HD);
+    int acc = 0;
+    if (p.q_codes) {
+        const uint4 *qr = reinterpret_cast<const uint4 *>(
+            p.q_codes + (static_cast<size_t>(t.b * p.Hq + t.hq) * p.nq32 + t.q0 + r) * HD);
+#pragma unroll 2
+        for (int v = 0; v < 8; ++v) {
+            const uint4 qv = __ldg(qr + v), kv = __ldg(kr + v);
+            acc = __dp4a(static_cast<int>(qv.x), static_cast<int>(kv.x), acc);
+            acc = __dp4a(static_cast<int>(qv.y), static_cast<int>(kv.y), acc);
+            acc = __dp4a(static_cast<int>(qv.z), static_cast<int>(kv.z), acc);
+            acc = __dp4a(static_cast<int>(qv.w), static_cast<int>(kv.w), acc);
+        }
+        return acc;
+    }
+    if (!(sq > 0.0f) || t.q0 + r >= p.Nq)   // a zero block scale, or a pad row: every code is 0
+        return 0;
+    const float rs = __frcp_rn(sq);
+    const uint4 *qr = reinterpret_cast<const uint4 *>(p.q_bf16 + (static_cast<size_t>(t.b * p.Hq + t.hq) * p.Nq + t.q0 + r) * HD);
+#pragma unroll 2
+    for (int v = 0; v < 8; ++v) {   // 16 channels: two 16-byte chunks of BF16 Q, one of K codes
+        const uint4 kv = __ldg(kr + v);
+        const uint2 c0 = int8_codes8(__ldg(qr + 2 * v), sq, rs), c1 = int8_codes8(__ldg(qr + 2 * v + 1), sq, rs);
+        acc = __dp4a(static_cast<int>(c0.x), static_cast<int>(kv.x), acc);
+        acc = __dp4a(static_cast<int>(c0.y), static_cast<int>(kv.y), acc);
+        acc = __dp4a(static_cast<int>(c1.x), static_cast<int>(kv.z), acc);
+        acc = __dp4a(static_cast<int>(c1.y), static_cast<int>(kv.w), acc);
+    }
+    return acc;
+}
+
+// Fix-up of one block whose accumulators were not kept: each key's
+// accumulator is recomputed from the codes (keys from `nvalid` on, the
+// masked ones, are -inf), its two brackets compared, and an undecided byte
+// recomputed by p8_exact.  Few registers; the rare case of the rare case.
+__device__ void p8_block_fix_codes(const FwdParams &p, const Tile &t, int r, int key0, int nvalid, float sq,
+                                   float sig, float mu, uint32_t (&out)[8])
+{
+    const uint64_t sg2 = ptx::f32x2(sig, sig), m2 = ptx::f32x2(mu, mu);
+#pragma unroll 1
+    for (int k = 0; k < 32; ++k) {
+        const uint32_t xk = k < nvalid ? __float_as_uint(static_cast<float>(dot_row_key(p, t, r, key0 + k, sq)))
+                                       : 0xff800000u;
+        uint32_t hi, lo;
+        p8_words4(xk, xk, xk, xk, sg2, m2, hi, lo);
+        uint32_t code = hi & 0xffu;
+        if ((hi ^ lo) & 0xffu)
+            code = p8_exact(__uint_as_float(xk), sig, mu);
+        const uint32_t sh = 8u * static_cast<uint32_t>(k & 3);
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+            if ((k >> 2) == w)
+                out[w] = (out[w] & ~(0xffu << sh)) | (code << sh);
+    }
+}
+
+// Both, for one block (the test hook's entry).
+__device__ __forceinline__ void p8_block(const uint32_t (&x)[32], float sig, float mu, uint32_t (&out)[8])
+{
+    if (p8_block_fast(x, sig, mu, out) != 0u)
+        p8_block_fix(x, sig, mu, out);
 }
 
 // K loader.  Half-tile u = 2 * (tile) + h (channels [64h, 64h + 64) of the
@@ -581,7 +839,6 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
     const int r = quarter * 32 + lane;                        // query row in the tile = TMEM lane
     const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t maxx = sb + OFF_MAXX;                      // [tile parity][half][row] row maxima
-    constexpr float kLog2_448 = 8.8073549220576041f;          // log2(448): P is stored as p * 448
 
     auto qscale = [&](const Tile &tq) {
         const int i = tq.q0 + r;
@@ -617,6 +874,9 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
 
     float ro[64];
     float m, d, alpha_prev;
+#ifdef SATTN_DEBUG_DUMP
+    float m_tile1 = 0.0f;   // running maximum after KV tile 1 of the dumped item
+#endif
     // RO = RO * alpha + PV partial of global tile gg (this half's 64 channels), d likewise
     auto fold_partial = [&](int gg, int jl, const Tile &tt, float alpha) -> bool {
         if (!wt.wait(bar(PVFULL), gg & 1, SITE_PV))
@@ -645,6 +905,17 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
         for (int c = 0; c < 64; ++c)
             ro[c] = fmaf(ro[c], alpha, __uint_as_float(part[c >> 5][c & 31]));
         d = fmaf(d, alpha, __uint_as_float(ds));
+#ifdef SATTN_DEBUG_DUMP
+        if (p.dbg && jl == 1 && tt.q0 == 0 && tt.hq == 0 && tt.b == 0) {   // the state after KV tile 1
+            for (int c = 0; c < 64; ++c)
+                p.dbg[DBG_RO1 + r * HD + 64 * half + c] = ro[c];
+            if (half == 0) {
+                p.dbg[DBG_M1 + r] = m_tile1;
+                p.dbg[DBG_A1 + r] = alpha;
+                p.dbg[DBG_D1 + r] = d;
+            }
+        }
+#endif
         if (r == 0 && half == 0)
             SATTN_TRACE(p, tt, 7, jl);
         return true;
@@ -662,7 +933,7 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
         m = -INFINITY;
         d = 0.0f;
         alpha_prev = 0.0f;
-#pragma unroll
+    #pragma unroll
         for (int c = 0; c < 64; ++c)
             ro[c] = 0.0f;
 
@@ -759,41 +1030,81 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
 
             const float mn = fmaxf(m, tmax);
             const float alpha = (m == -INFINITY) ? 0.0f : ptx::ex2_approx(__fsub_rn(m, mn));
-            // exponent offset of p * 448; a row with no kept key so far has
-            // mn = -inf and only -inf scores, which any finite offset maps to 0
-            const float nb = (mn == -INFINITY) ? 0.0f : kLog2_448 - mn;
-
-            // P8 = E4M3(exp2(acc * sig - m') * 448), four keys per 32-bit word,
-            // written 32 keys (8 columns) at a time into TMEM columns
-            // [TM_P + 32h, TM_P + 32h + 32) of this row's lane, where PV reads
-            // them as its A operand; the columns are free once the previous PV
-            // has completed
-            auto p_block = [&](int c) {
+            // P8 = E4M3(fl(fl(2^fl(fl(acc * sig) - m')) * 448)), four keys per
+            // 32-bit word, written 32 keys (8 columns) at a time into TMEM
+            // columns [TM_P + 32h, TM_P + 32h + 32) of this row's lane, where PV
+            // reads them as its A operand; the columns are free once the
+            // previous PV has completed.  A row with no kept key so far (mn =
+            // -inf) has only -inf scores, which any finite maximum maps to 0.
+            const float mu = (mn == -INFINITY) ? 0.0f : mn;
+            // Rare (about 3e-5 of the keys): a key within 2^-20 of an E4M3
+            // rounding midpoint.  Without any branch in this loop, a lane parks
+            // the accumulators of its first such block (predicated stores) in
+            // its 128-byte slot of the warp's own output staging slice, idle
+            // until the item's final conversion; further blocks, and all blocks
+            // with in-kernel Q quantisation (which stages Q there), are marked
+            // for a recomputation from the codes.  After the tile's P the warp
+            // (one vote) rewrites those blocks with the undecided keys
+            // recomputed by p8_exact.
+            const uint32_t slot = sb + OFF_STG + (quarter * 2 + half) * 4096 + lane * 128;
+            if (!kFuseQ && j == 0) {   // the previous item's output store has read the slice
+                if (lane == 0)
+                    ptx::bulk_wait_read();
+                __syncwarp();
+            }
+            int parked = -1;          // block parked in the slot
+            uint32_t recompute = 0;   // bit c: block c undecided, not parked
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
                 uint32_t pk[8];
-#pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    float e[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        e[u] = ptx::ex2_approx(fmaf(__uint_as_float(s[c][4 * w + u]), sig[c], nb));
-                    pk[w] = ptx::cvt_e4m3x4(e[0], e[1], e[2], e[3]);
-                }
-#ifdef SATTN_DEBUG_DUMP
-                if (p.dbg && j == 0 && t.q0 == 0 && t.hq == 0 && t.b == 0)
-                    for (int w = 0; w < 8; ++w)
-                        p.dbg[32768 + r * 64 + 32 * half + 8 * c + w] = __uint_as_float(pk[w]);
-#endif
+                const uint32_t undecided = p8_block_fast(s[c], sig[c], mu, pk);
                 if (c == 0 && gj >= 1 && !wt.wait(bar(PDONE), (gj - 1) & 1, SITE_PDONE))
                     return false;
                 ptx::tmem_st8(taddr + TM_P + 32 * half + 8 * c, pk);
-                return true;
-            };
-            bool p_ok = true;
+                const bool park = !kFuseQ && undecided != 0u && parked < 0;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                p_ok = p_ok && p_block(c);
-            if (!p_ok)
-                return false;
+                for (int w = 0; w < 8; ++w)
+                    ptx::st_shared_v4_if(park, slot + 16u * static_cast<uint32_t>(w ^ (lane & 7)), s[c][4 * w],
+                                         s[c][4 * w + 1], s[c][4 * w + 2], s[c][4 * w + 3]);
+                parked = park ? c : parked;
+                recompute |= (undecided != 0u && !park) ? (1u << c) : 0u;
+            }
+            if (__any_sync(0xffffffffu, parked >= 0 || recompute != 0u)) {
+                ptx::tmem_wait_st();   // the first stores are complete before blocks are read back
+                const int lo = j * BN + 128 * half;
+                const int nvalid = (j >= t.mask_from) ? max(0, min(128, min(p.Nkv - 1, lim) - lo + 1)) : 128;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    const bool mine = parked == c || ((recompute >> c) & 1u);
+                    if (!__any_sync(0xffffffffu, mine))
+                        continue;
+#ifdef SATTN_DEBUG_DUMP
+                    if (p.dbg && mine)
+                        atomicAdd(p.dbg + 60000, 1.0f);   // undecided blocks seen
+#endif
+                    const float sg = (c == 0) ? sig[0] : (c == 1) ? sig[1] : (c == 2) ? sig[2] : sig[3];
+                    uint32_t pk[8];
+                    ptx::tmem_ld8(taddr + TM_P + 32 * half + 8 * c, pk);
+                    ptx::tmem_wait_ld();
+                    if (parked == c)
+                        p8_block_fix_smem(slot, lane, sg, mu, pk);
+                    else if (mine)
+                        p8_block_fix_codes(p, t, r, lo + 32 * c, nvalid - 32 * c, sq, sg, mu, pk);
+                    ptx::tmem_st8(taddr + TM_P + 32 * half + 8 * c, pk);
+                }
+            }
+#ifdef SATTN_DEBUG_DUMP
+            if (p.dbg && j == 0 && t.q0 == 0 && t.hq == 0 && t.b == 0) {   // the bytes as PV will read them
+                ptx::tmem_wait_st();
+                uint32_t w32[32];
+                ptx::tmem_ld32(taddr + TM_P + 32 * half, w32);
+                ptx::tmem_wait_ld();
+                for (int w = 0; w < 32; ++w)
+                    p.dbg[32768 + r * 64 + 32 * half + w] = __uint_as_float(w32[w]);
+            }
+            if (j == 1)
+                m_tile1 = mn;
+#endif
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(PFULL));
@@ -827,6 +1138,12 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
                 ptx::bulk_wait_read();
             __syncwarp();
             const float rcp = d > 0.0f ? __frcp_rn(d) : 0.0f;
+#ifdef SATTN_DEBUG_DUMP
+            if (p.dbg && t.q0 == 0 && t.hq == 0 && t.b == 0 && half == 0) {
+                p.dbg[DBG_DF + r] = d;
+                p.dbg[DBG_RCP + r] = rcp;
+            }
+#endif
             const uint32_t sv4 = sb + OFF_SV + (n % 3) * SV_BYTES + 4 * 64 * half;   // landed with this item's Q
             const uint32_t stage = sb + OFF_STG + (quarter * 2 + half) * 4096;
 #pragma unroll
@@ -1016,6 +1333,33 @@ __global__ void __launch_bounds__(256) k_carrier_kernel(const uint4 *__restrict_
     }
 }
 
+// Test kernels of the P step: FP8 bytes of groups of 32 keys through p8_block
+// (group i: accumulators acc[32i .. 32i + 31], block scale product sig[i],
+// running maximum m[i]), and exp2_rn elementwise.
+__global__ void __launch_bounds__(128) test_p8_kernel(int n_groups, const float *__restrict__ acc,
+                                                      const float *__restrict__ sig, const float *__restrict__ m,
+                                                      uint32_t *__restrict__ out)
+{
+    const int gi = blockIdx.x * blockDim.x + threadIdx.x;
+    if (gi >= n_groups)
+        return;
+    uint32_t x[32], w[8];
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+        x[k] = __float_as_uint(acc[static_cast<size_t>(gi) * 32 + k]);
+    p8_block(x, sig[gi], m[gi], w);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        out[static_cast<size_t>(gi) * 8 + k] = w[k];
+}
+
+__global__ void __launch_bounds__(256) test_exp2_kernel(int n, const float *__restrict__ x, float *__restrict__ out)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n)
+        out[i] = exp2_rn(x[i]);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1159,6 +1503,7 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const i
 
     FwdParams prm;
     prm.q_codes = kFuseQ ? nullptr : static_cast<const int8_t *>(q);
+    prm.q_bf16 = kFuseQ ? static_cast<const __nv_bfloat16 *>(q) : nullptr;
     prm.q_scales = q_scales;
     prm.k_scales = k_scales;
     prm.v_scales = v_scales;
@@ -1184,6 +1529,8 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const i
     prm.nq32 = static_cast<int>(g.nq32);
     prm.nbq = static_cast<int>(g.nbq);
     prm.nbk = static_cast<int>(g.nbk);
+    prm.nk32 = static_cast<int>(g.nk32);
+    prm.k_codes = k_codes;
     const float sm = g.sm_scale > 0.0f ? g.sm_scale : 1.0f / sqrtf(static_cast<float>(HD));
     prm.c0 = sm * 1.44269504088896340736f;
 #ifdef SATTN_DEBUG_DUMP
@@ -1225,6 +1572,24 @@ int launch_forward_q_bf16(const Geometry &g, const void *q, const int8_t *k_code
 {
     return launch_impl<true>(g, q, nullptr, k_codes, k_scales, v_codes, v_scales, out, status, carrier, stream,
                              false, true);
+}
+
+cudaError_t launch_test_p8_codes(int n_groups, const float *acc, const float *sig, const float *m, uint8_t *out,
+                                 cudaStream_t stream)
+{
+    if (n_groups < 1)
+        return cudaSuccess;
+    test_p8_kernel<<<(n_groups + 127) / 128, 128, 0, stream>>>(n_groups, acc, sig, m,
+                                                               reinterpret_cast<uint32_t *>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_test_exp2_rn(int n, const float *x, float *out, cudaStream_t stream)
+{
+    if (n < 1)
+        return cudaSuccess;
+    test_exp2_kernel<<<(n + 255) / 256, 256, 0, stream>>>(n, x, out);
+    return cudaGetLastError();
 }
 
 }  // namespace sattn

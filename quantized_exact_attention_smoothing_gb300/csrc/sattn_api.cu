@@ -475,6 +475,33 @@ int sattn_test_int8_quantiser(uint32_t amax_lo, uint32_t amax_hi, unsigned long 
                : SATTN_ERR_LAUNCH;
 }
 
+int sattn_test_p8_codes(int n_groups, const float *acc, const float *sig, const float *m, uint8_t *out,
+                        void *stream)
+{
+    if (n_groups < 0 || (n_groups > 0 && (!acc || !sig || !m || !out)))
+        return SATTN_ERR_INVALID;
+    if (!aligned16(acc) || !aligned16(out))
+        return SATTN_ERR_MISALIGNED;
+    const int dev = check_device();
+    if (dev != SATTN_OK)
+        return dev;
+    return sattn::launch_test_p8_codes(n_groups, acc, sig, m, out, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SATTN_OK
+               : SATTN_ERR_LAUNCH;
+}
+
+int sattn_test_exp2(int n, const float *x, float *out, void *stream)
+{
+    if (n < 0 || (n > 0 && (!x || !out)))
+        return SATTN_ERR_INVALID;
+    const int dev = check_device();
+    if (dev != SATTN_OK)
+        return dev;
+    return sattn::launch_test_exp2_rn(n, x, out, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SATTN_OK
+               : SATTN_ERR_LAUNCH;
+}
+
 int sattn_test_host_chunks(const sattn_shape *shape, int n_sm, int64_t *bounds, int *nchunks)
 {
     Geometry g;

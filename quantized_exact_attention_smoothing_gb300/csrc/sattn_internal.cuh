@@ -79,3 +79,12 @@ int launch_forward_q_bf16(const Geometry &g, const void *q, const int8_t *k_code
                           void *carrier, cudaStream_t stream);
 
 }  // namespace sattn
+
+namespace sattn {
+// Test hooks of the forward's P step (attn_fwd.cu): the FP8 P bytes of groups
+// of 32 keys sharing a block scale product and a running maximum, through the
+// kernel's own per-block function; and its correctly rounded exp2.
+cudaError_t launch_test_p8_codes(int n_groups, const float *acc, const float *sig, const float *m, uint8_t *out,
+                                 cudaStream_t stream);
+cudaError_t launch_test_exp2_rn(int n, const float *x, float *out, cudaStream_t stream);
+}  // namespace sattn

@@ -1,15 +1,19 @@
-"""GPU parity of the forward kernel's intermediates against the oracle, for the
-first KV tile of query tile 0 of (batch 0, head 0): the raw QK accumulators,
-the FP8 P bytes and the first PV partial.
+"""GPU parity of the forward kernel's intermediates against the oracle
+("Experiment Log" page, entry "Phase 2B Fixed Aligned Numerical Prototype":
+QK, m, d, FP8 probability, rescale, PV, FP32 RO, reciprocal), for query tile 0
+of (batch 0, head 0).
 
 A build with SATTN_DEBUG_DUMP (quantized_exact_attention_smoothing_gb300.build
 .build_debug) makes the kernel write them to a buffer set with
-sattn_debug_set_dump.  The accumulators must equal the oracle's exact int32
-dot products.  P8 must equal the oracle's bytes, except that a value within
-rounding distance of an E4M3 tie may take the neighbouring code (the kernel
-forms exp2's argument with one FMA and uses ex2.approx).  The PV partial
-must equal the oracle's, up to FP32 summation order and one E4M3 step of
-weight at each key whose P8 byte differs.
+sattn_debug_set_dump: for KV tile 0 (256 keys) the raw QK accumulators, the FP8
+P bytes and the PV partial; for KV tile 1 the running maximum, its rescale factor
+alpha, d and RO after the outer update; at the end d and its reciprocal.
+
+Exact: the accumulators (the int32 dot products), the P bytes, and the running
+maximum.  Within FP32 rounding: the PV partial (tensor-core summation order),
+alpha (hardware exp2, relative error below 2^-22), d and RO (the outer update
+is one fused multiply-add per value) and the reciprocal, which must also be
+the correctly rounded reciprocal of the kernel's own d.
 """
 import ctypes
 
@@ -23,6 +27,10 @@ import synth
 from helpers import to_device_bf16
 
 pytestmark = pytest.mark.gpu
+
+TILE = 256
+DBG_S, DBG_P8, DBG_PV, DBG_M1, DBG_A1, DBG_D1, DBG_RO1, DBG_DF, DBG_RCP = (
+    0, 32768, 40960, 83000, 83128, 83256, 83384, 99768, 99896)
 
 
 @pytest.fixture(scope="module")
@@ -43,7 +51,7 @@ def _run_dump(lib, q, k, v, causal):
     buf = bnd.prepare_buffers(shape, dq.device)
     out = torch.empty((Bn, Hq, Nq, 128), dtype=torch.bfloat16, device="cuda")
     fws = torch.zeros(bnd.query_sizes(shape)["forward_workspace"] // 4, dtype=torch.int32, device="cuda")
-    dump = torch.zeros(98304, dtype=torch.float32, device="cuda")
+    dump = torch.zeros(102400, dtype=torch.float32, device="cuda")
     s = bnd._stream(None)
     p = bnd._ptr
     assert lib.sattn_prepare(ctypes.byref(shape), p(dq), p(dk), p(dv), p(buf["q_codes"]), p(buf["q_scales"]),
@@ -58,46 +66,69 @@ def _run_dump(lib, q, k, v, causal):
         lib.sattn_debug_set_dump(None)
     assert int(fws[0]) == 0
     d = dump.cpu().numpy()
-    s_acc = d[:32768].reshape(128, 256)
-    p8 = d[32768:40960].view(np.uint32).reshape(128, 64).view(np.uint8).reshape(128, 256)
-    part = d[40960:40960 + 128 * 144].reshape(128, 144)
-    return s_acc, p8, part
+    return dict(
+        s=d[DBG_S:DBG_S + 128 * TILE].reshape(128, TILE),
+        p8=d[DBG_P8:DBG_P8 + 128 * 64].view(np.uint32).reshape(128, 64).view(np.uint8).reshape(128, TILE),
+        part=d[DBG_PV:DBG_PV + 128 * 144].reshape(128, 144),
+        m1=d[DBG_M1:DBG_M1 + 128], a1=d[DBG_A1:DBG_A1 + 128], d1=d[DBG_D1:DBG_D1 + 128],
+        ro1=d[DBG_RO1:DBG_RO1 + 128 * 128].reshape(128, 128),
+        dfin=d[DBG_DF:DBG_DF + 128], rcp=d[DBG_RCP:DBG_RCP + 128])
 
 
-@pytest.mark.parametrize("shape", [
-    (1, 1, 1, 128, 192, False),    # c1: 192 kept keys of 256, every row
-    (1, 1, 1, 128, 512, False),    # a full first tile
-    (1, 2, 1, 256, 256, True),     # the causal diagonal runs through the tile
-    (1, 1, 1, 100, 300, True)])    # ragged rows, bottom-right causal offset
-def test_first_tile_intermediates_match_the_oracle(oracle_mod, dbg_lib, shape):
+SHAPES = [
+    (1, 1, 1, 128, 192, False),    # c1: one tile, 192 kept keys of 256
+    (1, 1, 1, 128, 700, False),    # three tiles, the last ragged
+    (1, 2, 1, 256, 256, True),     # the causal diagonal runs through the only tile of query tile 0
+    (1, 1, 1, 100, 300, True),     # ragged rows, bottom-right causal offset: rows below 56 keep no key of tile 1
+    (1, 1, 1, 128, 512, False)]    # two full tiles
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_intermediates_match_the_oracle(oracle_mod, dbg_lib, shape):
     Bn, Hq, Hkv, Nq, Nkv, causal = shape
     w = synth.workload("c1", B=Bn, Hq=Hq, Hkv=Hkv, Nq=Nq, Nkv=Nkv, causal=causal)
     q, k, v = synth.make_inputs(w, seed=500 + Nkv)
-    s_acc, p8, part = _run_dump(dbg_lib, q, k, v, causal)
+    got = _run_dump(dbg_lib, q, k, v, causal)
     ref = oracle_mod.prepare(q, k, v)
-    acc_o, p8_o, _ = oracle_mod.first_tile(ref, Nq, Nkv, causal)
-    rows, n = min(Nq, 128), min(Nkv, 256)
+    acc_o, p8_o, part_o = oracle_mod.first_tile(ref, Nq, Nkv, causal, tile=TILE)
+    rows, n = min(Nq, 128), min(Nkv, TILE)
 
     # QK: exact integers, every key of the tile (pad keys read zero codes)
-    assert np.array_equal(s_acc[:rows], acc_o[:rows].astype(np.float32))
+    assert np.array_equal(got["s"][:rows], acc_o[:rows].astype(np.float32))
 
-    # P8: bytes equal but for rare one-code steps at E4M3 ties
-    diff = p8[:rows].astype(np.int16) - p8_o[:rows].astype(np.int16)
-    assert np.abs(diff).max() <= 1, "P8 differs by more than one code"
-    assert np.count_nonzero(diff) <= max(2, rows * n // 1000), f"{np.count_nonzero(diff)} P8 codes differ"
+    # FP8 P: the same bytes
+    diff = np.count_nonzero(got["p8"][:rows] != p8_o[:rows])
+    assert diff == 0, f"{diff} P8 bytes differ"
 
-    # PV: the oracle's partial of its own P8.  Where the P8 bytes agree the
-    # sums agree up to FP32 summation order; each key whose byte differs by
-    # one code moves a channel by at most one E4M3 step of the oracle's
-    # weight (<= 1/8 of it, or 2^-9 below the normal range) times |v8|.
-    _, _, part_o = oracle_mod.first_tile(ref, Nq, Nkv, causal)
-    po = oracle_mod.e4m3_to_f32(p8_o[:rows].reshape(-1)).reshape(rows, 256).astype(np.float64)
-    vv = np.zeros((256, 128))
+    # PV partial of tile 0: the same products, summed in the tensor core's FP32 order
+    po = oracle_mod.e4m3_to_f32(p8_o[:rows].reshape(-1)).reshape(rows, TILE).astype(np.float64)
+    vv = np.zeros((TILE, 128))
     vv[:n] = oracle_mod.e4m3_to_f32(ref["v_codes"][0, 0, :n].reshape(-1)).reshape(n, 128)
-    step = np.where(diff != 0, 0.125 * po + 2.0 ** -9, 0.0)
-    bound = 4e-6 * (np.abs(po) @ np.abs(vv)) + step @ np.abs(vv) + 1e-30
-    got = part[:rows, :128].astype(np.float64)
-    assert np.all(np.abs(got - part_o[:rows, :128]) <= bound), "PV partial off beyond summation order and P8 steps"
-    dsum = 4e-6 * po.sum(axis=1) + step.sum(axis=1)   # the ones row: sum of p8
-    assert np.all(np.abs(part[:rows, 128].astype(np.float64) - part_o[:rows, 128]) <= dsum)
-    assert not part[:rows, 129:].any()
+    bound = 4e-6 * (np.abs(po) @ np.abs(vv)) + 1e-30
+    assert np.all(np.abs(got["part"][:rows, :128].astype(np.float64) - part_o[:rows, :128]) <= bound)
+    assert np.all(np.abs(got["part"][:rows, 128].astype(np.float64) - part_o[:rows, 128]) <= 4e-6 * po.sum(axis=1))
+    assert not got["part"][:rows, 129:].any()
+
+    # the end of the recurrence: d and its reciprocal
+    st_end = oracle_mod.tile_state(ref, Nq, Nkv, causal, which=0, tile=TILE)
+    np.testing.assert_allclose(got["dfin"][:rows], st_end["d_final"][:rows], rtol=2e-5)
+    rcp_own = (np.float32(1) / got["dfin"][:rows].astype(np.float32)).astype(np.float32)
+    assert np.array_equal(got["rcp"][:rows], rcp_own), "reciprocal is not the correctly rounded 1/d"
+    np.testing.assert_allclose(got["rcp"][:rows], st_end["rcp"][:rows], rtol=2e-5)
+
+    # tile 1 (where the item has one): running maximum, alpha, d and RO after the outer update
+    if Nkv <= TILE or (causal and min(127, Nq - 1) + (Nkv - Nq) < TILE):
+        return
+    st = oracle_mod.tile_state(ref, Nq, Nkv, causal, which=1, tile=TILE)
+    vis = st["visited"][:rows]
+    assert vis.any()
+    assert np.array_equal(got["m1"][:rows][vis], st["m"][:rows][vis].astype(np.float32))
+    np.testing.assert_allclose(got["a1"][:rows][vis], st["alpha"][:rows][vis], rtol=1e-6, atol=1e-30)
+    np.testing.assert_allclose(got["d1"][:rows][vis], st["d"][:rows][vis], rtol=2e-5)
+    ro_ref = st["ro"][:rows][vis]
+    scale = np.abs(ro_ref).max(axis=1, keepdims=True) + 1e-30
+    assert np.all(np.abs(got["ro1"][:rows][vis].astype(np.float64) - ro_ref) <= 2e-5 * scale)
+    # rows that keep no key of tile 1 pass it unchanged: alpha = 1, nothing added
+    if (~vis).any():
+        assert np.all(got["a1"][:rows][~vis] == 1.0)
+        np.testing.assert_allclose(got["d1"][:rows][~vis], st["d_final"][:rows][~vis], rtol=2e-5)
