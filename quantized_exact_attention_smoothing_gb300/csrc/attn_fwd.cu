@@ -49,12 +49,16 @@
 // Exactness of P: the FP8 byte of a key is E4M3(fl(fl(2^dd) * 448)) with
 // dd = fl(fl(acc * sig) - m), s2 and dd rounded exactly as stated (packed FP32
 // pairs), and 2^dd from ex2.approx, whose relative error is below 2^-22.7 over
-// the range used (measured for every FP32 input).  The byte is taken from
-// 2^dd * 448 * (1 + 2^-20) and 2^dd * 448 * (1 - 2^-20): the bracket holds the
-// exact value, so when both give the same byte (rounding is monotonic) that is
-// the byte.  Otherwise (within 2^-20 of an E4M3 rounding midpoint, about
-// 3e-5 of the keys) the byte is recomputed with a correctly rounded exp2,
-// after the tile's P pass (see the compute warpgroups).
+// the range used (measured for every FP32 input; the PTX ISA states 2^-22).
+// The byte is taken from y+ = fl(2^dd * 448 * (1 + 2^-21)) and
+// y- = fl(2^dd * 448 * (1 - 2^-21)).  With the approximation error, the
+// rounding of fl(2^dd) and of both products (2^-24 each), the exact
+// fl(fl(2^dd) * 448) lies in [y-, y+] for any approximation error up to
+// 2^-22: 2^-21 > 2^-22 + 3 * 2^-24.  Rounding to E4M3 is monotonic, so when
+// both give the same byte that is the byte.  Otherwise (within about 2^-21 of
+// an E4M3 rounding midpoint, about 1.5e-5 of the keys) the byte is recomputed
+// with a correctly rounded exp2, after the tile's P pass (see the compute
+// warpgroups).
 //
 // Every mbarrier wait is bounded: after about a second, or as soon as another
 // CTA has reported a failure, the thread records the failure in the status
@@ -112,7 +116,8 @@ constexpr uint32_t OFF_MAXX = OFF_QS + QS_BYTES;             // [tile parity][ha
 constexpr uint32_t OFF_SV = OFF_MAXX + 4 * BM * 4;          // [item % 3][128] V channel scales
 constexpr uint32_t SV_BYTES = HD * 4;
 constexpr uint32_t OFF_SQ = OFF_SV + 3 * SV_BYTES;          // [item % 2][4] Q block scales (in-kernel Q quantisation)
-constexpr uint32_t OFF_BAR = OFF_SQ + 2 * 4 * 4;
+constexpr uint32_t OFF_PARK = OFF_SQ + 2 * 4 * 4;         // [half][row] 16 bytes: exponent arguments of an undecided P8 word
+constexpr uint32_t OFF_BAR = OFF_PARK + 2 * BM * 16;
 enum Bar : int {
     KFULL = 0,
     KEMPTY = KFULL + KSLOTS,
@@ -148,9 +153,9 @@ enum Site : uint32_t {
 };
 
 struct FwdParams {
-    const int8_t *q_codes;
-    const __nv_bfloat16 *q_bf16;   // in-kernel Q quantisation: the BF16 Q [B*Hq][Nq][128]
-    const int8_t *k_codes;   // INT8 K codes [B*Hkv][nk32][128] (the rare exact path recomputes a score from them)
+    const int8_t *q_codes;           // prepared INT8 Q [B*Hq][nq32][128] (null with in-kernel Q quantisation)
+    const __nv_bfloat16 *q_bf16;     // in-kernel Q quantisation: the BF16 Q [B*Hq][Nq][128]
+    const uint4 *k_carrier;          // FP16 carrier of the K codes [B*Hkv][Nkv][128]
     const float *q_scales, *k_scales, *v_scales;
     __nv_bfloat16 *out;
     uint32_t *status;
@@ -158,8 +163,9 @@ struct FwdParams {
     int withhold_v;   // test hook: the V loader stages the first Q tile and loads no V
     // reciprocals for exact division by Hq * B, Hq and group (see udiv)
     unsigned long long m_hb, m_hq, m_group;
-    int nq32, nbq, nbk, nk32;
+    int nq32, nbq, nbk;
     float c0;
+    float zero;   // always +0 (see dd_pair)
 #ifdef SATTN_DEBUG_DUMP
     // intermediates of query tile 0 of (batch 0, head 0), KV tile 0:
     // [0, 32768) raw S accumulators (128 x 256), [32768, 40960) P8 words
@@ -342,21 +348,31 @@ __device__ __forceinline__ uint32_t p8_exact(float acc, float sig, float mu)
     return ptx::cvt_e4m3x2(0.0f, __fmul_rn(exp2_rn(dd), 448.0f)) & 0xffu;
 }
 
-constexpr float kP8Hi = 448.0f * (1.0f + 0x1p-20f), kP8Lo = 448.0f * (1.0f - 0x1p-20f);   // both exact in FP32
+constexpr float kP8Hi = 448.0f * (1.0f + 0x1p-21f), kP8Lo = 448.0f * (1.0f - 0x1p-21f);   // both exact in FP32
+
+// dd = fl(fl(x * sig) - mu) for two keys in packed FP32 pairs, both roundings
+// kept.  The assembler contracts a packed multiply whose only use is a packed
+// subtraction into one fused multiply-add (one rounding), .rn or not; the
+// product is therefore formed as fl(x * sig + z) with z a zero the compiler
+// cannot see (a kernel argument, always +0), which is the same rounded
+// product and cannot be fused with the subtraction.
+__device__ __forceinline__ uint64_t dd_pair(uint32_t x0, uint32_t x1, uint64_t sg2, uint64_t m2, uint64_t z2)
+{
+    return ptx::sub_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(x0), __uint_as_float(x1)), sg2, z2), m2);
+}
 
 // FP8 P bytes of 32 keys (one block of the tile: raw accumulators x as FP32
 // bit patterns, -inf for masked keys) with block scale product sig and running
 // maximum mu (finite), four bytes per word, key 4w + u in byte u of word w.
 // s2 = fl(x * sig), dd = fl(s2 - mu) in packed pairs; the bytes of
-// 2^dd * 448 * (1 + 2^-20) (the result) and of 2^dd * 448 * (1 - 2^-20)
+// 2^dd * 448 * (1 + 2^-21) (the result) and of 2^dd * 448 * (1 - 2^-21)
 // (compared, not kept); keys whose two bytes differ are recomputed with
-// p8_exact (per lane, rare), after recomputing the lower bytes of the block.
+// p8_exact (rare).
 __device__ __forceinline__ void p8_words4(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3, uint64_t sg2,
-                                          uint64_t m2, uint32_t &hi, uint32_t &lo)
+                                          uint64_t m2, uint64_t z2, uint32_t &hi, uint32_t &lo)
 {
     const uint64_t hi2 = ptx::f32x2(kP8Hi, kP8Hi), lo2 = ptx::f32x2(kP8Lo, kP8Lo);
-    const uint64_t d01 = ptx::sub_f32x2(ptx::mul_f32x2(ptx::f32x2(__uint_as_float(x0), __uint_as_float(x1)), sg2), m2);
-    const uint64_t d23 = ptx::sub_f32x2(ptx::mul_f32x2(ptx::f32x2(__uint_as_float(x2), __uint_as_float(x3)), sg2), m2);
+    const uint64_t d01 = dd_pair(x0, x1, sg2, m2, z2), d23 = dd_pair(x2, x3, sg2, m2, z2);
     const uint64_t e01 = ptx::f32x2(ptx::ex2_approx(ptx::f32x2_lo(d01)), ptx::ex2_approx(ptx::f32x2_hi(d01)));
     const uint64_t e23 = ptx::f32x2(ptx::ex2_approx(ptx::f32x2_lo(d23)), ptx::ex2_approx(ptx::f32x2_hi(d23)));
     const uint64_t p01 = ptx::mul_f32x2(e01, hi2), p23 = ptx::mul_f32x2(e23, hi2);
@@ -365,37 +381,77 @@ __device__ __forceinline__ void p8_words4(uint32_t x0, uint32_t x1, uint32_t x2,
     lo = ptx::cvt_e4m3x4(ptx::f32x2_lo(n01), ptx::f32x2_hi(n01), ptx::f32x2_lo(n23), ptx::f32x2_hi(n23));
 }
 
-__device__ __forceinline__ void p8_words(const uint32_t (&x)[32], int w, uint64_t sg2, uint64_t m2, uint32_t &hi,
-                                         uint32_t &lo)
+__device__ __forceinline__ void p8_words(const uint32_t (&x)[32], int w, uint64_t sg2, uint64_t m2, uint64_t z2,
+                                         uint32_t &hi, uint32_t &lo)
 {
-    p8_words4(x[4 * w], x[4 * w + 1], x[4 * w + 2], x[4 * w + 3], sg2, m2, hi, lo);
+    p8_words4(x[4 * w], x[4 * w + 1], x[4 * w + 2], x[4 * w + 3], sg2, m2, z2, hi, lo);
 }
 
 // Fast path of one block: the result bytes (upper bracket) in `out`; the
 // return value is nonzero if any key's two brackets differ.
-__device__ __forceinline__ uint32_t p8_block_fast(const uint32_t (&x)[32], float sig, float mu, uint32_t (&out)[8])
+__device__ __forceinline__ uint32_t p8_block_fast(const uint32_t (&x)[32], float sig, float mu, float zero,
+                                                  uint32_t (&out)[8])
 {
-    const uint64_t sg2 = ptx::f32x2(sig, sig), m2 = ptx::f32x2(mu, mu);
+    const uint64_t sg2 = ptx::f32x2(sig, sig), m2 = ptx::f32x2(mu, mu), z2 = ptx::f32x2(zero, zero);
     uint32_t diff = 0;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
         uint32_t lo;
-        p8_words(x, w, sg2, m2, out[w], lo);
+        p8_words(x, w, sg2, m2, z2, out[w], lo);
         diff |= out[w] ^ lo;
     }
     return diff;
 }
 
+// The fast path of one block inside the forward: as p8_block_fast, and for a
+// word whose two brackets differ, its four exponent arguments dd are stored
+// (predicated, no branch) in the thread's 16-byte slot and bit 8c + w of
+// wmask is set.  With one such word in the tile the slot holds it; with more,
+// only the last (the caller then recomputes them all from the codes).
+__device__ __forceinline__ void p8_block_park(const uint32_t (&x)[32], float sig, float mu, float zero,
+                                              uint32_t (&out)[8], uint32_t slot, int c, uint32_t &wmask,
+                                              uint32_t force = 0)
+{
+    const uint64_t sg2 = ptx::f32x2(sig, sig), m2 = ptx::f32x2(mu, mu), z2 = ptx::f32x2(zero, zero);
+    const uint64_t hi2 = ptx::f32x2(kP8Hi, kP8Hi), lo2 = ptx::f32x2(kP8Lo, kP8Lo);
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const uint64_t d01 = dd_pair(x[4 * w], x[4 * w + 1], sg2, m2, z2);
+        const uint64_t d23 = dd_pair(x[4 * w + 2], x[4 * w + 3], sg2, m2, z2);
+        const uint64_t e01 = ptx::f32x2(ptx::ex2_approx(ptx::f32x2_lo(d01)), ptx::ex2_approx(ptx::f32x2_hi(d01)));
+        const uint64_t e23 = ptx::f32x2(ptx::ex2_approx(ptx::f32x2_lo(d23)), ptx::ex2_approx(ptx::f32x2_hi(d23)));
+        const uint64_t p01 = ptx::mul_f32x2(e01, hi2), p23 = ptx::mul_f32x2(e23, hi2);
+        const uint64_t n01 = ptx::mul_f32x2(e01, lo2), n23 = ptx::mul_f32x2(e23, lo2);
+        out[w] = ptx::cvt_e4m3x4(ptx::f32x2_lo(p01), ptx::f32x2_hi(p01), ptx::f32x2_lo(p23), ptx::f32x2_hi(p23));
+        const uint32_t lo =
+            ptx::cvt_e4m3x4(ptx::f32x2_lo(n01), ptx::f32x2_hi(n01), ptx::f32x2_lo(n23), ptx::f32x2_hi(n23));
+        // (force: debug builds treat the words whose bit is set as undecided)
+        ptx::park_if_differ(out[w], ((force >> (8 * c + w)) & 1u) ? ~out[w] : lo, slot, __float_as_uint(ptx::f32x2_lo(d01)), __float_as_uint(ptx::f32x2_hi(d01)),
+                            __float_as_uint(ptx::f32x2_lo(d23)), __float_as_uint(ptx::f32x2_hi(d23)), wmask,
+                            1u << (8 * c + w));
+    }
+}
+
+// The exact FP8 byte of one key from its exponent argument dd.
+__device__ __forceinline__ uint32_t p8_of_dd(float dd)
+{
+    const float e = ptx::ex2_approx(dd);
+    const uint32_t hi = ptx::cvt_e4m3x2(0.0f, __fmul_rn(e, kP8Hi)) & 0xffu;
+    const uint32_t lo = ptx::cvt_e4m3x2(0.0f, __fmul_rn(e, kP8Lo)) & 0xffu;
+    return hi == lo ? hi : ptx::cvt_e4m3x2(0.0f, __fmul_rn(exp2_rn(dd), 448.0f)) & 0xffu;
+}
+
 // Fix-up of one block (rare): the bytes again, with the undecided keys
 // recomputed by p8_exact.
-__device__ __forceinline__ void p8_block_fix(const uint32_t (&x)[32], float sig, float mu, uint32_t (&out)[8])
+__device__ __forceinline__ void p8_block_fix(const uint32_t (&x)[32], float sig, float mu, float zero,
+                                             uint32_t (&out)[8])
 {
-    const uint64_t sg2 = ptx::f32x2(sig, sig), m2 = ptx::f32x2(mu, mu);
+    const uint64_t sg2 = ptx::f32x2(sig, sig), m2 = ptx::f32x2(mu, mu), z2 = ptx::f32x2(zero, zero);
     uint32_t flags = 0;   // bit 4w + u: byte u of word w undecided
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
         uint32_t lo;
-        p8_words(x, w, sg2, m2, out[w], lo);
+        p8_words(x, w, sg2, m2, z2, out[w], lo);
         const uint32_t dw = out[w] ^ lo;
 #pragma unroll
         for (int u = 0; u < 4; ++u)
@@ -417,100 +473,84 @@ __device__ __forceinline__ void p8_block_fix(const uint32_t (&x)[32], float sig,
     }
 }
 
-// Fix-up of one block whose 32 accumulators lie in shared memory at `slot`
-// (value e at slot + 16 * ((e / 4) ^ (lane % 8)) + 4 * (e % 4)); the words
-// of the block as written by the fast path are in `out`, and are rewritten
-// with the undecided keys recomputed by p8_exact.
-__device__ void p8_block_fix_smem(uint32_t slot, int lane, float sig, float mu, uint32_t (&out)[8])
+// The raw QK accumulators (exact int32 dot products of the codes) of keys
+// key0 .. key0 + 31 for query row r of the item, recomputed by the warp: lane
+// l returns key key0 + kl, kl = 2 (l % 16) + l / 16.  K: the 32 FP16 carrier
+// rows in global memory (the tile was just read from there; 8 KB, contiguous),
+// loaded coalesced, so that lane l holds channels 8 (l % 16) .. + 7 of keys
+// 2i + l / 16 (i = 0 .. 15), turned back into their codes; keys from Nkv on
+// are not read (their accumulators are not used).  Q: the same eight channels
+// of the row, from the FP16 carrier in shared memory while it still holds this
+// item (q_smem: KV tiles before the item's last two, whose QK may complete and
+// release it during this tile's P); else from the prepared INT8 codes or, with
+// in-kernel Q quantisation, quantised again from the BF16 Q with the row's
+// block scale sq by the preparation's own quantiser.  Then a transposing
+// butterfly over each half-warp sums the sixteen partial products of each key
+// (integer sums: any order is exact).
+__device__ __forceinline__ int block_accumulators(const FwdParams &p, const Tile &t, int r, int key0, float sq,
+                                                  uint32_t sb, bool q_smem, int lane)
 {
-    const uint64_t sg2 = ptx::f32x2(sig, sig), m2 = ptx::f32x2(mu, mu);
-#pragma unroll 1
-    for (int w = 0; w < 8; ++w) {
-        const uint4 a = ptx::ld_shared_v4(slot + 16u * static_cast<uint32_t>(w ^ (lane & 7)));
-        uint32_t hi, lo;
-        p8_words4(a.x, a.y, a.z, a.w, sg2, m2, hi, lo);
-        uint32_t dw = hi ^ lo, word = hi;
-        const uint32_t xs[4] = {a.x, a.y, a.z, a.w};
+    const int ch = lane & 15;   // channel chunk: channels 8 ch .. 8 ch + 7
+    const uint4 *kb = p.k_carrier + (static_cast<size_t>(t.b * p.Hkv + t.hk) * p.Nkv + key0) * (HD / 8);
+    uint4 kv[16];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (((dw >> (8 * u)) & 0xffu) != 0u)
-                word = (word & ~(0xffu << (8 * u))) | (p8_exact(__uint_as_float(xs[u]), sig, mu) << (8 * u));
-#pragma unroll
-        for (int v = 0; v < 8; ++v)
-            if (v == w)
-                out[v] = word;
-    }
-}
-
-// The raw QK accumulator (exact int32 dot product of the codes) of key `key`
-// for query row r of the item: K from the INT8 codes in global memory; Q from
-// the prepared INT8 codes, or, with in-kernel Q quantisation, quantised again
-// from the BF16 Q with the row's block scale sq by the preparation's own
-// quantiser (the Q carrier in shared memory may already hold the next item).
-__device__ int dot_row_key(const FwdParams &p, const Tile &t, int r, int key, float sq)
-{
-    const uint4 *kr = reinterpret_cast<const uint4 *>(p.k_codes +
-                                                      (static_cast<size_t>(t.b * p.Hkv + t.hk) * p.nk32 + key) * HD);
-    int acc = 0;
-    if (p.q_codes) {
-        const uint4 *qr = reinterpret_cast<const uint4 *>(
-            p.q_codes + (static_cast<size_t>(t.b * p.Hq + t.hq) * p.nq32 + t.q0 + r) * HD);
-#pragma unroll 2
-        for (int v = 0; v < 8; ++v) {
-            const uint4 qv = __ldg(qr + v), kv = __ldg(kr + v);
-            acc = __dp4a(static_cast<int>(qv.x), static_cast<int>(kv.x), acc);
-            acc = __dp4a(static_cast<int>(qv.y), static_cast<int>(kv.y), acc);
-            acc = __dp4a(static_cast<int>(qv.z), static_cast<int>(kv.z), acc);
-            acc = __dp4a(static_cast<int>(qv.w), static_cast<int>(kv.w), acc);
+    for (int i = 0; i < 16; ++i)
+        kv[i] = (key0 + 2 * i + (lane >> 4) < p.Nkv) ? __ldg(kb + 32 * i + lane) : make_uint4(0u, 0u, 0u, 0u);
+    uint32_t q0 = 0, q1 = 0;   // Q codes of the chunk
+    if (t.q0 + r < p.Nq) {     // (a pad row's codes are all 0)
+        if (q_smem) {
+            const uint4 a = ptx::ld_shared_v4(sb + OFF_Q + (ch >> 3) * Q_HALF_BYTES + r * 128 +
+                                              ((static_cast<uint32_t>((ch & 7) ^ (r & 7))) << 4));
+            q0 = ptx::i8x4_of_f16x2(a.x, a.y);
+            q1 = ptx::i8x4_of_f16x2(a.z, a.w);
+        } else if (p.q_codes) {
+            const uint2 a = __ldg(reinterpret_cast<const uint2 *>(
+                p.q_codes + (static_cast<size_t>(t.b * p.Hq + t.hq) * p.nq32 + t.q0 + r) * HD) + ch);
+            q0 = a.x, q1 = a.y;
+        } else if (sq > 0.0f) {   // (a zero block scale: every code is 0)
+            const uint2 c = int8_codes8(__ldg(reinterpret_cast<const uint4 *>(
+                                            p.q_bf16 + (static_cast<size_t>(t.b * p.Hq + t.hq) * p.Nq + t.q0 + r) * HD) + ch),
+                                        sq, __frcp_rn(sq));
+            q0 = c.x, q1 = c.y;
         }
-        return acc;
     }
-    if (!(sq > 0.0f) || t.q0 + r >= p.Nq)   // a zero block scale, or a pad row: every code is 0
-        return 0;
-    const float rs = __frcp_rn(sq);
-    const uint4 *qr = reinterpret_cast<const uint4 *>(p.q_bf16 + (static_cast<size_t>(t.b * p.Hq + t.hq) * p.Nq + t.q0 + r) * HD);
-#pragma unroll 2
-    for (int v = 0; v < 8; ++v) {   // 16 channels: two 16-byte chunks of BF16 Q, one of K codes
-        const uint4 kv = __ldg(kr + v);
-        const uint2 c0 = int8_codes8(__ldg(qr + 2 * v), sq, rs), c1 = int8_codes8(__ldg(qr + 2 * v + 1), sq, rs);
-        acc = __dp4a(static_cast<int>(c0.x), static_cast<int>(kv.x), acc);
-        acc = __dp4a(static_cast<int>(c0.y), static_cast<int>(kv.y), acc);
-        acc = __dp4a(static_cast<int>(c1.x), static_cast<int>(kv.z), acc);
-        acc = __dp4a(static_cast<int>(c1.y), static_cast<int>(kv.w), acc);
+    int part[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        part[i] = __dp4a(static_cast<int>(q1), static_cast<int>(ptx::i8x4_of_f16x2(kv[i].z, kv[i].w)),
+                         __dp4a(static_cast<int>(q0), static_cast<int>(ptx::i8x4_of_f16x2(kv[i].x, kv[i].y)), 0));
+    // butterfly: at the step over lane bit b, the lane with bit b clear keeps
+    // the entries whose index has bit b clear; after four steps lane l holds
+    // the half-warp's sum for entry i = l % 16
+#pragma unroll
+    for (int b = 3; b >= 0; --b) {
+        const bool up = (lane >> b) & 1;
+#pragma unroll
+        for (int i = 0; i < (1 << b); ++i) {
+            const int send = up ? part[i] : part[i + (1 << b)];
+            const int recv = __shfl_xor_sync(0xffffffffu, send, 1 << b);
+            part[i] = (up ? part[i + (1 << b)] : part[i]) + recv;
+        }
     }
-    return acc;
+    return part[0];
 }
 
-// Fix-up of one block whose accumulators were not kept: each key's
-// accumulator is recomputed from the codes (keys from `nvalid` on, the
-// masked ones, are -inf), its two brackets compared, and an undecided byte
-// recomputed by p8_exact.  Few registers; the rare case of the rare case.
-__device__ void p8_block_fix_codes(const FwdParams &p, const Tile &t, int r, int key0, int nvalid, float sq,
-                                   float sig, float mu, uint32_t (&out)[8])
+// The FP8 byte of one key: the bracket of the fast path (the same operations,
+// one lane at a time), and p8_exact where the two bytes differ.
+__device__ __forceinline__ uint32_t p8_byte(uint32_t x, float sig, float mu)
 {
-    const uint64_t sg2 = ptx::f32x2(sig, sig), m2 = ptx::f32x2(mu, mu);
-#pragma unroll 1
-    for (int k = 0; k < 32; ++k) {
-        const uint32_t xk = k < nvalid ? __float_as_uint(static_cast<float>(dot_row_key(p, t, r, key0 + k, sq)))
-                                       : 0xff800000u;
-        uint32_t hi, lo;
-        p8_words4(xk, xk, xk, xk, sg2, m2, hi, lo);
-        uint32_t code = hi & 0xffu;
-        if ((hi ^ lo) & 0xffu)
-            code = p8_exact(__uint_as_float(xk), sig, mu);
-        const uint32_t sh = 8u * static_cast<uint32_t>(k & 3);
-#pragma unroll
-        for (int w = 0; w < 8; ++w)
-            if ((k >> 2) == w)
-                out[w] = (out[w] & ~(0xffu << sh)) | (code << sh);
-    }
+    const float e = ptx::ex2_approx(__fsub_rn(__fmul_rn(__uint_as_float(x), sig), mu));
+    const uint32_t hi = ptx::cvt_e4m3x2(0.0f, __fmul_rn(e, kP8Hi)) & 0xffu;
+    const uint32_t lo = ptx::cvt_e4m3x2(0.0f, __fmul_rn(e, kP8Lo)) & 0xffu;
+    return hi == lo ? hi : p8_exact(__uint_as_float(x), sig, mu);
 }
 
 // Both, for one block (the test hook's entry).
-__device__ __forceinline__ void p8_block(const uint32_t (&x)[32], float sig, float mu, uint32_t (&out)[8])
+__device__ __forceinline__ void p8_block(const uint32_t (&x)[32], float sig, float mu, float zero,
+                                         uint32_t (&out)[8])
 {
-    if (p8_block_fast(x, sig, mu, out) != 0u)
-        p8_block_fix(x, sig, mu, out);
+    if (p8_block_fast(x, sig, mu, zero, out) != 0u)
+        p8_block_fix(x, sig, mu, zero, out);
 }
 
 // K loader.  Half-tile u = 2 * (tile) + h (channels [64h, 64h + 64) of the
@@ -1037,61 +1077,115 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
             // previous PV has completed.  A row with no kept key so far (mn =
             // -inf) has only -inf scores, which any finite maximum maps to 0.
             const float mu = (mn == -INFINITY) ? 0.0f : mn;
-            // Rare (about 3e-5 of the keys): a key within 2^-20 of an E4M3
-            // rounding midpoint.  Without any branch in this loop, a lane parks
-            // the accumulators of its first such block (predicated stores) in
-            // its 128-byte slot of the warp's own output staging slice, idle
-            // until the item's final conversion; further blocks, and all blocks
-            // with in-kernel Q quantisation (which stages Q there), are marked
-            // for a recomputation from the codes.  After the tile's P the warp
-            // (one vote) rewrites those blocks with the undecided keys
-            // recomputed by p8_exact.
-            const uint32_t slot = sb + OFF_STG + (quarter * 2 + half) * 4096 + lane * 128;
-            if (!kFuseQ && j == 0) {   // the previous item's output store has read the slice
-                if (lane == 0)
-                    ptx::bulk_wait_read();
-                __syncwarp();
+            // Rare (about 1.5e-5 of the keys): a key within 2^-21 of an E4M3
+            // rounding midpoint.  The loop has no branch on it: a word (four
+            // keys) with such a key leaves its four exponent arguments in the
+            // thread's slot and its bit in wmask.  Then one vote: if any lane
+            // of the warp has such a word, the warp rewrites them.  A lane with
+            // one word recomputes its four bytes from the slot (p8_of_dd).  A
+            // lane with more (rare again) has its blocks redone one at a time:
+            // for block c of the row of lane e, the warp recomputes the 32
+            // accumulators from the codes (exact, so equal to the tensor
+            // core's), each lane the byte of one key with p8_byte; lane e
+            // gathers the 32 bytes and rewrites its eight words of the block in
+            // TMEM.  The block scale product sig[c] is the same for the warp's
+            // 32 rows (one Q block).
+            const uint32_t slot = sb + OFF_PARK + (half * BM + r) * 16;
+            uint32_t wmask = 0;   // bit 8c + w: word w of block c holds an undecided key
+            uint32_t force = 0;
+#ifdef SATTN_DEBUG_DUMP
+            if (p.dbg) {   // test modes: one (1) or two (2) words of each row and tile taken as undecided
+                const int mode = static_cast<int>(p.dbg[60012]);
+                force = (mode >= 1 ? 1u << ((r + j) & 31) : 0u) | (mode >= 2 ? 1u << ((r + j + 7) & 31) : 0u);
             }
-            int parked = -1;          // block parked in the slot
-            uint32_t recompute = 0;   // bit c: block c undecided, not parked
+#endif
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t pk[8];
-                const uint32_t undecided = p8_block_fast(s[c], sig[c], mu, pk);
+                p8_block_park(s[c], sig[c], mu, p.zero, pk, slot, c, wmask, force);
                 if (c == 0 && gj >= 1 && !wt.wait(bar(PDONE), (gj - 1) & 1, SITE_PDONE))
                     return false;
                 ptx::tmem_st8(taddr + TM_P + 32 * half + 8 * c, pk);
-                const bool park = !kFuseQ && undecided != 0u && parked < 0;
-#pragma unroll
-                for (int w = 0; w < 8; ++w)
-                    ptx::st_shared_v4_if(park, slot + 16u * static_cast<uint32_t>(w ^ (lane & 7)), s[c][4 * w],
-                                         s[c][4 * w + 1], s[c][4 * w + 2], s[c][4 * w + 3]);
-                parked = park ? c : parked;
-                recompute |= (undecided != 0u && !park) ? (1u << c) : 0u;
             }
-            if (__any_sync(0xffffffffu, parked >= 0 || recompute != 0u)) {
-                ptx::tmem_wait_st();   // the first stores are complete before blocks are read back
-                const int lo = j * BN + 128 * half;
-                const int nvalid = (j >= t.mask_from) ? max(0, min(128, min(p.Nkv - 1, lim) - lo + 1)) : 128;
+            if (__any_sync(0xffffffffu, wmask != 0u)) {
+                uint32_t und = 0;   // bit c: block c holds an undecided word
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    und |= ((wmask >> (8 * c)) & 0xffu) ? (1u << c) : 0u;
+#ifdef SATTN_DEBUG_DUMP
+                const long long fix_t0 = clock64();
+                if (p.dbg)
+                    atomicAdd(p.dbg + 60000, static_cast<float>(__popc(und)));   // undecided blocks seen
+#endif
+                ptx::tmem_wait_st();   // the stores of the pass are complete before blocks are read back
+                const bool one = wmask != 0u && (wmask & (wmask - 1u)) == 0u;
+                const int wi = __ffs(wmask) - 1;
+                uint32_t word = 0;
+                if (one) {
+                    const uint4 dq = ptx::ld_shared_v4(slot);
+                    word = p8_of_dd(__uint_as_float(dq.x)) | (p8_of_dd(__uint_as_float(dq.y)) << 8) |
+                           (p8_of_dd(__uint_as_float(dq.z)) << 16) | (p8_of_dd(__uint_as_float(dq.w)) << 24);
+                }
+                const uint32_t blocks1 = __reduce_or_sync(0xffffffffu, one ? (1u << (wi >> 3)) : 0u);
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
-                    const bool mine = parked == c || ((recompute >> c) & 1u);
-                    if (!__any_sync(0xffffffffu, mine))
+                    if (!((blocks1 >> c) & 1u))
                         continue;
-#ifdef SATTN_DEBUG_DUMP
-                    if (p.dbg && mine)
-                        atomicAdd(p.dbg + 60000, 1.0f);   // undecided blocks seen
-#endif
-                    const float sg = (c == 0) ? sig[0] : (c == 1) ? sig[1] : (c == 2) ? sig[2] : sig[3];
                     uint32_t pk[8];
-                    ptx::tmem_ld8(taddr + TM_P + 32 * half + 8 * c, pk);
+                    ptx::tmem_ld8(taddr + TM_P + 32 * half + 8 * static_cast<uint32_t>(c), pk);
                     ptx::tmem_wait_ld();
-                    if (parked == c)
-                        p8_block_fix_smem(slot, lane, sg, mu, pk);
-                    else if (mine)
-                        p8_block_fix_codes(p, t, r, lo + 32 * c, nvalid - 32 * c, sq, sg, mu, pk);
-                    ptx::tmem_st8(taddr + TM_P + 32 * half + 8 * c, pk);
+#pragma unroll
+                    for (int w = 0; w < 8; ++w)
+                        pk[w] = (one && wi == 8 * c + w) ? word : pk[w];
+                    ptx::tmem_st8(taddr + TM_P + 32 * half + 8 * static_cast<uint32_t>(c), pk);
                 }
+                if (one)
+                    und = 0u;
+                uint32_t pend = und;
+#pragma unroll 1
+                for (;;) {
+                    const uint32_t bal = __ballot_sync(0xffffffffu, pend != 0u);
+                    if (bal == 0u)
+                        break;
+                    const int e = __ffs(bal) - 1;
+                    const int c = __ffs(__shfl_sync(0xffffffffu, pend, e)) - 1;
+                    if (lane == e)
+                        pend &= pend - 1u;
+                    const float mue = __shfl_sync(0xffffffffu, mu, e);
+                    const float sg = (c == 0) ? sig[0] : (c == 1) ? sig[1] : (c == 2) ? sig[2] : sig[3];
+                    const int re = quarter * 32 + e;
+                    const int key0 = j * BN + 128 * half + 32 * c;
+                    const int kl = 2 * (lane & 15) + (lane >> 4);   // this lane's key of the block
+                    const int lime = p.causal ? t.q0 + re + (p.Nkv - p.Nq) : 0x7fffffff;
+                    const int acc = block_accumulators(p, t, re, key0, sq, sb, j + 2 < t.ntiles, lane);
+                    const uint32_t xk = (key0 + kl <= min(p.Nkv - 1, lime)) ? __float_as_uint(static_cast<float>(acc))
+                                                                             : 0xff800000u;   // a masked key
+                    uint32_t v = p8_byte(xk, sg, mue) << (8 * (kl & 3));
+                    // keys 4w, 4w + 2 sit in lanes 2w, 2w + 1 and keys 4w + 1, 4w + 3 in
+                    // lanes 2w + 16, 2w + 17: two exchanges assemble word w in lane 2w
+                    v |= __shfl_xor_sync(0xffffffffu, v, 1);
+                    v |= __shfl_xor_sync(0xffffffffu, v, 16);
+                    uint32_t wd[8];
+#pragma unroll
+                    for (int w = 0; w < 8; ++w)
+                        wd[w] = __shfl_sync(0xffffffffu, v, 2 * w);
+                    ptx::tmem_wait_st();   // earlier stores of the block are complete before it is read back
+                    uint32_t pk[8];
+                    ptx::tmem_ld8(taddr + TM_P + 32 * half + 8 * static_cast<uint32_t>(c), pk);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int w = 0; w < 8; ++w)
+                        pk[w] = (lane == e) ? wd[w] : pk[w];
+                    ptx::tmem_st8(taddr + TM_P + 32 * half + 8 * static_cast<uint32_t>(c), pk);
+                }
+#ifdef SATTN_DEBUG_DUMP
+                ptx::tmem_wait_st();   // (the whole warp: the wait is a warp-wide instruction)
+                if (p.dbg && lane == 0) {   // cycles in the fix-up and its count, per warp
+                    atomicAdd(reinterpret_cast<unsigned long long *>(p.dbg + 60002),
+                              static_cast<unsigned long long>(clock64() - fix_t0));
+                    atomicAdd(reinterpret_cast<unsigned long long *>(p.dbg + 60004), 1ull);
+                }
+#endif
             }
 #ifdef SATTN_DEBUG_DUMP
             if (p.dbg && j == 0 && t.q0 == 0 && t.hq == 0 && t.b == 0) {   // the bytes as PV will read them
@@ -1338,7 +1432,7 @@ __global__ void __launch_bounds__(256) k_carrier_kernel(const uint4 *__restrict_
 // running maximum m[i]), and exp2_rn elementwise.
 __global__ void __launch_bounds__(128) test_p8_kernel(int n_groups, const float *__restrict__ acc,
                                                       const float *__restrict__ sig, const float *__restrict__ m,
-                                                      uint32_t *__restrict__ out)
+                                                      uint32_t *__restrict__ out, float zero)
 {
     const int gi = blockIdx.x * blockDim.x + threadIdx.x;
     if (gi >= n_groups)
@@ -1347,7 +1441,7 @@ __global__ void __launch_bounds__(128) test_p8_kernel(int n_groups, const float 
 #pragma unroll
     for (int k = 0; k < 32; ++k)
         x[k] = __float_as_uint(acc[static_cast<size_t>(gi) * 32 + k]);
-    p8_block(x, sig[gi], m[gi], w);
+    p8_block(x, sig[gi], m[gi], zero, w);
 #pragma unroll
     for (int k = 0; k < 8; ++k)
         out[static_cast<size_t>(gi) * 8 + k] = w[k];
@@ -1502,8 +1596,6 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const i
     }
 
     FwdParams prm;
-    prm.q_codes = kFuseQ ? nullptr : static_cast<const int8_t *>(q);
-    prm.q_bf16 = kFuseQ ? static_cast<const __nv_bfloat16 *>(q) : nullptr;
     prm.q_scales = q_scales;
     prm.k_scales = k_scales;
     prm.v_scales = v_scales;
@@ -1529,9 +1621,11 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const i
     prm.nq32 = static_cast<int>(g.nq32);
     prm.nbq = static_cast<int>(g.nbq);
     prm.nbk = static_cast<int>(g.nbk);
-    prm.nk32 = static_cast<int>(g.nk32);
-    prm.k_codes = k_codes;
     const float sm = g.sm_scale > 0.0f ? g.sm_scale : 1.0f / sqrtf(static_cast<float>(HD));
+    prm.q_codes = kFuseQ ? nullptr : static_cast<const int8_t *>(q);
+    prm.q_bf16 = kFuseQ ? static_cast<const __nv_bfloat16 *>(q) : nullptr;
+    prm.k_carrier = static_cast<const uint4 *>(k_carrier);
+    prm.zero = 0.0f;
     prm.c0 = sm * 1.44269504088896340736f;
 #ifdef SATTN_DEBUG_DUMP
     prm.dbg = debug_dump_buffer();
@@ -1580,7 +1674,7 @@ cudaError_t launch_test_p8_codes(int n_groups, const float *acc, const float *si
     if (n_groups < 1)
         return cudaSuccess;
     test_p8_kernel<<<(n_groups + 127) / 128, 128, 0, stream>>>(n_groups, acc, sig, m,
-                                                               reinterpret_cast<uint32_t *>(out));
+                                                               reinterpret_cast<uint32_t *>(out), 0.0f);
     return cudaGetLastError();
 }
 

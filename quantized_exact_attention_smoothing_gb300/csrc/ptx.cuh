@@ -34,6 +34,18 @@ __device__ __forceinline__ uint32_t f16x2_of_i8(uint32_t word, int byte)
     return h;
 }
 
+// The INT8 codes of four FP16 integers of magnitude <= 127 (two f16x2 words,
+// element 0 in the low half of a): adding 1536 = 0x6600 puts each in
+// [1409, 1663], where the FP16 step is 1, so the sum is exact and its low
+// byte is the two's-complement code.
+__device__ __forceinline__ uint32_t i8x4_of_f16x2(uint32_t a, uint32_t b)
+{
+    uint32_t ta, tb;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(ta) : "r"(a), "r"(0x66006600u));
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(tb) : "r"(b), "r"(0x66006600u));
+    return __byte_perm(ta, tb, 0x6420u);
+}
+
 // Read-only global load that the compiler may not move: issued where written,
 // so a value needed one loop iteration later hides its latency.
 __device__ __forceinline__ float ld_nc_f32(const float *p)
@@ -58,6 +70,22 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
 }
 
 // st_shared_v4 when `pred` holds, as one predicated instruction (no branch).
+// If a != b: store {d0, d1, d2, d3} at the shared address and set `bit` in
+// mask (one predicate, no branch).
+__device__ __forceinline__ void park_if_differ(uint32_t a, uint32_t b, uint32_t addr, uint32_t d0, uint32_t d1,
+                                               uint32_t d2, uint32_t d3, uint32_t &mask, uint32_t bit)
+{
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " setp.ne.u32 p, %1, %2;\n"
+        " @p st.shared.v4.b32 [%3], {%4, %5, %6, %7};\n"
+        " @p or.b32 %0, %0, %8;\n"
+        "}\n"
+        : "+r"(mask)
+        : "r"(a), "r"(b), "r"(addr), "r"(d0), "r"(d1), "r"(d2), "r"(d3), "r"(bit));
+}
+
 __device__ __forceinline__ void st_shared_v4_if(bool pred, uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                                 uint32_t d)
 {
@@ -445,6 +473,12 @@ __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b)
 {
     uint64_t d;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
 }
 __device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b)

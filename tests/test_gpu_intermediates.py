@@ -31,6 +31,11 @@ pytestmark = pytest.mark.gpu
 TILE = 256
 DBG_S, DBG_P8, DBG_PV, DBG_M1, DBG_A1, DBG_D1, DBG_RO1, DBG_DF, DBG_RCP = (
     0, 32768, 40960, 83000, 83128, 83256, 83384, 99768, 99896)
+# debug builds read a test mode here: 1 (2) = one (two) P8 words of each row and
+# tile are taken as undecided, so that the forward's exact fix-up runs on
+# every tile: from the parked exponent arguments (one word) or by recomputing
+# the blocks from the codes (two words)
+DBG_MODE = 60012
 
 
 @pytest.fixture(scope="module")
@@ -43,7 +48,7 @@ def dbg_lib():
     return lib
 
 
-def _run_dump(lib, q, k, v, causal):
+def _run_dump(lib, q, k, v, causal, mode=0):
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     dq, dk, dv = to_device_bf16(q), to_device_bf16(k), to_device_bf16(v)
     Bn, Hq, Nq, _ = q.shape
@@ -52,6 +57,7 @@ def _run_dump(lib, q, k, v, causal):
     out = torch.empty((Bn, Hq, Nq, 128), dtype=torch.bfloat16, device="cuda")
     fws = torch.zeros(bnd.query_sizes(shape)["forward_workspace"] // 4, dtype=torch.int32, device="cuda")
     dump = torch.zeros(102400, dtype=torch.float32, device="cuda")
+    dump[DBG_MODE] = mode
     s = bnd._stream(None)
     p = bnd._ptr
     assert lib.sattn_prepare(ctypes.byref(shape), p(dq), p(dk), p(dv), p(buf["q_codes"]), p(buf["q_scales"]),
@@ -72,7 +78,8 @@ def _run_dump(lib, q, k, v, causal):
         part=d[DBG_PV:DBG_PV + 128 * 144].reshape(128, 144),
         m1=d[DBG_M1:DBG_M1 + 128], a1=d[DBG_A1:DBG_A1 + 128], d1=d[DBG_D1:DBG_D1 + 128],
         ro1=d[DBG_RO1:DBG_RO1 + 128 * 128].reshape(128, 128),
-        dfin=d[DBG_DF:DBG_DF + 128], rcp=d[DBG_RCP:DBG_RCP + 128])
+        dfin=d[DBG_DF:DBG_DF + 128], rcp=d[DBG_RCP:DBG_RCP + 128],
+        out=out.view(torch.int16).cpu().numpy())
 
 
 SHAPES = [
@@ -115,6 +122,13 @@ def test_intermediates_match_the_oracle(oracle_mod, dbg_lib, shape):
     rcp_own = (np.float32(1) / got["dfin"][:rows].astype(np.float32)).astype(np.float32)
     assert np.array_equal(got["rcp"][:rows], rcp_own), "reciprocal is not the correctly rounded 1/d"
     np.testing.assert_allclose(got["rcp"][:rows], st_end["rcp"][:rows], rtol=2e-5)
+
+    # the fix-up paths forced on every tile give the same bytes, so every
+    # intermediate and the output are identical
+    for mode in (1, 2):
+        forced = _run_dump(dbg_lib, q, k, v, causal, mode)
+        for key in ("s", "p8", "part", "m1", "a1", "d1", "ro1", "dfin", "rcp", "out"):
+            assert np.array_equal(forced[key], got[key]), f"mode {mode}: {key} differs"
 
     # tile 1 (where the item has one): running maximum, alpha, d and RO after the outer update
     if Nkv <= TILE or (causal and min(127, Nq - 1) + (Nkv - Nq) < TILE):

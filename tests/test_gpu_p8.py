@@ -1,12 +1,14 @@
 """The forward's FP8 P step against the oracle, byte for byte ("Experiment
 Log" page, entry "Phase 1 State-Ownership Decision": exact FP8 score bytes).
 
-The kernel takes each byte from ex2.approx with a bracket of +-2^-20 and
+The kernel takes each byte from ex2.approx with a bracket of +-2^-21 and
 recomputes the keys the bracket cannot decide with a correctly rounded exp2
 (float-float arithmetic).  Both halves are checked through the kernel's own
 device functions (test hooks of the C ABI): the bytes of groups of 32 keys on
 random scores, on scores placed within a few FP32 ulps of every E4M3 rounding
-midpoint, and on masked keys; and the exp2 over a dense sample of [-40, 0.5].
+midpoint, on scores whose byte depends on the product acc * sig being
+rounded before the maximum is subtracted, and on masked keys; and the exp2
+over a dense sample of [-40, 0.5].
 """
 import numpy as np
 import pytest
@@ -63,6 +65,23 @@ def test_p8_bytes_random_scores_and_masks(oracle_mod):
     m = ((acc.max(axis=1) * sig).astype(np.float32) + rng.uniform(0, 2, G).astype(np.float32)).astype(np.float32)
     acc[rng.random((G, 32)) < 0.05] = -np.inf     # masked keys carry byte 0
     _check(oracle_mod, acc, sig, m)
+
+
+def test_p8_bytes_keep_both_roundings_of_the_score(oracle_mod):
+    # dd = fl(fl(acc * sig) - m): a fused multiply-add (one rounding) moves dd
+    # by up to an ulp of the product, which near an E4M3 rounding midpoint
+    # changes the byte.  Keep the scores where it does.
+    rng = np.random.default_rng(17)
+    n = 1 << 22
+    acc = rng.integers(-(1 << 21) + 1, 1 << 21, n).astype(np.float32)
+    sig = rng.uniform(1e-4, 3e-4, n).astype(np.float32)
+    s2 = (acc.astype(np.float64) * sig.astype(np.float64)).astype(np.float32)
+    m = (s2.astype(np.float64) + rng.uniform(0, 14, n)).astype(np.float32)
+    fused = (acc.astype(np.longdouble) * sig.astype(np.longdouble) - m.astype(np.longdouble)).astype(np.float32)
+    two = oracle_mod.p8_codes(acc, sig, m)
+    sel = two != oracle_mod.p8_codes(fused, np.float32(1), np.float32(0))
+    assert sel.sum() >= 50, "too few scores that tell the two roundings apart"
+    _check(oracle_mod, np.repeat(acc[sel][:, None], 32, axis=1), sig[sel], m[sel])
 
 
 def test_exp2_is_correctly_rounded(oracle_mod):
