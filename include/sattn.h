@@ -32,7 +32,10 @@
  *             product of the codes, c0 = sm_scale * log2(e) (FP32).
  *   softmax   per KV tile of 256 keys, ascending: m' = max(m, max s2),
  *             alpha = exp2(m - m') (0 while m = -inf),
- *             p8 = E4M3(exp2(s2 - m') * 448);
+ *             p8 = E4M3(fl(fl(exp2(fl(s2 - m'))) * 448)), every step rounded
+ *             to FP32 in this order (s2 rounded before m' is subtracted) and
+ *             exp2 correctly rounded, so each FP8 byte is fixed by the codes
+ *             and scales alone;
  *             RO = RO * alpha + sum_j p8_j * v8_j,  d = d * alpha + sum_j p8_j.
  *   output    out[c] = bf16_rne((RO[c] * (1 / d)) * s_v[c]).
  *   mask      key j of query row i is kept when j < Nkv and, if causal,
@@ -166,9 +169,14 @@ int sattn_prepare(const sattn_shape *shape, const void *q, const void *k, const 
  * HBM bandwidth), then a persistent CTA per SM walks the (query tile, head,
  * batch) items, longest first.
  * Exactness: QK^T is computed from the codes with products and sums that are
- * exact integers; P, PV and the output follow the arithmetic above, with the
- * inner PV sum in the tensor core's FP32 order and exp2 by the hardware
- * approximation.
+ * exact integers.  Every FP8 byte of P is the one the arithmetic above defines:
+ * the kernel encodes fl(2^x) from the hardware approximation (relative error
+ * below 2^-22) scaled by 448 * (1 + 2^-21) and by 448 * (1 - 2^-21); where the
+ * two bytes agree they bracket the exact value and that is the byte, and where
+ * they differ (about 1.5e-5 of the keys) the byte is recomputed with a
+ * correctly rounded 2^x (float-float arithmetic).  alpha uses the hardware
+ * approximation of 2^x; PV and the output follow the arithmetic above with
+ * the inner PV sum in the tensor core's FP32 order.
  */
 int sattn_forward(const sattn_shape *shape, const int8_t *q_codes, const float *q_scales,
                   const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
@@ -249,6 +257,18 @@ int sattn_test_p8_codes(int n_groups, const float *acc, const float *sig, const 
  * gives 0).  Results valid after the stream synchronises.
  */
 int sattn_test_exp2(int n, const float *x, float *out, void *stream);
+
+/*
+ * sattn_profile_events -- measurement hook, not part of the computation: while
+ * set, every sattn_forward / sattn_forward_q_bf16 call records `before` on its
+ * stream just before the attention kernel is launched and `after` just after
+ * it (the K carrier conversion that precedes it is outside the pair), so that
+ * cudaEventElapsedTime(before, after) is that kernel's own duration.  Both are
+ * cudaEvent_t handles owned by the caller (created, with timing, before the
+ * call), or both NULL to stop.  Process-wide, not thread-safe: set it from the
+ * thread that launches.  Returns SATTN_ERR_INVALID if exactly one is NULL.
+ */
+int sattn_profile_events(void *before, void *after);
 
 /*
  * sattn_test_host_chunks -- test hook, not part of the computation: the

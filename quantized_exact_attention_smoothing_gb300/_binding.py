@@ -77,6 +77,7 @@ def load_library(build: bool = True):
     lib.sattn_test_int8_quantiser.argtypes = [ctypes.c_uint32, ctypes.c_uint32, P, P]
     lib.sattn_test_p8_codes.argtypes = [ctypes.c_int, P, P, P, P, P]
     lib.sattn_test_exp2.argtypes = [ctypes.c_int, P, P, P]
+    lib.sattn_profile_events.argtypes = [P, P]
     lib.sattn_graph_create.argtypes = [SP] + [P] * 13 + [ctypes.POINTER(ctypes.c_void_p)]
     lib.sattn_test_host_chunks.argtypes = [SP, ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
                                            ctypes.POINTER(ctypes.c_int)]
@@ -88,7 +89,7 @@ def load_library(build: bool = True):
     for name in ("sattn_query_sizes", "sattn_prepare", "sattn_forward", "sattn_check_status",
                  "sattn_attention_host", "sattn_prepare_noalloc", "sattn_prepare_kv", "sattn_forward_q_bf16",
                  "sattn_test_int8_quantiser", "sattn_graph_create", "sattn_graph_launch", "sattn_graph_destroy",
-                 "sattn_test_host_chunks", "sattn_test_p8_codes", "sattn_test_exp2"):
+                 "sattn_test_host_chunks", "sattn_test_p8_codes", "sattn_test_exp2", "sattn_profile_events"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -358,6 +359,25 @@ def exp2_for_test(x: torch.Tensor) -> torch.Tensor:
     if rc != 0:
         raise SattnError(rc, "sattn_test_exp2")
     return out
+
+
+def profile_events(before=None, after=None) -> None:
+    """sattn_profile_events: while set, each forward records the two
+    torch.cuda.Event objects (created with enable_timing=True) just before and
+    just after its attention kernel; call with no arguments to stop."""
+    if (before is None) != (after is None):
+        raise ValueError("give both events or neither")
+    handles = []
+    for ev in (before, after):
+        if ev is None:
+            handles.append(None)
+            continue
+        if ev.cuda_event == 0:   # torch creates the CUDA event at its first record
+            ev.record()
+        handles.append(ctypes.c_void_p(ev.cuda_event))
+    rc = load_library().sattn_profile_events(*handles)
+    if rc != 0:
+        raise SattnError(rc, "sattn_profile_events")
 
 
 class Graph:

@@ -1471,6 +1471,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 
 }  // namespace
 
+static cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
+void set_profile_events(cudaEvent_t before, cudaEvent_t after)
+{
+    g_ev_before = before;
+    g_ev_after = after;
+}
+
 #ifdef SATTN_DEBUG_DUMP
 static float *g_debug_dump = nullptr;
 float *debug_dump_buffer() { return g_debug_dump; }
@@ -1637,8 +1644,15 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const i
         cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1)
         return static_cast<int>(cudaErrorInvalidDevice);
     const int grid = std::min(prm.n_items, n_sm);
+    if (g_ev_before && cudaEventRecord(g_ev_before, stream) != cudaSuccess)
+        return static_cast<int>(cudaGetLastError());
     attn_fwd_kernel<kFuseQ><<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, tmo, prm);
-    return static_cast<int>(cudaGetLastError());
+    const cudaError_t le = cudaGetLastError();
+    if (le != cudaSuccess)
+        return static_cast<int>(le);
+    if (g_ev_after && cudaEventRecord(g_ev_after, stream) != cudaSuccess)
+        return static_cast<int>(cudaGetLastError());
+    return static_cast<int>(cudaSuccess);
 }
 
 }  // namespace

@@ -502,6 +502,14 @@ int sattn_test_exp2(int n, const float *x, float *out, void *stream)
                : SATTN_ERR_LAUNCH;
 }
 
+int sattn_profile_events(void *before, void *after)
+{
+    if ((before == nullptr) != (after == nullptr))
+        return SATTN_ERR_INVALID;
+    sattn::set_profile_events(static_cast<cudaEvent_t>(before), static_cast<cudaEvent_t>(after));
+    return SATTN_OK;
+}
+
 int sattn_test_host_chunks(const sattn_shape *shape, int n_sm, int64_t *bounds, int *nchunks)
 {
     Geometry g;

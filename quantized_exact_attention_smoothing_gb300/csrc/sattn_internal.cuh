@@ -86,5 +86,8 @@ namespace sattn {
 // kernel's own per-block function; and its correctly rounded exp2.
 cudaError_t launch_test_p8_codes(int n_groups, const float *acc, const float *sig, const float *m, uint8_t *out,
                                  cudaStream_t stream);
+// Events recorded around every attention kernel launch (both null: none).
+void set_profile_events(cudaEvent_t before, cudaEvent_t after);
+
 cudaError_t launch_test_exp2_rn(int n, const float *x, float *out, cudaStream_t stream);
 }  // namespace sattn
