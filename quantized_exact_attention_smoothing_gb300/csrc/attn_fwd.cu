@@ -285,9 +285,12 @@ __device__ __forceinline__ Tile item_tile(const FwdParams &p, int it)
 // t = r ln 2, x = n + r (n the nearest integer, |r| <= 1/2, both exact), in
 // "float-float" arithmetic: each quantity is an unevaluated sum of two FP32
 // values, products split exactly with a fused multiply-add (Dekker) and sums
-// renormalised with the fast two-sum (Dekker; Knuth).  Terms up to t^7 / 7!
-// are carried in float-float, the tail from t^8 / 8! to t^12 / 12! in FP32
-// (its weight t^8 <= 2^-12 keeps its rounding below 2^-47); the result is
+// renormalised with the fast two-sum (Dekker; Knuth).  The series is split as
+// e^t = A(u) + t B(u) with u = t^2 (even and odd terms), two Horner chains in
+// u that run side by side (Estrin's idea: half the dependent steps of one
+// chain in t).  Terms above 2^-23 (up to t^6 / 6! in A, t^5 / 5! in B) are
+// carried in float-float, the tails (t^8 / 8! to t^12 / 12! and t^7 / 7! to
+// t^11 / 11!) in FP32, whose rounding stays below 2^-47; the result is
 // within about 2^-44 of 2^r, so its FP32 rounding is the correctly rounded one
 // unless 2^x lies that close to a point halfway between two FP32 values.
 // The constants are ln 2 and 1/k! split into FP32 high and low parts.
@@ -322,23 +325,27 @@ __device__ __forceinline__ float exp2_rn(float x)
     float tl = __fmaf_rn(r, L1, -th);
     tl = __fmaf_rn(r, L2, tl);
     fast_two_sum(th, tl, th, tl);
-    // tail sum_{k=8..12} t^(k-8) / k!
-    float q = 0x1.1eed8ep-29f;               // 1/12!
-    q = __fmaf_rn(q, th, 0x1.ae6456p-26f);   // 1/11!
-    q = __fmaf_rn(q, th, 0x1.27e4fcp-22f);   // 1/10!
-    q = __fmaf_rn(q, th, 0x1.71de3ap-19f);   // 1/9!
-    q = __fmaf_rn(q, th, 0x1.a01a02p-16f);   // 1/8!
-    float ph = q, pl = 0.0f;
-    ff_horner_step(ph, pl, th, tl, 0x1.a01a02p-13f, -0x1.7f97fap-39f);   // 1/7!
-    ff_horner_step(ph, pl, th, tl, 0x1.6c16c2p-10f, -0x1.27d27ep-35f);   // 1/6!
-    ff_horner_step(ph, pl, th, tl, 0x1.111112p-7f, -0x1.dddddep-32f);    // 1/5!
-    ff_horner_step(ph, pl, th, tl, 0x1.555556p-5f, -0x1.555556p-30f);    // 1/4!
-    ff_horner_step(ph, pl, th, tl, 0x1.555556p-3f, -0x1.555556p-28f);    // 1/3!
-    ff_horner_step(ph, pl, th, tl, 0.5f, 0.0f);                           // 1/2!
-    ff_horner_step(ph, pl, th, tl, 1.0f, 0.0f);                           // 1/1!
-    ff_horner_step(ph, pl, th, tl, 1.0f, 0.0f);                           // 1/0!
-    // ph = RN(ph + pl) after the renormalisation; scale by 2^n (exact, n >= -40)
-    return __fmul_rn(ph, __int_as_float((static_cast<int>(n) + 127) << 23));
+    // e^t = A(u) + t B(u), u = t^2: two independent Horner chains in u
+    float uh = __fmul_rn(th, th);
+    float ul = __fmaf_rn(th, th, -uh);
+    ul = __fmaf_rn(__fadd_rn(th, th), tl, ul);
+    fast_two_sum(uh, ul, uh, ul);
+    // FP32 tails (terms below 2^-23): A from u^4 / 8!, B from u^3 / 7!
+    float qa = __fmaf_rn(0x1.1eed8ep-29f, uh, 0x1.27e4fcp-22f);   // 1/12!, 1/10!
+    qa = __fmaf_rn(qa, uh, 0x1.a01a02p-16f);                      // 1/8!
+    float qb = __fmaf_rn(0x1.ae6456p-26f, uh, 0x1.71de3ap-19f);   // 1/11!, 1/9!
+    qb = __fmaf_rn(qb, uh, 0x1.a01a02p-13f);                      // 1/7!
+    float ah = qa, al = 0.0f, bh = qb, bl = 0.0f;
+    ff_horner_step(ah, al, uh, ul, 0x1.6c16c2p-10f, -0x1.27d27ep-35f);   // 1/6!
+    ff_horner_step(bh, bl, uh, ul, 0x1.111112p-7f, -0x1.dddddep-32f);    // 1/5!
+    ff_horner_step(ah, al, uh, ul, 0x1.555556p-5f, -0x1.555556p-30f);    // 1/4!
+    ff_horner_step(bh, bl, uh, ul, 0x1.555556p-3f, -0x1.555556p-28f);    // 1/3!
+    ff_horner_step(ah, al, uh, ul, 0.5f, 0.0f);                           // 1/2!
+    ff_horner_step(bh, bl, uh, ul, 1.0f, 0.0f);                           // 1/1!
+    ff_horner_step(ah, al, uh, ul, 1.0f, 0.0f);                           // 1/0!
+    ff_horner_step(bh, bl, th, tl, ah, al);                               // A + t B
+    // bh = RN(bh + bl) after the renormalisation; scale by 2^n (exact, n >= -40)
+    return __fmul_rn(bh, __int_as_float((static_cast<int>(n) + 127) << 23));
 }
 
 // The FP8 byte of one key, every step in the stated order (the slow path).
@@ -432,15 +439,6 @@ __device__ __forceinline__ void p8_block_park(const uint32_t (&x)[32], float sig
     }
 }
 
-// The exact FP8 byte of one key from its exponent argument dd.
-__device__ __forceinline__ uint32_t p8_of_dd(float dd)
-{
-    const float e = ptx::ex2_approx(dd);
-    const uint32_t hi = ptx::cvt_e4m3x2(0.0f, __fmul_rn(e, kP8Hi)) & 0xffu;
-    const uint32_t lo = ptx::cvt_e4m3x2(0.0f, __fmul_rn(e, kP8Lo)) & 0xffu;
-    return hi == lo ? hi : ptx::cvt_e4m3x2(0.0f, __fmul_rn(exp2_rn(dd), 448.0f)) & 0xffu;
-}
-
 // Fix-up of one block (rare): the bytes again, with the undecided keys
 // recomputed by p8_exact.
 __device__ __forceinline__ void p8_block_fix(const uint32_t (&x)[32], float sig, float mu, float zero,
@@ -492,10 +490,6 @@ __device__ __forceinline__ int block_accumulators(const FwdParams &p, const Tile
 {
     const int ch = lane & 15;   // channel chunk: channels 8 ch .. 8 ch + 7
     const uint4 *kb = p.k_carrier + (static_cast<size_t>(t.b * p.Hkv + t.hk) * p.Nkv + key0) * (HD / 8);
-    uint4 kv[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        kv[i] = (key0 + 2 * i + (lane >> 4) < p.Nkv) ? __ldg(kb + 32 * i + lane) : make_uint4(0u, 0u, 0u, 0u);
     uint32_t q0 = 0, q1 = 0;   // Q codes of the chunk
     if (t.q0 + r < p.Nq) {     // (a pad row's codes are all 0)
         if (q_smem) {
@@ -514,11 +508,24 @@ __device__ __forceinline__ int block_accumulators(const FwdParams &p, const Tile
             q0 = c.x, q1 = c.y;
         }
     }
+    // the 16 loads in four rounds of four (few registers: this runs beside
+    // the tile's live state)
     int part[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-        part[i] = __dp4a(static_cast<int>(q1), static_cast<int>(ptx::i8x4_of_f16x2(kv[i].z, kv[i].w)),
-                         __dp4a(static_cast<int>(q0), static_cast<int>(ptx::i8x4_of_f16x2(kv[i].x, kv[i].y)), 0));
+    for (int rd = 0; rd < 4; ++rd) {
+        uint4 kv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int ii = 4 * rd + i;
+            kv[i] = (key0 + 2 * ii + (lane >> 4) < p.Nkv) ? __ldg(kb + 32 * ii + lane) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            part[4 * rd + i] =
+                __dp4a(static_cast<int>(q1), static_cast<int>(ptx::i8x4_of_f16x2(kv[i].z, kv[i].w)),
+                       __dp4a(static_cast<int>(q0), static_cast<int>(ptx::i8x4_of_f16x2(kv[i].x, kv[i].y)), 0));
+        asm volatile("" ::: "memory");   // keep the next round's loads after these
+    }
     // butterfly: at the step over lane bit b, the lane with bit b clear keeps
     // the entries whose index has bit b clear; after four steps lane l holds
     // the half-warp's sum for entry i = l % 16
@@ -543,6 +550,50 @@ __device__ __forceinline__ uint32_t p8_byte(uint32_t x, float sig, float mu)
     const uint32_t hi = ptx::cvt_e4m3x2(0.0f, __fmul_rn(e, kP8Hi)) & 0xffu;
     const uint32_t lo = ptx::cvt_e4m3x2(0.0f, __fmul_rn(e, kP8Lo)) & 0xffu;
     return hi == lo ? hi : p8_exact(__uint_as_float(x), sig, mu);
+}
+
+// The forward's rare-of-rare P fix-up: lanes whose bit c of
+// `pend` is set have several undecided words and get their block c redone.
+// For block c of the row of lane e, the warp recomputes the 32 accumulators
+// from the codes (exact, so equal to the tensor core's), each lane the byte of
+// one key with p8_byte, and lane e takes the gathered words into its P8 words
+// pw (word 8c + w = keys 32c + 4w .. 32c + 4w + 3 of this half).  The block
+// scale product of block c is the same for the warp's 32 rows (one Q block).
+__device__ __forceinline__ void p8_fix_blocks(const FwdParams &p, const Tile &t, uint32_t pend, int quarter, int half,
+                                           int j, int lane, float mu, float sig0, float sig1, float sig2, float sig3,
+                                           float sq, uint32_t sb, uint32_t (&pw)[32])
+{
+#pragma unroll 1
+    for (;;) {
+        const uint32_t bal = __ballot_sync(0xffffffffu, pend != 0u);
+        if (bal == 0u)
+            break;
+        const int e = __ffs(bal) - 1;
+        const int c = __ffs(__shfl_sync(0xffffffffu, pend, e)) - 1;
+        if (lane == e)
+            pend &= pend - 1u;
+        const float mue = __shfl_sync(0xffffffffu, mu, e);
+        const float sg = (c == 0) ? sig0 : (c == 1) ? sig1 : (c == 2) ? sig2 : sig3;
+        const int re = quarter * 32 + e;
+        const int key0 = j * BN + 128 * half + 32 * c;
+        const int kl = 2 * (lane & 15) + (lane >> 4);   // this lane's key of the block
+        const int lime = p.causal ? t.q0 + re + (p.Nkv - p.Nq) : 0x7fffffff;
+        const int acc = block_accumulators(p, t, re, key0, sq, sb, j + 2 < t.ntiles, lane);
+        const uint32_t xk = (key0 + kl <= min(p.Nkv - 1, lime)) ? __float_as_uint(static_cast<float>(acc))
+                                                                 : 0xff800000u;   // a masked key
+        uint32_t v = p8_byte(xk, sg, mue) << (8 * (kl & 3));
+        // keys 4w, 4w + 2 sit in lanes 2w, 2w + 1 and keys 4w + 1, 4w + 3 in
+        // lanes 2w + 16, 2w + 17: two exchanges assemble word w in lane 2w
+        v |= __shfl_xor_sync(0xffffffffu, v, 1);
+        v |= __shfl_xor_sync(0xffffffffu, v, 16);
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            const uint32_t wd = __shfl_sync(0xffffffffu, v, 2 * w);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+                pw[8 * cc + w] = (lane == e && c == cc) ? wd : pw[8 * cc + w];
+        }
+    }
 }
 
 // Both, for one block (the test hook's entry).
@@ -1071,25 +1122,20 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
             const float mn = fmaxf(m, tmax);
             const float alpha = (m == -INFINITY) ? 0.0f : ptx::ex2_approx(__fsub_rn(m, mn));
             // P8 = E4M3(fl(fl(2^fl(fl(acc * sig) - m')) * 448)), four keys per
-            // 32-bit word, written 32 keys (8 columns) at a time into TMEM
-            // columns [TM_P + 32h, TM_P + 32h + 32) of this row's lane, where PV
-            // reads them as its A operand; the columns are free once the
-            // previous PV has completed.  A row with no kept key so far (mn =
+            // 32-bit word, written in one store into TMEM columns [TM_P + 32h,
+            // TM_P + 32h + 32) of this row's lane, where PV reads them as its A
+            // operand; the columns are free once the previous PV has completed.  A row with no kept key so far (mn =
             // -inf) has only -inf scores, which any finite maximum maps to 0.
             const float mu = (mn == -INFINITY) ? 0.0f : mn;
             // Rare (about 1.5e-5 of the keys): a key within 2^-21 of an E4M3
             // rounding midpoint.  The loop has no branch on it: a word (four
             // keys) with such a key leaves its four exponent arguments in the
-            // thread's slot and its bit in wmask.  Then one vote: if any lane
-            // of the warp has such a word, the warp rewrites them.  A lane with
-            // one word recomputes its four bytes from the slot (p8_of_dd).  A
-            // lane with more (rare again) has its blocks redone one at a time:
-            // for block c of the row of lane e, the warp recomputes the 32
-            // accumulators from the codes (exact, so equal to the tensor
-            // core's), each lane the byte of one key with p8_byte; lane e
-            // gathers the 32 bytes and rewrites its eight words of the block in
-            // TMEM.  The block scale product sig[c] is the same for the warp's
-            // 32 rows (one Q block).
+            // thread's slot and its bit in wmask.  The 32 words stay in
+            // registers; one vote: if any lane of the warp has such a word, the
+            // warp rewrites them there.  A lane with one word recomputes its
+            // four bytes from the slot.  A lane with more (rare
+            // again) has its blocks redone from the codes (p8_fix_blocks).
+            // Then the words go to TMEM in one store.
             const uint32_t slot = sb + OFF_PARK + (half * BM + r) * 16;
             uint32_t wmask = 0;   // bit 8c + w: word w of block c holds an undecided key
             uint32_t force = 0;
@@ -1099,13 +1145,14 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
                 force = (mode >= 1 ? 1u << ((r + j) & 31) : 0u) | (mode >= 2 ? 1u << ((r + j + 7) & 31) : 0u);
             }
 #endif
+            uint32_t pw[32];   // P8 words of this half: word 8c + w holds keys 32c + 4w .. 32c + 4w + 3
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t pk[8];
                 p8_block_park(s[c], sig[c], mu, p.zero, pk, slot, c, wmask, force);
-                if (c == 0 && gj >= 1 && !wt.wait(bar(PDONE), (gj - 1) & 1, SITE_PDONE))
-                    return false;
-                ptx::tmem_st8(taddr + TM_P + 32 * half + 8 * c, pk);
+#pragma unroll
+                for (int w = 0; w < 8; ++w)
+                    pw[8 * c + w] = pk[w];
             }
             if (__any_sync(0xffffffffu, wmask != 0u)) {
                 uint32_t und = 0;   // bit c: block c holds an undecided word
@@ -1117,69 +1164,37 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
                 if (p.dbg)
                     atomicAdd(p.dbg + 60000, static_cast<float>(__popc(und)));   // undecided blocks seen
 #endif
-                ptx::tmem_wait_st();   // the stores of the pass are complete before blocks are read back
                 const bool one = wmask != 0u && (wmask & (wmask - 1u)) == 0u;
-                const int wi = __ffs(wmask) - 1;
-                uint32_t word = 0;
-                if (one) {
+                if (one) {   // the parked word: both brackets per key, the exact path per undecided key
+                    const int wi = __ffs(wmask) - 1;
                     const uint4 dq = ptx::ld_shared_v4(slot);
-                    word = p8_of_dd(__uint_as_float(dq.x)) | (p8_of_dd(__uint_as_float(dq.y)) << 8) |
-                           (p8_of_dd(__uint_as_float(dq.z)) << 16) | (p8_of_dd(__uint_as_float(dq.w)) << 24);
-                }
-                const uint32_t blocks1 = __reduce_or_sync(0xffffffffu, one ? (1u << (wi >> 3)) : 0u);
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    if (!((blocks1 >> c) & 1u))
-                        continue;
-                    uint32_t pk[8];
-                    ptx::tmem_ld8(taddr + TM_P + 32 * half + 8 * static_cast<uint32_t>(c), pk);
-                    ptx::tmem_wait_ld();
+                    const float dd[4] = {__uint_as_float(dq.x), __uint_as_float(dq.y), __uint_as_float(dq.z),
+                                         __uint_as_float(dq.w)};
+                    uint32_t word = 0, undk = 0;
 #pragma unroll
-                    for (int w = 0; w < 8; ++w)
-                        pk[w] = (one && wi == 8 * c + w) ? word : pk[w];
-                    ptx::tmem_st8(taddr + TM_P + 32 * half + 8 * static_cast<uint32_t>(c), pk);
-                }
-                if (one)
+                    for (int u = 0; u < 4; ++u) {
+                        const float e = ptx::ex2_approx(dd[u]);
+                        const uint32_t hi = ptx::cvt_e4m3x2(0.0f, __fmul_rn(e, kP8Hi)) & 0xffu;
+                        const uint32_t lo = ptx::cvt_e4m3x2(0.0f, __fmul_rn(e, kP8Lo)) & 0xffu;
+                        word |= hi << (8 * u);
+                        undk |= (hi != lo) ? (1u << u) : 0u;
+                    }
+#pragma unroll 1
+                    while (undk != 0u) {   // one copy of the correctly rounded exp2
+                        const int u = __ffs(undk) - 1;
+                        undk &= undk - 1u;
+                        const float x = (u == 0) ? dd[0] : (u == 1) ? dd[1] : (u == 2) ? dd[2] : dd[3];
+                        const uint32_t code = ptx::cvt_e4m3x2(0.0f, __fmul_rn(exp2_rn(x), 448.0f)) & 0xffu;
+                        word = (word & ~(0xffu << (8 * u))) | (code << (8 * u));
+                    }
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        pw[k] = (wi == k) ? word : pw[k];
                     und = 0u;
-                uint32_t pend = und;
-#pragma unroll 1
-                for (;;) {
-                    const uint32_t bal = __ballot_sync(0xffffffffu, pend != 0u);
-                    if (bal == 0u)
-                        break;
-                    const int e = __ffs(bal) - 1;
-                    const int c = __ffs(__shfl_sync(0xffffffffu, pend, e)) - 1;
-                    if (lane == e)
-                        pend &= pend - 1u;
-                    const float mue = __shfl_sync(0xffffffffu, mu, e);
-                    const float sg = (c == 0) ? sig[0] : (c == 1) ? sig[1] : (c == 2) ? sig[2] : sig[3];
-                    const int re = quarter * 32 + e;
-                    const int key0 = j * BN + 128 * half + 32 * c;
-                    const int kl = 2 * (lane & 15) + (lane >> 4);   // this lane's key of the block
-                    const int lime = p.causal ? t.q0 + re + (p.Nkv - p.Nq) : 0x7fffffff;
-                    const int acc = block_accumulators(p, t, re, key0, sq, sb, j + 2 < t.ntiles, lane);
-                    const uint32_t xk = (key0 + kl <= min(p.Nkv - 1, lime)) ? __float_as_uint(static_cast<float>(acc))
-                                                                             : 0xff800000u;   // a masked key
-                    uint32_t v = p8_byte(xk, sg, mue) << (8 * (kl & 3));
-                    // keys 4w, 4w + 2 sit in lanes 2w, 2w + 1 and keys 4w + 1, 4w + 3 in
-                    // lanes 2w + 16, 2w + 17: two exchanges assemble word w in lane 2w
-                    v |= __shfl_xor_sync(0xffffffffu, v, 1);
-                    v |= __shfl_xor_sync(0xffffffffu, v, 16);
-                    uint32_t wd[8];
-#pragma unroll
-                    for (int w = 0; w < 8; ++w)
-                        wd[w] = __shfl_sync(0xffffffffu, v, 2 * w);
-                    ptx::tmem_wait_st();   // earlier stores of the block are complete before it is read back
-                    uint32_t pk[8];
-                    ptx::tmem_ld8(taddr + TM_P + 32 * half + 8 * static_cast<uint32_t>(c), pk);
-                    ptx::tmem_wait_ld();
-#pragma unroll
-                    for (int w = 0; w < 8; ++w)
-                        pk[w] = (lane == e) ? wd[w] : pk[w];
-                    ptx::tmem_st8(taddr + TM_P + 32 * half + 8 * static_cast<uint32_t>(c), pk);
                 }
+                if (__any_sync(0xffffffffu, und != 0u))
+                    p8_fix_blocks(p, t, und, quarter, half, j, lane, mu, sig[0], sig[1], sig[2], sig[3], sq, sb, pw);
 #ifdef SATTN_DEBUG_DUMP
-                ptx::tmem_wait_st();   // (the whole warp: the wait is a warp-wide instruction)
                 if (p.dbg && lane == 0) {   // cycles in the fix-up and its count, per warp
                     atomicAdd(reinterpret_cast<unsigned long long *>(p.dbg + 60002),
                               static_cast<unsigned long long>(clock64() - fix_t0));
@@ -1187,6 +1202,10 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
                 }
 #endif
             }
+            // the P8 columns are free once the previous tile's PV has completed
+            if (gj >= 1 && !wt.wait(bar(PDONE), (gj - 1) & 1, SITE_PDONE))
+                return false;
+            ptx::tmem_st32(taddr + TM_P + 32 * half, pw);
 #ifdef SATTN_DEBUG_DUMP
             if (p.dbg && j == 0 && t.q0 == 0 && t.hq == 0 && t.b == 0) {   // the bytes as PV will read them
                 ptx::tmem_wait_st();
