@@ -183,6 +183,25 @@ int sattn_forward(const sattn_shape *shape, const int8_t *q_codes, const float *
                   const float *v_scales, void *out, void *workspace, void *stream);
 
 /*
+ * sattn_attention_small -- sattn_prepare followed by sattn_forward in one
+ * kernel launch, for one query tile of one head: B = Hq = Hkv = 1, Nq <= 128,
+ * Nkv <= 1024 (the small-shape latency path; same page entries as the two
+ * calls).  The CTA first runs the preparation with the preparation kernels'
+ * own per-thread steps, writing every buffer sattn_prepare writes with the
+ * same bytes, then attends exactly as sattn_forward, so `out` equals the
+ * two-call result byte for byte.
+ *   q, k, v              in: BF16 [1][1][N][128]
+ *   q_codes .. v_scales  out: as sattn_prepare (sizes from sattn_query_sizes)
+ *   out                  out: BF16 [1][1][Nq][128]
+ *   workspace            sizes.forward_workspace bytes, as for sattn_forward
+ *                        (no preparation workspace is needed)
+ * Returns SATTN_ERR_INVALID for other shapes; other errors as sattn_forward.
+ */
+int sattn_attention_small(const sattn_shape *shape, const void *q, const void *k, const void *v, int8_t *q_codes,
+                          float *q_scales, int8_t *k_codes, float *k_scales, float *k_mean, uint8_t *v_codes,
+                          float *v_scales, void *out, void *workspace, void *stream);
+
+/*
  * sattn_prepare_kv -- the K and V part of sattn_prepare (K smoothing, INT8
  * K, FP8 V; same page entry), for sattn_forward_q_bf16, which quantises Q
  * itself.  Arguments as in sattn_prepare without q, q_codes and q_scales;

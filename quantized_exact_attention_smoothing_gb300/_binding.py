@@ -78,6 +78,7 @@ def load_library(build: bool = True):
     lib.sattn_test_p8_codes.argtypes = [ctypes.c_int, P, P, P, P, P]
     lib.sattn_test_exp2.argtypes = [ctypes.c_int, P, P, P]
     lib.sattn_profile_events.argtypes = [P, P]
+    lib.sattn_attention_small.argtypes = [SP] + [P] * 13
     lib.sattn_graph_create.argtypes = [SP] + [P] * 13 + [ctypes.POINTER(ctypes.c_void_p)]
     lib.sattn_test_host_chunks.argtypes = [SP, ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
                                            ctypes.POINTER(ctypes.c_int)]
@@ -89,7 +90,8 @@ def load_library(build: bool = True):
     for name in ("sattn_query_sizes", "sattn_prepare", "sattn_forward", "sattn_check_status",
                  "sattn_attention_host", "sattn_prepare_noalloc", "sattn_prepare_kv", "sattn_forward_q_bf16",
                  "sattn_test_int8_quantiser", "sattn_graph_create", "sattn_graph_launch", "sattn_graph_destroy",
-                 "sattn_test_host_chunks", "sattn_test_p8_codes", "sattn_test_exp2", "sattn_profile_events"):
+                 "sattn_test_host_chunks", "sattn_test_p8_codes", "sattn_test_exp2", "sattn_profile_events",
+                 "sattn_attention_small"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -248,6 +250,42 @@ def forward(prep: dict, out: torch.Tensor | None = None, workspace: torch.Tensor
     if rc != 0:
         raise SattnError(rc, "sattn_forward")
     return out
+
+
+SMALL_MAX_NKV = 1024
+
+
+def small_shape_ok(B: int, Hq: int, Hkv: int, Nq: int, Nkv: int) -> bool:
+    """Whether sattn_attention_small takes this shape (one query tile of one head)."""
+    return B == 1 and Hq == 1 and Hkv == 1 and Nq <= 128 and Nkv <= SMALL_MAX_NKV
+
+
+def attention_small(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                    sm_scale: float = 0.0, buffers: dict | None = None, out: torch.Tensor | None = None,
+                    workspace: torch.Tensor | None = None, stream=None) -> tuple:
+    """sattn_attention_small: preparation and attention in one launch for a
+    single query tile of one head.  Returns (out, buffers); the buffers hold
+    what prepare() would write."""
+    _need_cuda(q, k, v)
+    _need_inputs(q, k, v)
+    B, Hq, Nq, _ = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    shape = make_shape(B, Hq, Hkv, Nq, Nkv, causal, sm_scale)
+    if buffers is None:
+        buffers = prepare_buffers(shape, q.device)
+    if out is None:
+        out = torch.empty((B, Hq, Nq, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
+    if workspace is None:
+        workspace = _empty(query_sizes(shape)["forward_workspace"], q.device)
+    _need_cuda(out, workspace)
+    rc = load_library().sattn_attention_small(
+        ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(buffers["q_codes"]), _ptr(buffers["q_scales"]),
+        _ptr(buffers["k_codes"]), _ptr(buffers["k_scales"]), _ptr(buffers["k_mean"]), _ptr(buffers["v_codes"]),
+        _ptr(buffers["v_scales"]), _ptr(out), _ptr(workspace), _stream(stream))
+    if rc != 0:
+        raise SattnError(rc, "sattn_attention_small")
+    buffers["forward_workspace"] = workspace
+    return out, buffers
 
 
 def prepare_kv(k: torch.Tensor, v: torch.Tensor, Hq: int, Nq: int, causal: bool = False,

@@ -73,6 +73,7 @@
 
 #include <cudaTypedefs.h>
 
+#include "prep_device.cuh"
 #include "ptx.cuh"
 #include "quant.cuh"
 #include "sattn_internal.cuh"
@@ -166,6 +167,8 @@ struct FwdParams {
     int nq32, nbq, nbk;
     float c0;
     float zero;   // always +0 (see dd_pair)
+    int small;    // the single-launch small-shape path: prepare `sp` first (small_prepare)
+    SmallPrep sp;
 #ifdef SATTN_DEBUG_DUMP
     // intermediates of query tile 0 of (batch 0, head 0), KV tile 0:
     // [0, 32768) raw S accumulators (128 x 256), [32768, 40960) P8 words
@@ -933,14 +936,15 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
 
     auto qscale = [&](const Tile &tq) {
         const int i = tq.q0 + r;
-        return i < p.nq32 ? ptx::ld_nc_f32(p.q_scales + static_cast<size_t>(tq.b * p.Hq + tq.hq) * p.nbq + i / kQBlock)
-                          : 0.0f;
+        const float *a = p.q_scales + static_cast<size_t>(tq.b * p.Hq + tq.hq) * p.nbq + i / kQBlock;
+        return i < p.nq32 ? (p.small ? ptx::ld_f32(a) : ptx::ld_nc_f32(a)) : 0.0f;
     };
     // block scales of this half's four 32-key blocks of tile j of an item
     auto kscale = [&](const Tile &tk, int j, int c) {
         const int kb = j * (BN / kQBlock) + 4 * half + c;
         // (the load is pinned here: it is consumed one tile later)
-        return kb < p.nbk ? ptx::ld_nc_f32(p.k_scales + static_cast<size_t>(tk.b * p.Hkv + tk.hk) * p.nbk + kb) : 0.0f;
+        const float *a = p.k_scales + static_cast<size_t>(tk.b * p.Hkv + tk.hk) * p.nbk + kb;
+        return kb < p.nbk ? (p.small ? ptx::ld_f32(a) : ptx::ld_nc_f32(a)) : 0.0f;
     };
 
     int it = blockIdx.x;
@@ -1319,6 +1323,87 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, const CUtensorM
     }
 }
 
+// The single-launch small-shape path (one query tile of one head, Nkv <=
+// kSmallMaxNkv): all threads of the CTA run the preparation of the
+// preparation kernels, through the same device functions (prep_device.cuh),
+// so the buffers hold the same bytes: K column sums per 64-token chunk and
+// V column maxima, their ordered totals (mean, V scale), then the INT8 K
+// blocks, the FP8 V tiles and the INT8 Q blocks (256 threads, a named
+// barrier), then the FP16 carrier of the K codes.  Scratch: the K ring's
+// shared memory, which the pipeline fills only afterwards.  The writes are
+// ordered before the pipeline's TMA reads by a proxy fence and a CTA barrier.
+__device__ __forceinline__ void small_prepare(const FwdParams &p, uint8_t *smem)
+{
+    const SmallPrep &sp = p.sp;
+    const int tid = threadIdx.x;
+    const int Nkv = p.Nkv, Nq = p.Nq;
+    const int nch = (Nkv + kMeanChunk - 1) / kMeanChunk;   // <= 16
+    float *ks = reinterpret_cast<float *>(smem + OFF_K);         // [16][128] chunk sums of K
+    float *vm = ks + 16 * HD;                                      // [16][128] chunk maxima of |V|
+    float *mean = vm + 16 * HD, *sv = mean + HD, *rv = sv + HD;    // [128] each
+    float *warp_max = rv + HD;                                     // [8]
+    uint32_t *vtile = reinterpret_cast<uint32_t *>(smem + OFF_K + 24 * 1024);   // [128][32] words
+    const uint4 *k4 = static_cast<const uint4 *>(sp.k), *v4 = static_cast<const uint4 *>(sp.v);
+    if (tid < 16 * nch) {
+        const int chunk = tid >> 4, g = tid & 15;
+        float sum[8], mx[8];
+        prep::chunk_stats8(k4, v4, Nkv, 0, chunk, g, sum, mx);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            ks[chunk * HD + 8 * g + i] = sum[i];
+            vm[chunk * HD + 8 * g + i] = mx[i];
+        }
+    }
+    __syncthreads();
+    if (tid < HD) {   // chunk sums in ascending chunk order, as the finalize kernel
+        float total = 0.0f, amax = 0.0f;
+        for (int ch = 0; ch < nch; ++ch) {
+            total = __fadd_rn(total, ks[ch * HD + tid]);
+            amax = fmaxf(amax, vm[ch * HD + tid]);
+        }
+        const float mu = __fdiv_rn(total, static_cast<float>(Nkv));
+        const float s = __fdiv_rn(amax, 448.0f);
+        mean[tid] = mu;
+        sv[tid] = s;
+        rv[tid] = s > 0.0f ? __frcp_rn(s) : 0.0f;
+        sp.k_mean[tid] = mu;
+        sp.v_scales[tid] = s;
+    }
+    __syncthreads();
+    if (tid < 256) {
+        auto sync256 = [] { asm volatile("bar.sync 1, 256;" ::: "memory"); };
+        const int64_t nk32 = (Nkv + kQBlock - 1) / kQBlock * kQBlock, nq32 = (Nq + kQBlock - 1) / kQBlock * kQBlock;
+        const int64_t nk128 = (Nkv + kVPad - 1) / kVPad * kVPad;
+        for (int blk = 0; blk < p.nbk; ++blk) {
+            prep::quant_block<true>(k4, Nkv, nk32, p.nbk, mean, sp.k_codes, sp.k_scales, 0, blk, tid, warp_max,
+                                    sync256);
+            sync256();
+        }
+        for (int t0 = 0; t0 < nk128; t0 += kVPad) {
+            prep::quant_v_tile(v4, Nkv, nk128, sv, rv, sp.v_codes, 0, t0, tid, vtile, sync256);
+            sync256();
+        }
+        for (int blk = 0; blk < p.nbq; ++blk) {
+            prep::quant_block<false>(static_cast<const uint4 *>(sp.q), Nq, nq32, p.nbq, nullptr, sp.q_codes,
+                                     sp.q_scales, 0, blk, tid, warp_max, sync256);
+            sync256();
+        }
+    }
+    __syncthreads();
+    // the FP16 carrier of the K codes (as k_carrier_kernel)
+    uint4 *dst = const_cast<uint4 *>(p.k_carrier);
+    const uint4 *src = reinterpret_cast<const uint4 *>(sp.k_codes);
+    for (int c = tid; c < Nkv * (HD / 16); c += NTHREADS) {
+        const uint4 a = src[c];
+        dst[2 * c] = make_uint4(ptx::f16x2_of_i8(a.x, 0), ptx::f16x2_of_i8(a.x, 2), ptx::f16x2_of_i8(a.y, 0),
+                                ptx::f16x2_of_i8(a.y, 2));
+        dst[2 * c + 1] = make_uint4(ptx::f16x2_of_i8(a.z, 0), ptx::f16x2_of_i8(a.z, 2), ptx::f16x2_of_i8(a.w, 0),
+                                    ptx::f16x2_of_i8(a.w, 2));
+    }
+    ptx::fence_proxy_async_global();
+    __syncthreads();
+}
+
 template <bool kFuseQ>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -1336,6 +1421,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #endif
     const Waiter wt{p.status};
     volatile uint32_t *flag = reinterpret_cast<volatile uint32_t *>(smem + OFF_FLAG);
+    if (p.small)
+        small_prepare(p, smem);
 
     if (threadIdx.x == 0) {
         *flag = *reinterpret_cast<volatile uint32_t *>(p.status);
@@ -1540,7 +1627,8 @@ cudaError_t kernel_attributes()
 template <bool kFuseQ>
 int launch_impl(const Geometry &g, const void *q, const float *q_scales, const int8_t *k_codes,
                 const float *k_scales, const uint8_t *v_codes, const float *v_scales, void *out,
-                void *status_block, void *k_carrier, cudaStream_t stream, bool withhold_v, bool reset_status)
+                void *status_block, void *k_carrier, cudaStream_t stream, bool withhold_v, bool reset_status,
+                const SmallPrep *small = nullptr)
 {
     auto encode = tensor_map_encoder();
     if (!encode)
@@ -1613,7 +1701,7 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const i
     if (attr_err != cudaSuccess)
         return static_cast<int>(attr_err);
 
-    {   // the FP16 carrier of the K codes, read by the attention kernel's K loader
+    if (!small) {   // the FP16 carrier of the K codes, read by the attention kernel's K loader
         const int64_t nchunk = static_cast<int64_t>(g.Nkv) * (HD / 16);
         const dim3 grid(static_cast<unsigned>((nchunk + 256 * kCarrierUnroll - 1) / (256 * kCarrierUnroll)),
                         static_cast<unsigned>(bhk));
@@ -1652,6 +1740,8 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const i
     prm.q_bf16 = kFuseQ ? static_cast<const __nv_bfloat16 *>(q) : nullptr;
     prm.k_carrier = static_cast<const uint4 *>(k_carrier);
     prm.zero = 0.0f;
+    prm.small = small ? 1 : 0;
+    prm.sp = small ? *small : SmallPrep{};
     prm.c0 = sm * 1.44269504088896340736f;
 #ifdef SATTN_DEBUG_DUMP
     prm.dbg = debug_dump_buffer();
@@ -1699,6 +1789,12 @@ int launch_forward_q_bf16(const Geometry &g, const void *q, const int8_t *k_code
 {
     return launch_impl<true>(g, q, nullptr, k_codes, k_scales, v_codes, v_scales, out, status, carrier, stream,
                              false, true);
+}
+
+int launch_small(const Geometry &g, const SmallPrep &sp, void *out, void *status, void *carrier, cudaStream_t stream)
+{
+    return launch_impl<false>(g, sp.q_codes, sp.q_scales, sp.k_codes, sp.k_scales, sp.v_codes, sp.v_scales, out,
+                              status, carrier, stream, false, true, &sp);
 }
 
 cudaError_t launch_test_p8_codes(int n_groups, const float *acc, const float *sig, const float *m, uint8_t *out,

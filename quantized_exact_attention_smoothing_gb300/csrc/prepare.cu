@@ -14,29 +14,11 @@
 // order, so codes and scales are bit-exact functions of the inputs.
 #include <cuda_bf16.h>
 
-#include "ptx.cuh"
-#include "quant.cuh"
-#include "sattn_internal.cuh"
+#include "prep_device.cuh"
 
 namespace sattn {
 namespace {
 
-__device__ __forceinline__ void unpack8(const uint4 &a, float (&f)[8])
-{
-    f[0] = bf16_lo(a.x); f[1] = bf16_hi(a.x);
-    f[2] = bf16_lo(a.y); f[3] = bf16_hi(a.y);
-    f[4] = bf16_lo(a.z); f[5] = bf16_hi(a.z);
-    f[6] = bf16_lo(a.w); f[7] = bf16_hi(a.w);
-}
-
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p)
-{
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
 
 // Block: 16 chunks x 16 channel groups of 8 channels.  Each thread walks its
 // chunk's tokens in ascending order, one FP32 add per token and channel.
@@ -50,32 +32,8 @@ __global__ void __launch_bounds__(256) kv_chunk_stats_kernel(const uint4 *__rest
     const int chunk = blockIdx.x * 16 + (threadIdx.x >> 4);
     if (chunk >= nchunks)
         return;
-    const int t0 = chunk * kMeanChunk;
-    const int t1 = min(Nkv, t0 + kMeanChunk);
-    const size_t row0 = static_cast<size_t>(bh) * Nkv + t0;
-    const uint4 *kp = k + row0 * 16 + g;
-    const uint4 *vp = v + row0 * 16 + g;
-    float s[8], mx[8], f[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        s[i] = 0.0f;
-        mx[i] = 0.0f;
-    }
-#pragma unroll 16
-    for (int t = t0; t < t1; ++t) {
-        const uint4 a = ld_stream(kp);
-        const uint4 c = ld_stream(vp);
-        kp += 16;
-        vp += 16;
-        unpack8(a, f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            s[i] = __fadd_rn(s[i], f[i]);
-        unpack8(c, f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            mx[i] = fmaxf(mx[i], fabsf(f[i]));
-    }
+    float s[8], mx[8];
+    prep::chunk_stats8(k, v, Nkv, bh, chunk, g, s, mx);
     const size_t o = (static_cast<size_t>(bh) * nchunks + chunk) * kHeadDim + g * 8;
     reinterpret_cast<float4 *>(ksum + o)[0] = make_float4(s[0], s[1], s[2], s[3]);
     reinterpret_cast<float4 *>(ksum + o)[1] = make_float4(s[4], s[5], s[6], s[7]);
@@ -115,20 +73,6 @@ __global__ void __launch_bounds__(128) kv_finalize_kernel(const float *__restric
     v_scales[bh * kHeadDim + c] = __fdiv_rn(amax, 448.0f);
 }
 
-// E4M3(fl(v / s)) (round to nearest even, saturating) without a division in
-// the common case: y = fl(v * fl(1/s)) is within 3 ulp (relative 2^-22.4) of
-// fl(v / s), so if y * (1 - 2^-21) and y * (1 + 2^-21) round to the same code
-// (the conversion is monotonic), fl(v / s) does too.  Otherwise (values near a
-// rounding midpoint) the IEEE division decides.  Returns the byte.
-__device__ __forceinline__ uint32_t e4m3_code(float v, float s, float rs)
-{
-    const float y = __fmul_rn(v, rs);
-    const uint32_t two = ptx::cvt_e4m3x2(__fmul_rn(y, 1.0f + 0x1p-21f), __fmul_rn(y, 1.0f - 0x1p-21f));
-    if ((two & 0xffu) == (two >> 8))
-        return two & 0xffu;
-    return ptx::cvt_e4m3x2(0.0f, __fdiv_rn(v, s)) & 0xffu;
-}
-
 // One CTA per 32-token block of one head; thread = (token, eighth of the
 // channels: 16 values), so a thread holds few registers and many CTAs stay
 // resident to keep loads in flight.  With kSmooth (K), the per-channel mean
@@ -141,80 +85,11 @@ __global__ void __launch_bounds__(256) quant_int8_kernel(const uint4 *__restrict
                                                          float *__restrict__ scales)
 {
     __shared__ float warp_max[8];
-    const int bh = blockIdx.y, blk = blockIdx.x;
-    const int r = threadIdx.x >> 3, part = threadIdx.x & 7;
-    const int t = blk * kQBlock + r;
-    const bool valid = t < N;
-    float val[16];
-    if (valid) {
-        const uint4 *src = x + (static_cast<size_t>(bh) * N + t) * 16 + part * 2;
-        const uint4 a = ld_stream(src), b = ld_stream(src + 1);
-        float f[8];
-        unpack8(a, f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            val[i] = f[i];
-        unpack8(b, f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            val[8 + i] = f[i];
-        if (kSmooth) {
-            const float4 *mu = reinterpret_cast<const float4 *>(mean + bh * kHeadDim + part * 16);
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const float4 m4 = mu[w];
-                val[4 * w] = __fsub_rn(val[4 * w], m4.x);
-                val[4 * w + 1] = __fsub_rn(val[4 * w + 1], m4.y);
-                val[4 * w + 2] = __fsub_rn(val[4 * w + 2], m4.z);
-                val[4 * w + 3] = __fsub_rn(val[4 * w + 3], m4.w);
-            }
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            val[i] = 0.0f;
-    }
-    float am = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        am = fmaxf(am, fabsf(val[i]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-    if ((threadIdx.x & 31) == 0)
-        warp_max[threadIdx.x >> 5] = am;
-    __syncthreads();
-    float amax = warp_max[0];
-#pragma unroll
-    for (int w = 1; w < 8; ++w)
-        amax = fmaxf(amax, warp_max[w]);
-    const float s = __fdiv_rn(amax, 127.0f);
-    const float rs = s > 0.0f ? __frcp_rn(s) : 0.0f;
-    uint32_t packed[4];
-    if (valid && s > 0.0f) {
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const uint32_t lo = __byte_perm(int8_code(val[w * 4], s, rs), int8_code(val[w * 4 + 1], s, rs), 0x0040u);
-            const uint32_t hi = __byte_perm(int8_code(val[w * 4 + 2], s, rs), int8_code(val[w * 4 + 3], s, rs), 0x0040u);
-            packed[w] = __byte_perm(lo, hi, 0x5410u);
-        }
-    } else {
-#pragma unroll
-        for (int w = 0; w < 4; ++w)
-            packed[w] = 0u;
-    }
-    *reinterpret_cast<uint4 *>(codes + (static_cast<size_t>(bh) * npad + t) * kHeadDim + part * 16) =
-        make_uint4(packed[0], packed[1], packed[2], packed[3]);
-    if (threadIdx.x == 0)
-        scales[static_cast<size_t>(bh) * nblk + blk] = s;
+    prep::quant_block<kSmooth>(x, N, npad, nblk, mean, codes, scales, blockIdx.y, blockIdx.x, threadIdx.x,
+                               warp_max, [] { __syncthreads(); });
 }
 
-// One CTA per 128-token tile of one KV head.  Phase 1: coalesced 16-byte
-// loads of 8 channels of one token, E4M3 codes written token-major into
-// shared memory (8 bytes per store).  Phase 2: each thread gathers 16
-// consecutive tokens of one channel and writes them channel-major (16-byte
-// stores).  Word j of token row t is stored at word j ^ (2 * ((t >> 4) & 7)),
-// so the 16-token gathers of one warp hit eight distinct banks.
+// One CTA per 128-token tile of one KV head (prep::quant_v_tile).
 __global__ void __launch_bounds__(256) quant_v_kernel(const uint4 *__restrict__ v, int Nkv,
                                                       int64_t nk128,
                                                       const float *__restrict__ v_scales,
@@ -223,56 +98,14 @@ __global__ void __launch_bounds__(256) quant_v_kernel(const uint4 *__restrict__ 
     __shared__ __align__(16) uint32_t tile[kVPad * 32];   // [token][32 words]
     __shared__ float sv[kHeadDim], rv[kHeadDim];
     const int bh = blockIdx.y;
-    const int t0 = blockIdx.x * kVPad;
     if (threadIdx.x < kHeadDim) {
         const float x = v_scales[bh * kHeadDim + threadIdx.x];
         sv[threadIdx.x] = x;
         rv[threadIdx.x] = x > 0.0f ? __frcp_rn(x) : 0.0f;
     }
     __syncthreads();
-    const int g = threadIdx.x & 15;                        // this thread's 8 channels, every item
-    float s8[8], r8[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        s8[i] = sv[g * 8 + i];
-        r8[i] = rv[g * 8 + i];
-    }
-#pragma unroll 2
-    for (int it = 0; it < 8; ++it) {
-        const int row = (threadIdx.x + it * 256) >> 4;
-        const int t = t0 + row;
-        uint32_t w0 = 0, w1 = 0;
-        if (t < Nkv) {
-            float f[8];
-            uint32_t cd[8];
-            unpack8(ld_stream(v + (static_cast<size_t>(bh) * Nkv + t) * 16 + g), f);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                cd[i] = s8[i] > 0.0f ? e4m3_code(f[i], s8[i], r8[i]) : 0u;
-            w0 = __byte_perm(__byte_perm(cd[0], cd[1], 0x0040u), __byte_perm(cd[2], cd[3], 0x0040u), 0x5410u);
-            w1 = __byte_perm(__byte_perm(cd[4], cd[5], 0x0040u), __byte_perm(cd[6], cd[7], 0x0040u), 0x5410u);
-        }
-        const int sw = ((row >> 4) & 7) << 1;
-        *reinterpret_cast<uint2 *>(&tile[row * 32 + ((2 * g) ^ sw)]) = make_uint2(w0, w1);
-    }
-    __syncthreads();
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int idx = threadIdx.x + it * 256;
-        const int c = idx >> 3, w = idx & 7;               // channel, 16-token group
-        const int word = (c >> 2) ^ (2 * w);
-        const uint32_t sel = (c & 3) | ((4 + (c & 3)) << 4);   // byte c % 4 of each of two words
-        uint32_t o[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint32_t *rowp = tile + (16 * w + 4 * q) * 32 + word;
-            const uint32_t ab = __byte_perm(rowp[0], rowp[32], sel);
-            const uint32_t cdw = __byte_perm(rowp[64], rowp[96], sel);
-            o[q] = __byte_perm(ab, cdw, 0x5410u);
-        }
-        *reinterpret_cast<uint4 *>(vcodes + (static_cast<size_t>(bh) * kHeadDim + c) * nk128 + t0 + w * 16) =
-            make_uint4(o[0], o[1], o[2], o[3]);
-    }
+    prep::quant_v_tile(v, Nkv, nk128, sv, rv, vcodes, bh, blockIdx.x * kVPad, threadIdx.x, tile,
+                       [] { __syncthreads(); });
 }
 
 // Test kernel: every BF16 x with |x| <= amax against the INT8 quantiser of

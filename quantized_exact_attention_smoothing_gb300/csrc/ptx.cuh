@@ -55,6 +55,21 @@ __device__ __forceinline__ float ld_nc_f32(const float *p)
     return v;
 }
 
+// Coherent global load, pinned like ld_nc_f32 (for data this kernel wrote).
+__device__ __forceinline__ float ld_f32(const float *p)
+{
+    float v;
+    asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+// Order this thread's earlier generic-proxy global writes before later
+// async-proxy (TMA) reads of them.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- shared memory by 32-bit address
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {

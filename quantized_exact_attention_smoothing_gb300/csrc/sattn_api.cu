@@ -448,6 +448,33 @@ int sattn_forward_q_bf16(const sattn_shape *shape, const void *q, const int8_t *
                         static_cast<cudaStream_t>(stream), false, q);
 }
 
+int sattn_attention_small(const sattn_shape *shape, const void *q, const void *k, const void *v, int8_t *q_codes,
+                          float *q_scales, int8_t *k_codes, float *k_scales, float *k_mean, uint8_t *v_codes,
+                          float *v_scales, void *out, void *workspace, void *stream)
+{
+    Geometry g;
+    const int rc = make_geometry(shape, &g);
+    if (rc != SATTN_OK)
+        return rc;
+    if (g.B != 1 || g.Hq != 1 || g.Hkv != 1 || g.Nq > sattn::kQTile || g.Nkv > sattn::kSmallMaxNkv)
+        return SATTN_ERR_INVALID;
+    const void *ptrs[] = {q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes, v_scales, out, workspace};
+    for (const void *p : ptrs) {
+        if (!p)
+            return SATTN_ERR_INVALID;
+        if (!aligned16(p))
+            return SATTN_ERR_MISALIGNED;
+    }
+    const int dev = check_device();
+    if (dev != SATTN_OK)
+        return dev;
+    const sattn::SmallPrep sp{q, k, v, q_codes, q_scales, k_codes, k_scales, k_mean, v_codes, v_scales};
+    const int lc = sattn::launch_small(g, sp, out, workspace, carrier_of(workspace), static_cast<cudaStream_t>(stream));
+    if (lc == 1)
+        return SATTN_ERR_DEVICE;   // no tensor-map encoder in this driver
+    return lc == 0 ? SATTN_OK : SATTN_ERR_LAUNCH;
+}
+
 int sattn_test_forward_withhold_v(const sattn_shape *shape, const int8_t *q_codes, const float *q_scales,
                                   const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
                                   const float *v_scales, void *out, void *workspace, void *stream)

@@ -86,6 +86,24 @@ namespace sattn {
 // kernel's own per-block function; and its correctly rounded exp2.
 cudaError_t launch_test_p8_codes(int n_groups, const float *acc, const float *sig, const float *m, uint8_t *out,
                                  cudaStream_t stream);
+// The preparation's buffers, for the single-launch small-shape path: the
+// forward kernel writes them from the BF16 inputs before it attends.
+struct SmallPrep {
+    const void *q, *k, *v;   // BF16 inputs [1][1][N][128]
+    int8_t *q_codes;
+    float *q_scales;
+    int8_t *k_codes;
+    float *k_scales, *k_mean;
+    uint8_t *v_codes;
+    float *v_scales;
+};
+// Largest Nkv of the small-shape path (its K-mean chunk sums stay in shared memory).
+constexpr int kSmallMaxNkv = 1024;
+// prepare + forward in one launch for B = Hq = Hkv = 1, Nq <= 128, Nkv <= kSmallMaxNkv;
+// status and carrier as for launch_forward.
+int launch_small(const Geometry &g, const SmallPrep &sp, void *out, void *status, void *carrier,
+                 cudaStream_t stream);
+
 // Events recorded around every attention kernel launch (both null: none).
 void set_profile_events(cudaEvent_t before, cudaEvent_t after);
 
