@@ -58,18 +58,29 @@ def load_peaks() -> dict:
             "source": "fallback"}
 
 
-# tcgen05.mma throughput per SM and clock, measured on this part with a
-# microbenchmark of back-to-back MMAs (M = 128, operands in shared memory,
-# accumulator in TMEM): kind::f16 8183 FLOP/clk, kind::f8f6f4 16366 FLOP/clk
-# at N = 128 to 256, so FP8 runs at 2.00x the FP16 rate.
-FP8_OVER_FP16 = 16366.0 / 8183.0
+# The FP8 / FP16 throughput ratio of tcgen05.mma, measured in each run with
+# sattn_measure_mma_rate on the forward's own shapes (kind::f16 N = 256 as
+# QK^T, kind::f8f6f4 N = 144 as PV); this value (the ratio measured when the
+# hook was added: 16366 / 8183 FLOP per SM-clock) stands in if that fails.
+FP8_OVER_FP16 = 2.0
 
 
-def mixed_peak(bf16_tflops: float) -> dict:
+def tcgen05_rates(sattn) -> dict:
+    try:
+        f16 = sattn.measure_mma_rate("f16", 256)
+        f8 = sattn.measure_mma_rate("f8", 144)
+    except Exception as e:  # reported, not fatal: the recorded ratio is used
+        return {"error": str(e), "fp8_over_fp16": FP8_OVER_FP16, "source": "recorded"}
+    return {"f16_n256_flop_per_clk_sm": round(f16["flop_per_clk_sm"], 1), "f16_n256_tflops": round(f16["tflops"], 1),
+            "f8_n144_flop_per_clk_sm": round(f8["flop_per_clk_sm"], 1), "f8_n144_tflops": round(f8["tflops"], 1),
+            "fp8_over_fp16": round(f8["flop_per_clk_sm"] / f16["flop_per_clk_sm"], 4), "source": "measured"}
+
+
+def mixed_peak(bf16_tflops: float, fp8_over_fp16: float = FP8_OVER_FP16) -> dict:
     """Roofline of the forward kernel: half of the algorithmic operations are
     QK^T on the FP16 carrier (FP16 rate = the measured BF16 GEMM rate), half
     are PV in FP8 at the measured FP8 / FP16 ratio of tcgen05.mma."""
-    r16, r8 = bf16_tflops, FP8_OVER_FP16 * bf16_tflops
+    r16, r8 = bf16_tflops, fp8_over_fp16 * bf16_tflops
     return {"mixed": 2.0 / (1.0 / r16 + 1.0 / r8), "fp8": r8, "fp16": r16}
 
 
@@ -315,7 +326,8 @@ def summarise(w, evs, peaks) -> dict:
     ms_fwd = sum(e[1].elapsed_time(e[4]) for e in evs) / K
     ms_attn = sum(e[2].elapsed_time(e[3]) for e in evs) / K
     per_step = [e[0].elapsed_time(e[4]) for e in evs]
-    mp = mixed_peak(peaks["bf16_tflops"])
+    ratio = peaks.get("fp8_over_fp16", FP8_OVER_FP16)
+    mp = mixed_peak(peaks["bf16_tflops"], ratio)
     achieved = w.algorithmic_ops / (ms_attn * 1e-3) / 1e12
     tr = measured_traffic(w)
     return {
@@ -332,7 +344,8 @@ def summarise(w, evs, peaks) -> dict:
                      "achieved_basis": "algorithmic ops (4 * D per unmasked query-key pair) / mean duration of "
                                        "the attention kernel (CUDA events recorded by sattn_profile_events)",
                      "peak_basis": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s (burst) for the FP16 "
-                                   f"half, x{FP8_OVER_FP16:.2f} (measured tcgen05 FP8/FP16) for the FP8 half",
+                                   f"half, x{ratio:.2f} (tcgen05 FP8/FP16, {peaks.get('ratio_source', 'recorded')}) "
+                                   f"for the FP8 half",
                      "frac_of_fp8_dense": round(achieved / mp["fp8"], 4)},
     }
 
@@ -366,6 +379,35 @@ def measure_workload(r: Runner, steps: int, warmup: int, peaks: dict, flush: boo
     return res
 
 
+def measure_small(sattn, torch, r: Runner, steps: int, warmup: int, flush: bool) -> dict:
+    """The same step through sattn_attention_small (preparation and attention
+    in one launch), timed like measure_workload."""
+    st = r.stream
+    buf = sattn.prepare_buffers(r.shape, r.dev)
+    ws = torch.empty(r.sizes["forward_workspace"], dtype=torch.uint8, device=r.dev)
+    out = torch.empty_like(r.out)
+    call = lambda: sattn.attention_small(r.dq, r.dk, r.dv, r.w.causal, buffers=buf, out=out, workspace=ws, stream=st)
+    scratch = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=r.dev) if flush else None
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for e in evs:
+        if scratch is not None:
+            scratch.zero_()
+        e[0].record(st)
+        call()
+        e[1].record(st)
+    torch.cuda.synchronize()
+    if sattn.check_status(ws) != 0:
+        raise RuntimeError("device status reports a timeout in the small-path steps")
+    same = bool(torch.equal(out.view(torch.int16), r.out.view(torch.int16)))
+    ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in evs)
+    return {"ms_step_mean": round(ms, 5), "value": round(r.w.literal_ops / (ms * 1e-3) / 1e12, 4),
+            "launches_per_step": 1, "output_equals_two_calls": same,
+            "path": "sattn_attention_small (preparation inside the attention kernel)"}
+
+
 def prepare_roofline(r: Runner, ms_prep: float, peaks: dict) -> dict:
     pb = r.prep_bytes()
     gbs = pb / (ms_prep * 1e-3) / 1e9
@@ -382,6 +424,14 @@ def run_ours(args, world, rank, local):
     dist_init(world, "nccl")
     sattn.load_library()
     peaks = load_peaks()
+    rates = tcgen05_rates(sattn)
+    peaks["fp8_over_fp16"] = rates["fp8_over_fp16"]
+    peaks["ratio_source"] = rates["source"]
+    if args.mma_rates:
+        if rank == 0:
+            print(json.dumps({"tcgen05": rates, "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count}),
+                  flush=True)
+        return
     stream = torch.cuda.current_stream()
     w = synth.workload(args.workload)
     if args.batch:
@@ -462,6 +512,7 @@ def run_ours(args, world, rank, local):
         # per step: five prepare kernels, the K carrier conversion and the attention kernel
         "gpu_launches": 7 * K,
         "clocks": clk,
+        "tcgen05": rates,
     }
     if e2e is not None:
         result["e2e"] = e2e
@@ -480,6 +531,8 @@ def run_ours(args, world, rank, local):
             flush = ro.prep_bytes() < 4 * 129e6
             steps = 50 if wo.literal_ops < 1e13 else 20
             res = measure_workload(ro, steps, args.warmup, peaks, flush)
+            if sattn.small_shape_ok(wo.B, wo.Hq, wo.Hkv, wo.Nq, wo.Nkv):
+                res["small_path"] = measure_small(sattn, torch, ro, steps, args.warmup, flush)
             if not args.no_cpu_baseline:
                 res["cpu_baseline"] = cpu_baseline(wo, budget_s=6.0)
             others[name] = res
@@ -548,6 +601,8 @@ def main():
                     help="override the workload's batch size (smaller profiling captures)")
     ap.add_argument("--heads", type=int, default=None,
                     help="override the workload's query heads (smaller profiling captures)")
+    ap.add_argument("--mma-rates", action="store_true",
+                    help="print the measured tcgen05.mma rates and exit")
     ap.add_argument("--headline-only", action="store_true",
                     help="measure the headline workload only (no c1-c4 lines)")
     args = ap.parse_args()

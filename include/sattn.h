@@ -278,6 +278,22 @@ int sattn_test_p8_codes(int n_groups, const float *acc, const float *sig, const 
 int sattn_test_exp2(int n, const float *x, float *out, void *stream);
 
 /*
+ * sattn_measure_mma_rate -- measurement hook, not part of the computation:
+ * the dense throughput of tcgen05.mma on the current device for the forward's
+ * own instruction shapes (M = 128, N = n, a multiple of 16 in [16, 256]):
+ * kind 0 = kind::f16 with both operands in shared memory (as QK^T on the FP16
+ * carrier), kind 1 = kind::f8f6f4 E4M3 x E4M3 with A in tensor memory (as PV).
+ * One CTA per SM issues iters x 4 back-to-back MMAs from one thread.
+ *   flop_per_clk_sm  out (host): 2*M*N*K per instruction / SM clock cycles
+ *   tflops           out (host): the same over all SMs / wall time (events)
+ * Allocates and frees a few bytes of device memory and synchronises the
+ * device (a measurement, not a stream operation).  Returns SATTN_OK,
+ * SATTN_ERR_INVALID for bad arguments, SATTN_ERR_DEVICE, or SATTN_ERR_LAUNCH
+ * if the launch failed or the completion wait ran out.
+ */
+int sattn_measure_mma_rate(int kind, int n, int iters, double *flop_per_clk_sm, double *tflops);
+
+/*
  * sattn_profile_events -- measurement hook, not part of the computation: while
  * set, every sattn_forward / sattn_forward_q_bf16 call records `before` on its
  * stream just before the attention kernel is launched and `after` just after

@@ -79,6 +79,8 @@ def load_library(build: bool = True):
     lib.sattn_test_exp2.argtypes = [ctypes.c_int, P, P, P]
     lib.sattn_profile_events.argtypes = [P, P]
     lib.sattn_attention_small.argtypes = [SP] + [P] * 13
+    lib.sattn_measure_mma_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
     lib.sattn_graph_create.argtypes = [SP] + [P] * 13 + [ctypes.POINTER(ctypes.c_void_p)]
     lib.sattn_test_host_chunks.argtypes = [SP, ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
                                            ctypes.POINTER(ctypes.c_int)]
@@ -91,7 +93,7 @@ def load_library(build: bool = True):
                  "sattn_attention_host", "sattn_prepare_noalloc", "sattn_prepare_kv", "sattn_forward_q_bf16",
                  "sattn_test_int8_quantiser", "sattn_graph_create", "sattn_graph_launch", "sattn_graph_destroy",
                  "sattn_test_host_chunks", "sattn_test_p8_codes", "sattn_test_exp2", "sattn_profile_events",
-                 "sattn_attention_small"):
+                 "sattn_attention_small", "sattn_measure_mma_rate"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -397,6 +399,17 @@ def exp2_for_test(x: torch.Tensor) -> torch.Tensor:
     if rc != 0:
         raise SattnError(rc, "sattn_test_exp2")
     return out
+
+
+def measure_mma_rate(kind: str, n: int, iters: int = 4096) -> dict:
+    """sattn_measure_mma_rate: tcgen05.mma throughput for kind "f16" (A and B
+    in shared memory) or "f8" (E4M3, A in tensor memory), M = 128, N = n."""
+    k = {"f16": 0, "f8": 1}[kind]
+    f, t = ctypes.c_double(), ctypes.c_double()
+    rc = load_library().sattn_measure_mma_rate(k, n, iters, ctypes.byref(f), ctypes.byref(t))
+    if rc != 0:
+        raise SattnError(rc, "sattn_measure_mma_rate")
+    return {"kind": kind, "n": n, "flop_per_clk_sm": f.value, "tflops": t.value}
 
 
 def profile_events(before=None, after=None) -> None:

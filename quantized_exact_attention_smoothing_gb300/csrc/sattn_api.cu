@@ -529,6 +529,17 @@ int sattn_test_exp2(int n, const float *x, float *out, void *stream)
                : SATTN_ERR_LAUNCH;
 }
 
+int sattn_measure_mma_rate(int kind, int n, int iters, double *flop_per_clk_sm, double *tflops)
+{
+    if ((kind != 0 && kind != 1) || n < 16 || n > 256 || n % 16 != 0 || iters < 1 || iters > (1 << 20) ||
+        !flop_per_clk_sm || !tflops)
+        return SATTN_ERR_INVALID;
+    const int dev = check_device();
+    if (dev != SATTN_OK)
+        return dev;
+    return sattn::measure_mma_rate(kind, n, iters, flop_per_clk_sm, tflops) == 0 ? SATTN_OK : SATTN_ERR_LAUNCH;
+}
+
 int sattn_profile_events(void *before, void *after)
 {
     if ((before == nullptr) != (after == nullptr))

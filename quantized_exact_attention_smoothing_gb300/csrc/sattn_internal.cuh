@@ -104,6 +104,11 @@ constexpr int kSmallMaxNkv = 1024;
 int launch_small(const Geometry &g, const SmallPrep &sp, void *out, void *status, void *carrier,
                  cudaStream_t stream);
 
+// tcgen05.mma throughput (mma_rate.cu): kind 0 = kind::f16 with A and B in
+// shared memory, kind 1 = kind::f8f6f4 (E4M3) with A in tensor memory; M = 128,
+// N = n.  Synchronises the device.  0 on success.
+int measure_mma_rate(int kind, int n, int iters, double *flop_per_clk_sm, double *tflops);
+
 // Events recorded around every attention kernel launch (both null: none).
 void set_profile_events(cudaEvent_t before, cudaEvent_t after);
 
