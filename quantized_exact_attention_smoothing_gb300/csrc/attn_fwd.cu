@@ -1323,6 +1323,156 @@ __device__ __forceinline__ void compute_role(const FwdParams &p, const CUtensorM
     }
 }
 
+// The small-shape preparation for Nkv <= 256, staged: every input is first
+// copied into shared memory (bulk copies into the CTA's free buffers, 212 KB
+// from OFF_K), so
+// the phases that follow read no global memory and run side by side on
+// different warps.  Same arithmetic as the preparation kernels, element by
+// element: the K column sums of each 64-token chunk in ascending token order,
+// chunk sums in ascending chunk order, divided by Nkv; the V column maxima;
+// per 32-token block the maximum |x| (of K - mean for K), s = amax / 127 and
+// int8_code of every value (pad tokens 0); E4M3 codes v * (1 / s_v) by
+// e4m3_code, channel-major, pad keys 0.  Only the assignment of work to
+// threads differs, which no result depends on (maxima and elementwise codes).
+constexpr int kSmallStagedNkv = 256;
+__device__ __forceinline__ bool small_prepare_staged(const FwdParams &p, uint8_t *smem, const Waiter &wt)
+{
+    const SmallPrep &sp = p.sp;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int Nkv = p.Nkv, Nq = p.Nq;
+    uint8_t *base = smem + OFF_K;
+    const uint4 *k4 = static_cast<const uint4 *>(sp.k), *v4 = static_cast<const uint4 *>(sp.v),
+                *q4 = static_cast<const uint4 *>(sp.q);
+    uint4 *sk4 = reinterpret_cast<uint4 *>(base), *sv4 = reinterpret_cast<uint4 *>(base + 65536),
+          *sq4 = reinterpret_cast<uint4 *>(base + 131072);
+    float *ks = reinterpret_cast<float *>(base + 163840);   // [4][128] chunk sums
+    float *vm = ks + 4 * HD;                                 // [4][128] chunk maxima
+    float *mean = vm + 4 * HD, *svs = mean + HD, *rvs = svs + HD;
+    // 1. inputs into shared memory: three bulk copies on one mbarrier
+    const uint32_t bar = ptx::smem_u32(base + 196608);
+    if (tid == 0) {
+        ptx::mbar_init(bar, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const uint32_t kb = static_cast<uint32_t>(Nkv) * 256u, qb = static_cast<uint32_t>(Nq) * 256u;
+        ptx::mbar_arrive_expect_tx(bar, 2u * kb + qb);
+        ptx::bulk_load(ptx::smem_u32(sk4), k4, kb, bar);
+        ptx::bulk_load(ptx::smem_u32(sv4), v4, kb, bar);
+        ptx::bulk_load(ptx::smem_u32(sq4), q4, qb, bar);
+    }
+    if (!wt.wait(bar, 0, SITE_Q) && tid == 0)
+        wt.drain(bar, 0);   // the copies land before the CTA may leave
+    __syncthreads();
+    if (tid == 0)
+        ptx::mbar_inval(bar);   // its memory is scratch again from here on
+    if (*reinterpret_cast<volatile uint32_t *>(p.status) != 0)
+        return false;
+    const uint32_t *skw = reinterpret_cast<const uint32_t *>(sk4), *svw = reinterpret_cast<const uint32_t *>(sv4),
+                   *sqw = reinterpret_cast<const uint32_t *>(sq4);
+    auto kval = [&](int t, int c) {   // BF16 K[t][c] as FP32
+        const uint32_t w = skw[t * 64 + (c >> 1)];
+        return (c & 1) ? bf16_hi(w) : bf16_lo(w);
+    };
+    auto vval = [&](int t, int c) {
+        const uint32_t w = svw[t * 64 + (c >> 1)];
+        return (c & 1) ? bf16_hi(w) : bf16_lo(w);
+    };
+    auto qval = [&](int t, int c) {
+        const uint32_t w = sqw[t * 64 + (c >> 1)];
+        return (c & 1) ? bf16_hi(w) : bf16_lo(w);
+    };
+    // 2. per (chunk, channel): the column sum of K and the column max |V|
+    const int nch = (Nkv + kMeanChunk - 1) / kMeanChunk;
+    for (int it = tid; it < nch * HD; it += NTHREADS) {
+        const int ch = it / HD, c = it % HD;
+        const int t1 = min(Nkv, (ch + 1) * kMeanChunk);
+        float sum = 0.0f, mx = 0.0f;
+        for (int t = ch * kMeanChunk; t < t1; ++t) {
+            sum = __fadd_rn(sum, kval(t, c));
+            mx = fmaxf(mx, fabsf(vval(t, c)));
+        }
+        ks[ch * HD + c] = sum;
+        vm[ch * HD + c] = mx;
+    }
+    __syncthreads();
+    if (tid < HD) {
+        float total = 0.0f, amax = 0.0f;
+        for (int ch = 0; ch < nch; ++ch) {
+            total = __fadd_rn(total, ks[ch * HD + tid]);
+            amax = fmaxf(amax, vm[ch * HD + tid]);
+        }
+        const float mu = __fdiv_rn(total, static_cast<float>(Nkv));
+        const float sc = __fdiv_rn(amax, 448.0f);
+        mean[tid] = mu;
+        svs[tid] = sc;
+        rvs[tid] = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+        sp.k_mean[tid] = mu;
+        sp.v_scales[tid] = sc;
+    }
+    __syncthreads();
+    // 3. one warp per 32-token block of K (then of Q): lane l holds channels
+    // 4l .. 4l + 3 of the block's 32 tokens
+    const int nbk = p.nbk, nbq = p.nbq;
+    for (int job = warp; job < nbk + nbq; job += NTHREADS / 32) {
+        const bool isk = job < nbk;
+        const int blk = isk ? job : job - nbk, N = isk ? Nkv : Nq;
+        float am = 0.0f;
+        for (int r = 0; r < kQBlock; ++r) {
+            const int t = blk * kQBlock + r;
+            if (t < N)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = 4 * lane + u;
+                    const float x = isk ? __fsub_rn(kval(t, c), mean[c]) : qval(t, c);
+                    am = fmaxf(am, fabsf(x));
+                }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        const float sc = __fdiv_rn(am, 127.0f);
+        const float rs = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+        int8_t *codes = isk ? sp.k_codes : sp.q_codes;
+        for (int r = 0; r < kQBlock; ++r) {
+            const int t = blk * kQBlock + r;
+            uint32_t word = 0;
+            if (t < N && sc > 0.0f)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = 4 * lane + u;
+                    const float x = isk ? __fsub_rn(kval(t, c), mean[c]) : qval(t, c);
+                    word |= int8_code(x, sc, rs) << (8 * u);
+                }
+            reinterpret_cast<uint32_t *>(codes + static_cast<size_t>(t) * HD)[lane] = word;
+            if (isk && t < Nkv) {   // the FP16 carrier of the same four codes
+                uint2 *dst = reinterpret_cast<uint2 *>(const_cast<uint4 *>(p.k_carrier) + static_cast<size_t>(t) * 16);
+                dst[lane] = make_uint2(ptx::f16x2_of_i8(word, 0), ptx::f16x2_of_i8(word, 2));
+            }
+        }
+        if (lane == 0)
+            (isk ? sp.k_scales : sp.q_scales)[blk] = sc;
+    }
+    // 4. V: per (channel, 16-token group), channel-major
+    const int nk128 = (Nkv + kVPad - 1) / kVPad * kVPad;
+    for (int it = tid; it < HD * (nk128 / 16); it += NTHREADS) {
+        const int c = it % HD, g = it / HD;
+        const float sc = svs[c], rc = rvs[c];
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int t = 16 * g + u;
+            const uint32_t code = (t < Nkv && sc > 0.0f) ? prep::e4m3_code(vval(t, c), sc, rc) : 0u;
+            w[u >> 2] |= code << (8 * (u & 3));
+        }
+        *reinterpret_cast<uint4 *>(sp.v_codes + static_cast<size_t>(c) * nk128 + 16 * g) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    ptx::fence_proxy_async_global();
+    __syncthreads();
+    return true;
+}
+
 // The single-launch small-shape path (one query tile of one head, Nkv <=
 // kSmallMaxNkv): all threads of the CTA run the preparation of the
 // preparation kernels, through the same device functions (prep_device.cuh),
@@ -1421,8 +1571,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #endif
     const Waiter wt{p.status};
     volatile uint32_t *flag = reinterpret_cast<volatile uint32_t *>(smem + OFF_FLAG);
-    if (p.small)
-        small_prepare(p, smem);
+    if (p.small) {
+        if (p.Nkv <= kSmallStagedNkv)
+            small_prepare_staged(p, smem, wt);   // a failed copy leaves the status set: the CTA does no more
+        else
+            small_prepare(p, smem);
+    }
 
     if (threadIdx.x == 0) {
         *flag = *reinterpret_cast<volatile uint32_t *>(p.status);

@@ -1,7 +1,9 @@
 """GPU parity of the single-launch small-shape path (sattn_attention_small):
 for one query tile of one head it must write the preparation's buffers with
 the bytes sattn_prepare writes and the output sattn_prepare + sattn_forward
-give, and match the oracle."""
+give, and match the oracle.  Shapes on both sides of Nkv = 256, where the
+in-kernel preparation switches from staging the inputs in shared memory to
+reading them from global memory."""
 import numpy as np
 import pytest
 import torch
@@ -17,7 +19,7 @@ BUFFERS = ("q_codes", "q_scales", "k_codes", "k_scales", "k_mean", "v_codes", "v
 
 @pytest.mark.parametrize("Nq, Nkv, causal", [
     (128, 192, False), (128, 192, True), (100, 300, True), (1, 1, False), (128, 1024, False),
-    (37, 700, False), (128, 129, True), (64, 64, True)])
+    (37, 700, False), (128, 129, True), (64, 64, True), (128, 256, False), (5, 257, True), (128, 33, False)])
 def test_small_path_equals_two_calls_and_oracle(oracle_mod, Nq, Nkv, causal):
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     w = synth.workload("c1", Nq=Nq, Nkv=Nkv, causal=causal)
