@@ -175,8 +175,8 @@ __device__ __forceinline__ void quant_v_tile(const uint4 *__restrict__ v, int Nk
         s8[i] = sv[g * 8 + i];
         r8[i] = rv[g * 8 + i];
     }
-#pragma unroll 2
-    for (int it = 0; it < 8; ++it) {
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {   // all eight loads in flight
         const int row = (tid + it * 256) >> 4;
         const int t = t0 + row;
         uint32_t w0 = 0, w1 = 0;
