@@ -105,6 +105,9 @@ static_assert(2 * 128 * kRegsCompute + 128 * kRegsOther == NTHREADS * kLaunchReg
 constexpr uint32_t IDESC_QK = ptx::make_idesc(0, 0, BM, BN);     // F16 x F16 -> F32, N = 256
 constexpr uint32_t IDESC_PV = ptx::make_idesc(0, 0, BM, PV_N);   // E4M3 x E4M3 -> F32
 constexpr uint64_t TIMEOUT_NS = 1000000000ull;
+// K and V bytes of the heads whose items run together (see item_tile): well
+// inside the 126 MB L2, which also carries the Q tiles and the output.
+constexpr int64_t kL2ChunkBytes = 48ll << 20;
 
 // shared memory map, offsets from a 1024-byte aligned base
 constexpr uint32_t OFF_K = 0;
@@ -162,8 +165,12 @@ struct FwdParams {
     uint32_t *status;
     int B, Hq, Hkv, Nq, Nkv, group, n_qtiles, n_items, causal;
     int withhold_v;   // test hook: the V loader stages the first Q tile and loads no V
-    // reciprocals for exact division by Hq * B, Hq and group (see udiv)
-    unsigned long long m_hb, m_hq, m_group;
+    // item order (see item_tile): B * Hkv units, chunk_units per chunk,
+    // chunk_items = chunk_units * group * n_qtiles items per full chunk
+    int n_units, chunk_units, chunk_items;
+    // reciprocals for exact division (see udiv) by chunk_items, by the items of
+    // one query tile in a full chunk and in the last chunk, by Hkv and by group
+    unsigned long long m_chunk, m_row, m_row_tail, m_hkv, m_group;
     int nq32, nbq, nbk;
     float c0;
     float zero;   // always +0 (see dd_pair)
@@ -253,20 +260,31 @@ __device__ __forceinline__ int udiv(int x, int d, unsigned long long m)
     return d == 1 ? x : static_cast<int>(__umul64hi(static_cast<unsigned long long>(x), m));
 }
 
-// Work item `it` of [0, n_items): query tiles in decreasing order (with a
+// Work item `it` of [0, n_items).  The (batch, KV head) units are cut into
+// chunks of chunk_units consecutive units whose K and V fit in L2 together,
+// and the chunks are walked in order, so that the CTAs running at the same
+// time read the K and V tiles of a few heads, which then come from L2 after
+// the first read.  Within a chunk: query tiles in decreasing order (with a
 // causal mask the last rows visit the most KV tiles, so the longest items are
-// scheduled first), then heads, then batches.  Every item has at least one KV
-// tile: a causal mask requires Nq <= Nkv, so each row keeps key 0.
+// scheduled first), then the chunk's units, then the query heads of a unit's
+// GQA group.  Every item has at least one KV tile: a causal mask requires
+// Nq <= Nkv, so each row keeps key 0.
 __device__ __forceinline__ Tile item_tile(const FwdParams &p, int it)
 {
     Tile t;
-    const int hb = p.Hq * p.B;
-    const int qi = udiv(it, hb, p.m_hb);
+    const int c = udiv(it, p.chunk_items, p.m_chunk);
+    const int r = it - c * p.chunk_items;
+    const int u0 = c * p.chunk_units;
+    const bool tail = u0 + p.chunk_units > p.n_units;   // the last chunk may hold fewer units
+    const int row = (tail ? p.n_units - u0 : p.chunk_units) * p.group;   // items per query tile
+    const int qi = udiv(r, row, tail ? p.m_row_tail : p.m_row);
     const int qt = p.n_qtiles - 1 - qi;
-    const int rem = it - qi * hb;
-    t.b = udiv(rem, p.Hq, p.m_hq);
-    t.hq = rem - t.b * p.Hq;
-    t.hk = udiv(t.hq, p.group, p.m_group);
+    const int rem = r - qi * row;
+    const int ul = udiv(rem, p.group, p.m_group);
+    const int u = u0 + ul;
+    t.b = udiv(u, p.Hkv, p.m_hkv);
+    t.hk = u - t.b * p.Hkv;
+    t.hq = t.hk * p.group + (rem - ul * p.group);
     t.q0 = qt * BM;
     const int off = p.Nkv - p.Nq;
     int kv_end = p.Nkv;
@@ -1882,8 +1900,20 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const i
         return static_cast<int>(cudaErrorInvalidValue);   // item indices must fit udiv's range
     prm.n_items = static_cast<int>(n_items);
     auto recip = [](int d) { return d == 1 ? 0ull : ~0ull / static_cast<unsigned long long>(d) + 1ull; };
-    prm.m_hb = recip(g.Hq * g.B);
-    prm.m_hq = recip(g.Hq);
+    prm.n_units = g.B * g.Hkv;
+    {   // the fewest chunks whose units' K carrier (2 bytes) and V codes (1 byte) fit in
+        // kL2ChunkBytes, with the units spread evenly over them
+        const int64_t unit_bytes = static_cast<int64_t>(g.Nkv) * HD * 3;
+        const int64_t cap = std::max<int64_t>(1, std::min<int64_t>(prm.n_units, kL2ChunkBytes / unit_bytes));
+        const int64_t n_chunks = (prm.n_units + cap - 1) / cap;
+        prm.chunk_units = static_cast<int>((prm.n_units + n_chunks - 1) / n_chunks);
+    }
+    prm.chunk_items = prm.chunk_units * prm.group * prm.n_qtiles;
+    const int tail_units = prm.n_units - (prm.n_units - 1) / prm.chunk_units * prm.chunk_units;
+    prm.m_chunk = recip(prm.chunk_items);
+    prm.m_row = recip(prm.chunk_units * prm.group);
+    prm.m_row_tail = recip(tail_units * prm.group);
+    prm.m_hkv = recip(g.Hkv);
     prm.m_group = recip(prm.group);
     prm.causal = g.causal;
     prm.nq32 = static_cast<int>(g.nq32);
