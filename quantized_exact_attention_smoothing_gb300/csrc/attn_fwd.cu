@@ -1572,7 +1572,9 @@ __device__ __forceinline__ void small_prepare(const FwdParams &p, uint8_t *smem)
     __syncthreads();
 }
 
-template <bool kFuseQ>
+// kSmall: the single-launch small-shape path, whose preparation runs first
+// (a separate instantiation, so that the other launches carry none of its code)
+template <bool kFuseQ, bool kSmall>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
@@ -1589,7 +1591,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #endif
     const Waiter wt{p.status};
     volatile uint32_t *flag = reinterpret_cast<volatile uint32_t *>(smem + OFF_FLAG);
-    if (p.small) {
+    if (kSmall && p.small) {
         if (p.Nkv <= kSmallStagedNkv)
             small_prepare_staged(p, smem, wt);   // a failed copy leaves the status set: the CTA does no more
         else
@@ -1675,20 +1677,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 // The K codes [B*Hkv][nk32][128] (INT8) -> their FP16 carrier [B*Hkv][Nkv][128],
 // the operand of QK^T on the tensor cores (this part has no INT8 tensor-core
-// product; integers of magnitude <= 127 are exact in FP16).  Thread = 16
-// codes (one 16-byte load, two 16-byte stores), kCarrierUnroll chunks per
-// thread; grid y = KV head.  Bound by HBM bandwidth: 128 bytes read and 256
-// written per key.
-constexpr int kCarrierUnroll = 4;
-__global__ void __launch_bounds__(256) k_carrier_kernel(const uint4 *__restrict__ codes, int Nkv, int64_t nk32,
+// product; integers of magnitude <= 127 are exact in FP16).  Thread = 8 codes
+// (an 8-byte load, one 16-byte store, so a warp's store covers 512 contiguous
+// bytes), kCarrierUnroll groups per thread; grid y = KV head.  Bound by HBM
+// bandwidth: 128 bytes read and 256 written per key.
+constexpr int kCarrierUnroll = 8;
+__global__ void __launch_bounds__(256) k_carrier_kernel(const uint2 *__restrict__ codes, int Nkv, int64_t nk32,
                                                         uint4 *__restrict__ carrier)
 {
     const int64_t bh = blockIdx.y;
-    const int64_t n = static_cast<int64_t>(Nkv) * (HD / 16);   // 16-code chunks of this head
-    const uint4 *src = codes + bh * nk32 * (HD / 16);
-    uint4 *dst = carrier + bh * Nkv * static_cast<int64_t>(HD / 8);
+    const int64_t n = static_cast<int64_t>(Nkv) * (HD / 8);   // 8-code groups of this head
+    const uint2 *src = codes + bh * nk32 * (HD / 8);
+    uint4 *dst = carrier + bh * n;
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * (256 * kCarrierUnroll) + threadIdx.x;
-    uint4 a[kCarrierUnroll];
+    uint2 a[kCarrierUnroll];
 #pragma unroll
     for (int u = 0; u < kCarrierUnroll; ++u)
         if (c0 + 256 * u < n)
@@ -1696,12 +1698,9 @@ __global__ void __launch_bounds__(256) k_carrier_kernel(const uint4 *__restrict_
 #pragma unroll
     for (int u = 0; u < kCarrierUnroll; ++u) {
         const int64_t c = c0 + 256 * u;
-        if (c < n) {
-            dst[2 * c] = make_uint4(ptx::f16x2_of_i8(a[u].x, 0), ptx::f16x2_of_i8(a[u].x, 2),
-                                    ptx::f16x2_of_i8(a[u].y, 0), ptx::f16x2_of_i8(a[u].y, 2));
-            dst[2 * c + 1] = make_uint4(ptx::f16x2_of_i8(a[u].z, 0), ptx::f16x2_of_i8(a[u].z, 2),
-                                        ptx::f16x2_of_i8(a[u].w, 0), ptx::f16x2_of_i8(a[u].w, 2));
-        }
+        if (c < n)
+            dst[c] = make_uint4(ptx::f16x2_of_i8(a[u].x, 0), ptx::f16x2_of_i8(a[u].x, 2),
+                                ptx::f16x2_of_i8(a[u].y, 0), ptx::f16x2_of_i8(a[u].y, 2));
     }
 }
 
@@ -1777,19 +1776,19 @@ namespace {
 // The per-warpgroup register split only adds up when the kernel is launched
 // with exactly kLaunchRegs registers per thread; refuse to launch otherwise.
 // Also raises the kernel's dynamic shared-memory limit.  Once per process.
-template <bool kFuseQ>
+template <bool kFuseQ, bool kSmall>
 cudaError_t kernel_attributes()
 {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
         cudaFuncAttributes fa;
-        attr_err = cudaFuncGetAttributes(&fa, attn_fwd_kernel<kFuseQ>);
+        attr_err = cudaFuncGetAttributes(&fa, attn_fwd_kernel<kFuseQ, kSmall>);
         if (attr_err == cudaSuccess && fa.numRegs != kLaunchRegs)
             attr_err = cudaErrorInvalidConfiguration;
         if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(attn_fwd_kernel<kFuseQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            static_cast<int>(SMEM_BYTES));
+            attr_err = cudaFuncSetAttribute(attn_fwd_kernel<kFuseQ, kSmall>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
     });
     return attr_err;
 }
@@ -1869,15 +1868,18 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const i
             return 1;
     }
 
-    const cudaError_t attr_err = kernel_attributes<kFuseQ>();
+    cudaError_t attr_err = kernel_attributes<kFuseQ, false>();
+    if constexpr (!kFuseQ)
+        if (small)
+            attr_err = kernel_attributes<false, true>();
     if (attr_err != cudaSuccess)
         return static_cast<int>(attr_err);
 
     if (!small) {   // the FP16 carrier of the K codes, read by the attention kernel's K loader
-        const int64_t nchunk = static_cast<int64_t>(g.Nkv) * (HD / 16);
-        const dim3 grid(static_cast<unsigned>((nchunk + 256 * kCarrierUnroll - 1) / (256 * kCarrierUnroll)),
+        const int64_t ngroup = static_cast<int64_t>(g.Nkv) * (HD / 8);
+        const dim3 grid(static_cast<unsigned>((ngroup + 256 * kCarrierUnroll - 1) / (256 * kCarrierUnroll)),
                         static_cast<unsigned>(bhk));
-        k_carrier_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4 *>(k_codes), g.Nkv, g.nk32,
+        k_carrier_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint2 *>(k_codes), g.Nkv, g.nk32,
                                                     static_cast<uint4 *>(k_carrier));
     }
 
@@ -1939,7 +1941,14 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const i
     const int grid = std::min(prm.n_items, n_sm);
     if (g_ev_before && cudaEventRecord(g_ev_before, stream) != cudaSuccess)
         return static_cast<int>(cudaGetLastError());
-    attn_fwd_kernel<kFuseQ><<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, tmo, prm);
+    bool launched = false;
+    if constexpr (!kFuseQ)
+        if (small) {
+            attn_fwd_kernel<false, true><<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, tmo, prm);
+            launched = true;
+        }
+    if (!launched)
+        attn_fwd_kernel<kFuseQ, false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, tmo, prm);
     const cudaError_t le = cudaGetLastError();
     if (le != cudaSuccess)
         return static_cast<int>(le);
@@ -1963,8 +1972,9 @@ int forward_init()
 {
     if (!tensor_map_encoder())
         return 1;
-    const cudaError_t a = kernel_attributes<false>(), b = kernel_attributes<true>();
-    return a != cudaSuccess ? static_cast<int>(a) : static_cast<int>(b);
+    const cudaError_t a = kernel_attributes<false, false>(), b = kernel_attributes<true, false>(),
+                      c = kernel_attributes<false, true>();
+    return static_cast<int>(a != cudaSuccess ? a : b != cudaSuccess ? b : c);
 }
 
 int launch_forward_q_bf16(const Geometry &g, const void *q, const int8_t *k_codes, const float *k_scales,

@@ -77,52 +77,120 @@ __device__ __forceinline__ uint32_t e4m3_code(float v, float s, float rs)
     return ptx::cvt_e4m3x2(0.0f, __fdiv_rn(v, s)) & 0xffu;
 }
 
-// INT8 codes and scale of one 32-token block (blk) of head bh: thread tid of
-// 256 = (token tid / 8, channels 16 (tid % 8) .. + 15); with kSmooth (K) the
-// per-channel mean is subtracted first.  warp_max: 8 floats of shared memory;
-// sync(): a barrier over the 256 threads.
-template <bool kSmooth, class Sync>
-__device__ __forceinline__ void quant_block(const uint4 *__restrict__ x, int N, int64_t npad, int nblk,
-                                            const float *__restrict__ mean, int8_t *__restrict__ codes,
-                                            float *__restrict__ scales, int bh, int blk, int tid,
-                                            float *warp_max, Sync sync)
+// e4m3_code of eight values of one token against their eight channel scales
+// s (rs2: the reciprocals in packed pairs; keep: byte mask of the channels
+// with s > 0, whose codes are kept, the others 0), four bytes per word, value
+// i in byte i % 4 of word i / 4.  The same decision as e4m3_code on packed
+// pairs: both brackets of fl(v * fl(1/s)) for two values per instruction, and
+// IEEE division for the values of a word whose brackets differ (rare).
+__device__ __forceinline__ void e4m3_codes8(const float (&v)[8], const float (&s)[8], const uint64_t (&rs2)[4],
+                                            const uint32_t (&keep)[2], uint32_t (&w)[2])
+{
+    const uint64_t up2 = ptx::f32x2(1.0f + 0x1p-21f, 1.0f + 0x1p-21f);
+    const uint64_t dn2 = ptx::f32x2(1.0f - 0x1p-21f, 1.0f - 0x1p-21f);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t hi[2], lo[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int i = 4 * h + 2 * k;
+            const uint64_t y2 = ptx::mul_f32x2(ptx::f32x2(v[i], v[i + 1]), rs2[2 * h + k]);
+            const uint64_t a2 = ptx::mul_f32x2(y2, up2), b2 = ptx::mul_f32x2(y2, dn2);
+            // value i in the low byte, i + 1 in the high byte
+            hi[k] = ptx::cvt_e4m3x2(ptx::f32x2_hi(a2), ptx::f32x2_lo(a2));
+            lo[k] = ptx::cvt_e4m3x2(ptx::f32x2_hi(b2), ptx::f32x2_lo(b2));
+        }
+        uint32_t word = __byte_perm(hi[0], hi[1], 0x5410u);
+        const uint32_t other = __byte_perm(lo[0], lo[1], 0x5410u);
+        if (word != other) {   // a value of this word is within 2^-21 of an E4M3 rounding boundary
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t d = (word ^ other) >> (8 * u) & 0xffu;
+                if (d != 0u && s[4 * h + u] > 0.0f) {
+                    const uint32_t code = ptx::cvt_e4m3x2(0.0f, __fdiv_rn(v[4 * h + u], s[4 * h + u])) & 0xffu;
+                    word = (word & ~(0xffu << (8 * u))) | (code << (8 * u));
+                }
+            }
+        }
+        w[h] = word & keep[h];
+    }
+}
+
+// int8_code of 16 values (value i -> byte i % 4 of word i / 4) on packed
+// pairs: q = fl(x * rs), r = fl(q + 1.5 * 2^23) and the distance of q from
+// the integer r - 1.5 * 2^23, for two values per instruction.  A pair with a
+// value near a rounding tie (or not finite) takes int8_code_div for both.
+// (If the assembler fuses the product into the addition, r can differ from
+// the two-step value only when q is within 2^-16 of a half-integer, which the
+// tie test sends to the division as well.)
+__device__ __forceinline__ void int8_codes16(const float (&val)[16], float s, float rs, uint32_t (&packed)[4])
+{
+    const uint64_t rs2 = ptx::f32x2(rs, rs), m2 = ptx::f32x2(kRoundMagic, kRoundMagic);
+    uint32_t b[16];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint64_t q2 = ptx::mul_f32x2(ptx::f32x2(val[2 * k], val[2 * k + 1]), rs2);
+        const uint64_t r2 = ptx::add_f32x2(q2, m2);
+        const uint64_t d2 = ptx::sub_f32x2(q2, ptx::sub_f32x2(r2, m2));
+        b[2 * k] = __float_as_uint(ptx::f32x2_lo(r2));
+        b[2 * k + 1] = __float_as_uint(ptx::f32x2_hi(r2));
+        if (!(fabsf(ptx::f32x2_lo(d2)) < kTieMargin && fabsf(ptx::f32x2_hi(d2)) < kTieMargin)) {
+            b[2 * k] = int8_code_div(val[2 * k], s);
+            b[2 * k + 1] = int8_code_div(val[2 * k + 1], s);
+        }
+    }
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+        packed[w] = __byte_perm(__byte_perm(b[4 * w], b[4 * w + 1], 0x0040u),
+                                __byte_perm(b[4 * w + 2], b[4 * w + 3], 0x0040u), 0x5410u);
+}
+
+// The 16 values of one thread of a 32-token block (its token's channels
+// 16 part .. 16 part + 15, from two 16-byte chunks), with the per-channel mean
+// of head bh subtracted first for K (kSmooth).
+template <bool kSmooth>
+__device__ __forceinline__ void block_values(const uint4 &a, const uint4 &b, const float *__restrict__ mean, int bh,
+                                             int part, float (&val)[16])
+{
+    float f[8];
+    unpack8(a, f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        val[i] = f[i];
+    unpack8(b, f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        val[8 + i] = f[i];
+    if (kSmooth) {
+        const float4 *mu = reinterpret_cast<const float4 *>(mean + bh * kHeadDim + part * 16);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float4 m4 = mu[w];
+            val[4 * w] = __fsub_rn(val[4 * w], m4.x);
+            val[4 * w + 1] = __fsub_rn(val[4 * w + 1], m4.y);
+            val[4 * w + 2] = __fsub_rn(val[4 * w + 2], m4.z);
+            val[4 * w + 3] = __fsub_rn(val[4 * w + 3], m4.w);
+        }
+    }
+}
+
+// INT8 codes and scale of one 32-token block (blk) of head bh from the
+// values of thread tid of 256 = (token tid / 8, channels 16 (tid % 8) .. + 15;
+// val all 0 for a token past N): amax over the block, s = amax / 127, codes
+// and s written.  warp_max: 8 floats of shared memory; sync(): a barrier
+// over the 256 threads.
+template <class Sync>
+__device__ __forceinline__ void quant_block_values(const float (&val)[16], int N, int64_t npad, int nblk,
+                                                   int8_t *__restrict__ codes, float *__restrict__ scales, int bh,
+                                                   int blk, int tid, float *warp_max, Sync sync)
 {
     const int r = tid >> 3, part = tid & 7;
     const int t = blk * kQBlock + r;
     const bool valid = t < N;
-    float val[16];
-    if (valid) {
-        const uint4 *src = x + (static_cast<size_t>(bh) * N + t) * 16 + part * 2;
-        const uint4 a = ld_stream(src), b = ld_stream(src + 1);
-        float f[8];
-        unpack8(a, f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            val[i] = f[i];
-        unpack8(b, f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            val[8 + i] = f[i];
-        if (kSmooth) {
-            const float4 *mu = reinterpret_cast<const float4 *>(mean + bh * kHeadDim + part * 16);
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const float4 m4 = mu[w];
-                val[4 * w] = __fsub_rn(val[4 * w], m4.x);
-                val[4 * w + 1] = __fsub_rn(val[4 * w + 1], m4.y);
-                val[4 * w + 2] = __fsub_rn(val[4 * w + 2], m4.z);
-                val[4 * w + 3] = __fsub_rn(val[4 * w + 3], m4.w);
-            }
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-            val[i] = 0.0f;
-    }
     float am = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-        am = fmaxf(am, fabsf(val[i]));
+    for (int i = 0; i < 16; i += 2)
+        am = ptx::fmax3(am, fabsf(val[i]), fabsf(val[i + 1]));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
@@ -137,12 +205,7 @@ __device__ __forceinline__ void quant_block(const uint4 *__restrict__ x, int N, 
     const float rs = s > 0.0f ? __frcp_rn(s) : 0.0f;
     uint32_t packed[4];
     if (valid && s > 0.0f) {
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const uint32_t lo = __byte_perm(int8_code(val[w * 4], s, rs), int8_code(val[w * 4 + 1], s, rs), 0x0040u);
-            const uint32_t hi = __byte_perm(int8_code(val[w * 4 + 2], s, rs), int8_code(val[w * 4 + 3], s, rs), 0x0040u);
-            packed[w] = __byte_perm(lo, hi, 0x5410u);
-        }
+        int8_codes16(val, s, rs, packed);
     } else {
 #pragma unroll
         for (int w = 0; w < 4; ++w)
@@ -152,6 +215,28 @@ __device__ __forceinline__ void quant_block(const uint4 *__restrict__ x, int N, 
         make_uint4(packed[0], packed[1], packed[2], packed[3]);
     if (tid == 0)
         scales[static_cast<size_t>(bh) * nblk + blk] = s;
+}
+
+// INT8 codes and scale of one 32-token block (blk) of head bh, loaded by the
+// 256 threads themselves (see block_values, quant_block_values).
+template <bool kSmooth, class Sync>
+__device__ __forceinline__ void quant_block(const uint4 *__restrict__ x, int N, int64_t npad, int nblk,
+                                            const float *__restrict__ mean, int8_t *__restrict__ codes,
+                                            float *__restrict__ scales, int bh, int blk, int tid,
+                                            float *warp_max, Sync sync)
+{
+    const int r = tid >> 3, part = tid & 7;
+    const int t = blk * kQBlock + r;
+    float val[16];
+    if (t < N) {
+        const uint4 *src = x + (static_cast<size_t>(bh) * N + t) * 16 + part * 2;
+        block_values<kSmooth>(ld_stream(src), ld_stream(src + 1), mean, bh, part, val);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            val[i] = 0.0f;
+    }
+    quant_block_values(val, N, npad, nblk, codes, scales, bh, blk, tid, warp_max, sync);
 }
 
 // E4M3 codes of one 128-token tile (t0 = tile * 128) of KV head bh, written
@@ -169,29 +254,34 @@ __device__ __forceinline__ void quant_v_tile(const uint4 *__restrict__ v, int Nk
                                              int bh, int t0, int tid, uint32_t *tile, Sync sync)
 {
     const int g = tid & 15;   // this thread's 8 channels, every item
-    float s8[8], r8[8];
+    float s8[8];
+    uint64_t rs2[4];
+    uint32_t keep[2] = {0u, 0u};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         s8[i] = sv[g * 8 + i];
-        r8[i] = rv[g * 8 + i];
+        keep[i >> 2] |= (s8[i] > 0.0f ? 0xffu : 0u) << (8 * (i & 3));
     }
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {   // all eight loads in flight
-        const int row = (tid + it * 256) >> 4;
-        const int t = t0 + row;
-        uint32_t w0 = 0, w1 = 0;
-        if (t < Nkv) {
-            float f[8];
-            uint32_t cd[8];
-            unpack8(ld_stream(v + (static_cast<size_t>(bh) * Nkv + t) * 16 + g), f);
+    for (int k = 0; k < 4; ++k)
+        rs2[k] = ptx::f32x2(rv[g * 8 + 2 * k], rv[g * 8 + 2 * k + 1]);
+    uint4 raw[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                cd[i] = s8[i] > 0.0f ? e4m3_code(f[i], s8[i], r8[i]) : 0u;
-            w0 = __byte_perm(__byte_perm(cd[0], cd[1], 0x0040u), __byte_perm(cd[2], cd[3], 0x0040u), 0x5410u);
-            w1 = __byte_perm(__byte_perm(cd[4], cd[5], 0x0040u), __byte_perm(cd[6], cd[7], 0x0040u), 0x5410u);
+    for (int it = 0; it < 8; ++it) {   // all eight loads in flight
+        const int t = t0 + ((tid + it * 256) >> 4);
+        raw[it] = t < Nkv ? ld_stream(v + (static_cast<size_t>(bh) * Nkv + t) * 16 + g) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int row = (tid + it * 256) >> 4;
+        uint32_t w[2] = {0u, 0u};
+        if (t0 + row < Nkv) {
+            float f[8];
+            unpack8(raw[it], f);
+            e4m3_codes8(f, s8, rs2, keep, w);
         }
         const int sw = ((row >> 4) & 7) << 1;
-        *reinterpret_cast<uint2 *>(&tile[row * 32 + ((2 * g) ^ sw)]) = make_uint2(w0, w1);
+        *reinterpret_cast<uint2 *>(&tile[row * 32 + ((2 * g) ^ sw)]) = make_uint2(w[0], w[1]);
     }
     sync();
 #pragma unroll

@@ -12,6 +12,8 @@
 //   quant_v         per 128-token tile: E4M3(v / s_v) written channel-major
 // Every FP32 operation that decides a code is an IEEE operation in a fixed
 // order, so codes and scales are bit-exact functions of the inputs.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 
 #include "prep_device.cuh"
@@ -20,57 +22,149 @@ namespace sattn {
 namespace {
 
 
-// Block: 16 chunks x 16 channel groups of 8 channels.  Each thread walks its
-// chunk's tokens in ascending order, one FP32 add per token and channel.
+// Stages of the statistics pass's copy pipeline, 32 KB each: the 64 tokens of
+// one K-mean chunk of K and of V.
+constexpr int kStatStages = 3;
+constexpr uint32_t kStatStageBytes = 2 * kMeanChunk * kHeadDim * 2;
+
+// FP32 column sums of K (ascending token order) and column max |V| of every
+// 64-token chunk, by persistent CTAs: CTA c takes the (KV head, chunk) pairs
+// u = c, c + gridDim.x, ... in memory order.  All 256 threads copy the
+// chunk's K and V rows (16 KB each, contiguous) into a shared-memory stage
+// (cp.async), kStatStages - 1 chunks ahead; then thread j < 128 sums channel j
+// of K over the chunk's tokens in ascending order and thread 128 + j takes the
+// max |V| of channel j.
 __global__ void __launch_bounds__(256) kv_chunk_stats_kernel(const uint4 *__restrict__ k,
                                                              const uint4 *__restrict__ v, int Nkv,
-                                                             int nchunks, float *__restrict__ ksum,
+                                                             int nchunks, int total, float *__restrict__ ksum,
                                                              float *__restrict__ vmax)
 {
-    const int bh = blockIdx.y;
-    const int g = threadIdx.x & 15;
-    const int chunk = blockIdx.x * 16 + (threadIdx.x >> 4);
-    if (chunk >= nchunks)
-        return;
-    float s[8], mx[8];
-    prep::chunk_stats8(k, v, Nkv, bh, chunk, g, s, mx);
-    const size_t o = (static_cast<size_t>(bh) * nchunks + chunk) * kHeadDim + g * 8;
-    reinterpret_cast<float4 *>(ksum + o)[0] = make_float4(s[0], s[1], s[2], s[3]);
-    reinterpret_cast<float4 *>(ksum + o)[1] = make_float4(s[4], s[5], s[6], s[7]);
-    reinterpret_cast<float4 *>(vmax + o)[0] = make_float4(mx[0], mx[1], mx[2], mx[3]);
-    reinterpret_cast<float4 *>(vmax + o)[1] = make_float4(mx[4], mx[5], mx[6], mx[7]);
+    extern __shared__ __align__(16) uint8_t stat_smem[];
+    const int tid = threadIdx.x;
+    auto copy = [&](int u, int slot) {   // this thread's 8 of the 2048 16-byte pieces of pair u
+        const int bh = u / nchunks, t0 = (u - bh * nchunks) * kMeanChunk;
+        const uint32_t dst = ptx::smem_u32(stat_smem + slot * kStatStageBytes);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int j = tid + 256 * (e & 3), tok = j >> 4, piece = j & 15;
+            if (t0 + tok < Nkv) {
+                const uint4 *src = (e < 4 ? k : v) + (static_cast<size_t>(bh) * Nkv + t0 + tok) * 16 + piece;
+                ptx::cp_async16(dst + (e < 4 ? 0u : kStatStageBytes / 2) + 16u * j, src);
+            }
+        }
+    };
+    const int step = static_cast<int>(gridDim.x);
+#pragma unroll
+    for (int s = 0; s < kStatStages - 1; ++s) {
+        const int64_t un = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(s) * step;
+        if (un < total)
+            copy(static_cast<int>(un), s);
+        ptx::cp_async_commit();
+    }
+    const bool is_v = tid >= 128;
+    const int c = tid & 127;
+    int i = 0;
+    for (int u = blockIdx.x; u < total; u += step, ++i) {
+        const int64_t un = static_cast<int64_t>(u) + static_cast<int64_t>(kStatStages - 1) * step;
+        if (un < total)   // the stage of pair u - step, free since the barrier that ended it
+            copy(static_cast<int>(un), (i + kStatStages - 1) % kStatStages);
+        ptx::cp_async_commit();
+        ptx::cp_async_wait<kStatStages - 1>();
+        __syncthreads();   // every thread's pieces of pair u have landed
+        const int bh = u / nchunks, chunk = u - bh * nchunks;
+        const int n = min(kMeanChunk, Nkv - chunk * kMeanChunk);
+        const uint16_t *col = reinterpret_cast<const uint16_t *>(stat_smem + (i % kStatStages) * kStatStageBytes +
+                                                                 (is_v ? kStatStageBytes / 2 : 0u)) + c;
+        float acc = 0.0f;
+        if (!is_v) {
+#pragma unroll 16
+            for (int t = 0; t < n; ++t)
+                acc = __fadd_rn(acc, __uint_as_float(static_cast<uint32_t>(col[t * kHeadDim]) << 16));
+            ksum[static_cast<size_t>(u) * kHeadDim + c] = acc;
+        } else {
+#pragma unroll 16
+            for (int t = 0; t < n; ++t)
+                acc = fmaxf(acc, fabsf(__uint_as_float(static_cast<uint32_t>(col[t * kHeadDim]) << 16)));
+            vmax[static_cast<size_t>(u) * kHeadDim + c] = acc;
+        }
+        __syncthreads();   // the stage is read: the next pair's copies may overwrite it
+    }
+    ptx::cp_async_wait<0>();
 }
 
-// One thread per (KV head, channel): chunk sums in ascending chunk order.
-__global__ void __launch_bounds__(128) kv_finalize_kernel(const float *__restrict__ ksum,
+// One CTA per KV head: thread j < 128 adds the chunk sums of channel j of K in
+// ascending chunk order (mean = sum / Nkv); thread 128 + j takes the max of
+// channel j's chunk maxima of |V| (s_v = amax / 448).  The loads of the next
+// 32 chunks are issued before the current 32 are combined, so the chain of
+// additions, not the load latency, sets the time.
+template <bool kMax>
+__device__ __forceinline__ float finalize_column(const float *__restrict__ src, int nchunks)
+{
+    constexpr int kBatch = 32;
+    auto combine = [](float acc, float x) { return kMax ? fmaxf(acc, x) : __fadd_rn(acc, x); };
+    float acc = 0.0f;
+    const int full = nchunks / kBatch;
+    float a[kBatch];
+    if (full > 0) {
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            a[u] = ptx::ld_nc_f32(src + static_cast<size_t>(u) * kHeadDim);
+    }
+    for (int b = 0; b < full; ++b) {
+        float nx[kBatch];
+        const int nb = b + 1 < full ? b + 1 : b;   // the last batch reloads itself (never used)
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            nx[u] = ptx::ld_nc_f32(src + static_cast<size_t>(nb * kBatch + u) * kHeadDim);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            acc = combine(acc, a[u]);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            a[u] = nx[u];
+    }
+    for (int ch = full * kBatch; ch < nchunks; ++ch)
+        acc = combine(acc, ptx::ld_nc_f32(src + static_cast<size_t>(ch) * kHeadDim));
+    return acc;
+}
+
+__global__ void __launch_bounds__(256) kv_finalize_kernel(const float *__restrict__ ksum,
                                                           const float *__restrict__ vmax, int Nkv,
                                                           int nchunks, float *__restrict__ k_mean,
                                                           float *__restrict__ v_scales)
 {
-    const int bh = blockIdx.x, c = threadIdx.x;
-    const float *ks = ksum + static_cast<size_t>(bh) * nchunks * kHeadDim + c;
-    const float *vm = vmax + static_cast<size_t>(bh) * nchunks * kHeadDim + c;
-    float total = 0.0f, amax = 0.0f;
-    int ch = 0;
-    for (; ch + 64 <= nchunks; ch += 64) {   // 128 loads in flight, then the ordered sum
-        float a[64], b[64];
-#pragma unroll
-        for (int u = 0; u < 64; ++u) {
-            a[u] = ks[static_cast<size_t>(ch + u) * kHeadDim];
-            b[u] = vm[static_cast<size_t>(ch + u) * kHeadDim];
-        }
-#pragma unroll
-        for (int u = 0; u < 64; ++u) {
-            total = __fadd_rn(total, a[u]);
-            amax = fmaxf(amax, b[u]);
-        }
+    const int bh = blockIdx.x, c = threadIdx.x & 127;
+    const size_t off = static_cast<size_t>(bh) * nchunks * kHeadDim + c;
+    if (threadIdx.x >= 128)
+        v_scales[bh * kHeadDim + c] = __fdiv_rn(finalize_column<true>(vmax + off, nchunks), 448.0f);
+    else
+        k_mean[bh * kHeadDim + c] = __fdiv_rn(finalize_column<false>(ksum + off, nchunks), static_cast<float>(Nkv));
+}
+
+// The statistics pass: a persistent grid of kv_chunk_stats_kernel (all CTAs
+// resident), then kv_finalize_kernel.
+cudaError_t launch_kv_stats(const Geometry &g, const uint4 *k4, const uint4 *v4, float *ksum, float *vmax,
+                            float *k_mean, float *v_scales, cudaStream_t stream)
+{
+    static int ctas = 0;
+    const int smem = kStatStages * static_cast<int>(kStatStageBytes);
+    if (ctas == 0) {
+        int dev = 0, n_sm = 0, per_sm = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+        const cudaError_t e = cudaFuncSetAttribute(kv_chunk_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   smem);
+        if (e != cudaSuccess)
+            return e;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_chunk_stats_kernel, 256, smem);
+        ctas = std::max(1, n_sm) * std::max(1, per_sm);
     }
-    for (; ch < nchunks; ++ch) {
-        total = __fadd_rn(total, ks[static_cast<size_t>(ch) * kHeadDim]);
-        amax = fmaxf(amax, vm[static_cast<size_t>(ch) * kHeadDim]);
-    }
-    k_mean[bh * kHeadDim + c] = __fdiv_rn(total, static_cast<float>(Nkv));
-    v_scales[bh * kHeadDim + c] = __fdiv_rn(amax, 448.0f);
+    const int64_t total = g.nchunks * g.B * g.Hkv;
+    kv_chunk_stats_kernel<<<static_cast<int>(std::min<int64_t>(total, ctas)), 256, smem, stream>>>(
+        k4, v4, g.Nkv, static_cast<int>(g.nchunks), static_cast<int>(total), ksum, vmax);
+    kv_finalize_kernel<<<g.B * g.Hkv, 256, 0, stream>>>(ksum, vmax, g.Nkv, static_cast<int>(g.nchunks), k_mean,
+                                                        v_scales);
+    return cudaGetLastError();
 }
 
 // One CTA per 32-token block of one head; thread = (token, eighth of the
@@ -78,7 +172,7 @@ __global__ void __launch_bounds__(128) kv_finalize_kernel(const float *__restric
 // resident to keep loads in flight.  With kSmooth (K), the per-channel mean
 // is subtracted first.
 template <bool kSmooth>
-__global__ void __launch_bounds__(256) quant_int8_kernel(const uint4 *__restrict__ x, int N,
+__global__ void __launch_bounds__(256, 6) quant_int8_kernel(const uint4 *__restrict__ x, int N,
                                                          int64_t npad, int nblk,
                                                          const float *__restrict__ mean,
                                                          int8_t *__restrict__ codes,
@@ -90,7 +184,7 @@ __global__ void __launch_bounds__(256) quant_int8_kernel(const uint4 *__restrict
 }
 
 // One CTA per 128-token tile of one KV head (prep::quant_v_tile).
-__global__ void __launch_bounds__(256) quant_v_kernel(const uint4 *__restrict__ v, int Nkv,
+__global__ void __launch_bounds__(256, 4) quant_v_kernel(const uint4 *__restrict__ v, int Nkv,
                                                       int64_t nk128,
                                                       const float *__restrict__ v_scales,
                                                       uint8_t *__restrict__ vcodes)
@@ -163,10 +257,9 @@ cudaError_t launch_prepare(const Geometry &g, const void *q, const void *k, cons
     const uint4 *k4 = static_cast<const uint4 *>(k);
     const uint4 *v4 = static_cast<const uint4 *>(v);
 
-    kv_chunk_stats_kernel<<<dim3(static_cast<unsigned>((g.nchunks + 15) / 16), bhk), 256, 0,
-                            stream>>>(k4, v4, g.Nkv, static_cast<int>(g.nchunks), ksum, vmax);
-    kv_finalize_kernel<<<bhk, kHeadDim, 0, stream>>>(ksum, vmax, g.Nkv, static_cast<int>(g.nchunks),
-                                                     k_mean, v_scales);
+    const cudaError_t se = launch_kv_stats(g, k4, v4, ksum, vmax, k_mean, v_scales, stream);
+    if (se != cudaSuccess)
+        return se;
     quant_int8_kernel<true><<<dim3(static_cast<unsigned>(g.nbk), bhk), 256, 0, stream>>>(
         k4, g.Nkv, g.nk32, static_cast<int>(g.nbk), k_mean, k_codes, k_scales);
     quant_v_kernel<<<dim3(static_cast<unsigned>(g.nk128 / kVPad), bhk), 256, 0, stream>>>(
@@ -187,10 +280,9 @@ cudaError_t launch_prepare_kv_split(const Geometry &g, const void *k, const void
     float *vmax = ksum + static_cast<size_t>(bhk) * g.nchunks * kHeadDim;
     const uint4 *k4 = static_cast<const uint4 *>(k);
     const uint4 *v4 = static_cast<const uint4 *>(v);
-    kv_chunk_stats_kernel<<<dim3(static_cast<unsigned>((g.nchunks + 15) / 16), bhk), 256, 0,
-                            stream>>>(k4, v4, g.Nkv, static_cast<int>(g.nchunks), ksum, vmax);
-    kv_finalize_kernel<<<bhk, kHeadDim, 0, stream>>>(ksum, vmax, g.Nkv, static_cast<int>(g.nchunks),
-                                                     k_mean, v_scales);
+    const cudaError_t se = launch_kv_stats(g, k4, v4, ksum, vmax, k_mean, v_scales, stream);
+    if (se != cudaSuccess)
+        return se;
     cudaError_t e = cudaEventRecord(fork, stream);
     if (e == cudaSuccess)
         e = cudaStreamWaitEvent(v_stream, fork, 0);
