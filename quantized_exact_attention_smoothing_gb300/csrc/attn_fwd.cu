@@ -1083,6 +1083,9 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
             ptx::tmem_wait_ld();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(SFREE));                          // S may be overwritten now
+            // read early, tested before the pair barrier: a partner that gives
+            // up after this read arrives on that barrier once, releasing it
+            const uint32_t aborted = ptx::ld_shared_u32(sb + OFF_ABORT);
             if (r == 0 && half == 0)
                 SATTN_TRACE(p, t, 1, j);
             if ((r & 31) == 0)
@@ -1134,7 +1137,7 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
             ptx::st_shared_f32(maxx + 4 * (((gj & 1) * 2 + half) * BM + r), tmax);
             if ((r & 31) == 0)
                 SATTN_TRACE(p, t, 21 + 4 * half + (r >> 5), j);
-            if (ptx::ld_shared_u32(sb + OFF_ABORT) != 0)   // a warp gave up: leave, do not wait for it
+            if (aborted != 0)   // a warp gave up: leave, do not wait for it
                 return false;
             ptx::named_bar_sync(1 + quarter, 64);
             tmax = fmaxf(tmax, ptx::ld_shared_f32(maxx + 4 * (((gj & 1) * 2 + (half ^ 1)) * BM + r)));
