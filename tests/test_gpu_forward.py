@@ -184,3 +184,18 @@ def test_forward_gqa_groups(oracle_mod, heads):
     w = synth.workload("c1", B=2, Hq=Hq, Hkv=Hkv, Nq=160, Nkv=416, causal=False)
     q, k, v = synth.make_inputs(w, seed=97 + Hq)
     _full(oracle_mod, q, k, v, False, f"GQA {Hq}/{Hkv}")
+
+
+# Work items run in chunks of (batch, KV head) units whose K carrier and V
+# codes fit in 48 MB (32768 keys: 12.6 MB per unit, at most 4 units per
+# chunk), the units spread evenly over the chunks; these shapes leave an
+# uneven last chunk (5 units: 3 + 2; 7 units: 4 + 3), with GQA, several
+# batches and a causal mask with Nq < Nkv.  Every output row is compared.
+@pytest.mark.parametrize("shape", [
+    (1, 10, 5, 256, 32768, False),
+    (7, 2, 1, 128, 32768, True)])
+def test_forward_chunked_item_order(oracle_mod, shape):
+    B, Hq, Hkv, Nq, Nkv, causal = shape
+    w = synth.workload("c4", B=B, Hq=Hq, Hkv=Hkv, Nq=Nq, Nkv=Nkv, causal=causal)
+    q, k, v = synth.make_inputs(w, seed=900 + B)
+    _full(oracle_mod, q, k, v, causal, f"chunked order {shape}")
