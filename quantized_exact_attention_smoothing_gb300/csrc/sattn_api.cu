@@ -739,24 +739,17 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_prepare_scratch[SATTN_NOALLOC_SCRATCH_BYTES];
 
-// Device address of g_prepare_scratch on the current device, looked up once per
-// device.  In host code the array's name is only a host-side handle; the
-// kernels must be given this address.
+// Device address of g_prepare_scratch in the current context.  In host code
+// the array's name is only a host-side handle; the kernels must be given this
+// address.  Looked up on every call (the runtime keeps the module's symbol
+// table), so a device reset or a new primary context never leaves a stale
+// address behind.
 int prepare_scratch_address(void **out)
 {
-    static void *addr[64];
-    static std::mutex mu;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_prepare_scratch) != cudaSuccess || !p)
         return SATTN_ERR_DEVICE;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_prepare_scratch) != cudaSuccess || !p)
-            return SATTN_ERR_DEVICE;
-        addr[dev] = p;
-    }
-    *out = addr[dev];
+    *out = p;
     return SATTN_OK;
 }
 
