@@ -212,6 +212,46 @@ int sattn_prepare_kv(const sattn_shape *shape, const void *k, const void *v, int
                      float *v_scales, void *workspace, void *stream);
 
 /*
+ * sattn_prepare_kv_onepass -- sattn_prepare_kv as one cooperative kernel
+ * launch ("Experiment Log" page, "Closed Prior Work" table, row "P2 direct V
+ * preparation": V prepared as soon as its per-channel amax is known).  The
+ * chunk statistics, the per-head K mean and V scales, and the K and V
+ * quantisers run as three phases of one persistent grid, separated by two
+ * grid-wide barriers, so the quantisers' second read of K and V follows the
+ * statistics' read while K and V are still in L2.  Arguments and outputs as
+ * in sattn_prepare_kv, byte for byte.  The launch is cooperative: every CTA
+ * is resident, and the barriers' waits are bounded (about one second); a
+ * wait that runs out sets a status word in `workspace`, which
+ * sattn_check_prepare_status reads (the outputs are then undefined).  Resets
+ * its counter with a memset on `stream` first.  Measured slower than
+ * sattn_prepare's split launches (c5 0.207 against 0.175 ms): the
+ * cooperative grid takes every SM, so sattn_prepare's Q quantiser cannot run
+ * beside it.
+ */
+int sattn_prepare_kv_onepass(const sattn_shape *shape, const void *k, const void *v, int8_t *k_codes,
+                             float *k_scales, float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace,
+                             void *stream);
+
+/*
+ * sattn_check_prepare_status -- synchronise `stream` and read the status word
+ * that sattn_prepare_kv_onepass left in `prepare_workspace` (sized for
+ * `shape` by sattn_query_sizes).  Returns SATTN_OK, SATTN_ERR_TIMEOUT if a
+ * grid barrier's bounded wait ran out, or SATTN_ERR_DEVICE.  Blocks the
+ * calling host thread.
+ */
+int sattn_check_prepare_status(const sattn_shape *shape, const void *prepare_workspace, void *stream);
+
+/*
+ * sattn_test_prepare_kv_onepass_withhold -- test hook: sattn_prepare_kv_onepass
+ * whose first grid barrier waits for one CTA more than the grid has, so the
+ * bounded wait runs out (after about one second), the status word is set and
+ * every CTA returns; the context stays usable.
+ */
+int sattn_test_prepare_kv_onepass_withhold(const sattn_shape *shape, const void *k, const void *v, int8_t *k_codes,
+                                           float *k_scales, float *k_mean, uint8_t *v_codes, float *v_scales,
+                                           void *workspace, void *stream);
+
+/*
  * sattn_forward_q_bf16 -- sattn_forward with the Q stage of the preparation
  * (the INT8 block quantiser of sattn_prepare) moved into the kernel: each
  * work item's 128 x 128 BF16 Q tile is quantised in shared memory while the

@@ -72,6 +72,9 @@ def load_library(build: bool = True):
     lib.sattn_test_forward_withhold_v.argtypes = [SP] + [P] * 9
     lib.sattn_prepare_noalloc.argtypes = [SP] + [P] * 11
     lib.sattn_prepare_kv.argtypes = [SP] + [P] * 9
+    lib.sattn_prepare_kv_onepass.argtypes = [SP] + [P] * 9
+    lib.sattn_test_prepare_kv_onepass_withhold.argtypes = [SP] + [P] * 9
+    lib.sattn_check_prepare_status.argtypes = [SP, P, P]
     lib.sattn_forward_q_bf16.argtypes = [SP] + [P] * 8
     lib.sattn_check_status.argtypes = [P, P]
     lib.sattn_test_int8_quantiser.argtypes = [ctypes.c_uint32, ctypes.c_uint32, P, P]
@@ -93,7 +96,8 @@ def load_library(build: bool = True):
                  "sattn_attention_host", "sattn_prepare_noalloc", "sattn_prepare_kv", "sattn_forward_q_bf16",
                  "sattn_test_int8_quantiser", "sattn_graph_create", "sattn_graph_launch", "sattn_graph_destroy",
                  "sattn_test_host_chunks", "sattn_test_p8_codes", "sattn_test_exp2", "sattn_profile_events",
-                 "sattn_attention_small", "sattn_measure_mma_rate"):
+                 "sattn_attention_small", "sattn_measure_mma_rate", "sattn_prepare_kv_onepass",
+                 "sattn_test_prepare_kv_onepass_withhold", "sattn_check_prepare_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -288,6 +292,35 @@ def attention_small(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: b
         raise SattnError(rc, "sattn_attention_small")
     buffers["forward_workspace"] = workspace
     return out, buffers
+
+
+def prepare_kv_onepass(k: torch.Tensor, v: torch.Tensor, Hq: int, Nq: int, causal: bool = False,
+                       sm_scale: float = 0.0, buffers: dict | None = None, stream=None,
+                       _withhold_for_test: bool = False) -> dict:
+    """sattn_prepare_kv_onepass: prepare_kv() as one cooperative kernel launch
+    (statistics, per-head mean and V scales, quantisers, separated by grid
+    barriers); the same bytes.  check_prepare_status() reads its status."""
+    _need_cuda(k, v)
+    _need_inputs(None, k, v)
+    B, Hkv, Nkv, _ = k.shape
+    shape = make_shape(B, Hq, Hkv, Nq, Nkv, causal, sm_scale)
+    if buffers is None:
+        buffers = prepare_buffers(shape, k.device, with_q=False)
+    lib = load_library()
+    fn = lib.sattn_test_prepare_kv_onepass_withhold if _withhold_for_test else lib.sattn_prepare_kv_onepass
+    rc = fn(ctypes.byref(shape), _ptr(k), _ptr(v), _ptr(buffers["k_codes"]), _ptr(buffers["k_scales"]),
+            _ptr(buffers["k_mean"]), _ptr(buffers["v_codes"]), _ptr(buffers["v_scales"]),
+            _ptr(buffers["workspace"]), _stream(stream))
+    if rc != 0:
+        raise SattnError(rc, "sattn_prepare_kv_onepass")
+    buffers["shape"] = shape
+    return buffers
+
+
+def check_prepare_status(buffers: dict, stream=None) -> int:
+    """sattn_check_prepare_status on the buffers of prepare_kv_onepass()."""
+    return load_library().sattn_check_prepare_status(ctypes.byref(buffers["shape"]), _ptr(buffers["workspace"]),
+                                                     _stream(stream))
 
 
 def prepare_kv(k: torch.Tensor, v: torch.Tensor, Hq: int, Nq: int, causal: bool = False,

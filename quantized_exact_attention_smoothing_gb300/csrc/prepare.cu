@@ -34,12 +34,10 @@ constexpr uint32_t kStatStageBytes = 2 * kMeanChunk * kHeadDim * 2;
 // (cp.async), kStatStages - 1 chunks ahead; then thread j < 128 sums channel j
 // of K over the chunk's tokens in ascending order and thread 128 + j takes the
 // max |V| of channel j.
-__global__ void __launch_bounds__(256) kv_chunk_stats_kernel(const uint4 *__restrict__ k,
-                                                             const uint4 *__restrict__ v, int Nkv,
-                                                             int nchunks, int total, float *__restrict__ ksum,
-                                                             float *__restrict__ vmax)
+__device__ __forceinline__ void chunk_stats_pass(const uint4 *__restrict__ k, const uint4 *__restrict__ v, int Nkv,
+                                                 int nchunks, int total, float *__restrict__ ksum,
+                                                 float *__restrict__ vmax, uint8_t *stat_smem)
 {
-    extern __shared__ __align__(16) uint8_t stat_smem[];
     const int tid = threadIdx.x;
     auto copy = [&](int u, int slot) {   // this thread's 8 of the 2048 16-byte pieces of pair u
         const int bh = u / nchunks, t0 = (u - bh * nchunks) * kMeanChunk;
@@ -90,6 +88,15 @@ __global__ void __launch_bounds__(256) kv_chunk_stats_kernel(const uint4 *__rest
         __syncthreads();   // the stage is read: the next pair's copies may overwrite it
     }
     ptx::cp_async_wait<0>();
+}
+
+__global__ void __launch_bounds__(256) kv_chunk_stats_kernel(const uint4 *__restrict__ k,
+                                                             const uint4 *__restrict__ v, int Nkv,
+                                                             int nchunks, int total, float *__restrict__ ksum,
+                                                             float *__restrict__ vmax)
+{
+    extern __shared__ __align__(16) uint8_t stat_smem[];
+    chunk_stats_pass(k, v, Nkv, nchunks, total, ksum, vmax, stat_smem);
 }
 
 // One CTA per KV head: thread j < 128 adds the chunk sums of channel j of K in
@@ -167,6 +174,139 @@ cudaError_t launch_kv_stats(const Geometry &g, const uint4 *k4, const uint4 *v4,
     return cudaGetLastError();
 }
 
+// ---- the K/V preparation as one cooperative launch ----------------------
+//
+// Statistics, finalize and the K and V quantisers in one persistent kernel,
+// phases separated by two grid barriers; the quantisers' second read of K and
+// V then follows the statistics' first read directly, walking the heads in
+// the reverse order so that the heads read last (still in L2) come first.
+
+constexpr uint64_t kGridBarrierTimeoutNs = 1000000000ull;
+constexpr size_t kPrepSyncBytes = 256;   // grid counter and status word, after the statistics
+
+// A barrier over the grid: each CTA arrives once on the counter sync[0]
+// (zeroed before the launch) and waits until the counter reaches `target`
+// (k * gridDim.x for the k-th barrier).  The launch is cooperative, so every
+// CTA is resident and the wait ends; it still gives up after about a second,
+// or as soon as another CTA has given up, setting bit 0 of sync[1], and
+// returns false.
+__device__ __forceinline__ bool grid_barrier(unsigned *sync, unsigned target)
+{
+    __syncthreads();
+    int ok = 1;
+    if (threadIdx.x == 0) {
+        __threadfence();   // the CTA's writes (ordered by the barrier above) before its arrival
+        atomicAdd(sync, 1u);
+        const uint64_t t0 = ptx::globaltimer();
+        for (unsigned it = 0;; ++it) {
+            unsigned c;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(c) : "l"(sync) : "memory");
+            if (c >= target)
+                break;
+            if ((it & 63u) == 63u &&
+                (*reinterpret_cast<volatile unsigned *>(sync + 1) != 0u || ptx::globaltimer() - t0 > kGridBarrierTimeoutNs)) {
+                atomicOr(sync + 1, 1u);
+                ok = 0;
+                break;
+            }
+        }
+        __threadfence();
+    }
+    return __syncthreads_and(ok) != 0;
+}
+
+// finalize_column for data written earlier in the same launch (loads through L2)
+template <bool kMax>
+__device__ __forceinline__ float finalize_column_l2(const float *src, int nchunks)
+{
+    float acc = 0.0f;
+    for (int ch = 0; ch < nchunks; ch += 16) {
+        float a[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+            a[u] = ch + u < nchunks ? __ldcg(src + static_cast<size_t>(ch + u) * kHeadDim) : 0.0f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+            if (ch + u < nchunks)
+                acc = kMax ? fmaxf(acc, a[u]) : __fadd_rn(acc, a[u]);
+    }
+    return acc;
+}
+
+__global__ void __launch_bounds__(256) kv_prep_fused_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                                                            int Nkv, int nchunks, int bhk, int64_t nk32, int nbk,
+                                                            int64_t nk128, float *ksum, float *vmax, float *k_mean,
+                                                            float *v_scales, int8_t *__restrict__ k_codes,
+                                                            float *__restrict__ k_scales, uint8_t *__restrict__ v_codes,
+                                                            unsigned *sync, unsigned withhold)
+{
+    extern __shared__ __align__(16) uint8_t fsmem[];
+    const int tid = threadIdx.x;
+    // phase 1: chunk statistics
+    chunk_stats_pass(k, v, Nkv, nchunks, bhk * nchunks, ksum, vmax, fsmem);
+    // (withhold: test hook, the first barrier waits for CTAs that do not exist)
+    if (!grid_barrier(sync, gridDim.x + withhold))
+        return;
+    // phase 2: per-head mean of K and scale of V
+    for (int bh = blockIdx.x; bh < bhk; bh += gridDim.x) {
+        const int c = tid & 127;
+        const size_t off = static_cast<size_t>(bh) * nchunks * kHeadDim + c;
+        if (tid >= 128)
+            v_scales[bh * kHeadDim + c] = __fdiv_rn(finalize_column_l2<true>(vmax + off, nchunks), 448.0f);
+        else
+            k_mean[bh * kHeadDim + c] = __fdiv_rn(finalize_column_l2<false>(ksum + off, nchunks), static_cast<float>(Nkv));
+    }
+    if (!grid_barrier(sync, 2 * gridDim.x + withhold))
+        return;
+    // phase 3: the quantisers, heads in reverse order; per head its V tiles, then its K blocks
+    uint32_t *tile = reinterpret_cast<uint32_t *>(fsmem);                  // V: [kVPad][32] words
+    float *sv = reinterpret_cast<float *>(fsmem + kVPad * 32 * 4);           // V scales of the head
+    float *rv = sv + kHeadDim;                                               // and their reciprocals
+    float *mean = rv + kHeadDim;                                             // K mean of the head
+    float *warp_max = mean + kHeadDim;
+    const int nvt = static_cast<int>(nk128 / kVPad);
+    const int per_head = nvt + nbk;
+    const int64_t total = static_cast<int64_t>(bhk) * per_head;
+    auto sync256 = [] { __syncthreads(); };
+    int have_v = -1, have_k = -1;   // the head whose scales / mean are in shared memory
+    for (int64_t it = blockIdx.x; it < total; it += gridDim.x) {
+        const int hi = static_cast<int>(it / per_head), r = static_cast<int>(it - static_cast<int64_t>(hi) * per_head);
+        const int bh = bhk - 1 - hi;
+        if (r < nvt) {
+            if (have_v != bh) {
+                if (tid < kHeadDim) {
+                    const float x = __ldcg(v_scales + bh * kHeadDim + tid);
+                    sv[tid] = x;
+                    rv[tid] = x > 0.0f ? __frcp_rn(x) : 0.0f;
+                }
+                have_v = bh;
+            }
+            __syncthreads();
+            prep::quant_v_tile(v, Nkv, nk128, sv, rv, v_codes, bh, r * kVPad, tid, tile, sync256);
+        } else {
+            if (have_k != bh) {
+                if (tid < kHeadDim)
+                    mean[tid] = __ldcg(k_mean + bh * kHeadDim + tid);
+                have_k = bh;
+            }
+            __syncthreads();
+            const int blk = r - nvt, row = tid >> 3, part = tid & 7;
+            const int t = blk * kQBlock + row;
+            float val[16];
+            if (t < Nkv) {
+                const uint4 *src = k + (static_cast<size_t>(bh) * Nkv + t) * 16 + part * 2;
+                prep::block_values<true>(prep::ld_stream(src), prep::ld_stream(src + 1), mean, 0, part, val);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    val[e] = 0.0f;
+            }
+            prep::quant_block_values(val, Nkv, nk32, nbk, k_codes, k_scales, bh, blk, tid, warp_max, sync256);
+        }
+        __syncthreads();   // shared memory is reused by the next item
+    }
+}
+
 // One CTA per 32-token block of one head; thread = (token, eighth of the
 // channels: 16 values), so a thread holds few registers and many CTAs stay
 // resident to keep loads in flight.  With kSmooth (K), the per-channel mean
@@ -240,9 +380,49 @@ __global__ void __launch_bounds__(256) int8_quantiser_sweep_kernel(uint32_t amax
 
 }  // namespace
 
+size_t prepare_status_offset(const Geometry &g)
+{
+    return 2 * static_cast<size_t>(g.B) * g.Hkv * g.nchunks * kHeadDim * sizeof(float) + sizeof(unsigned);
+}
+
 size_t prepare_workspace_bytes(const Geometry &g)
 {
-    return 2 * static_cast<size_t>(g.B) * g.Hkv * g.nchunks * kHeadDim * sizeof(float);
+    return 2 * static_cast<size_t>(g.B) * g.Hkv * g.nchunks * kHeadDim * sizeof(float) + kPrepSyncBytes;
+}
+
+cudaError_t launch_prepare_kv_fused(const Geometry &g, const void *k, const void *v, int8_t *k_codes,
+                                    float *k_scales, float *k_mean, uint8_t *v_codes, float *v_scales,
+                                    void *workspace, cudaStream_t stream, bool withhold)
+{
+    static int ctas = 0;
+    const int smem = kStatStages * static_cast<int>(kStatStageBytes);
+    if (ctas == 0) {
+        int dev = 0, n_sm = 0, per_sm = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+        const cudaError_t e =
+            cudaFuncSetAttribute(kv_prep_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess)
+            return e;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_prep_fused_kernel, 256, smem);
+        ctas = std::max(1, n_sm) * std::max(1, per_sm);
+    }
+    const int bhk = g.B * g.Hkv;
+    float *ksum = static_cast<float *>(workspace);
+    float *vmax = ksum + static_cast<size_t>(bhk) * g.nchunks * kHeadDim;
+    unsigned *sync = reinterpret_cast<unsigned *>(vmax + static_cast<size_t>(bhk) * g.nchunks * kHeadDim);
+    cudaError_t e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), stream);
+    if (e != cudaSuccess)
+        return e;
+    const uint4 *k4 = static_cast<const uint4 *>(k);
+    const uint4 *v4 = static_cast<const uint4 *>(v);
+    int Nkv = g.Nkv, nchunks = static_cast<int>(g.nchunks), nbk = static_cast<int>(g.nbk);
+    int64_t nk32 = g.nk32, nk128 = g.nk128;
+    unsigned wh = withhold ? 1u : 0u;
+    void *args[] = {&k4, &v4, &Nkv, &nchunks, const_cast<int *>(&bhk), &nk32, &nbk, &nk128, &ksum, &vmax,
+                    &k_mean, &v_scales, &k_codes, &k_scales, &v_codes, &sync, &wh};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kv_prep_fused_kernel), dim3(ctas), dim3(256),
+                                       args, static_cast<size_t>(smem), stream);
 }
 
 cudaError_t launch_prepare(const Geometry &g, const void *q, const void *k, const void *v,

@@ -437,6 +437,67 @@ int sattn_prepare_kv(const sattn_shape *shape, const void *k, const void *v, int
                         workspace, static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+int prepare_kv_onepass_impl(const sattn_shape *shape, const void *k, const void *v, int8_t *k_codes,
+                            float *k_scales, float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace,
+                            void *stream, bool withhold)
+{
+    Geometry g;
+    const int rc = make_geometry(shape, &g);
+    if (rc != SATTN_OK)
+        return rc;
+    const void *ptrs[] = {k, v, k_codes, k_scales, k_mean, v_codes, v_scales, workspace};
+    for (const void *p : ptrs) {
+        if (!p)
+            return SATTN_ERR_INVALID;
+        if (!aligned16(p))
+            return SATTN_ERR_MISALIGNED;
+    }
+    const int dc = check_device();
+    if (dc != SATTN_OK)
+        return dc;
+    return sattn::launch_prepare_kv_fused(g, k, v, k_codes, k_scales, k_mean, v_codes, v_scales, workspace,
+                                          static_cast<cudaStream_t>(stream), withhold) == cudaSuccess
+               ? SATTN_OK
+               : SATTN_ERR_LAUNCH;
+}
+}  // namespace
+
+int sattn_prepare_kv_onepass(const sattn_shape *shape, const void *k, const void *v, int8_t *k_codes,
+                             float *k_scales, float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace,
+                             void *stream)
+{
+    return prepare_kv_onepass_impl(shape, k, v, k_codes, k_scales, k_mean, v_codes, v_scales, workspace, stream,
+                                   false);
+}
+
+int sattn_test_prepare_kv_onepass_withhold(const sattn_shape *shape, const void *k, const void *v, int8_t *k_codes,
+                                           float *k_scales, float *k_mean, uint8_t *v_codes, float *v_scales,
+                                           void *workspace, void *stream)
+{
+    return prepare_kv_onepass_impl(shape, k, v, k_codes, k_scales, k_mean, v_codes, v_scales, workspace, stream,
+                                   true);
+}
+
+int sattn_check_prepare_status(const sattn_shape *shape, const void *prepare_workspace, void *stream)
+{
+    Geometry g;
+    const int rc = make_geometry(shape, &g);
+    if (rc != SATTN_OK)
+        return rc;
+    if (!prepare_workspace)
+        return SATTN_ERR_INVALID;
+    if (!aligned16(prepare_workspace))
+        return SATTN_ERR_MISALIGNED;
+    uint32_t word = 0;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SATTN_ERR_DEVICE;
+    if (cudaMemcpy(&word, static_cast<const char *>(prepare_workspace) + sattn::prepare_status_offset(g),
+                   sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SATTN_ERR_DEVICE;
+    return word != 0 ? SATTN_ERR_TIMEOUT : SATTN_OK;
+}
+
 int sattn_forward_q_bf16(const sattn_shape *shape, const void *q, const int8_t *k_codes, const float *k_scales,
                          const uint8_t *v_codes, const float *v_scales, void *out, void *workspace, void *stream)
 {

@@ -35,6 +35,15 @@ cudaError_t launch_prepare_kv_split(const Geometry &g, const void *k, const void
                                     float *k_scales, float *k_mean, uint8_t *v_codes, float *v_scales,
                                     void *workspace, cudaStream_t stream, cudaStream_t v_stream,
                                     cudaEvent_t fork, cudaEvent_t join);
+// The K/V part of launch_prepare as one cooperative launch (statistics,
+// finalize, K and V quantisers, separated by grid barriers whose bounded
+// waits report through the status word at prepare_status_offset; withhold:
+// test hook, the first barrier waits for CTAs that do not exist).
+cudaError_t launch_prepare_kv_fused(const Geometry &g, const void *k, const void *v, int8_t *k_codes,
+                                    float *k_scales, float *k_mean, uint8_t *v_codes, float *v_scales,
+                                    void *workspace, cudaStream_t stream, bool withhold = false);
+// Byte offset of the one-pass preparation's status word in the prepare workspace.
+size_t prepare_status_offset(const Geometry &g);
 // The Q part of launch_prepare alone (INT8 codes and block scales of Q).
 cudaError_t launch_prepare_q(const Geometry &g, const void *q, int8_t *q_codes, float *q_scales,
                              cudaStream_t stream);
