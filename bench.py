@@ -577,8 +577,7 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": DTYPE, "data": "synthetic",
-        "config": {"workload": f"{w.name}: B{w.B} Hq{w.Hq}/Hkv{w.Hkv} (GQA) Nq=Nkv={w.Nq} D128 "
-                               f"{'causal' if w.causal else 'non-causal'}",
+        "config": {"workload": describe(w),
                    "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Nq": w.Nq, "Nkv": w.Nkv, "D": 128,
                    "causal": w.causal, "step": f"oracle prepare + forward on a {rows}-row sample"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
