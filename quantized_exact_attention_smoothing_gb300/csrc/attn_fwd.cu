@@ -985,7 +985,7 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
     for (int c = 0; c < 4; ++c)
         sk[c] = kscale(t, 0, c);
 
-    float ro[64];
+    uint64_t ro2[32];   // RO in packed pairs: channels 2i, 2i + 1
     float m, d, alpha_prev;
 #ifdef SATTN_DEBUG_DUMP
     float m_tile1 = 0.0f;   // running maximum after KV tile 1 of the dumped item
@@ -1016,12 +1016,15 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
         ptx::mbar_arrive(bar(PVEMPTY));                        // the partial buffer may be reused
 #pragma unroll
         for (int c = 0; c < 64; ++c)
-            ro[c] = fmaf(ro[c], alpha, __uint_as_float(part[c >> 5][c & 31]));
+            if ((c & 1) == 0)   // one packed fused multiply-add per channel pair, each lane rounded once
+                ro2[c >> 1] = ptx::fma_f32x2(ro2[c >> 1], ptx::f32x2(alpha, alpha),
+                                             ptx::f32x2(__uint_as_float(part[c >> 5][c & 31]),
+                                                        __uint_as_float(part[(c + 1) >> 5][(c + 1) & 31])));
         d = fmaf(d, alpha, __uint_as_float(ds));
 #ifdef SATTN_DEBUG_DUMP
         if (p.dbg && jl == 1 && tt.q0 == 0 && tt.hq == 0 && tt.b == 0) {   // the state after KV tile 1
             for (int c = 0; c < 64; ++c)
-                p.dbg[DBG_RO1 + r * HD + 64 * half + c] = ro[c];
+                p.dbg[DBG_RO1 + r * HD + 64 * half + c] = (c & 1) ? ptx::f32x2_hi(ro2[c >> 1]) : ptx::f32x2_lo(ro2[c >> 1]);
             if (half == 0) {
                 p.dbg[DBG_M1 + r] = m_tile1;
                 p.dbg[DBG_A1 + r] = alpha;
@@ -1048,7 +1051,7 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
         alpha_prev = 0.0f;
     #pragma unroll
         for (int c = 0; c < 64; ++c)
-            ro[c] = 0.0f;
+            ro2[c >> 1] = 0ull;
 
         if (r == 0 && half == 0)
             SATTN_TRACE(p, t, 39, 1);
@@ -1294,8 +1297,8 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int c = 8 * w + 2 * e;
-                    const float o0 = __fmul_rn(__fmul_rn(ro[c], rcp), sv[2 * e]);
-                    const float o1 = __fmul_rn(__fmul_rn(ro[c + 1], rcp), sv[2 * e + 1]);
+                    const float o0 = __fmul_rn(__fmul_rn(ptx::f32x2_lo(ro2[c >> 1]), rcp), sv[2 * e]);
+                    const float o1 = __fmul_rn(__fmul_rn(ptx::f32x2_hi(ro2[c >> 1]), rcp), sv[2 * e + 1]);
                     const __nv_bfloat162 pr = __floats2bfloat162_rn(o0, o1);
                     memcpy(&u[e], &pr, sizeof(uint32_t));
                 }
