@@ -13,6 +13,7 @@
 // Every FP32 operation that decides a code is an IEEE operation in a fixed
 // order, so codes and scales are bit-exact functions of the inputs.
 #include <algorithm>
+#include <mutex>
 
 #include <cuda_bf16.h>
 
@@ -148,24 +149,42 @@ __global__ void __launch_bounds__(256) kv_finalize_kernel(const float *__restric
         k_mean[bh * kHeadDim + c] = __fdiv_rn(finalize_column<false>(ksum + off, nchunks), static_cast<float>(Nkv));
 }
 
+// Grid of a persistent kernel on the current device: SMs x CTAs resident per
+// SM with `smem` bytes of dynamic shared memory, whose limit is raised first.
+// Looked up once per device and kernel (`cache`: one slot per device).
+template <class Kernel>
+int persistent_grid(Kernel kernel, int smem, int (&cache)[64], cudaError_t *err)
+{
+    static std::mutex mu;
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess || dev < 0 || dev >= 64) {
+        *err = *err != cudaSuccess ? *err : cudaErrorInvalidDevice;
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int n_sm = 0, per_sm = 0;
+        if ((*err = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (*err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
+            (*err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, smem)) != cudaSuccess)
+            return 0;
+        cache[dev] = std::max(1, n_sm) * std::max(1, per_sm);
+    }
+    return cache[dev];
+}
+
 // The statistics pass: a persistent grid of kv_chunk_stats_kernel (all CTAs
 // resident), then kv_finalize_kernel.
 cudaError_t launch_kv_stats(const Geometry &g, const uint4 *k4, const uint4 *v4, float *ksum, float *vmax,
                             float *k_mean, float *v_scales, cudaStream_t stream)
 {
-    static int ctas = 0;
+    static int cache[64];
     const int smem = kStatStages * static_cast<int>(kStatStageBytes);
-    if (ctas == 0) {
-        int dev = 0, n_sm = 0, per_sm = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-        const cudaError_t e = cudaFuncSetAttribute(kv_chunk_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   smem);
-        if (e != cudaSuccess)
-            return e;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_chunk_stats_kernel, 256, smem);
-        ctas = std::max(1, n_sm) * std::max(1, per_sm);
-    }
+    cudaError_t e = cudaSuccess;
+    const int ctas = persistent_grid(kv_chunk_stats_kernel, smem, cache, &e);
+    if (e != cudaSuccess)
+        return e;
     const int64_t total = g.nchunks * g.B * g.Hkv;
     kv_chunk_stats_kernel<<<static_cast<int>(std::min<int64_t>(total, ctas)), 256, smem, stream>>>(
         k4, v4, g.Nkv, static_cast<int>(g.nchunks), static_cast<int>(total), ksum, vmax);
@@ -394,19 +413,12 @@ cudaError_t launch_prepare_kv_fused(const Geometry &g, const void *k, const void
                                     float *k_scales, float *k_mean, uint8_t *v_codes, float *v_scales,
                                     void *workspace, cudaStream_t stream, bool withhold)
 {
-    static int ctas = 0;
+    static int cache[64];
     const int smem = kStatStages * static_cast<int>(kStatStageBytes);
-    if (ctas == 0) {
-        int dev = 0, n_sm = 0, per_sm = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-        const cudaError_t e =
-            cudaFuncSetAttribute(kv_prep_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess)
-            return e;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_prep_fused_kernel, 256, smem);
-        ctas = std::max(1, n_sm) * std::max(1, per_sm);
-    }
+    cudaError_t ge = cudaSuccess;
+    const int ctas = persistent_grid(kv_prep_fused_kernel, smem, cache, &ge);
+    if (ge != cudaSuccess)
+        return ge;
     const int bhk = g.B * g.Hkv;
     float *ksum = static_cast<float *>(workspace);
     float *vmax = ksum + static_cast<size_t>(bhk) * g.nchunks * kHeadDim;
