@@ -357,6 +357,25 @@ int sattn_profile_events(void *before, void *after);
 int sattn_test_host_chunks(const sattn_shape *shape, int n_sm, int64_t *bounds, int *nchunks);
 
 /*
+ * sattn_test_item_schedule -- test hook, not part of the computation: the
+ * order in which sattn_forward's attention kernel walks its work items (an
+ * item = 128 query rows of one batch and query head) for `shape` on a device
+ * with `n_sm` SMs.  Pure host function.  The kernel is persistent, one CTA
+ * per SM; the host hands the items, in the kernel's fixed item order, to the
+ * CTA that a cost model (KV tiles of the item + 1.5) says becomes free first.
+ *   grid      out: CTAs launched, min(items, n_sm)
+ *   first     out: host array of at least n_sm + 1 entries
+ *   list      out: host array of at least B * Hq * ceil(Nq / 128) entries
+ *   n_listed  out: the number of items; CTA c walks list[first[c]] ..
+ *             list[first[c + 1] - 1].  0: no list (at most one item per CTA,
+ *             or more than the kernel argument holds); CTA c then walks items
+ *             c, c + grid, c + 2 grid, ...
+ * Which items exist does not change, and no output depends on the order.
+ */
+int sattn_test_item_schedule(const sattn_shape *shape, int n_sm, int *grid, uint16_t *first, uint16_t *list,
+                             int *n_listed);
+
+/*
  * sattn_check_status -- synchronise `stream` and read the status word that
  * sattn_forward left in `forward_workspace`.  Returns SATTN_OK, or
  * SATTN_ERR_TIMEOUT if a bounded device wait ran out, or SATTN_ERR_DEVICE if

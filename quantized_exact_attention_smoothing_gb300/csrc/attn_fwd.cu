@@ -5,8 +5,9 @@
 // per-tile RO rescaling, two-level PV accumulation, final conversion).
 //
 // Persistent: one CTA per SM walks work items (128 query rows of one batch and
-// query head) longest first; each item visits its KV tiles of 256 keys in
-// increasing order.  Twelve warps:
+// query head), the longest of each L2 chunk first, as a host-made list
+// schedule assigns them (ItemSchedule); each item visits its KV tiles of 256
+// keys in increasing order.  Twelve warps:
 //   warps 0-7   two compute warpgroups, thread = query row = TMEM lane; half h
 //               owns keys [128h, 128h + 128) of every tile and output channels
 //               [64h, 64h + 64): score scaling, masks, running max m (exchanged
@@ -69,7 +70,11 @@
 
 #include <cfloat>
 #include <cstring>
+#include <functional>
 #include <mutex>
+#include <queue>
+#include <type_traits>
+#include <vector>
 
 #include <cudaTypedefs.h>
 
@@ -145,7 +150,10 @@ enum Bar : int {
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBARS * 8;
 constexpr uint32_t OFF_FLAG = OFF_TMEM_SLOT + 4;
 constexpr uint32_t OFF_ABORT = OFF_FLAG + 4;          // set by a compute warp that gave up
-constexpr uint32_t SMEM_BYTES = OFF_ABORT + 4 + 1024;   // + alignment slack
+// this CTA's items under a list schedule (see ItemSchedule), then 0xffff
+constexpr int kSchedCtaMax = 1023;
+constexpr uint32_t OFF_ITEMS = OFF_ABORT + 4;
+constexpr uint32_t SMEM_BYTES = OFF_ITEMS + 2 * (kSchedCtaMax + 1) + 1024;   // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(OFF_V % 1024 == 0 && V_SLOT_BYTES % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_QS % 1024 == 0,
               "swizzle atoms must be 1024-aligned");
@@ -176,6 +184,7 @@ struct FwdParams {
     float zero;   // always +0 (see dd_pair)
     int small;    // the single-launch small-shape path: prepare `sp` first (small_prepare)
     SmallPrep sp;
+    int sched;    // 1: each CTA walks its list of the ItemSchedule argument; 0: the stride (cta_item)
 #ifdef SATTN_DEBUG_DUMP
     // intermediates of query tile 0 of (batch 0, head 0), KV tile 0:
     // [0, 32768) raw S accumulators (128 x 256), [32768, 40960) P8 words
@@ -297,6 +306,41 @@ __device__ __forceinline__ Tile item_tile(const FwdParams &p, int it)
     t.trace = (blockIdx.x == 0);
     t.g0 = 0;
     return t;
+}
+
+// Which items a CTA walks.  Items cost in proportion to their KV tiles, and
+// the stride c, c + grid, c + 2 grid, ... gives each CTA the same number of
+// items, so the CTAs whose items were shorter finish early while the others
+// still run (most where a chunk of item_tile's order ends inside a wave).  The
+// host therefore makes a list schedule: it hands the items, in item_tile's
+// order, one by one to the CTA that a cost model (KV tiles + 1.5 per item)
+// says becomes free first, equal times to the lower CTA.  That is the order a
+// shared counter taken by CTAs as they free up would give, without a counter
+// and without the hand-over of each fetched index to the CTA's five roles.
+// The schedule travels as a kernel argument (CTA c's items are
+// list[first[c]] .. list[first[c + 1] - 1]); the kernel copies the CTA's part
+// to shared memory, closed by 0xffff.  The stride remains for launches with at
+// most one item per CTA, more items than the list holds, or a CTA share above
+// kSchedCtaMax.
+constexpr int kSchedMaxItems = 15360, kSchedMaxGrid = 192;
+template <int kItems, int kGrid>
+struct ItemScheduleT {
+    uint16_t first[kGrid + 1];
+    uint16_t list[kItems];
+};
+using ItemSchedule = ItemScheduleT<kSchedMaxItems, kSchedMaxGrid>;
+using NoSchedule = ItemScheduleT<1, 1>;   // the small path: always the stride
+
+// Item number n (0, 1, ...) of this CTA, or -1 past its last item.  With a
+// schedule, n is at most the CTA's item count (every caller stops at -1).
+__device__ __forceinline__ int cta_item(const FwdParams &p, uint32_t sb, int n)
+{
+    if (p.sched) {
+        const uint32_t v = ptx::ld_shared_u16(sb + OFF_ITEMS + 2u * static_cast<uint32_t>(n));
+        return v == 0xffffu ? -1 : static_cast<int>(v);
+    }
+    const long long it = static_cast<long long>(blockIdx.x) + static_cast<long long>(n) * gridDim.x;
+    return it < p.n_items ? static_cast<int>(it) : -1;
 }
 
 // ---------------------------------------------------------------- the P step
@@ -637,8 +681,8 @@ __device__ __forceinline__ void kload_role(const FwdParams &p, const CUtensorMap
     ptx::prefetch_tensormap(tm_k);
     int issued = -1;
     bool ok = true;
-    int g = 0;   // KV tiles of the earlier items
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
+    int g = 0, n = 0;   // KV tiles and items of the earlier items
+    for (int it = cta_item(p, sb, 0); it >= 0 && ok; it = cta_item(p, sb, ++n)) {
         Tile t = item_tile(p, it);
         t.g0 = g;
         const int bhk = t.b * p.Hkv + t.hk;
@@ -685,14 +729,14 @@ __device__ __forceinline__ void vload_role(const FwdParams &p, const CUtensorMap
                        SV_BYTES, bar(QSTAGE));
     };
     if (p.withhold_v) {   // test hook: the MMA thread's wait for V runs out
-        load_q(item_tile(p, blockIdx.x), 0);
+        load_q(item_tile(p, cta_item(p, sb, 0)), 0);
         wt.drain(bar(QSTAGE), 0);
         return;
     }
     int issued_v = -1, issued_q = -1;
     bool ok = true;
     int g = 0, n = 0;   // KV tiles and items of this CTA before the current item
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++n) {
+    for (int it = cta_item(p, sb, 0); it >= 0 && ok; it = cta_item(p, sb, ++n)) {
         Tile t = item_tile(p, it);
         t.g0 = g;
         const int bhk = t.b * p.Hkv + t.hk;
@@ -714,8 +758,8 @@ __device__ __forceinline__ void vload_role(const FwdParams &p, const CUtensorMap
             if (!ok)
                 break;
             SATTN_TRACE(p, t, 12, j);
-            const int nx = it + static_cast<int>(gridDim.x);
-            if (j == 0 && nx < p.n_items) {
+            const int nx = j == 0 ? cta_item(p, sb, n + 1) : -1;
+            if (nx >= 0) {
                 if (!wt.wait(bar(QFULL), n & 1, SITE_QE)) {
                     ok = false;
                     break;
@@ -742,7 +786,7 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
     auto bar = [sb](int i) { return sb + OFF_BAR + 8u * i; };
     bool ok = true;
     int g = 0, n = 0;
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++n) {
+    for (int it = cta_item(p, sb, 0); it >= 0 && ok; it = cta_item(p, sb, ++n)) {
         Tile t = item_tile(p, it);
         t.g0 = g;
         SATTN_TRACE(p, t, 39, 0);
@@ -897,11 +941,11 @@ __device__ __forceinline__ void qconv_role(const FwdParams &p, const CUtensorMap
     if (kFuseQ) {
         if (lane == 0)
             ptx::prefetch_tensormap(tm_q);
-        if (!quantize_item(blockIdx.x, 0))
+        if (!quantize_item(cta_item(p, sb, 0), 0))
             return;
     }
     int n = 0;
-    for (int it = blockIdx.x; it < p.n_items; it += gridDim.x, ++n) {
+    for (int it = cta_item(p, sb, 0); it >= 0; it = cta_item(p, sb, ++n)) {
         if ((n >= 1 && !wt.wait(bar(QEMPTY), (n - 1) & 1, SITE_QEMPTY)) ||
             !wt.wait(bar(QSTAGE), n & 1, SITE_QS))
             return;
@@ -923,8 +967,8 @@ __device__ __forceinline__ void qconv_role(const FwdParams &p, const CUtensorMap
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(bar(QFULL));
         if (kFuseQ) {
-            const int nx = it + static_cast<int>(gridDim.x);
-            if (nx < p.n_items) {
+            const int nx = cta_item(p, sb, n + 1);
+            if (nx >= 0) {
                 __syncwarp();   // every lane has read the INT8 tile before it is rewritten
                 if (!wt.wait(bar(STGFREE), n & 1, SITE_STG) || !quantize_item(nx, n + 1))
                     return;
@@ -965,7 +1009,7 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
         return kb < p.nbk ? (p.small ? ptx::ld_f32(a) : ptx::ld_nc_f32(a)) : 0.0f;
     };
 
-    int it = blockIdx.x;
+    int it = cta_item(p, sb, 0);
     Tile t = item_tile(p, it);
     if (r == 0 && half == 0)
         SATTN_TRACE(p, t, 38, 1);
@@ -1042,8 +1086,8 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
         t.g0 = g;
         const int i = t.q0 + r;
         const int lim = p.causal ? i + (p.Nkv - p.Nq) : 0x7fffffff;   // last kept key of row i
-        const int nx = it + static_cast<int>(gridDim.x);
-        const bool has_next = nx < p.n_items;
+        const int nx = cta_item(p, sb, n + 1);
+        const bool has_next = nx >= 0;
         // (the next item's tile is recomputed where needed rather than kept live)
         float sq_next = (!kFuseQ && has_next) ? qscale(item_tile(p, nx)) : 0.0f;
         m = -INFINITY;
@@ -1580,11 +1624,14 @@ __device__ __forceinline__ void small_prepare(const FwdParams &p, uint8_t *smem)
 
 // kSmall: the single-launch small-shape path, whose preparation runs first
 // (a separate instantiation, so that the other launches carry none of its code)
-template <bool kFuseQ, bool kSmall>
+// kList: the launch carries a list schedule (a ~30 KB argument, which costs
+// about 2 us per launch; launches without a list use the small argument).
+template <bool kFuseQ, bool kSmall, bool kList>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
-                    const FwdParams p)
+                    const FwdParams p,
+                    const __grid_constant__ std::conditional_t<kList, ItemSchedule, NoSchedule> sched)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1604,6 +1651,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             small_prepare(p, smem);
     }
 
+    if (kList && p.sched) {   // this CTA's items, closed by 0xffff (read after the barrier below)
+        const int b = sched.first[blockIdx.x], cnt = sched.first[blockIdx.x + 1] - b;
+        for (int k = threadIdx.x; k <= cnt; k += NTHREADS)
+            reinterpret_cast<uint16_t *>(smem + OFF_ITEMS)[k] = k < cnt ? sched.list[b + k] : uint16_t{0xffff};
+    }
     if (threadIdx.x == 0) {
         *flag = *reinterpret_cast<volatile uint32_t *>(p.status);
         *reinterpret_cast<volatile uint32_t *>(smem + OFF_ABORT) = 0u;
@@ -1648,7 +1700,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + OFF_TMEM_SLOT);
 
-    if (*flag == 0 && static_cast<int>(blockIdx.x) < p.n_items) {
+    if (*flag == 0 && cta_item(p, sb, 0) >= 0) {
         if (warp < WARP_PRODUCER) {
             ptx::setmaxnreg_inc<kRegsCompute>();
             compute_role<kFuseQ>(p, &tm_o, sb, tmem, warp, lane, wt);
@@ -1782,21 +1834,126 @@ namespace {
 // The per-warpgroup register split only adds up when the kernel is launched
 // with exactly kLaunchRegs registers per thread; refuse to launch otherwise.
 // Also raises the kernel's dynamic shared-memory limit.  Once per process.
-template <bool kFuseQ, bool kSmall>
+template <bool kFuseQ, bool kSmall, bool kList>
 cudaError_t kernel_attributes()
 {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
         cudaFuncAttributes fa;
-        attr_err = cudaFuncGetAttributes(&fa, attn_fwd_kernel<kFuseQ, kSmall>);
+        attr_err = cudaFuncGetAttributes(&fa, attn_fwd_kernel<kFuseQ, kSmall, kList>);
         if (attr_err == cudaSuccess && fa.numRegs != kLaunchRegs)
             attr_err = cudaErrorInvalidConfiguration;
         if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(attn_fwd_kernel<kFuseQ, kSmall>,
+            attr_err = cudaFuncSetAttribute(attn_fwd_kernel<kFuseQ, kSmall, kList>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
     });
     return attr_err;
+}
+
+// The shape fields of the item order (item_tile): the query tiles, the items,
+// and the chunks of (batch, KV head) units with the reciprocals of udiv.
+// False if the item indices leave udiv's range.
+bool plan_items(const Geometry &g, FwdParams &prm)
+{
+    prm.B = g.B;
+    prm.Hq = g.Hq;
+    prm.Hkv = g.Hkv;
+    prm.Nq = g.Nq;
+    prm.Nkv = g.Nkv;
+    prm.group = g.Hq / g.Hkv;
+    prm.n_qtiles = static_cast<int>((g.Nq + BM - 1) / BM);
+    const int64_t n_items = static_cast<int64_t>(prm.n_qtiles) * g.Hq * g.B;
+    if (n_items >= (int64_t(1) << 31))
+        return false;
+    prm.n_items = static_cast<int>(n_items);
+    auto recip = [](int d) { return d == 1 ? 0ull : ~0ull / static_cast<unsigned long long>(d) + 1ull; };
+    prm.n_units = g.B * g.Hkv;
+    {   // the fewest chunks whose units' K carrier (2 bytes) and V codes (1 byte) fit in
+        // kL2ChunkBytes, with the units spread evenly over them
+        const int64_t unit_bytes = static_cast<int64_t>(g.Nkv) * HD * 3;
+        const int64_t cap = std::max<int64_t>(1, std::min<int64_t>(prm.n_units, kL2ChunkBytes / unit_bytes));
+        const int64_t n_chunks = (prm.n_units + cap - 1) / cap;
+        prm.chunk_units = static_cast<int>((prm.n_units + n_chunks - 1) / n_chunks);
+    }
+    prm.chunk_items = prm.chunk_units * prm.group * prm.n_qtiles;
+    const int tail_units = prm.n_units - (prm.n_units - 1) / prm.chunk_units * prm.chunk_units;
+    prm.m_chunk = recip(prm.chunk_items);
+    prm.m_row = recip(prm.chunk_units * prm.group);
+    prm.m_row_tail = recip(tail_units * prm.group);
+    prm.m_hkv = recip(g.Hkv);
+    prm.m_group = recip(prm.group);
+    prm.causal = g.causal;
+    return true;
+}
+
+// KV tiles of item `it` as item_tile computes them (host copy, for the cost
+// model of the schedule only: no result depends on it).
+int host_item_ntiles(const FwdParams &p, int it)
+{
+    const int c = it / p.chunk_items, r = it - c * p.chunk_items, u0 = c * p.chunk_units;
+    const int row = (u0 + p.chunk_units > p.n_units ? p.n_units - u0 : p.chunk_units) * p.group;
+    const int q0 = (p.n_qtiles - 1 - r / row) * BM;
+    int kv_end = p.Nkv;
+    if (p.causal)
+        kv_end = std::min(p.Nkv, std::min(q0 + BM, p.Nq) + (p.Nkv - p.Nq));
+    return (kv_end + BN - 1) / BN;
+}
+
+// The list schedule of the items over `grid` CTAs (see ItemSchedule): items in
+// order, each to the CTA with the earliest modelled finish, costs in half
+// tiles (2 per KV tile, 3 per item).  False where the stride is kept.
+bool build_item_schedule(const FwdParams &p, int grid, ItemSchedule &s)
+{
+    if (grid > kSchedMaxGrid || p.n_items > kSchedMaxItems || p.n_items <= grid)
+        return false;
+    using Slot = std::pair<long long, int>;   // (modelled finish, CTA)
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
+    for (int c = 0; c < grid; ++c)
+        free_at.push({0, c});
+    std::vector<int> owner(p.n_items), count(grid, 0);
+    for (int it = 0; it < p.n_items; ++it) {
+        const Slot f = free_at.top();
+        free_at.pop();
+        owner[it] = f.second;
+        if (++count[f.second] > kSchedCtaMax)
+            return false;
+        free_at.push({f.first + 2 * host_item_ntiles(p, it) + 3, f.second});
+    }
+    std::vector<int> next(grid);
+    int k = 0;
+    for (int c = 0; c < grid; ++c) {
+        s.first[c] = static_cast<uint16_t>(k);
+        next[c] = k;
+        k += count[c];
+    }
+    s.first[grid] = static_cast<uint16_t>(k);
+    for (int it = 0; it < p.n_items; ++it)   // each CTA's items in increasing order
+        s.list[next[owner[it]]++] = static_cast<uint16_t>(it);
+    return true;
+}
+
+// The schedule of the last launch shape of this thread, rebuilt when the
+// shape or the grid changes.
+struct ScheduleCache {
+    int key[10] = {-1};
+    bool valid = false;
+    ItemSchedule s;
+};
+static_assert(kSchedMaxItems < 0xffff && kSchedCtaMax < kSchedMaxItems, "item indices and the end mark fit 16 bits");
+static_assert(4 * sizeof(CUtensorMap) + sizeof(FwdParams) + sizeof(ItemSchedule) + 256 <= 32764,
+              "kernel arguments within the 32764-byte limit");
+
+const ItemSchedule *item_schedule(const FwdParams &p, int grid)
+{
+    static thread_local ScheduleCache cache;
+    const int key[10] = {p.n_items, grid, p.n_qtiles, p.causal, p.Nq, p.Nkv, p.n_units, p.chunk_units, p.group,
+                         p.chunk_items};
+    if (std::memcmp(key, cache.key, sizeof key) != 0) {
+        std::memcpy(cache.key, key, sizeof key);
+        cache.valid = build_item_schedule(p, grid, cache.s);
+    }
+    return cache.valid ? &cache.s : nullptr;
 }
 
 // q: INT8 codes [B, Hq, nq32, 128] with q_scales, or with kFuseQ the BF16 Q
@@ -1874,10 +2031,12 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const i
             return 1;
     }
 
-    cudaError_t attr_err = kernel_attributes<kFuseQ, false>();
+    cudaError_t attr_err = kernel_attributes<kFuseQ, false, false>();
+    if (attr_err == cudaSuccess)
+        attr_err = kernel_attributes<kFuseQ, false, true>();
     if constexpr (!kFuseQ)
-        if (small)
-            attr_err = kernel_attributes<false, true>();
+        if (small && attr_err == cudaSuccess)
+            attr_err = kernel_attributes<false, true, false>();
     if (attr_err != cudaSuccess)
         return static_cast<int>(attr_err);
 
@@ -1896,33 +2055,8 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const i
     prm.out = static_cast<__nv_bfloat16 *>(out);
     prm.status = status;
     prm.withhold_v = withhold_v ? 1 : 0;
-    prm.B = g.B;
-    prm.Hq = g.Hq;
-    prm.Hkv = g.Hkv;
-    prm.Nq = g.Nq;
-    prm.Nkv = g.Nkv;
-    prm.group = g.Hq / g.Hkv;
-    prm.n_qtiles = static_cast<int>((g.Nq + BM - 1) / BM);
-    const int64_t n_items = static_cast<int64_t>(prm.n_qtiles) * g.Hq * g.B;
-    if (n_items >= (int64_t(1) << 31))
+    if (!plan_items(g, prm))
         return static_cast<int>(cudaErrorInvalidValue);   // item indices must fit udiv's range
-    prm.n_items = static_cast<int>(n_items);
-    auto recip = [](int d) { return d == 1 ? 0ull : ~0ull / static_cast<unsigned long long>(d) + 1ull; };
-    prm.n_units = g.B * g.Hkv;
-    {   // the fewest chunks whose units' K carrier (2 bytes) and V codes (1 byte) fit in
-        // kL2ChunkBytes, with the units spread evenly over them
-        const int64_t unit_bytes = static_cast<int64_t>(g.Nkv) * HD * 3;
-        const int64_t cap = std::max<int64_t>(1, std::min<int64_t>(prm.n_units, kL2ChunkBytes / unit_bytes));
-        const int64_t n_chunks = (prm.n_units + cap - 1) / cap;
-        prm.chunk_units = static_cast<int>((prm.n_units + n_chunks - 1) / n_chunks);
-    }
-    prm.chunk_items = prm.chunk_units * prm.group * prm.n_qtiles;
-    const int tail_units = prm.n_units - (prm.n_units - 1) / prm.chunk_units * prm.chunk_units;
-    prm.m_chunk = recip(prm.chunk_items);
-    prm.m_row = recip(prm.chunk_units * prm.group);
-    prm.m_row_tail = recip(tail_units * prm.group);
-    prm.m_hkv = recip(g.Hkv);
-    prm.m_group = recip(prm.group);
     prm.causal = g.causal;
     prm.nq32 = static_cast<int>(g.nq32);
     prm.nbq = static_cast<int>(g.nbq);
@@ -1939,22 +2073,28 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const i
     prm.dbg = debug_dump_buffer();
 #endif
 
-    // persistent: one CTA per SM, each walking the items it, it + grid, ...
+    // persistent: one CTA per SM, each walking its items (cta_item)
     int dev = 0, n_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1)
         return static_cast<int>(cudaErrorInvalidDevice);
     const int grid = std::min(prm.n_items, n_sm);
+    const ItemSchedule *sched = small ? nullptr : item_schedule(prm, grid);
+    prm.sched = sched ? 1 : 0;
     if (g_ev_before && cudaEventRecord(g_ev_before, stream) != cudaSuccess)
         return static_cast<int>(cudaGetLastError());
     bool launched = false;
     if constexpr (!kFuseQ)
         if (small) {
-            attn_fwd_kernel<false, true><<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, tmo, prm);
+            attn_fwd_kernel<false, true, false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, tmo, prm,
+                                                                                         NoSchedule{});
             launched = true;
         }
-    if (!launched)
-        attn_fwd_kernel<kFuseQ, false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, tmo, prm);
+    if (!launched && sched)
+        attn_fwd_kernel<kFuseQ, false, true><<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, tmo, prm, *sched);
+    else if (!launched)
+        attn_fwd_kernel<kFuseQ, false, false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, tmo, prm,
+                                                                                      NoSchedule{});
     const cudaError_t le = cudaGetLastError();
     if (le != cudaSuccess)
         return static_cast<int>(le);
@@ -1978,9 +2118,13 @@ int forward_init()
 {
     if (!tensor_map_encoder())
         return 1;
-    const cudaError_t a = kernel_attributes<false, false>(), b = kernel_attributes<true, false>(),
-                      c = kernel_attributes<false, true>();
-    return static_cast<int>(a != cudaSuccess ? a : b != cudaSuccess ? b : c);
+    const cudaError_t r[5] = {kernel_attributes<false, false, false>(), kernel_attributes<false, false, true>(),
+                              kernel_attributes<true, false, false>(), kernel_attributes<true, false, true>(),
+                              kernel_attributes<false, true, false>()};
+    for (const cudaError_t e : r)
+        if (e != cudaSuccess)
+            return static_cast<int>(e);
+    return 0;
 }
 
 int launch_forward_q_bf16(const Geometry &g, const void *q, const int8_t *k_codes, const float *k_scales,
@@ -1989,6 +2133,22 @@ int launch_forward_q_bf16(const Geometry &g, const void *q, const int8_t *k_code
 {
     return launch_impl<true>(g, q, nullptr, k_codes, k_scales, v_codes, v_scales, out, status, carrier, stream,
                              false, true);
+}
+
+int item_schedule(const Geometry &g, int n_sm, int *grid, uint16_t *first, uint16_t *list, int *n_listed)
+{
+    FwdParams prm{};
+    if (n_sm < 1 || !plan_items(g, prm))
+        return 1;
+    *grid = std::min(prm.n_items, n_sm);
+    *n_listed = 0;
+    std::vector<ItemSchedule> s(1);
+    if (!build_item_schedule(prm, *grid, s[0]))
+        return 0;   // the stride
+    std::memcpy(first, s[0].first, sizeof(uint16_t) * (*grid + 1));
+    std::memcpy(list, s[0].list, sizeof(uint16_t) * prm.n_items);
+    *n_listed = prm.n_items;
+    return 0;
 }
 
 int launch_small(const Geometry &g, const SmallPrep &sp, void *out, void *status, void *carrier, cudaStream_t stream)

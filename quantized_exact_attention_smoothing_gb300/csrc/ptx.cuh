@@ -497,6 +497,13 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Packed pairs of FP32 values (low word = first element): elementwise
 // products, differences, each rounded to nearest even like the scalar ops.
 __device__ __forceinline__ uint64_t f32x2(float lo, float hi)

@@ -624,6 +624,18 @@ int sattn_test_host_chunks(const sattn_shape *shape, int n_sm, int64_t *bounds, 
     return SATTN_OK;
 }
 
+int sattn_test_item_schedule(const sattn_shape *shape, int n_sm, int *grid, uint16_t *first, uint16_t *list,
+                              int *n_listed)
+{
+    Geometry g;
+    const int rc = make_geometry(shape, &g);
+    if (rc != SATTN_OK)
+        return rc;
+    if (!grid || !first || !list || !n_listed || n_sm < 1)
+        return SATTN_ERR_INVALID;
+    return sattn::item_schedule(g, n_sm, grid, first, list, n_listed) == 0 ? SATTN_OK : SATTN_ERR_INVALID;
+}
+
 int sattn_check_status(const void *forward_workspace, void *stream)
 {
     if (!forward_workspace)

@@ -106,6 +106,12 @@ struct SmallPrep {
     uint8_t *v_codes;
     float *v_scales;
 };
+// The attention kernel's list schedule of work items for `g` on n_sm SMs
+// (host only): grid = the CTAs launched; with n_listed = n_items > 0, CTA c
+// walks list[first[c]] .. list[first[c + 1] - 1], with n_listed = 0 the
+// stride c, c + grid, ...  first holds n_sm + 1 entries, list n_items.
+// 0 on success.
+int item_schedule(const Geometry &g, int n_sm, int *grid, uint16_t *first, uint16_t *list, int *n_listed);
 // Largest Nkv of the small-shape path (its K-mean chunk sums stay in shared memory).
 constexpr int kSmallMaxNkv = 1024;
 // prepare + forward in one launch for B = Hq = Hkv = 1, Nq <= 128, Nkv <= kSmallMaxNkv;
