@@ -112,8 +112,9 @@ typedef struct {
     size_t v_codes, v_scales;   /* E4M3 [B][Hkv][128][Nkv128] (channel-major), FP32 [B][Hkv][128] */
     size_t out;                 /* BF16 [B][Hq][Nq][128] */
     size_t prepare_workspace;   /* scratch of sattn_prepare */
-    size_t forward_workspace;   /* scratch of sattn_forward: a 256-byte status block,
-                                   then the FP16 copy of the K codes that the
+    size_t forward_workspace;   /* scratch of sattn_forward: a 256-byte status block
+                                   (status words, then the attention kernel's work-item
+                                   counters), then the FP16 copy of the K codes that the
                                    tensor cores read (B * Hkv * Nkv * 256 bytes) */
     size_t arena;               /* one device block holding all of the above,
                                    for sattn_attention_host */
@@ -165,9 +166,11 @@ int sattn_prepare(const sattn_shape *shape, const void *q, const void *k, const 
  *               (every INT8 code as the same integer in FP16, exact) that the
  *               tensor cores read, since this part has no INT8 tensor-core
  *               product; contents on entry are ignored
- * Two kernels: the K codes are copied to FP16 into the workspace (bound by
- * HBM bandwidth), then a persistent CTA per SM walks the (query tile, head,
- * batch) items, longest first.
+ * Two kernels (after a memset of the status block): the K codes are copied to
+ * FP16 into the workspace (bound by HBM bandwidth), then a persistent CTA per
+ * SM takes the (query tile, head, batch) items, longest first within groups
+ * of KV heads that fit in L2, from a counter in the status block as it frees
+ * up.  Concurrent calls must use separate workspaces.
  * Exactness: QK^T is computed from the codes with products and sums that are
  * exact integers.  Every FP8 byte of P is the one the arithmetic above defines:
  * the kernel encodes fl(2^x) from the hardware approximation (relative error
@@ -355,25 +358,6 @@ int sattn_profile_events(void *before, void *after);
  *   nchunks  out: the number of chunks (1 to 8)
  */
 int sattn_test_host_chunks(const sattn_shape *shape, int n_sm, int64_t *bounds, int *nchunks);
-
-/*
- * sattn_test_item_schedule -- test hook, not part of the computation: the
- * order in which sattn_forward's attention kernel walks its work items (an
- * item = 128 query rows of one batch and query head) for `shape` on a device
- * with `n_sm` SMs.  Pure host function.  The kernel is persistent, one CTA
- * per SM; the host hands the items, in the kernel's fixed item order, to the
- * CTA that a cost model (KV tiles of the item + 1.5) says becomes free first.
- *   grid      out: CTAs launched, min(items, n_sm)
- *   first     out: host array of at least n_sm + 1 entries
- *   list      out: host array of at least B * Hq * ceil(Nq / 128) entries
- *   n_listed  out: the number of items; CTA c walks list[first[c]] ..
- *             list[first[c + 1] - 1].  0: no list (at most one item per CTA,
- *             or more than the kernel argument holds); CTA c then walks items
- *             c, c + grid, c + 2 grid, ...
- * Which items exist does not change, and no output depends on the order.
- */
-int sattn_test_item_schedule(const sattn_shape *shape, int n_sm, int *grid, uint16_t *first, uint16_t *list,
-                             int *n_listed);
 
 /*
  * sattn_check_status -- synchronise `stream` and read the status word that

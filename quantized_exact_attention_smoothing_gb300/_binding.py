@@ -87,9 +87,6 @@ def load_library(build: bool = True):
     lib.sattn_graph_create.argtypes = [SP] + [P] * 13 + [ctypes.POINTER(ctypes.c_void_p)]
     lib.sattn_test_host_chunks.argtypes = [SP, ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
                                            ctypes.POINTER(ctypes.c_int)]
-    lib.sattn_test_item_schedule.argtypes = [SP, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
-                                             ctypes.POINTER(ctypes.c_uint16), ctypes.POINTER(ctypes.c_uint16),
-                                             ctypes.POINTER(ctypes.c_int)]
     lib.sattn_graph_launch.argtypes = [P, P]
     lib.sattn_graph_destroy.argtypes = [P]
     lib.sattn_attention_host.argtypes = [SP, P, P, P, P, P, ctypes.c_size_t, P]
@@ -100,8 +97,7 @@ def load_library(build: bool = True):
                  "sattn_test_int8_quantiser", "sattn_graph_create", "sattn_graph_launch", "sattn_graph_destroy",
                  "sattn_test_host_chunks", "sattn_test_p8_codes", "sattn_test_exp2", "sattn_profile_events",
                  "sattn_attention_small", "sattn_measure_mma_rate", "sattn_prepare_kv_onepass",
-                 "sattn_test_prepare_kv_onepass_withhold", "sattn_check_prepare_status",
-                 "sattn_test_item_schedule"):
+                 "sattn_test_prepare_kv_onepass_withhold", "sattn_check_prepare_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib

@@ -5,9 +5,9 @@
 // per-tile RO rescaling, two-level PV accumulation, final conversion).
 //
 // Persistent: one CTA per SM walks work items (128 query rows of one batch and
-// query head), the longest of each L2 chunk first, as a host-made list
-// schedule assigns them (ItemSchedule); each item visits its KV tiles of 256
-// keys in increasing order.  Twelve warps:
+// query head), the longest of each L2 chunk first, taking each next item from
+// a counter shared by the CTAs as it frees up (cta_item); each item visits its
+// KV tiles of 256 keys in increasing order.  Twelve warps:
 //   warps 0-7   two compute warpgroups, thread = query row = TMEM lane; half h
 //               owns keys [128h, 128h + 128) of every tile and output channels
 //               [64h, 64h + 64): score scaling, masks, running max m (exchanged
@@ -127,6 +127,7 @@ constexpr uint32_t SV_BYTES = HD * 4;
 constexpr uint32_t OFF_SQ = OFF_SV + 3 * SV_BYTES;          // [item % 2][4] Q block scales (in-kernel Q quantisation)
 constexpr uint32_t OFF_PARK = OFF_SQ + 2 * 4 * 4;         // [half][row] 16 bytes: exponent arguments of an undecided P8 word
 constexpr uint32_t OFF_BAR = OFF_PARK + 2 * BM * 16;
+constexpr int kItemSlots = 4;   // ring of the CTA's next item indices (see cta_item)
 enum Bar : int {
     KFULL = 0,
     KEMPTY = KFULL + KSLOTS,
@@ -145,15 +146,15 @@ enum Bar : int {
     QBF = MMADONE + 1,          // in-kernel Q quantisation: the BF16 Q tile landed in the staging buffer
     QQDONE = QBF + 1,           // its codes and block scales are written; the staging buffer is free
     STGFREE = QQDONE + 1,       // an item's final conversion has left the staging buffer
-    NBARS = STGFREE + 1
+    ITEMFULL = STGFREE + 1,     // kItemSlots barriers: an item index was written into its ring slot
+    NBARS = ITEMFULL + kItemSlots
 };
 constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBARS * 8;
 constexpr uint32_t OFF_FLAG = OFF_TMEM_SLOT + 4;
 constexpr uint32_t OFF_ABORT = OFF_FLAG + 4;          // set by a compute warp that gave up
-// this CTA's items under a list schedule (see ItemSchedule), then 0xffff
-constexpr int kSchedCtaMax = 1023;
+// ring of this CTA's next item indices (see cta_item)
 constexpr uint32_t OFF_ITEMS = OFF_ABORT + 4;
-constexpr uint32_t SMEM_BYTES = OFF_ITEMS + 2 * (kSchedCtaMax + 1) + 1024;   // + alignment slack
+constexpr uint32_t SMEM_BYTES = OFF_ITEMS + 4 * kItemSlots + 1024;   // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 static_assert(OFF_V % 1024 == 0 && V_SLOT_BYTES % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_QS % 1024 == 0,
               "swizzle atoms must be 1024-aligned");
@@ -161,7 +162,8 @@ static_assert(OFF_V % 1024 == 0 && V_SLOT_BYTES % 1024 == 0 && OFF_Q % 1024 == 0
 // where a wait gave up (second status word)
 enum Site : uint32_t {
     SITE_KE = 1, SITE_VE, SITE_Q, SITE_K, SITE_P, SITE_V, SITE_PVE, SITE_DONE, SITE_S,
-    SITE_PV, SITE_DRAIN, SITE_SFREE, SITE_PDONE, SITE_QS, SITE_QE, SITE_QEMPTY, SITE_QBF, SITE_QQ, SITE_STG
+    SITE_PV, SITE_DRAIN, SITE_SFREE, SITE_PDONE, SITE_QS, SITE_QE, SITE_QEMPTY, SITE_QBF, SITE_QQ, SITE_STG,
+    SITE_ITEM
 };
 
 struct FwdParams {
@@ -184,7 +186,7 @@ struct FwdParams {
     float zero;   // always +0 (see dd_pair)
     int small;    // the single-launch small-shape path: prepare `sp` first (small_prepare)
     SmallPrep sp;
-    int sched;    // 1: each CTA walks its list of the ItemSchedule argument; 0: the stride (cta_item)
+    uint32_t *ticket;   // the item counter of this launch (one word of the status block, zero at launch)
 #ifdef SATTN_DEBUG_DUMP
     // intermediates of query tile 0 of (batch 0, head 0), KV tile 0:
     // [0, 32768) raw S accumulators (128 x 256), [32768, 40960) P8 words
@@ -309,38 +311,31 @@ __device__ __forceinline__ Tile item_tile(const FwdParams &p, int it)
 }
 
 // Which items a CTA walks.  Items cost in proportion to their KV tiles, and
-// the stride c, c + grid, c + 2 grid, ... gives each CTA the same number of
-// items, so the CTAs whose items were shorter finish early while the others
-// still run (most where a chunk of item_tile's order ends inside a wave).  The
-// host therefore makes a list schedule: it hands the items, in item_tile's
-// order, one by one to the CTA that a cost model (KV tiles + 1.5 per item)
-// says becomes free first, equal times to the lower CTA.  That is the order a
-// shared counter taken by CTAs as they free up would give, without a counter
-// and without the hand-over of each fetched index to the CTA's five roles.
-// The schedule travels as a kernel argument (CTA c's items are
-// list[first[c]] .. list[first[c + 1] - 1]); the kernel copies the CTA's part
-// to shared memory, closed by 0xffff.  The stride remains for launches with at
-// most one item per CTA, more items than the list holds, or a CTA share above
-// kSchedCtaMax.
-constexpr int kSchedMaxItems = 15360, kSchedMaxGrid = 192;
-template <int kItems, int kGrid>
-struct ItemScheduleT {
-    uint16_t first[kGrid + 1];
-    uint16_t list[kItems];
-};
-using ItemSchedule = ItemScheduleT<kSchedMaxItems, kSchedMaxGrid>;
-using NoSchedule = ItemScheduleT<1, 1>;   // the small path: always the stride
+// a fixed assignment (the stride c, c + grid, ..., or any list made in
+// advance from a cost model) leaves CTAs idle while others finish, most where
+// a chunk of item_tile's order ends inside a wave.  So the items are handed
+// out as the CTAs free up: CTA c starts with item c; its V loader, which runs
+// ahead of the other roles, takes each further item from a counter shared by
+// the CTAs (item = grid + ticket, in item_tile's order) two items before the
+// CTA needs it, and writes it into a ring of kItemSlots slots in shared
+// memory (ITEMFULL per slot).  The other roles read item n once, after the V
+// loader has reached item n - 2; by then every role has read item n - 3, so a
+// slot is never rewritten before all have read it, and no barrier runs two
+// phases ahead of a reader.  An index past the last item is written as -1.
 
-// Item number n (0, 1, ...) of this CTA, or -1 past its last item.  With a
-// schedule, n is at most the CTA's item count (every caller stops at -1).
-__device__ __forceinline__ int cta_item(const FwdParams &p, uint32_t sb, int n)
+// Item number n (0, 1, ...) of this CTA, or -1 past its last item; false if
+// the wait gave up.
+__device__ __forceinline__ bool cta_item(uint32_t sb, const Waiter &wt, int n, int &it)
 {
-    if (p.sched) {
-        const uint32_t v = ptx::ld_shared_u16(sb + OFF_ITEMS + 2u * static_cast<uint32_t>(n));
-        return v == 0xffffu ? -1 : static_cast<int>(v);
+    if (n == 0) {
+        it = static_cast<int>(blockIdx.x);
+        return true;
     }
-    const long long it = static_cast<long long>(blockIdx.x) + static_cast<long long>(n) * gridDim.x;
-    return it < p.n_items ? static_cast<int>(it) : -1;
+    const int s = (n - 1) & (kItemSlots - 1);
+    if (!wt.wait(sb + OFF_BAR + 8u * (ITEMFULL + s), ((n - 1) / kItemSlots) & 1, SITE_ITEM))
+        return false;
+    it = static_cast<int>(ptx::ld_shared_u32(sb + OFF_ITEMS + 4u * s));
+    return true;
 }
 
 // ---------------------------------------------------------------- the P step
@@ -682,7 +677,7 @@ __device__ __forceinline__ void kload_role(const FwdParams &p, const CUtensorMap
     int issued = -1;
     bool ok = true;
     int g = 0, n = 0;   // KV tiles and items of the earlier items
-    for (int it = cta_item(p, sb, 0); it >= 0 && ok; it = cta_item(p, sb, ++n)) {
+    for (int it = static_cast<int>(blockIdx.x); it >= 0 && ok; ok = ok && cta_item(sb, wt, ++n, it)) {
         Tile t = item_tile(p, it);
         t.g0 = g;
         const int bhk = t.b * p.Hkv + t.hk;
@@ -709,7 +704,8 @@ __device__ __forceinline__ void kload_role(const FwdParams &p, const CUtensorMap
 // V and Q loader.  V half-tiles (128 keys x 128 channels, E4M3) go to the two
 // V slots; at the first tile of every item, once that item's Q has left the
 // staging buffer (QFULL), the next item's INT8 Q tile (prepared codes only)
-// and V channel scales are staged.
+// and V channel scales are staged, and the item after it is taken from the
+// shared counter and written into the ring (cta_item).
 template <bool kFuseQ>
 __device__ __forceinline__ void vload_role(const FwdParams &p, const CUtensorMap *tm_v,
                                            const CUtensorMap *tm_q, uint32_t sb, const Waiter &wt)
@@ -728,15 +724,32 @@ __device__ __forceinline__ void vload_role(const FwdParams &p, const CUtensorMap
         ptx::bulk_load(sb + OFF_SV + (nq % 3) * SV_BYTES, p.v_scales + static_cast<size_t>(tq.b * p.Hkv + tq.hk) * HD,
                        SV_BYTES, bar(QSTAGE));
     };
+    // the items after the first: grid + a ticket of the launch's counter, -1
+    // past the last item (no tickets are taken when every CTA has one item)
+    const bool shared = p.n_items > static_cast<int>(gridDim.x);
+    auto take = [&]() { return shared ? atomicAdd(p.ticket, 1u) : 0xffffffffu; };
+    auto item_of = [&](uint32_t ticket) {
+        const long long v = static_cast<long long>(gridDim.x) + ticket;
+        return ticket != 0xffffffffu && v < p.n_items ? static_cast<int>(v) : -1;
+    };
+    auto publish = [&](int k, int v) {   // item k >= 1 of this CTA into its ring slot
+        const int sl = (k - 1) & (kItemSlots - 1);
+        ptx::st_shared_u32(sb + OFF_ITEMS + 4u * sl, static_cast<uint32_t>(v));
+        ptx::mbar_arrive(bar(ITEMFULL + sl));   // (release: the index is visible to the slot's readers)
+    };
+    int nx = item_of(take());   // item 1
+    publish(1, nx);
+    uint32_t pending = nx >= 0 ? take() : 0xffffffffu;   // ticket of item 2, in flight until item 0's first tile
     if (p.withhold_v) {   // test hook: the MMA thread's wait for V runs out
-        load_q(item_tile(p, cta_item(p, sb, 0)), 0);
+        load_q(item_tile(p, static_cast<int>(blockIdx.x)), 0);
         wt.drain(bar(QSTAGE), 0);
         return;
     }
     int issued_v = -1, issued_q = -1;
     bool ok = true;
     int g = 0, n = 0;   // KV tiles and items of this CTA before the current item
-    for (int it = cta_item(p, sb, 0); it >= 0 && ok; it = cta_item(p, sb, ++n)) {
+    int nx2 = -1;       // item n + 2, once written
+    for (int it = static_cast<int>(blockIdx.x); it >= 0 && ok; ++n, it = nx, nx = nx2) {
         Tile t = item_tile(p, it);
         t.g0 = g;
         const int bhk = t.b * p.Hkv + t.hk;
@@ -758,14 +771,16 @@ __device__ __forceinline__ void vload_role(const FwdParams &p, const CUtensorMap
             if (!ok)
                 break;
             SATTN_TRACE(p, t, 12, j);
-            const int nx = j == 0 ? cta_item(p, sb, n + 1) : -1;
-            if (nx >= 0) {
+            if (j == 0 && nx >= 0) {
                 if (!wt.wait(bar(QFULL), n & 1, SITE_QE)) {
                     ok = false;
                     break;
                 }
                 load_q(item_tile(p, nx), n + 1);
                 issued_q = n + 1;
+                nx2 = item_of(pending);   // item n + 2 (the ticket was taken one item ago)
+                publish(n + 2, nx2);
+                pending = nx2 >= 0 ? take() : 0xffffffffu;
             }
         }
         g += t.ntiles;
@@ -786,7 +801,7 @@ __device__ __forceinline__ void mma_role(const FwdParams &p, uint32_t sb, uint32
     auto bar = [sb](int i) { return sb + OFF_BAR + 8u * i; };
     bool ok = true;
     int g = 0, n = 0;
-    for (int it = cta_item(p, sb, 0); it >= 0 && ok; it = cta_item(p, sb, ++n)) {
+    for (int it = static_cast<int>(blockIdx.x); it >= 0 && ok; ok = ok && cta_item(sb, wt, ++n, it)) {
         Tile t = item_tile(p, it);
         t.g0 = g;
         SATTN_TRACE(p, t, 39, 0);
@@ -941,11 +956,11 @@ __device__ __forceinline__ void qconv_role(const FwdParams &p, const CUtensorMap
     if (kFuseQ) {
         if (lane == 0)
             ptx::prefetch_tensormap(tm_q);
-        if (!quantize_item(cta_item(p, sb, 0), 0))
+        if (!quantize_item(static_cast<int>(blockIdx.x), 0))
             return;
     }
     int n = 0;
-    for (int it = cta_item(p, sb, 0); it >= 0; it = cta_item(p, sb, ++n)) {
+    for (int it = static_cast<int>(blockIdx.x); it >= 0;) {
         if ((n >= 1 && !wt.wait(bar(QEMPTY), (n - 1) & 1, SITE_QEMPTY)) ||
             !wt.wait(bar(QSTAGE), n & 1, SITE_QS))
             return;
@@ -966,14 +981,17 @@ __device__ __forceinline__ void qconv_role(const FwdParams &p, const CUtensorMap
         }
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(bar(QFULL));
+        if (!cta_item(sb, wt, n + 1, it))
+            return;
         if (kFuseQ) {
-            const int nx = cta_item(p, sb, n + 1);
+            const int nx = it;
             if (nx >= 0) {
                 __syncwarp();   // every lane has read the INT8 tile before it is rewritten
                 if (!wt.wait(bar(STGFREE), n & 1, SITE_STG) || !quantize_item(nx, n + 1))
                     return;
             }
         }
+        ++n;
     }
 }
 
@@ -1009,7 +1027,7 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
         return kb < p.nbk ? (p.small ? ptx::ld_f32(a) : ptx::ld_nc_f32(a)) : 0.0f;
     };
 
-    int it = cta_item(p, sb, 0);
+    int it = static_cast<int>(blockIdx.x);
     Tile t = item_tile(p, it);
     if (r == 0 && half == 0)
         SATTN_TRACE(p, t, 38, 1);
@@ -1086,7 +1104,9 @@ __device__ __forceinline__ bool compute_loop(const FwdParams &p, const CUtensorM
         t.g0 = g;
         const int i = t.q0 + r;
         const int lim = p.causal ? i + (p.Nkv - p.Nq) : 0x7fffffff;   // last kept key of row i
-        const int nx = cta_item(p, sb, n + 1);
+        int nx;
+        if (!cta_item(sb, wt, n + 1, nx))
+            return false;
         const bool has_next = nx >= 0;
         // (the next item's tile is recomputed where needed rather than kept live)
         float sq_next = (!kFuseQ && has_next) ? qscale(item_tile(p, nx)) : 0.0f;
@@ -1624,14 +1644,11 @@ __device__ __forceinline__ void small_prepare(const FwdParams &p, uint8_t *smem)
 
 // kSmall: the single-launch small-shape path, whose preparation runs first
 // (a separate instantiation, so that the other launches carry none of its code)
-// kList: the launch carries a list schedule (a ~30 KB argument, which costs
-// about 2 us per launch; launches without a list use the small argument).
-template <bool kFuseQ, bool kSmall, bool kList>
+template <bool kFuseQ, bool kSmall>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
-                    const FwdParams p,
-                    const __grid_constant__ std::conditional_t<kList, ItemSchedule, NoSchedule> sched)
+                    const FwdParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1651,11 +1668,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             small_prepare(p, smem);
     }
 
-    if (kList && p.sched) {   // this CTA's items, closed by 0xffff (read after the barrier below)
-        const int b = sched.first[blockIdx.x], cnt = sched.first[blockIdx.x + 1] - b;
-        for (int k = threadIdx.x; k <= cnt; k += NTHREADS)
-            reinterpret_cast<uint16_t *>(smem + OFF_ITEMS)[k] = k < cnt ? sched.list[b + k] : uint16_t{0xffff};
-    }
     if (threadIdx.x == 0) {
         *flag = *reinterpret_cast<volatile uint32_t *>(p.status);
         *reinterpret_cast<volatile uint32_t *>(smem + OFF_ABORT) = 0u;
@@ -1681,6 +1693,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ptx::mbar_init(b0 + 8u * QBF, 1);
         ptx::mbar_init(b0 + 8u * QQDONE, 1);
         ptx::mbar_init(b0 + 8u * STGFREE, 8);
+        for (int s = 0; s < kItemSlots; ++s)
+            ptx::mbar_init(b0 + 8u * (ITEMFULL + s), 1);
         ptx::fence_mbar_init();
     }
     // constant rows of every V slot: row 128 holds E4M3 1.0 (0x38), rows 129..143 hold 0
@@ -1700,7 +1714,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + OFF_TMEM_SLOT);
 
-    if (*flag == 0 && cta_item(p, sb, 0) >= 0) {
+    if (*flag == 0 && static_cast<int>(blockIdx.x) < p.n_items) {
         if (warp < WARP_PRODUCER) {
             ptx::setmaxnreg_inc<kRegsCompute>();
             compute_role<kFuseQ>(p, &tm_o, sb, tmem, warp, lane, wt);
@@ -1834,18 +1848,18 @@ namespace {
 // The per-warpgroup register split only adds up when the kernel is launched
 // with exactly kLaunchRegs registers per thread; refuse to launch otherwise.
 // Also raises the kernel's dynamic shared-memory limit.  Once per process.
-template <bool kFuseQ, bool kSmall, bool kList>
+template <bool kFuseQ, bool kSmall>
 cudaError_t kernel_attributes()
 {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
         cudaFuncAttributes fa;
-        attr_err = cudaFuncGetAttributes(&fa, attn_fwd_kernel<kFuseQ, kSmall, kList>);
+        attr_err = cudaFuncGetAttributes(&fa, attn_fwd_kernel<kFuseQ, kSmall>);
         if (attr_err == cudaSuccess && fa.numRegs != kLaunchRegs)
             attr_err = cudaErrorInvalidConfiguration;
         if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(attn_fwd_kernel<kFuseQ, kSmall, kList>,
+            attr_err = cudaFuncSetAttribute(attn_fwd_kernel<kFuseQ, kSmall>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
     });
     return attr_err;
@@ -1887,82 +1901,13 @@ bool plan_items(const Geometry &g, FwdParams &prm)
     return true;
 }
 
-// KV tiles of item `it` as item_tile computes them (host copy, for the cost
-// model of the schedule only: no result depends on it).
-int host_item_ntiles(const FwdParams &p, int it)
-{
-    const int c = it / p.chunk_items, r = it - c * p.chunk_items, u0 = c * p.chunk_units;
-    const int row = (u0 + p.chunk_units > p.n_units ? p.n_units - u0 : p.chunk_units) * p.group;
-    const int q0 = (p.n_qtiles - 1 - r / row) * BM;
-    int kv_end = p.Nkv;
-    if (p.causal)
-        kv_end = std::min(p.Nkv, std::min(q0 + BM, p.Nq) + (p.Nkv - p.Nq));
-    return (kv_end + BN - 1) / BN;
-}
-
-// The list schedule of the items over `grid` CTAs (see ItemSchedule): items in
-// order, each to the CTA with the earliest modelled finish, costs in half
-// tiles (2 per KV tile, 3 per item).  False where the stride is kept.
-bool build_item_schedule(const FwdParams &p, int grid, ItemSchedule &s)
-{
-    if (grid > kSchedMaxGrid || p.n_items > kSchedMaxItems || p.n_items <= grid)
-        return false;
-    using Slot = std::pair<long long, int>;   // (modelled finish, CTA)
-    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
-    for (int c = 0; c < grid; ++c)
-        free_at.push({0, c});
-    std::vector<int> owner(p.n_items), count(grid, 0);
-    for (int it = 0; it < p.n_items; ++it) {
-        const Slot f = free_at.top();
-        free_at.pop();
-        owner[it] = f.second;
-        if (++count[f.second] > kSchedCtaMax)
-            return false;
-        free_at.push({f.first + 2 * host_item_ntiles(p, it) + 3, f.second});
-    }
-    std::vector<int> next(grid);
-    int k = 0;
-    for (int c = 0; c < grid; ++c) {
-        s.first[c] = static_cast<uint16_t>(k);
-        next[c] = k;
-        k += count[c];
-    }
-    s.first[grid] = static_cast<uint16_t>(k);
-    for (int it = 0; it < p.n_items; ++it)   // each CTA's items in increasing order
-        s.list[next[owner[it]]++] = static_cast<uint16_t>(it);
-    return true;
-}
-
-// The schedule of the last launch shape of this thread, rebuilt when the
-// shape or the grid changes.
-struct ScheduleCache {
-    int key[10] = {-1};
-    bool valid = false;
-    ItemSchedule s;
-};
-static_assert(kSchedMaxItems < 0xffff && kSchedCtaMax < kSchedMaxItems, "item indices and the end mark fit 16 bits");
-static_assert(4 * sizeof(CUtensorMap) + sizeof(FwdParams) + sizeof(ItemSchedule) + 256 <= 32764,
-              "kernel arguments within the 32764-byte limit");
-
-const ItemSchedule *item_schedule(const FwdParams &p, int grid)
-{
-    static thread_local ScheduleCache cache;
-    const int key[10] = {p.n_items, grid, p.n_qtiles, p.causal, p.Nq, p.Nkv, p.n_units, p.chunk_units, p.group,
-                         p.chunk_items};
-    if (std::memcmp(key, cache.key, sizeof key) != 0) {
-        std::memcpy(cache.key, key, sizeof key);
-        cache.valid = build_item_schedule(p, grid, cache.s);
-    }
-    return cache.valid ? &cache.s : nullptr;
-}
-
 // q: INT8 codes [B, Hq, nq32, 128] with q_scales, or with kFuseQ the BF16 Q
 // [B, Hq, Nq, 128] itself (q_scales unused)
 template <bool kFuseQ>
 int launch_impl(const Geometry &g, const void *q, const float *q_scales, const int8_t *k_codes,
                 const float *k_scales, const uint8_t *v_codes, const float *v_scales, void *out,
                 void *status_block, void *k_carrier, cudaStream_t stream, bool withhold_v, bool reset_status,
-                const SmallPrep *small = nullptr)
+                const SmallPrep *small = nullptr, int ticket_slot = 0)
 {
     auto encode = tensor_map_encoder();
     if (!encode)
@@ -2031,12 +1976,10 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const i
             return 1;
     }
 
-    cudaError_t attr_err = kernel_attributes<kFuseQ, false, false>();
-    if (attr_err == cudaSuccess)
-        attr_err = kernel_attributes<kFuseQ, false, true>();
+    cudaError_t attr_err = kernel_attributes<kFuseQ, false>();
     if constexpr (!kFuseQ)
         if (small && attr_err == cudaSuccess)
-            attr_err = kernel_attributes<false, true, false>();
+            attr_err = kernel_attributes<false, true>();
     if (attr_err != cudaSuccess)
         return static_cast<int>(attr_err);
 
@@ -2073,28 +2016,26 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const i
     prm.dbg = debug_dump_buffer();
 #endif
 
-    // persistent: one CTA per SM, each walking its items (cta_item)
+    // persistent: one CTA per SM, each taking items as it frees up (cta_item);
+    // the launch's item counter is a word of the status block, zeroed here
     int dev = 0, n_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm < 1)
         return static_cast<int>(cudaErrorInvalidDevice);
     const int grid = std::min(prm.n_items, n_sm);
-    const ItemSchedule *sched = small ? nullptr : item_schedule(prm, grid);
-    prm.sched = sched ? 1 : 0;
+    prm.ticket = status + 2 + (ticket_slot & 1);
+    if (prm.n_items > grid && cudaMemsetAsync(prm.ticket, 0, sizeof(uint32_t), stream) != cudaSuccess)
+        return static_cast<int>(cudaGetLastError());
     if (g_ev_before && cudaEventRecord(g_ev_before, stream) != cudaSuccess)
         return static_cast<int>(cudaGetLastError());
     bool launched = false;
     if constexpr (!kFuseQ)
         if (small) {
-            attn_fwd_kernel<false, true, false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, tmo, prm,
-                                                                                         NoSchedule{});
+            attn_fwd_kernel<false, true><<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, tmo, prm);
             launched = true;
         }
-    if (!launched && sched)
-        attn_fwd_kernel<kFuseQ, false, true><<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, tmo, prm, *sched);
-    else if (!launched)
-        attn_fwd_kernel<kFuseQ, false, false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, tmo, prm,
-                                                                                      NoSchedule{});
+    if (!launched)
+        attn_fwd_kernel<kFuseQ, false><<<grid, NTHREADS, SMEM_BYTES, stream>>>(tmk, tmv, tmq, tmo, prm);
     const cudaError_t le = cudaGetLastError();
     if (le != cudaSuccess)
         return static_cast<int>(le);
@@ -2108,19 +2049,18 @@ int launch_impl(const Geometry &g, const void *q, const float *q_scales, const i
 int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scales,
                    const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
                    const float *v_scales, void *out, void *status, void *carrier, cudaStream_t stream,
-                   bool withhold_v, bool reset_status)
+                   bool withhold_v, bool reset_status, int ticket_slot)
 {
     return launch_impl<false>(g, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, out, status, carrier,
-                              stream, withhold_v, reset_status);
+                              stream, withhold_v, reset_status, nullptr, ticket_slot);
 }
 
 int forward_init()
 {
     if (!tensor_map_encoder())
         return 1;
-    const cudaError_t r[5] = {kernel_attributes<false, false, false>(), kernel_attributes<false, false, true>(),
-                              kernel_attributes<true, false, false>(), kernel_attributes<true, false, true>(),
-                              kernel_attributes<false, true, false>()};
+    const cudaError_t r[3] = {kernel_attributes<false, false>(), kernel_attributes<true, false>(),
+                              kernel_attributes<false, true>()};
     for (const cudaError_t e : r)
         if (e != cudaSuccess)
             return static_cast<int>(e);
@@ -2133,22 +2073,6 @@ int launch_forward_q_bf16(const Geometry &g, const void *q, const int8_t *k_code
 {
     return launch_impl<true>(g, q, nullptr, k_codes, k_scales, v_codes, v_scales, out, status, carrier, stream,
                              false, true);
-}
-
-int item_schedule(const Geometry &g, int n_sm, int *grid, uint16_t *first, uint16_t *list, int *n_listed)
-{
-    FwdParams prm{};
-    if (n_sm < 1 || !plan_items(g, prm))
-        return 1;
-    *grid = std::min(prm.n_items, n_sm);
-    *n_listed = 0;
-    std::vector<ItemSchedule> s(1);
-    if (!build_item_schedule(prm, *grid, s[0]))
-        return 0;   // the stride
-    std::memcpy(first, s[0].first, sizeof(uint16_t) * (*grid + 1));
-    std::memcpy(list, s[0].list, sizeof(uint16_t) * prm.n_items);
-    *n_listed = prm.n_items;
-    return 0;
 }
 
 int launch_small(const Geometry &g, const SmallPrep &sp, void *out, void *status, void *carrier, cudaStream_t stream)

@@ -358,7 +358,7 @@ int attention_host_pipelined(const Geometry &g, const sattn_shape &shape, const 
                                   hb.pws[c & 1], st) != cudaSuccess)
             return SATTN_ERR_LAUNCH;
         const int frc = sattn::launch_forward(gc, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, out,
-                                              hb.fws, hb.carrier[c & 1], st, false, false);
+                                              hb.fws, hb.carrier[c & 1], st, false, false, c & 1);
         if (frc == 1)
             return SATTN_ERR_DEVICE;
         if (frc != 0)
@@ -622,18 +622,6 @@ int sattn_test_host_chunks(const sattn_shape *shape, int n_sm, int64_t *bounds, 
     for (int c = 0; c <= *nchunks; ++c)
         bounds[c] = b[c];
     return SATTN_OK;
-}
-
-int sattn_test_item_schedule(const sattn_shape *shape, int n_sm, int *grid, uint16_t *first, uint16_t *list,
-                              int *n_listed)
-{
-    Geometry g;
-    const int rc = make_geometry(shape, &g);
-    if (rc != SATTN_OK)
-        return rc;
-    if (!grid || !first || !list || !n_listed || n_sm < 1)
-        return SATTN_ERR_INVALID;
-    return sattn::item_schedule(g, n_sm, grid, first, list, n_listed) == 0 ? SATTN_OK : SATTN_ERR_INVALID;
 }
 
 int sattn_check_status(const void *forward_workspace, void *stream)

@@ -70,10 +70,13 @@ size_t forward_workspace_bytes(const Geometry &g);
 // withhold_v (test hook): no V tile is loaded, so the launch ends through its
 // bounded waits and reports a timeout in the status block.  With reset_status false
 // the status block is not cleared first (several launches report into one).
+// Status block: words 0-1 the status (flag, site of a wait that gave up),
+// words 2-3 the item counters of launches in flight at the same time (the
+// launch's ticket_slot, 0 or 1, picks one; it is zeroed before each launch).
 int launch_forward(const Geometry &g, const int8_t *q_codes, const float *q_scales,
                    const int8_t *k_codes, const float *k_scales, const uint8_t *v_codes,
                    const float *v_scales, void *out, void *status, void *carrier, cudaStream_t stream,
-                   bool withhold_v = false, bool reset_status = true);
+                   bool withhold_v = false, bool reset_status = true, int ticket_slot = 0);
 
 // One-time host setup of the forward kernels (tensor-map encoder, register
 // check, shared-memory limit), so that launches captured into a CUDA graph
@@ -106,12 +109,6 @@ struct SmallPrep {
     uint8_t *v_codes;
     float *v_scales;
 };
-// The attention kernel's list schedule of work items for `g` on n_sm SMs
-// (host only): grid = the CTAs launched; with n_listed = n_items > 0, CTA c
-// walks list[first[c]] .. list[first[c + 1] - 1], with n_listed = 0 the
-// stride c, c + grid, ...  first holds n_sm + 1 entries, list n_items.
-// 0 on success.
-int item_schedule(const Geometry &g, int n_sm, int *grid, uint16_t *first, uint16_t *list, int *n_listed);
 // Largest Nkv of the small-shape path (its K-mean chunk sums stay in shared memory).
 constexpr int kSmallMaxNkv = 1024;
 // prepare + forward in one launch for B = Hq = Hkv = 1, Nq <= 128, Nkv <= kSmallMaxNkv;

@@ -185,71 +185,3 @@ def test_host_chunk_plan_properties_over_many_shapes(lib):
             if len(sizes) > 1:
                 assert min(sizes) * (-(-N // 128) * g) >= 2 * n_sm
 
-
-def _item_schedule(lib, dims, n_sm=152):
-    B, Hq, Hkv, Nq, Nkv, causal = dims
-    n_items = B * Hq * -(-Nq // 128)
-    first = (ctypes.c_uint16 * (n_sm + 1))()
-    lst = (ctypes.c_uint16 * max(1, n_items))()
-    grid, n = ctypes.c_int(), ctypes.c_int()
-    shape = sattn.make_shape(*dims)
-    assert lib.sattn_test_item_schedule(ctypes.byref(shape), n_sm, ctypes.byref(grid), first, lst,
-                                        ctypes.byref(n)) == 0
-    return n_items, grid.value, list(first)[:grid.value + 1], list(lst)[:n.value], n.value
-
-
-def _item_costs(dims):
-    """KV tiles of every work item in the kernel's order: (batch, KV head) units
-    in chunks whose K carrier and V codes (3 bytes per key and channel) fit in
-    48 MB, spread evenly; within a chunk query tiles in decreasing order, then
-    units, then the query heads of a unit's group.  Cost = KV tiles + 1.5."""
-    B, Hq, Hkv, Nq, Nkv, causal = dims
-    units, group, nqt = B * Hkv, Hq // Hkv, -(-Nq // 128)
-    cap = max(1, min(units, (48 << 20) // (Nkv * 128 * 3)))
-    n_chunks = -(-units // cap)
-    cu = -(-units // n_chunks)
-    costs = []
-    for u0 in range(0, units, cu):
-        for qi in range(nqt):
-            q0 = (nqt - 1 - qi) * 128
-            kv_end = min(Nkv, min(q0 + 128, Nq) + Nkv - Nq) if causal else Nkv
-            costs += [-(-kv_end // 256) + 1.5] * (min(cu, units - u0) * group)
-    return costs
-
-
-@pytest.mark.parametrize("dims", [
-    (4, 32, 8, 8192, 8192, True),       # c5
-    (1, 16, 16, 32760, 32760, False),   # c4
-    (2, 32, 32, 4000, 4000, True),      # c3
-    (3, 6, 2, 3000, 3300, True),        # ragged, bottom-right causal, GQA 3
-    (2, 4, 4, 20000, 20000, False)])    # one chunk per unit
-def test_item_schedule_is_a_list_schedule(lib, dims):
-    n_items, grid, first, lst, n = _item_schedule(lib, dims)
-    assert grid == 152 and n == n_items
-    assert sorted(lst) == list(range(n_items))                       # every item exactly once
-    assert first[0] == 0 and first[-1] == n_items
-    per = [lst[first[c]:first[c + 1]] for c in range(grid)]
-    assert all(len(x) >= 1 and x == sorted(x) for x in per)          # each CTA in the kernel's order
-    assert [x[0] for x in per] == list(range(grid))                  # the first wave as the stride's
-    costs = _item_costs(dims)
-    assert len(costs) == n_items
-    owner = [0] * n_items
-    for c, x in enumerate(per):
-        for it in x:
-            owner[it] = c
-    finish = [0.0] * grid
-    for it in range(n_items):    # list scheduling: each item to a CTA that is free first
-        assert finish[owner[it]] == min(finish), it
-        finish[owner[it]] += costs[it]
-    stride = [sum(costs[c::grid]) for c in range(grid)]
-    total, longest = sum(costs), max(costs)
-    assert max(finish) <= total / grid + (1 - 1 / grid) * longest + 1e-9   # Graham's bound
-    assert max(finish) <= max(stride)
-
-
-def test_item_schedule_keeps_the_stride_where_no_list_is_needed(lib):
-    assert _item_schedule(lib, (1, 8, 8, 1024, 1024, False))[4] == 0    # 64 items, one per CTA
-    assert _item_schedule(lib, (1, 1, 1, 128, 192, False))[4] == 0      # one item
-    assert _item_schedule(lib, (8, 32, 8, 8192, 8192, True))[4] == 0    # 16384 items: above the list's size
-    n_items, grid, *_ , n = _item_schedule(lib, (4, 32, 8, 8192, 8192, True), n_sm=8)
-    assert grid == 8 and n == 0                                         # a CTA's share above its list
