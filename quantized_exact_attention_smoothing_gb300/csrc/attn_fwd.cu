@@ -315,13 +315,18 @@ __device__ __forceinline__ Tile item_tile(const FwdParams &p, int it)
 // advance from a cost model) leaves CTAs idle while others finish, most where
 // a chunk of item_tile's order ends inside a wave.  So the items are handed
 // out as the CTAs free up: CTA c starts with item c; its V loader, which runs
-// ahead of the other roles, takes each further item from a counter shared by
-// the CTAs (item = grid + ticket, in item_tile's order) two items before the
-// CTA needs it, and writes it into a ring of kItemSlots slots in shared
-// memory (ITEMFULL per slot).  The other roles read item n once, after the V
-// loader has reached item n - 2; by then every role has read item n - 3, so a
-// slot is never rewritten before all have read it, and no barrier runs two
-// phases ahead of a reader.  An index past the last item is written as -1.
+// ahead of the other roles, takes item n + 1 from a counter shared by the
+// CTAs (item = grid + ticket, in item_tile's order) as it starts loading the
+// V tiles of item n, and writes it into a ring of kItemSlots slots in shared
+// memory (ITEMFULL per slot).  A CTA thus holds at most one item beyond the
+// one it works on, so the CTAs finish within about one short item of each
+// other.  Item n + 1 is written once the PV of item n - 1 has freed the V
+// slots, so the compute warps and the MMA thread are in item n - 1 or later
+// and have read item n - 1; the K loader runs ahead of them, and the Q
+// converter has arrived on QFULL of item n - 1 and read item n - 1.  The slot
+// rewritten held item n - 3: no slot is rewritten before all have read it, and
+// no barrier runs two phases ahead of a reader.  An index past the last item
+// is written as -1.
 
 // Item number n (0, 1, ...) of this CTA, or -1 past its last item; false if
 // the wait gave up.
@@ -704,8 +709,8 @@ __device__ __forceinline__ void kload_role(const FwdParams &p, const CUtensorMap
 // V and Q loader.  V half-tiles (128 keys x 128 channels, E4M3) go to the two
 // V slots; at the first tile of every item, once that item's Q has left the
 // staging buffer (QFULL), the next item's INT8 Q tile (prepared codes only)
-// and V channel scales are staged, and the item after it is taken from the
-// shared counter and written into the ring (cta_item).
+// and V channel scales are staged; the next item is taken from the shared
+// counter and written into the ring (cta_item) just before.
 template <bool kFuseQ>
 __device__ __forceinline__ void vload_role(const FwdParams &p, const CUtensorMap *tm_v,
                                            const CUtensorMap *tm_q, uint32_t sb, const Waiter &wt)
@@ -737,10 +742,8 @@ __device__ __forceinline__ void vload_role(const FwdParams &p, const CUtensorMap
         ptx::st_shared_u32(sb + OFF_ITEMS + 4u * sl, static_cast<uint32_t>(v));
         ptx::mbar_arrive(bar(ITEMFULL + sl));   // (release: the index is visible to the slot's readers)
     };
-    int nx = item_of(take());   // item 1
-    publish(1, nx);
-    uint32_t pending = nx >= 0 ? take() : 0xffffffffu;   // ticket of item 2, in flight until item 0's first tile
     if (p.withhold_v) {   // test hook: the MMA thread's wait for V runs out
+        publish(1, -1);
         load_q(item_tile(p, static_cast<int>(blockIdx.x)), 0);
         wt.drain(bar(QSTAGE), 0);
         return;
@@ -748,8 +751,8 @@ __device__ __forceinline__ void vload_role(const FwdParams &p, const CUtensorMap
     int issued_v = -1, issued_q = -1;
     bool ok = true;
     int g = 0, n = 0;   // KV tiles and items of this CTA before the current item
-    int nx2 = -1;       // item n + 2, once written
-    for (int it = static_cast<int>(blockIdx.x); it >= 0 && ok; ++n, it = nx, nx = nx2) {
+    int nx = -1;        // item n + 1, taken at the first V tile of item n
+    for (int it = static_cast<int>(blockIdx.x); it >= 0 && ok; ++n, it = nx) {
         Tile t = item_tile(p, it);
         t.g0 = g;
         const int bhk = t.b * p.Hkv + t.hk;
@@ -771,16 +774,17 @@ __device__ __forceinline__ void vload_role(const FwdParams &p, const CUtensorMap
             if (!ok)
                 break;
             SATTN_TRACE(p, t, 12, j);
-            if (j == 0 && nx >= 0) {
-                if (!wt.wait(bar(QFULL), n & 1, SITE_QE)) {
-                    ok = false;
-                    break;
+            if (j == 0) {   // the CTA commits to its next item only now, one item ahead
+                nx = item_of(take());
+                publish(n + 1, nx);
+                if (nx >= 0) {
+                    if (!wt.wait(bar(QFULL), n & 1, SITE_QE)) {
+                        ok = false;
+                        break;
+                    }
+                    load_q(item_tile(p, nx), n + 1);
+                    issued_q = n + 1;
                 }
-                load_q(item_tile(p, nx), n + 1);
-                issued_q = n + 1;
-                nx2 = item_of(pending);   // item n + 2 (the ticket was taken one item ago)
-                publish(n + 2, nx2);
-                pending = nx2 >= 0 ? take() : 0xffffffffu;
             }
         }
         g += t.ntiles;
