@@ -502,13 +502,6 @@ __device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v)
     asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr)
-{
-    uint16_t v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
-    return v;
-}
-
 // Packed pairs of FP32 values (low word = first element): elementwise
 // products, differences, each rounded to nearest even like the scalar ops.
 __device__ __forceinline__ uint64_t f32x2(float lo, float hi)
