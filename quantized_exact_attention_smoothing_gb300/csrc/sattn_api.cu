@@ -232,7 +232,9 @@ int forward_impl(const Geometry &g, const int8_t *q_codes, const float *q_scales
 // and a second one (so one chunk's forward tail overlaps the next chunk's
 // start), and the copies back run on a third; events hand each chunk from
 // stage to stage.  Every chunk's forward reports into the one status block,
-// cleared once before the fork.
+// cleared once before the fork; the forwards of the two kernel streams, which
+// may run at the same time, take their work items from separate counter words
+// of that block (ticket slot = chunk parity).
 // ---------------------------------------------------------------------------
 struct HostBuffers {
     void *q, *k, *v, *out, *carrier[2], *pws[2], *fws;
